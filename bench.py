@@ -1,0 +1,520 @@
+#!/usr/bin/env python3
+"""Throughput of the dense bf16 GEMM on GB300, as one JSON line.
+
+Workload (one "step"): C = GELU_tanh(A @ B + bias) with M = N = K = 8192,
+A row-major and B column-major bf16, Uniform(-1,1)/sqrt(K) from a seed, bias
+fp32 N(0,1), fp32 accumulation, bf16 output; one call of the library's C ABI
+(``gemm_batched``) on the current stream.  Metric: TFLOPS = 2MNK / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--rows FILE]
+
+--impl reference times the CPU oracle (plain fp64 C, one host core) on a
+bounded slice of the same workload: the deliberately slow baseline.
+--rows FILE additionally measures the other library paths (SGEMM 4096^3,
+ragged 4097x3001x1000, split-K 256x256x65536, skinny 16x8192x8192, batched
+64x1024^3) and writes one JSON object per path to FILE.
+Multi-GPU runs (torchrun) run one independent replica per GPU (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2MNK/s), bf16 8192^3, and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOPS"
+M = N = K = 8192
+WORKLOAD = ("bf16 GEMM M=N=K=8192, A row-major, B column-major, fused bias + GELU(tanh), "
+            "fp32 accumulate, bf16 output")
+WORKLOAD_ID = 3  # seeds 3001 (A), 3002 (B), 3004 (bias)
+L2_NOTE = "inputs larger than L2: A + B = 256 MiB and C = 128 MiB vs a 126.5 MiB L2; no flush"
+TC_SOURCES = ["tc_gemm.cu", "ptx.cuh", "epilogue.cuh", "tile_order.h", "internal.h"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--rows", default=None, help="also measure the other paths into this file")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def tc_source_sha():
+    h = hashlib.sha256()
+    for name in TC_SOURCES:
+        with open(os.path.join(ROOT, "dense_gemm_bf16_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "tc_gemm_bf16_8192_bias_gelu.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = traffic = None
+    for line in text.splitlines():
+        if line.startswith("kernel_source_sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if sha == tc_source_sha() else None
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def c3_host_inputs():
+    import numpy as np
+
+    import datagen
+    a = datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(WORKLOAD_ID, datagen.ROLE_A),
+                                             (M, K)) / math.sqrt(K))
+    b = datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(WORKLOAD_ID, datagen.ROLE_B),
+                                             (K, N)) / math.sqrt(K))
+    b_cm = np.ascontiguousarray(b.T)  # column-major storage: B(k, n) at n*K + k
+    bias = datagen.to_f32(datagen.normal(datagen.seed_for(WORKLOAD_ID, datagen.ROLE_BIAS), (N,)))
+    return a, b_cm, bias
+
+
+class Gemm:
+    """The C3 call through the C ABI, bound to fixed device buffers."""
+
+    def __init__(self, dA, dB, dbias, dC, stream):
+        import dense_gemm_bf16_gb300 as dg
+        self.dg = dg
+        self.args = [int(dg.DType.BF16), 1, M, N, K, dA.data_ptr(), K, 0, 0, dB.data_ptr(), K,
+                     1, 0, dC.data_ptr(), N, 0, 0, int(dg.DType.BF16), 1.0, 0.0,
+                     dbias.data_ptr(), int(dg.Epi.BIAS_GELU_TANH), 0]
+        st, plan = dg.gemm_plan_query(*self.args, 0)
+        if st != 0:
+            raise RuntimeError(f"plan: {dg.gemm_status_string(st)}")
+        self.plan = plan.as_dict()
+        self.stream = stream
+
+    def __call__(self):
+        st = self.dg.gemm_batched(*self.args, None, 0, self.stream)
+        if st != 0:
+            raise RuntimeError(f"gemm_batched: {self.dg.gemm_status_string(st)}")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+        self.proc = None
+        target = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"] + target, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, pw, reasons = [], [], [], set()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(fn, steps, warmup, barrier=None):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        fn()
+    stop.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(stop)  # ms for all steps
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_tflops(a, b_cm, bias, rows, cols):
+    """The oracle, as it stands, on the first `rows` x `cols` outputs of the
+    workload (full K).  Returns (seconds, flops)."""
+    import numpy as np
+
+    import oracle
+    b_sub = np.ascontiguousarray(b_cm[:cols])  # first `cols` columns of the column-major B
+    p = oracle.Problem(ab_dtype="bf16", M=rows, N=cols, K=K, A=a[:rows].ravel(), lda=K,
+                       la="row", B=b_sub.ravel(), ldb=K, lb="col", c_dtype="bf16",
+                       bias=bias[:cols], act="gelu_tanh")
+    t0 = time.perf_counter()
+    oracle.gemm(p)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * cols * K
+
+
+def cpu_baseline(a, b_cm, bias, target_s=12.0):
+    # calibrate on 1 x 512 outputs, then size the sample for ~target_s of CPU work
+    dt, fl = oracle_sample_tflops(a, b_cm, bias, 1, 512)
+    per_out = dt / 512
+    n_out = max(512, min(int(target_s / max(per_out, 1e-9)), 64 * N))
+    rows = max(1, n_out // N)
+    cols = N if n_out >= N else n_out
+    dt, fl = oracle_sample_tflops(a, b_cm, bias, rows, cols)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} row(s) x {cols} column(s) of C (full K = {K}), "
+                      f"{dt:.1f} s, fp64 oracle, one thread"}
+
+
+def reference_arm(args):
+    """Times the oracle on this host's cores: one bounded slice per step."""
+    a, b_cm, bias = c3_host_inputs()
+    dt, _ = oracle_sample_tflops(a, b_cm, bias, 1, 256)
+    per_out = dt / 256
+    budget = 150.0 / (args.steps + args.warmup)  # whole run within a few minutes
+    cols = int(max(16, min(N, budget / max(per_out, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_sample_tflops(a, b_cm, bias, 1, cols)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        t, f = oracle_sample_tflops(a, b_cm, bias, 1, cols)
+        tot_t += t
+        tot_f += f
+    value = tot_f / tot_t / 1e12
+    sample = (f"per step: 1 row x {cols} columns of C (full K = {K}), fp64 oracle, one thread; "
+              f"{args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main arm
+
+def main():
+    args = parse_args()
+    rank, world, local = env_rank()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        reference_arm(args)
+        return
+
+    import numpy as np
+    import torch
+
+    import dense_gemm_bf16_gb300 as dg
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", local if world > 1 else 0)
+    dg.build()
+    dg.lib()
+
+    a, b_cm, bias = c3_host_inputs()
+    hA = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hB = torch.from_numpy(b_cm.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hbias = torch.from_numpy(bias).pin_memory()
+    dA = hA.to(device)
+    dB = hB.to(device)
+    dbias = hbias.to(device)
+    dC = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream(device).cuda_stream
+    gemm = Gemm(dA, dB, dbias, dC, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # device-resident throughput (clocks sampled during the timed region)
+    sampler = ClockSampler(device.index)
+    time.sleep(0.3)
+    ms_total = time_steps(gemm, args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+    flops = 2.0 * M * N * K
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H result
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dbias.copy_(hbias, non_blocking=True)
+            gemm()
+            hC.copy_(dC, non_blocking=True)
+        e2e_steps = max(5, min(args.steps, 50))
+        ms_e2e = max_over_ranks(time_steps(e2e_step, e2e_steps, 3, barrier)) / e2e_steps
+        h2d = hA.numel() * 2 + hB.numel() * 2 + hbias.numel() * 4
+        e2e = {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 2,
+               "ms_per_step": ms_e2e}
+
+    peaks, peak_src = measured_peaks()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": profiled_traffic(), "peak_source": peak_src + " (bf16 burst)",
+                "frac_vs_sustained_peak": achieved / peaks.get("bf16_tflops_sustained",
+                                                               peaks["bf16_tflops"]),
+                "kernel": "tc_gemm_kernel<256>"}
+
+    rows_out = None
+    if args.rows and rank == 0:
+        rows_out = measure_rows(args, device)
+        with open(args.rows, "w") as f:
+            json.dump(rows_out, f, indent=1)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(a, b_cm, bias)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K,
+                           "layout": "A row-major, B column-major, C row-major",
+                           "epilogue": "bias + GELU(tanh)", "l2": L2_NOTE,
+                           "parallelism": "replicas" if world > 1 else "single GPU",
+                           "plan": gemm.plan},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps * gemm.plan["launches"],
+                "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- other paths
+
+def measure_rows(args, device):
+    """Times each other library path once (median of repeats), with its roofline."""
+    import numpy as np
+    import torch
+
+    import datagen
+    import dense_gemm_bf16_gb300 as dg
+    peaks, _ = measured_peaks()
+    bw = peaks["hbm_gbs"]
+    out = []
+    stream = torch.cuda.current_stream(device).cuda_stream
+
+    def dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+
+    def bf16(seed, shape, scale=1.0):
+        return dev(datagen.to_bf16_bits(datagen.uniform(seed, shape) * scale).view(np.int16))
+
+    def timeit(fn, reps=20):
+        ts = []
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        return statistics.median(ts), min(ts)
+
+    def record(name, flops, bytes_, med, mn, bound, plan, extra=None):
+        r = {"path": name, "ms_median": med, "ms_min": mn, "tflops": flops / (med * 1e-3) / 1e12,
+             "gbs": bytes_ / (med * 1e-3) / 1e9, "algorithmic_bytes": bytes_, "flops": flops,
+             "bound": bound, "plan": plan}
+        if bound == "hbm":
+            r["frac"] = r["gbs"] / bw
+            r["peak"] = bw
+        elif bound == "alu":
+            r["peak"] = None
+        else:
+            r["frac"] = r["tflops"] / peaks["bf16_tflops"]
+            r["peak"] = peaks["bf16_tflops"]
+        if extra:
+            r.update(extra)
+        out.append(r)
+
+    def call16(batch, m, n, k, A, lda, la, sa, B, ldb, lb, sb, C, ldc, sc, cdt, alpha, beta,
+               ws=None):
+        args_ = [0, batch, m, n, k, A.data_ptr(), lda, la, sa, B.data_ptr(), ldb, lb, sb,
+                 C.data_ptr(), ldc, 0, sc, cdt, alpha, beta, None, 0, 0]
+        st, plan = dg.gemm_plan_query(*args_, 1 << 62)
+        need = int(plan.workspace_bytes)
+        wst = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+
+        def fn():
+            s = dg.gemm_batched(*args_, wst.data_ptr(), wst.numel(), stream)
+            if s != 0:
+                raise RuntimeError(dg.gemm_status_string(s))
+        return fn, plan.as_dict()
+
+    # SGEMM 4096^3, alpha 1.5, beta 0.5
+    n = 4096
+    A = dev(datagen.to_f32(datagen.uniform(2001, (n, n))))
+    B = dev(datagen.to_f32(datagen.uniform(2002, (n, n))))
+    C = dev(datagen.to_f32(datagen.uniform(2003, (n, n))))
+
+    def sg():
+        s = dg.sgemm_f32(n, n, n, A.data_ptr(), n, 0, B.data_ptr(), n, 0, C.data_ptr(), n, 0, 1.5,
+                         0.5, None, 0, stream)
+        if s != 0:
+            raise RuntimeError(dg.gemm_status_string(s))
+    med, mn = timeit(sg)
+    record("sgemm_f32 4096^3", 2.0 * n ** 3, 4 * n * n * 4, med, mn, "alu",
+           {"kernel": 2, "block": "128x128x8"})
+    del A, B, C
+
+    # ragged 4097 x 3001 x 1000, unaligned ldb / ldc, fp32 out
+    m_, n_, k_ = 4097, 3001, 1000
+    A = bf16(4001, (m_, k_))
+    B = bf16(4002, (k_, n_))
+    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
+    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
+    med, mn = timeit(fn)
+    record("bf16 4097x3001x1000 -> f32", 2.0 * m_ * n_ * k_,
+           (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4, med, mn, "tensor", plan)
+    del A, B, C
+
+    # split-K 256 x 256 x 65536, fp32 out
+    m_, n_, k_ = 256, 256, 65536
+    A = bf16(4011, (m_, k_))
+    B = bf16(4012, (k_, n_))
+    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
+    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
+    med, mn = timeit(fn)
+    record("bf16 256x256x65536 split-K -> f32", 2.0 * m_ * n_ * k_,
+           (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4, med, mn, "hbm", plan)
+    del A, B, C
+
+    # skinny 16 x 8192 x 8192, fp32 out
+    m_, n_, k_ = 16, 8192, 8192
+    A = bf16(4021, (m_, k_))
+    B = bf16(4022, (k_, n_))
+    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
+    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
+    med, mn = timeit(fn)
+    record("bf16 16x8192x8192 -> f32", 2.0 * m_ * n_ * k_, (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4,
+           med, mn, "hbm", plan)
+    del A, B, C
+
+    # batched 64 x 1024^3, alpha 0.5, beta 1, bf16 C in place; per-batch and broadcast B
+    bt, s = 64, 1024
+    A = bf16(5001, (bt, s, s))
+    Bp = bf16(5002, (bt, s, s))
+    C = dev(datagen.to_bf16_bits(datagen.normal(5003, (bt, s, s))).view(np.int16))
+    for label, Bt, sb in (("per-batch B", Bp, s * s), ("broadcast B", Bp, 0)):
+        fn, plan = call16(bt, s, s, s, A, s, 0, s * s, Bt, s, 0, sb, C, s, s * s, 0, 0.5, 1.0)
+        med, mn = timeit(fn)
+        nbytes = (bt * s * s + (bt if sb else 1) * s * s + 2 * bt * s * s) * 2
+        flops = 2.0 * bt * s ** 3
+        t_comp = flops / (peaks["bf16_tflops"] * 1e12)
+        t_mem = nbytes / (bw * 1e9)
+        record(f"batched 64x1024^3 {label}", flops, nbytes, med, mn,
+               "hbm" if t_mem > t_comp else "tensor", plan)
+    return out
+
+
+if __name__ == "__main__":
+    main()

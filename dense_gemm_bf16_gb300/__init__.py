@@ -1,0 +1,27 @@
+"""GB300-native (sm_103a) dense GEMM: C = act(alpha * A @ B + beta * C + bias).
+
+The compute lives in the CUDA library libdgemm_gb300.so (C ABI:
+include/gemm.h): a persistent tcgen05/TMA tensor-core kernel for bf16/fp16,
+a register-tiled CUDA-core SGEMM for fp32, and their split-K / operand-copy
+helpers.  This package is its binding: ``_abi`` mirrors the C entry points
+one to one; ``api.gemm`` is the tensor-level convenience.
+"""
+from ._abi import (EXPORTED, DType, Epi, GemmError, Layout, Option, Plan, Status, build,
+                   gemm_batched, gemm_bf16, gemm_check_device_status, gemm_f16,
+                   gemm_get_option, gemm_plan_query, gemm_set_option, gemm_status_string,
+                   gemm_tile_order, gemm_workspace_size, lib, library_path, sgemm_f32)
+
+__all__ = [
+    "EXPORTED", "DType", "Epi", "GemmError", "Layout", "Option", "Plan", "Status", "build",
+    "gemm_batched", "gemm_bf16", "gemm_check_device_status", "gemm_f16", "gemm_get_option",
+    "gemm_plan_query", "gemm_set_option", "gemm_status_string", "gemm_tile_order",
+    "gemm_workspace_size", "lib", "library_path", "sgemm_f32", "gemm", "plan",
+]
+
+
+def __getattr__(name):
+    # the tensor-level API imports torch; load it on first use only
+    if name in ("gemm", "plan", "api"):
+        from . import api
+        return api if name == "api" else getattr(api, name)
+    raise AttributeError(name)

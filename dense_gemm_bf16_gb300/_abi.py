@@ -1,0 +1,191 @@
+"""ctypes binding of libdgemm_gb300.so, one Python function per C entry point
+(include/gemm.h), with the same names and arguments.  Pointers are plain ints
+(device addresses), streams are ints (cudaStream_t); every function returns
+the C status code.  No arithmetic happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID_ARG = 1
+    ERR_UNSUPPORTED = 2
+    ERR_WORKSPACE = 3
+    ERR_CUDA = 4
+    ERR_TIMEOUT = 5
+    ERR_NO_DEVICE = 6
+
+
+class Layout(enum.IntEnum):
+    ROW_MAJOR = 0
+    COL_MAJOR = 1
+
+
+class DType(enum.IntEnum):
+    BF16 = 0
+    F16 = 1
+    F32 = 2
+
+
+class Epi(enum.IntEnum):
+    NONE = 0
+    BIAS = 1
+    GELU_TANH = 2
+    BIAS_GELU_TANH = 3
+
+
+class Option(enum.IntEnum):
+    GROUP_M = 1
+    MAX_CTAS = 2
+    TIMEOUT_US = 3
+    TEST_STALL = 4
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("block_m", ctypes.c_int32),
+                ("block_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("swap_ab", ctypes.c_int32), ("pack_a", ctypes.c_int32),
+                ("pack_b", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("group_m", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status):
+        self.status = Status(status)
+        super().__init__(gemm_status_string(int(status)))
+
+
+_i64, _i32, _f32, _vp, _sz = (ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                              ctypes.c_size_t)
+
+_GEMM16 = [_i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i32, _i32,
+           _f32, _f32, _vp, _i32, _i32, _vp, _sz, _vp]
+_SIGNATURES = {
+    "gemm_bf16": (_GEMM16, _i32),
+    "gemm_f16": (_GEMM16, _i32),
+    "sgemm_f32": ([_i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i32,
+                   _f32, _f32, _vp, _i32, _vp], _i32),
+    "gemm_batched": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp, _i64, _i32, _i64,
+                      _vp, _i64, _i32, _i64, _i32, _f32, _f32, _vp, _i32, _i32, _vp, _sz, _vp],
+                     _i32),
+    "gemm_workspace_size": ([_i32, _i64, _i64, _i64, _i64, _i32], _sz),
+    "gemm_status_string": ([_i32], ctypes.c_char_p),
+    "gemm_check_device_status": ([_vp], _i32),
+    "gemm_plan_query": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp, _i64, _i32,
+                         _i64, _vp, _i64, _i32, _i64, _i32, _f32, _f32, _vp, _i32, _i32, _sz,
+                         ctypes.POINTER(Plan)], _i32),
+    "gemm_set_option": ([_i32, _i64], _i32),
+    "gemm_get_option": ([_i32], _i64),
+    "gemm_tile_order": ([_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int),
+                         ctypes.POINTER(ctypes.c_int)], None),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (incremental)."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build the CUDA library first "
+                    "(dense_gemm_bf16_gb300.build() or __graft_entry__.build())")
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def gemm_bf16(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta, bias, epi,
+              split_k, workspace, workspace_bytes, stream) -> int:
+    return lib().gemm_bf16(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta,
+                           bias, epi, split_k, workspace, workspace_bytes, stream)
+
+
+def gemm_f16(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta, bias, epi,
+             split_k, workspace, workspace_bytes, stream) -> int:
+    return lib().gemm_f16(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta,
+                          bias, epi, split_k, workspace, workspace_bytes, stream)
+
+
+def sgemm_f32(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, alpha, beta, bias, epi,
+              stream) -> int:
+    return lib().sgemm_f32(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, alpha, beta, bias, epi,
+                           stream)
+
+
+def gemm_batched(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, stride_b, C, ldc,
+                 lc, stride_c, c_dtype, alpha, beta, bias, epi, split_k, workspace,
+                 workspace_bytes, stream) -> int:
+    return lib().gemm_batched(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb,
+                              stride_b, C, ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi,
+                              split_k, workspace, workspace_bytes, stream)
+
+
+def gemm_workspace_size(ab_dtype, batch, M, N, K, split_k) -> int:
+    return lib().gemm_workspace_size(ab_dtype, batch, M, N, K, split_k)
+
+
+def gemm_status_string(status) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+def gemm_check_device_status(stream) -> int:
+    return lib().gemm_check_device_status(stream)
+
+
+def gemm_plan_query(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, stride_b, C, ldc,
+                    lc, stride_c, c_dtype, alpha, beta, bias, epi, split_k, workspace_bytes):
+    """Returns (status, Plan)."""
+    plan = Plan()
+    st = lib().gemm_plan_query(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb,
+                               stride_b, C, ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi,
+                               split_k, workspace_bytes, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_set_option(option, value) -> int:
+    return lib().gemm_set_option(int(option), int(value))
+
+
+def gemm_get_option(option) -> int:
+    return lib().gemm_get_option(int(option))
+
+
+def gemm_tile_order(num_pid_m, num_pid_n, group_m):
+    """Returns two lists: pid_m[t], pid_n[t] for t in [0, num_pid_m*num_pid_n)."""
+    n = num_pid_m * num_pid_n
+    pm = (ctypes.c_int * max(n, 1))()
+    pn = (ctypes.c_int * max(n, 1))()
+    lib().gemm_tile_order(num_pid_m, num_pid_n, group_m, pm, pn)
+    return list(pm[:n]), list(pn[:n])

@@ -1,0 +1,105 @@
+"""Tensor-level convenience over the C ABI: reads pointers, leading dimensions,
+layouts and batch strides off torch tensors and calls ``gemm_batched``.
+PyTorch only provides device memory and the current stream; every step of the
+GEMM runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+from ._abi import DType, Epi, GemmError, Layout, Status
+
+_DT = {torch.bfloat16: DType.BF16, torch.float16: DType.F16, torch.float32: DType.F32}
+_EPI = {"none": Epi.NONE, "bias": Epi.BIAS, "gelu_tanh": Epi.GELU_TANH,
+        "bias_gelu_tanh": Epi.BIAS_GELU_TANH}
+
+
+def matrix_desc(t: torch.Tensor):
+    """(ptr, ld, layout, batch, batch_stride) of a 2-D or 3-D tensor whose
+    last two dims form a row- or column-major matrix with unit inner stride."""
+    if t.dim() == 2:
+        t3 = t.unsqueeze(0)
+        batch, bstride = 1, 0
+    elif t.dim() == 3:
+        t3 = t
+        batch, bstride = t.shape[0], (t.stride(0) if t.shape[0] > 1 else 0)
+    else:
+        raise ValueError("expected a 2-D or 3-D tensor")
+    rows, cols = t3.shape[1], t3.shape[2]
+    s_r, s_c = t3.stride(1), t3.stride(2)
+    if s_c == 1 or cols == 1 and s_r != 1:
+        return t.data_ptr(), max(s_r, cols, 1), Layout.ROW_MAJOR, batch, bstride
+    if s_r == 1:
+        return t.data_ptr(), max(s_c, rows, 1), Layout.COL_MAJOR, batch, bstride
+    raise ValueError("the innermost stride must be 1 (row- or column-major matrix)")
+
+
+def check(status: int) -> None:
+    if status != Status.OK:
+        raise GemmError(status)
+
+
+def plan(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, alpha=1.0, beta=0.0, bias=None,
+         epilogue="none", split_k=0, workspace_bytes=None):
+    """The kernel plan gemm() would use (a dict), without launching anything."""
+    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
+    ws = (1 << 62) if workspace_bytes is None else int(workspace_bytes)
+    st, p = _abi.gemm_plan_query(*args, ws)
+    check(st)
+    return p.as_dict()
+
+
+def _args(A, B, C, alpha, beta, bias, epilogue, split_k):
+    if A.dtype != B.dtype or A.dtype not in _DT:
+        raise TypeError("A and B must share one dtype among bfloat16, float16, float32")
+    pa, lda, la, ba, sa = matrix_desc(A)
+    pb, ldb, lb, bb, sb = matrix_desc(B)
+    pc, ldc, lc, bc, sc = matrix_desc(C)
+    batch = max(ba, bb, bc)
+    M, K = A.shape[-2], A.shape[-1]
+    N = B.shape[-1]
+    if B.shape[-2] != K or C.shape[-2] != M or C.shape[-1] != N:
+        raise ValueError(f"shape mismatch: A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    if bc != batch:
+        raise ValueError("C must carry the full batch")
+    bias_ptr = 0 if bias is None else bias.data_ptr()
+    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N):
+        raise ValueError("bias must be an fp32 vector of length N")
+    return [int(_DT[A.dtype]), batch, M, N, K, pa, lda, int(la), sa, pb, ldb, int(lb), sb,
+            pc, ldc, int(lc), sc, int(_DT[C.dtype]), float(alpha), float(beta), bias_ptr,
+            int(_EPI[epilogue]), int(split_k)]
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alpha=1.0,
+         beta=0.0, bias=None, epilogue=None, out_dtype=None, split_k=0, workspace=None,
+         stream=None) -> torch.Tensor:
+    """C <- act(alpha * A @ B + beta * C + bias) on the current CUDA device.
+
+    A: [M,K] or [batch,M,K]; B: [K,N] or [batch,K,N] (a batch stride of 0,
+    e.g. from ``expand``, broadcasts); C: output (allocated when None, in
+    ``out_dtype`` or A's dtype).  ``epilogue`` defaults to "bias" when a bias
+    is given.  A workspace is allocated with torch when the plan needs one
+    and none is given.
+    """
+    if epilogue is None:
+        epilogue = "bias" if bias is not None else "none"
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        batch = max(A.shape[0] if A.dim() == 3 else 1, B.shape[0] if B.dim() == 3 else 1)
+        shape = (A.shape[-2], B.shape[-1]) if A.dim() == 2 and B.dim() == 2 else \
+            (batch, A.shape[-2], B.shape[-1])
+        C = torch.empty(shape, dtype=out_dtype or A.dtype, device=A.device)
+    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
+    if workspace is None:
+        st, p = _abi.gemm_plan_query(*args, 1 << 62)
+        check(st)
+        need = int(p.workspace_bytes)
+        workspace = torch.empty(need, dtype=torch.uint8, device=A.device) if need > 0 else None
+    ws_ptr = 0 if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    check(_abi.gemm_batched(*args, ws_ptr, ws_bytes, stream))
+    return C

@@ -1,0 +1,156 @@
+// Element-wise epilogue shared by the tensor-core kernel, the CUDA-core
+// SGEMM and the split-K reduction:
+//     x = act(alpha * acc + beta * C + bias)
+// applied once, after accumulation ("Skill: Write a Triton GEMM Kernel",
+// Required reasoning process step 6 and Common failure modes on beta*C),
+// then rounded once to the output type ("GEMM Kernel Optimization", Common
+// Pitfalls).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace dg {
+
+// GELU, tanh form (Hendrycks & Gimpel 2016):
+//   gelu(x) = 0.5 x (1 + tanh(y)),  y = sqrt(2/pi) (x + 0.044715 x^3),
+// with tanh(y) = 1 - 2 / (exp(2y) + 1), an identity that stays finite for
+// every y (exp overflow gives tanh = 1, underflow gives -1).  exp and the
+// division use the CUDA fast intrinsics; the absolute error of 1 + tanh(y)
+// stays at the fp32 rounding level (~1e-7), so the relative error of the
+// result is ~1e-7 wherever the result is not tiny.
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    const float k1 = 0.044715f;
+    const float y = k0 * fmaf(k1 * x, x * x, x);
+    const float e = __expf(2.0f * y);
+    const float t = 1.0f - __fdividef(2.0f, e + 1.0f);
+    return 0.5f * x * (1.0f + t);
+}
+
+__device__ __forceinline__ float load_elem(const void* p, int dt) {
+    if (dt == DT_BF16) return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+    if (dt == DT_F16) return __half2float(*reinterpret_cast<const __half*>(p));
+    return *reinterpret_cast<const float*>(p);
+}
+
+__device__ __forceinline__ void store_elem(void* p, int dt, float x) {
+    if (dt == DT_BF16)
+        *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+    else if (dt == DT_F16)
+        *reinterpret_cast<__half*>(p) = __float2half_rn(x);
+    else
+        *reinterpret_cast<float*>(p) = x;
+}
+
+__device__ __forceinline__ int dt_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+// Address of C(b, i, j).
+__device__ __forceinline__ char* c_addr(const Epilogue& e, int64_t b, int64_t i, int64_t j) {
+    const int64_t off = b * e.stride_c + (e.c_row_major ? i * e.ldc + j : j * e.ldc + i);
+    return reinterpret_cast<char*>(e.C) + off * dt_size(e.c_dtype);
+}
+
+// One element: acc is the fp32 accumulator value of C(b, i, j).
+__device__ __forceinline__ void epilogue_store(const Epilogue& e, int64_t b, int64_t i, int64_t j,
+                                               float acc) {
+    char* c = c_addr(e, b, i, j);
+    float x = e.alpha * acc;
+    if (e.beta != 0.0f) x = fmaf(e.beta, load_elem(c, e.c_dtype), x);
+    if (e.bias) x += e.bias_on_rows ? e.bias[i] : e.bias[j];
+    if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
+    store_elem(c, e.c_dtype, x);
+}
+
+// 16-bit pack/unpack helpers for vectorised epilogues.
+__device__ __forceinline__ uint32_t pack2(int dt, float a, float b) {
+    if (dt == DT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2(int dt, uint32_t v) {
+    if (dt == DT_BF16) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+        return __bfloat1622float2(h);
+    }
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
+}
+
+// A contiguous run of W (a multiple of 8) elements of one row of a row-major
+// C, starting at a 16-byte aligned address: v holds alpha*acc on entry.
+template <int W>
+__device__ __forceinline__ void epilogue_row_vec(const Epilogue& e, char* c, const float* bias_run,
+                                                 float bias_row, float (&v)[W]) {
+    if (e.c_dtype == DT_F32) {
+        float4* c4 = reinterpret_cast<float4*>(c);
+        if (e.beta != 0.0f) {
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q) {
+                const float4 o = c4[q];
+                v[4 * q + 0] = fmaf(e.beta, o.x, v[4 * q + 0]);
+                v[4 * q + 1] = fmaf(e.beta, o.y, v[4 * q + 1]);
+                v[4 * q + 2] = fmaf(e.beta, o.z, v[4 * q + 2]);
+                v[4 * q + 3] = fmaf(e.beta, o.w, v[4 * q + 3]);
+            }
+        }
+    } else {
+        const uint4* c4 = reinterpret_cast<const uint4*>(c);
+        if (e.beta != 0.0f) {
+#pragma unroll
+            for (int q = 0; q < W / 8; ++q) {
+                const uint4 o = c4[q];
+                const uint32_t w4[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float2 f = unpack2(e.c_dtype, w4[h]);
+                    v[8 * q + 2 * h + 0] = fmaf(e.beta, f.x, v[8 * q + 2 * h + 0]);
+                    v[8 * q + 2 * h + 1] = fmaf(e.beta, f.y, v[8 * q + 2 * h + 1]);
+                }
+            }
+        }
+    }
+    if (bias_run) {
+#pragma unroll
+        for (int q = 0; q < W / 4; ++q) {
+            const float4 bb = reinterpret_cast<const float4*>(bias_run)[q];
+            v[4 * q + 0] += bb.x;
+            v[4 * q + 1] += bb.y;
+            v[4 * q + 2] += bb.z;
+            v[4 * q + 3] += bb.w;
+        }
+    } else if (bias_row != 0.0f) {
+#pragma unroll
+        for (int q = 0; q < W; ++q) v[q] += bias_row;
+    }
+    if (e.act == ACT_GELU_TANH) {
+#pragma unroll
+        for (int q = 0; q < W; ++q) v[q] = gelu_tanh(v[q]);
+    }
+    if (e.c_dtype == DT_F32) {
+        float4* c4 = reinterpret_cast<float4*>(c);
+#pragma unroll
+        for (int q = 0; q < W / 4; ++q)
+            c4[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+        uint4* c4 = reinterpret_cast<uint4*>(c);
+#pragma unroll
+        for (int q = 0; q < W / 8; ++q) {
+            uint4 o;
+            o.x = pack2(e.c_dtype, v[8 * q + 0], v[8 * q + 1]);
+            o.y = pack2(e.c_dtype, v[8 * q + 2], v[8 * q + 3]);
+            o.z = pack2(e.c_dtype, v[8 * q + 4], v[8 * q + 5]);
+            o.w = pack2(e.c_dtype, v[8 * q + 6], v[8 * q + 7]);
+            c4[q] = o;
+        }
+    }
+}
+
+}  // namespace dg

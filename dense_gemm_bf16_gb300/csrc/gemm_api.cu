@@ -1,0 +1,675 @@
+// Host side of the C ABI declared in include/gemm.h: argument validation,
+// planning (tile width, swap-AB, split-K, operand copies), TMA tensor-map
+// encoding and kernel launches.  No device memory is allocated here; the
+// only per-device state is a `__device__` error word and kernel attributes.
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.h"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tile_order.h"
+
+namespace dg {
+
+// Error word written by kernels whose bounded waits expire.
+__device__ int g_status_word;
+
+namespace {
+
+std::atomic<int64_t> g_opt_group_m{8};
+std::atomic<int64_t> g_opt_max_ctas{0};
+std::atomic<int64_t> g_opt_timeout_us{1000000};
+std::atomic<int64_t> g_opt_test_stall{0};
+
+constexpr int kMaxDevices = 64;
+constexpr int kBlockN[] = {16, 32, 64, 128, 256};
+
+struct DevState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sm_count = 0;
+    int cc = 0;
+    int* status = nullptr;
+};
+DevState g_dev[kMaxDevices];
+
+gemm_status_t device_state(DevState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    DevState& d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        int sms = 0, major = 0, minor = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        d.cc = major * 10 + minor;
+        if (e == cudaSuccess && d.cc == 103) {
+            e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
+            for (int bn : kBlockN)
+                if (e == cudaSuccess) e = tc_prepare(bn);
+        }
+        d.sm_count = sms;
+        d.err = e;
+        if (e != cudaSuccess) cudaGetLastError();
+    });
+    if (d.err != cudaSuccess) return GEMM_ERR_CUDA;
+    if (d.cc != 103) return GEMM_ERR_NO_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline int dt_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Call {
+    int ab;
+    int64_t batch, M, N, K;
+    const void* A;
+    int64_t lda;
+    int la;
+    int64_t sa;
+    const void* B;
+    int64_t ldb;
+    int lb;
+    int64_t sb;
+    void* C;
+    int64_t ldc;
+    int lc;
+    int64_t sc;
+    int cdt;
+    float alpha, beta;
+    const float* bias;
+    int epi;
+    int split_k;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+// One operand in the role it plays in the computed problem.
+struct Operand {
+    const void* ptr;
+    int64_t ld, stride;
+    bool mn;          // stored MN-contiguous
+    int64_t mn_ext;   // extent along M (A role) or N (B role)
+    int64_t k_ext;
+    bool pack;
+    int64_t pack_ld;
+    int64_t pack_batch;
+    size_t pack_off;
+    size_t pack_bytes;
+    int64_t inner() const { return mn ? mn_ext : k_ext; }
+    int64_t outer() const { return mn ? k_ext : mn_ext; }
+};
+
+struct Plan {
+    int kernel = 0;  // 0 none, 1 tensor core, 2 CUDA-core fp32, 3 epilogue only
+    bool swap = false;
+    int64_t Mc = 0, Nc = 0;
+    int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0;
+    int64_t kblocks = 0, tiles = 0, units = 0;
+    Operand a{}, b{};
+    bool c_row_major_c = true;
+    size_t part_off = 0, part_bytes = 0, ws_need = 0;
+};
+
+gemm_status_t validate(const Call& c) {
+    if (c.ab != DT_BF16 && c.ab != DT_F16 && c.ab != DT_F32) return GEMM_ERR_INVALID_ARG;
+    if (c.cdt != DT_BF16 && c.cdt != DT_F16 && c.cdt != DT_F32) return GEMM_ERR_INVALID_ARG;
+    if (c.ab == DT_F32 && c.cdt != DT_F32) return GEMM_ERR_UNSUPPORTED;
+    if (c.ab != DT_F32 && c.cdt != DT_F32 && c.cdt != c.ab) return GEMM_ERR_UNSUPPORTED;
+    for (int l : {c.la, c.lb, c.lc})
+        if (l != GEMM_ROW_MAJOR && l != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
+    if (c.epi < GEMM_EPI_NONE || c.epi > GEMM_EPI_BIAS_GELU_TANH) return GEMM_ERR_INVALID_ARG;
+    if (c.batch < 0 || c.M < 0 || c.N < 0 || c.K < 0 || c.split_k < 0) return GEMM_ERR_INVALID_ARG;
+    const int64_t lim = 0x7FFFFFFF;
+    if (c.batch > lim || c.M > lim || c.N > lim || c.K > lim) return GEMM_ERR_INVALID_ARG;
+    if (c.batch == 0 || c.M == 0 || c.N == 0) return GEMM_OK;
+    if (!c.C) return GEMM_ERR_INVALID_ARG;
+    if (!aligned(c.C, dt_bytes(c.cdt))) return GEMM_ERR_INVALID_ARG;
+    const int64_t c_inner = c.lc == GEMM_ROW_MAJOR ? c.N : c.M;
+    const int64_t c_outer = c.lc == GEMM_ROW_MAJOR ? c.M : c.N;
+    if (c.ldc < c_inner) return GEMM_ERR_INVALID_ARG;
+    if (c.batch > 1) {
+        // C[b] must not overlap
+        if (c.sc < (c_outer - 1) * c.ldc + c_inner) return GEMM_ERR_INVALID_ARG;
+    }
+    const bool has_bias = c.epi == GEMM_EPI_BIAS || c.epi == GEMM_EPI_BIAS_GELU_TANH;
+    if (has_bias && (!c.bias || !aligned(c.bias, 4))) return GEMM_ERR_INVALID_ARG;
+    if (c.K > 0 && c.alpha != 0.0f) {
+        if (!c.A || !c.B) return GEMM_ERR_INVALID_ARG;
+        if (!aligned(c.A, dt_bytes(c.ab)) || !aligned(c.B, dt_bytes(c.ab)))
+            return GEMM_ERR_INVALID_ARG;
+        const int64_t a_inner = c.la == GEMM_ROW_MAJOR ? c.K : c.M;
+        const int64_t b_inner = c.lb == GEMM_ROW_MAJOR ? c.N : c.K;
+        if (c.lda < a_inner || c.ldb < b_inner) return GEMM_ERR_INVALID_ARG;
+        if (c.sa < 0 || c.sb < 0) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+// Can TMA address this 16-bit operand in place?
+bool tma_addressable(const Operand& o, int64_t batch) {
+    if (!aligned(o.ptr, 16)) return false;
+    if ((o.ld * 2) % 16 != 0) return false;
+    if (batch > 1 && o.stride != 0) {
+        if ((o.stride * 2) % 16 != 0) return false;
+        if (o.stride < o.outer() * o.ld) return false;
+    }
+    return true;
+}
+
+// Split-K factor: minimises an estimate of the critical path, in units of one
+// 64-wide K block of one tile: waves * (K blocks per slice + per-unit fixed
+// cost) + (second launch + partial traffic) when split.
+int auto_splits(int64_t units, int64_t kblocks, int ctas, int64_t batch, int64_t Mc, int64_t Nc,
+                int bn) {
+    if (units >= ctas || kblocks < 4) return 1;
+    const double unit_cost = 4.0, launch_cost = 10.0;
+    const double red_per_split =
+        2.0 * batch * Mc * Nc * 4.0 / (static_cast<double>(ctas) * (128 + bn) * 128.0);
+    int best = 1;
+    double best_cost = static_cast<double>(cdiv(units, ctas)) * (kblocks + unit_cost);
+    const int64_t smax = kblocks / 2 < 128 ? kblocks / 2 : 128;
+    for (int64_t s = 2; s <= smax; ++s) {
+        const double waves = static_cast<double>(cdiv(units * s, ctas));
+        const double cost = waves * (static_cast<double>(kblocks) / s + unit_cost) + launch_cost +
+                            s * red_per_split;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = static_cast<int>(s);
+        }
+    }
+    return best;
+}
+
+gemm_status_t make_plan(const Call& c, int sm_count, Plan& pl) {
+    pl = Plan{};
+    pl.group_m = static_cast<int>(g_opt_group_m.load());
+    int ctas = sm_count;
+    const int64_t cap = g_opt_max_ctas.load();
+    if (cap > 0 && cap < ctas) ctas = static_cast<int>(cap);
+    if (c.batch == 0 || c.M == 0 || c.N == 0) return GEMM_OK;
+    if (c.K == 0 || c.alpha == 0.0f) {
+        pl.kernel = 3;
+        pl.launches = 1;
+        return GEMM_OK;
+    }
+    if (c.ab == DT_F32) {
+        pl.kernel = 2;
+        pl.launches = 1;
+        pl.bn = 128;
+        pl.grid = static_cast<int>(c.batch * cdiv(c.M, 128) * cdiv(c.N, 128));
+        if (c.batch * cdiv(c.M, 128) * cdiv(c.N, 128) > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED;
+        return GEMM_OK;
+    }
+    pl.kernel = 1;
+    pl.swap = c.M <= 64 && c.N > c.M;
+    const Operand opA{c.A, c.lda, c.sa, c.la == GEMM_COL_MAJOR, c.M, c.K};
+    const Operand opB{c.B, c.ldb, c.sb, c.lb == GEMM_ROW_MAJOR, c.N, c.K};
+    pl.a = pl.swap ? opB : opA;
+    pl.b = pl.swap ? opA : opB;
+    pl.Mc = pl.swap ? c.N : c.M;
+    pl.Nc = pl.swap ? c.M : c.N;
+    pl.c_row_major_c = pl.swap ? (c.lc == GEMM_COL_MAJOR) : (c.lc == GEMM_ROW_MAJOR);
+
+    const int64_t tiles_m = cdiv(pl.Mc, TC_BLOCK_M);
+    if (pl.Nc <= 16)
+        pl.bn = 16;
+    else if (pl.Nc <= 32)
+        pl.bn = 32;
+    else if (pl.Nc <= 64)
+        pl.bn = 64;
+    else
+        pl.bn = (c.batch * tiles_m * cdiv(pl.Nc, 256) >= ctas) ? 256 : 128;
+    if (pl.b.mn && pl.bn < 64) pl.bn = 64;  // MN-major B tiles come in 64-wide swizzle atoms
+    pl.stages = tc_stages_for(pl.bn);
+
+    // operand copies for what TMA cannot address
+    size_t off = 0;
+    for (Operand* o : {&pl.a, &pl.b}) {
+        o->pack = !tma_addressable(*o, c.batch);
+        if (o->pack) {
+            o->pack_ld = round_up(o->inner(), 8);
+            o->pack_batch = (c.batch > 1 && o->stride != 0) ? c.batch : 1;
+            o->pack_bytes = static_cast<size_t>(o->pack_batch * o->outer() * o->pack_ld * 2);
+            o->pack_off = off;
+            off += static_cast<size_t>(round_up(static_cast<int64_t>(o->pack_bytes), 256));
+            pl.launches += 1;
+        }
+    }
+
+    pl.kblocks = cdiv(c.K, TC_BLOCK_K);
+    pl.tiles = tiles_m * cdiv(pl.Nc, pl.bn);
+    pl.units = c.batch * pl.tiles;
+    const size_t per_split = static_cast<size_t>(c.batch * pl.Mc * pl.Nc * 4);
+    if (c.split_k >= 1) {
+        pl.splits = static_cast<int>(c.split_k < pl.kblocks ? c.split_k : pl.kblocks);
+    } else {
+        pl.splits = auto_splits(pl.units, pl.kblocks, ctas, c.batch, pl.Mc, pl.Nc, pl.bn);
+        // never ask for more workspace than was given
+        const size_t avail = c.ws_bytes > off + 256 ? c.ws_bytes - off - 256 : 0;
+        if (pl.splits > 1 && per_split * pl.splits > avail)
+            pl.splits = static_cast<int>(per_split ? avail / per_split : 1);
+        if (pl.splits < 2) pl.splits = 1;
+    }
+    if (pl.splits > 1) {
+        pl.part_off = off;
+        pl.part_bytes = per_split * pl.splits;
+        off += round_up(static_cast<int64_t>(pl.part_bytes), 256);
+        pl.launches += 1;
+    }
+    pl.ws_need = off;
+    const int64_t total_units = pl.units * pl.splits;
+    if (total_units > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED;
+    pl.grid = static_cast<int>(total_units < ctas ? total_units : ctas);
+    pl.launches += 1;
+    if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
+    if (pl.ws_need > 0 && !aligned(c.ws, 256)) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
+    Epilogue e{};
+    e.C = c.C;
+    e.ldc = c.ldc;
+    e.stride_c = c.batch > 1 ? c.sc : 0;
+    e.c_row_major = row_major ? 1 : 0;
+    e.c_dtype = c.cdt;
+    const int es = dt_bytes(c.cdt);
+    e.c_vec_ok = (row_major && aligned(c.C, 16) && (c.ldc * es) % 16 == 0 &&
+                  (e.stride_c * es) % 16 == 0)
+                     ? 1
+                     : 0;
+    e.alpha = c.alpha;
+    e.beta = c.beta;
+    const bool has_bias = c.epi == GEMM_EPI_BIAS || c.epi == GEMM_EPI_BIAS_GELU_TANH;
+    e.bias = has_bias ? c.bias : nullptr;
+    e.bias_on_rows = bias_on_rows ? 1 : 0;
+    e.bias_vec_ok = (e.bias && aligned(e.bias, 16)) ? 1 : 0;
+    e.act = (c.epi == GEMM_EPI_GELU_TANH || c.epi == GEMM_EPI_BIAS_GELU_TANH) ? ACT_GELU_TANH
+                                                                               : ACT_NONE;
+    return e;
+}
+
+gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const void* ptr,
+                             int64_t ld, int64_t stride, int64_t batch, uint32_t box_k_major_rows,
+                             bool* is3d) {
+    auto fn = encode_fn();
+    if (!fn) return GEMM_ERR_CUDA;
+    const bool three = batch > 1 && stride != 0;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(o.inner()), static_cast<cuuint64_t>(o.outer()),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(stride * 2)};
+    // K-major: box = 64 K x rows-of-tile; MN-major: box = 64 MN x 64 K (one swizzle atom column)
+    cuuint32_t box[3] = {64u, o.mn ? 64u : box_k_major_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map,
+                          ab == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          three ? 3u : 2u, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+    *is3d = three;
+    return GEMM_OK;
+}
+
+gemm_status_t run(const Call& c) {
+    gemm_status_t st = validate(c);
+    if (st != GEMM_OK) return st;
+    if (c.batch == 0 || c.M == 0 || c.N == 0) return GEMM_OK;
+    DevState* d = nullptr;
+    st = device_state(&d);
+    if (st != GEMM_OK) return st;
+    Plan pl;
+    st = make_plan(c, d->sm_count, pl);
+    if (st != GEMM_OK) return st;
+
+    if (pl.kernel == 3) {
+        const Epilogue e = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
+        return splitk_epilogue_launch(nullptr, 0, c.batch, c.M, c.N, e, c.stream) == cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_CUDA;
+    }
+    if (pl.kernel == 2) {
+        SgemmParams p{};
+        p.A = static_cast<const float*>(c.A);
+        p.lda = c.lda;
+        p.stride_a = c.batch > 1 ? c.sa : 0;
+        p.a_row = c.la == GEMM_ROW_MAJOR;
+        p.B = static_cast<const float*>(c.B);
+        p.ldb = c.ldb;
+        p.stride_b = c.batch > 1 ? c.sb : 0;
+        p.b_row = c.lb == GEMM_ROW_MAJOR;
+        p.M = static_cast<int32_t>(c.M);
+        p.N = static_cast<int32_t>(c.N);
+        p.K = static_cast<int32_t>(c.K);
+        p.batch = static_cast<int32_t>(c.batch);
+        p.a_vec_ok = aligned(c.A, 16) && c.lda % 4 == 0 && p.stride_a % 4 == 0;
+        p.b_vec_ok = aligned(c.B, 16) && c.ldb % 4 == 0 && p.stride_b % 4 == 0;
+        p.num_pid_m = static_cast<int32_t>(cdiv(c.M, 128));
+        p.num_pid_n = static_cast<int32_t>(cdiv(c.N, 128));
+        p.group_m = pl.group_m;
+        p.epi = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
+        return sgemm_launch(p, c.stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    // tensor-core path
+    char* ws = static_cast<char*>(c.ws);
+    const void* a_ptr = pl.a.ptr;
+    const void* b_ptr = pl.b.ptr;
+    int64_t a_ld = pl.a.ld, b_ld = pl.b.ld;
+    int64_t a_stride = c.batch > 1 ? pl.a.stride : 0, b_stride = c.batch > 1 ? pl.b.stride : 0;
+    if (pl.a.pack) {
+        if (pack16_launch(pl.a.ptr, pl.a.ld, a_stride, pl.a.outer(), pl.a.inner(), pl.a.pack_batch,
+                          ws + pl.a.pack_off, pl.a.pack_ld, c.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        a_ptr = ws + pl.a.pack_off;
+        a_ld = pl.a.pack_ld;
+        a_stride = pl.a.pack_batch > 1 ? pl.a.outer() * pl.a.pack_ld : 0;
+    }
+    if (pl.b.pack) {
+        if (pack16_launch(pl.b.ptr, pl.b.ld, b_stride, pl.b.outer(), pl.b.inner(), pl.b.pack_batch,
+                          ws + pl.b.pack_off, pl.b.pack_ld, c.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        b_ptr = ws + pl.b.pack_off;
+        b_ld = pl.b.pack_ld;
+        b_stride = pl.b.pack_batch > 1 ? pl.b.outer() * pl.b.pack_ld : 0;
+    }
+
+    TcParams p;
+    std::memset(&p, 0, sizeof(p));
+    bool a3 = false, b3 = false;
+    st = encode_operand(&p.tmap_a, c.ab, pl.a, a_ptr, a_ld, a_stride, c.batch, TC_BLOCK_M, &a3);
+    if (st != GEMM_OK) return st;
+    st = encode_operand(&p.tmap_b, c.ab, pl.b, b_ptr, b_ld, b_stride, c.batch,
+                        static_cast<uint32_t>(pl.bn), &b3);
+    if (st != GEMM_OK) return st;
+    p.M = static_cast<int32_t>(pl.Mc);
+    p.N = static_cast<int32_t>(pl.Nc);
+    p.K = static_cast<int32_t>(c.K);
+    p.batch = static_cast<int32_t>(c.batch);
+    p.num_pid_m = static_cast<int32_t>(cdiv(pl.Mc, TC_BLOCK_M));
+    p.num_pid_n = static_cast<int32_t>(cdiv(pl.Nc, pl.bn));
+    p.tiles_per_batch = static_cast<int32_t>(pl.tiles);
+    p.splits = pl.splits;
+    p.kblocks = static_cast<int32_t>(pl.kblocks);
+    p.group_m = pl.group_m;
+    p.total_units = static_cast<int32_t>(pl.units * pl.splits);
+    p.a_mn = pl.a.mn ? 1 : 0;
+    p.b_mn = pl.b.mn ? 1 : 0;
+    p.a_3d = a3 ? 1 : 0;
+    p.b_3d = b3 ? 1 : 0;
+    p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, TC_BLOCK_M, pl.bn);
+    p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
+    p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
+    p.status = d->status;
+    p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
+    p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
+    if (tc_launch(pl.bn, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (pl.splits > 1) {
+        if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
+                                   c.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+Call make_call(int ab, int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+               gemm_layout_t la, int64_t sa, const void* B, int64_t ldb, gemm_layout_t lb,
+               int64_t sb, void* C, int64_t ldc, gemm_layout_t lc, int64_t sc, int cdt,
+               float alpha, float beta, const float* bias, gemm_epilogue_t epi, int split_k,
+               void* ws, size_t ws_bytes, gemm_stream_t stream) {
+    Call c;
+    c.ab = ab;
+    c.batch = batch;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.A = A;
+    c.lda = lda;
+    c.la = la;
+    c.sa = sa;
+    c.B = B;
+    c.ldb = ldb;
+    c.lb = lb;
+    c.sb = sb;
+    c.C = C;
+    c.ldc = ldc;
+    c.lc = lc;
+    c.sc = sc;
+    c.cdt = cdt;
+    c.alpha = alpha;
+    c.beta = beta;
+    c.bias = bias;
+    c.epi = epi;
+    c.split_k = split_k;
+    c.ws = ws;
+    c.ws_bytes = ws_bytes;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return c;
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                        gemm_layout_t la, const void* B, int64_t ldb, gemm_layout_t lb, void* C,
+                        int64_t ldc, gemm_layout_t lc, gemm_dtype_t c_dtype, float alpha,
+                        float beta, const float* bias, gemm_epilogue_t epi, int split_k,
+                        void* workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    if (c_dtype == GEMM_DT_F16) return GEMM_ERR_UNSUPPORTED;
+    return run(make_call(DT_BF16, 1, M, N, K, A, lda, la, 0, B, ldb, lb, 0, C, ldc, lc, 0, c_dtype,
+                         alpha, beta, bias, epi, split_k, workspace, workspace_bytes, stream));
+}
+
+gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                       gemm_layout_t la, const void* B, int64_t ldb, gemm_layout_t lb, void* C,
+                       int64_t ldc, gemm_layout_t lc, gemm_dtype_t c_dtype, float alpha,
+                       float beta, const float* bias, gemm_epilogue_t epi, int split_k,
+                       void* workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    if (c_dtype == GEMM_DT_BF16) return GEMM_ERR_UNSUPPORTED;
+    return run(make_call(DT_F16, 1, M, N, K, A, lda, la, 0, B, ldb, lb, 0, C, ldc, lc, 0, c_dtype,
+                         alpha, beta, bias, epi, split_k, workspace, workspace_bytes, stream));
+}
+
+gemm_status_t sgemm_f32(int64_t M, int64_t N, int64_t K, const float* A, int64_t lda,
+                        gemm_layout_t la, const float* B, int64_t ldb, gemm_layout_t lb, float* C,
+                        int64_t ldc, gemm_layout_t lc, float alpha, float beta, const float* bias,
+                        gemm_epilogue_t epi, gemm_stream_t stream) {
+    return run(make_call(DT_F32, 1, M, N, K, A, lda, la, 0, B, ldb, lb, 0, C, ldc, lc, 0, DT_F32,
+                         alpha, beta, bias, epi, 1, nullptr, 0, stream));
+}
+
+gemm_status_t gemm_batched(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N, int64_t K,
+                           const void* A, int64_t lda, gemm_layout_t la, int64_t stride_a,
+                           const void* B, int64_t ldb, gemm_layout_t lb, int64_t stride_b,
+                           void* C, int64_t ldc, gemm_layout_t lc, int64_t stride_c,
+                           gemm_dtype_t c_dtype, float alpha, float beta, const float* bias,
+                           gemm_epilogue_t epi, int split_k, void* workspace,
+                           size_t workspace_bytes, gemm_stream_t stream) {
+    return run(make_call(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, stride_b, C,
+                         ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi, split_k, workspace,
+                         workspace_bytes, stream));
+}
+
+size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N, int64_t K,
+                           int split_k) {
+    if (ab_dtype != GEMM_DT_BF16 && ab_dtype != GEMM_DT_F16) return 0;
+    if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || split_k < 0) return 0;
+    if (batch > 0x7FFFFFFF || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return 0;
+    DevState* d = nullptr;
+    if (device_state(&d) != GEMM_OK) return 0;
+    const int64_t pa = batch * (M * round_up(K, 8) > K * round_up(M, 8) ? M * round_up(K, 8)
+                                                                         : K * round_up(M, 8));
+    const int64_t pb = batch * (N * round_up(K, 8) > K * round_up(N, 8) ? N * round_up(K, 8)
+                                                                         : K * round_up(N, 8));
+    size_t worst_part = 0;
+    static const char dummy[16] __attribute__((aligned(256))) = {0};
+    for (int la = 0; la < 2; ++la)
+        for (int lb = 0; lb < 2; ++lb)
+            for (int lc = 0; lc < 2; ++lc) {
+                // aligned, unpacked operands with unlimited workspace: the largest split
+                const int64_t lda = la == 0 ? round_up(K, 8) : round_up(M, 8);
+                const int64_t ldb = lb == 0 ? round_up(N, 8) : round_up(K, 8);
+                const int64_t ldc = lc == 0 ? N : M;
+                const int64_t sa = la == 0 ? M * lda : K * lda;
+                const int64_t sb = lb == 0 ? K * ldb : N * ldb;
+                const int64_t sc = lc == 0 ? M * ldc : N * ldc;
+                Call c = make_call(ab_dtype, batch, M, N, K, dummy, lda,
+                                   static_cast<gemm_layout_t>(la), sa, dummy, ldb,
+                                   static_cast<gemm_layout_t>(lb), sb, const_cast<char*>(dummy),
+                                   ldc, static_cast<gemm_layout_t>(lc), sc, GEMM_DT_F32, 1.0f,
+                                   0.0f, nullptr, GEMM_EPI_NONE, split_k,
+                                   const_cast<char*>(dummy), SIZE_MAX / 2, nullptr);
+                Plan pl;
+                if (make_plan(c, d->sm_count, pl) == GEMM_OK && pl.part_bytes > worst_part)
+                    worst_part = pl.part_bytes;
+            }
+    return static_cast<size_t>(round_up(pa * 2, 256) + round_up(pb * 2, 256)) +
+           static_cast<size_t>(round_up(static_cast<int64_t>(worst_part), 256));
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+        case GEMM_ERR_WORKSPACE: return "GEMM_ERR_WORKSPACE";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+gemm_status_t gemm_check_device_status(gemm_stream_t stream) {
+    DevState* d = nullptr;
+    const gemm_status_t st = device_state(&d);
+    if (st != GEMM_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int v = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N,
+                              int64_t K, const void* A, int64_t lda, gemm_layout_t la,
+                              int64_t stride_a, const void* B, int64_t ldb, gemm_layout_t lb,
+                              int64_t stride_b, void* C, int64_t ldc, gemm_layout_t lc,
+                              int64_t stride_c, gemm_dtype_t c_dtype, float alpha, float beta,
+                              const float* bias, gemm_epilogue_t epi, int split_k,
+                              size_t workspace_bytes, gemm_plan_t* plan) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    std::memset(plan, 0, sizeof(*plan));
+    // a non-null stand-in so that the plan can be made without a real workspace
+    static const char probe[16] __attribute__((aligned(256))) = {0};
+    const Call c = make_call(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, stride_b,
+                             C, ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi, split_k,
+                             const_cast<char*>(probe), workspace_bytes, nullptr);
+    gemm_status_t st = validate(c);
+    if (st != GEMM_OK) return st;
+    DevState* d = nullptr;
+    st = device_state(&d);
+    if (st != GEMM_OK) return st;
+    Plan pl;
+    st = make_plan(c, d->sm_count, pl);
+    plan->kernel = pl.kernel;
+    plan->block_m = pl.kernel == 1 ? TC_BLOCK_M : (pl.kernel == 2 ? 128 : 0);
+    plan->block_n = pl.bn;
+    plan->block_k = pl.kernel == 1 ? TC_BLOCK_K : (pl.kernel == 2 ? 8 : 0);
+    plan->stages = pl.stages;
+    plan->split_k = pl.splits;
+    plan->swap_ab = pl.swap ? 1 : 0;
+    plan->pack_a = pl.a.pack ? 1 : 0;
+    plan->pack_b = pl.b.pack ? 1 : 0;
+    plan->grid = pl.grid;
+    plan->group_m = pl.group_m;
+    plan->launches = pl.launches;
+    plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
+    return st;
+}
+
+gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
+    switch (option) {
+        case GEMM_OPT_GROUP_M:
+            if (value < 1 || value > 64) return GEMM_ERR_INVALID_ARG;
+            g_opt_group_m.store(value);
+            return GEMM_OK;
+        case GEMM_OPT_MAX_CTAS:
+            if (value < 0 || value > 0x7FFFFFFF) return GEMM_ERR_INVALID_ARG;
+            g_opt_max_ctas.store(value);
+            return GEMM_OK;
+        case GEMM_OPT_TIMEOUT_US:
+            if (value < 1 || value > 60ll * 1000 * 1000) return GEMM_ERR_INVALID_ARG;
+            g_opt_timeout_us.store(value);
+            return GEMM_OK;
+        case GEMM_OPT_TEST_STALL:
+            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            g_opt_test_stall.store(value);
+            return GEMM_OK;
+    }
+    return GEMM_ERR_INVALID_ARG;
+}
+
+int64_t gemm_get_option(gemm_option_t option) {
+    switch (option) {
+        case GEMM_OPT_GROUP_M: return g_opt_group_m.load();
+        case GEMM_OPT_MAX_CTAS: return g_opt_max_ctas.load();
+        case GEMM_OPT_TIMEOUT_US: return g_opt_timeout_us.load();
+        case GEMM_OPT_TEST_STALL: return g_opt_test_stall.load();
+    }
+    return -1;
+}
+
+void gemm_tile_order(int num_pid_m, int num_pid_n, int group_m, int* pid_m, int* pid_n) {
+    if (num_pid_m <= 0 || num_pid_n <= 0 || group_m <= 0 || !pid_m || !pid_n) return;
+    const int64_t n = static_cast<int64_t>(num_pid_m) * num_pid_n;
+    for (int64_t t = 0; t < n; ++t)
+        tile_coord(static_cast<int>(t), num_pid_m, num_pid_n, group_m, pid_m[t], pid_n[t]);
+}
+
+}  // extern "C"

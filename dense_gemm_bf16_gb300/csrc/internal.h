@@ -1,0 +1,84 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dg {
+
+enum : int { DT_BF16 = 0, DT_F16 = 1, DT_F32 = 2 };
+enum : int { ACT_NONE = 0, ACT_GELU_TANH = 1 };
+
+// Tile of the tensor-core kernel: BLOCK_M x BLOCK_N output, K consumed in
+// BLOCK_K = 64 slices (64 bf16 = one 128-byte swizzle row).
+constexpr int TC_BLOCK_M = 128;
+constexpr int TC_BLOCK_K = 64;
+constexpr int TC_THREADS = 192;       // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int TC_EPI_THREADS = 128;
+
+// Epilogue description shared by the tensor-core kernel and the split-K reduce.
+struct Epilogue {
+    void* C;                 // output (and beta input), c_dtype
+    int64_t ldc;             // leading dimension of C in elements
+    int64_t stride_c;        // batch stride of C in elements
+    int32_t c_row_major;     // 1: C(i,j) at i*ldc + j; 0: at j*ldc + i
+    int32_t c_dtype;         // DT_BF16 / DT_F16 / DT_F32
+    int32_t c_vec_ok;        // C base and ldc allow 16-byte vector access along rows
+    float alpha, beta;
+    const float* bias;       // may be null
+    int32_t bias_on_rows;    // 1: bias indexed by row i (swapped problem), 0: by column j
+    int32_t bias_vec_ok;     // bias pointer 16-byte aligned
+    int32_t act;             // ACT_NONE / ACT_GELU_TANH
+};
+
+// Parameters of the persistent tcgen05 kernel (passed as a __grid_constant__).
+struct TcParams {
+    CUtensorMap tmap_a;      // A-role operand (rows = M of the computed problem)
+    CUtensorMap tmap_b;      // B-role operand (rows = N of the computed problem)
+    int32_t M, N, K, batch;
+    int32_t num_pid_m, num_pid_n;
+    int32_t tiles_per_batch;
+    int32_t splits;          // K slices per tile
+    int32_t kblocks;         // ceil(K / 64)
+    int32_t group_m;
+    int32_t total_units;     // batch * splits * tiles_per_batch
+    int32_t a_mn, b_mn;      // 1: operand stored MN-contiguous (MN-major), 0: K-contiguous
+    int32_t a_3d, b_3d;      // 1: tensor map carries the batch as its third dimension
+    uint32_t idesc;          // tcgen05 instruction descriptor
+    Epilogue epi;
+    float* partials;         // split-K: fp32 partial tiles [split][batch][M][N] in C's layout; else null
+    int* status;             // device error word
+    uint64_t timeout_ns;     // bound on every wait
+    int32_t test_stall;      // test only: leave one stage unfilled
+};
+
+// Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).
+int tc_stages_for(int block_n);
+size_t tc_smem_bytes(int block_n);
+cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
+cudaError_t tc_launch(int block_n, const TcParams& p, int grid, cudaStream_t stream);
+
+struct SgemmParams {
+    const float* A; int64_t lda; int64_t stride_a; int32_t a_row;
+    const float* B; int64_t ldb; int64_t stride_b; int32_t b_row;
+    int32_t M, N, K, batch;
+    int32_t a_vec_ok, b_vec_ok;   // float4 global loads allowed
+    int32_t num_pid_m, num_pid_n, group_m;
+    Epilogue epi;
+};
+cudaError_t sgemm_launch(const SgemmParams& p, cudaStream_t stream);
+
+// Dense copy of a rows x cols 16-bit matrix stored with (ld, batch stride) into
+// dst with leading dimension ld_dst and batch stride rows*ld_dst.
+cudaError_t pack16_launch(const void* src, int64_t ld, int64_t stride, int64_t rows,
+                          int64_t cols, int64_t batch, void* dst, int64_t ld_dst,
+                          cudaStream_t stream);
+
+// C = act(alpha * sum_s P[s] + beta*C + bias) for splits >= 0 partial slices
+// stored densely in C's layout ([split][batch][M][N] row-major or its transpose).
+cudaError_t splitk_epilogue_launch(const float* partials, int splits, int64_t batch,
+                                   int64_t M, int64_t N, const Epilogue& e,
+                                   cudaStream_t stream);
+
+}  // namespace dg

@@ -1,0 +1,416 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a (bf16 / fp16 in, fp32 accumulate).
+//
+// The tiled algorithm of "GEMM Kernel Optimization", Core Technique (one
+// BLOCK_M x BLOCK_N output tile per work unit, K consumed in BLOCK_K slices,
+// fp32 accumulator, cast after the loop) mapped onto GB300:
+//
+//   warp 0 (one lane)  TMA producer: fills a ring of STAGES shared-memory
+//                      stages with the A tile [128 x 64] and the B tile
+//                      [BN x 64], 128-byte swizzled, out-of-range elements
+//                      zero-filled by the TMA unit (the K / M / N masks of
+//                      "Skill: Write a Triton GEMM Kernel", step 5).
+//   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16,
+//                      four per stage, into one of two TMEM accumulators;
+//                      tcgen05.commit frees the stage / publishes the tile.
+//   warps 2-5          epilogue: tcgen05.ld of the accumulator (one TMEM lane =
+//                      one output row per thread), alpha/beta/bias/GELU in fp32,
+//                      one rounding to the output type, masked global stores;
+//                      or, for split-K, the raw fp32 partial tile.
+//
+// The two TMEM accumulators let the epilogue of tile i overlap the main loop
+// of tile i+1.  Work units (batch, K slice, tile) are dealt to CTAs round
+// robin (persistent grid, one CTA per SM); tiles follow the grouped order of
+// tile_order.h.  Every mbarrier wait is bounded: on expiry the kernel records an
+// error word, lets its own copies and MMAs drain, frees TMEM and returns.
+#include <stdint.h>
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tile_order.h"
+
+namespace dg {
+namespace {
+
+constexpr int BM = TC_BLOCK_M;
+constexpr int BK = TC_BLOCK_K;
+constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
+
+template <int BN>
+struct Cfg {
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t BAR_BYTES = 256;
+    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
+    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int CHUNK = BN < 32 ? BN : 32;
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
+};
+
+struct Unit {
+    int b, split, pid_m, pid_n, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+    const int per_batch = p.splits * p.tiles_per_batch;
+    Unit w;
+    w.b = u / per_batch;
+    const int r = u - w.b * per_batch;
+    w.split = r / p.tiles_per_batch;
+    const int t = r - w.split * p.tiles_per_batch;
+    tile_coord(t, p.num_pid_m, p.num_pid_n, p.group_m, w.pid_m, w.pid_n);
+    w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
+    w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
+    return w;
+}
+
+// Bounded wait used while draining: ignores the abort flag.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, int x,
+                                          int y, int z, bool is3d, uint64_t pol) {
+    if (is3d)
+        tma_load_3d(dst, map, bar, x, y, z, pol);
+    else
+        tma_load_2d(dst, map, bar, x, y, pol);
+}
+
+// Epilogue of one CH-column chunk held by this thread (row `row` of the
+// computed problem, columns col0 .. col0+CH-1).
+template <int CH>
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w, int64_t row,
+                                               int col0, const uint32_t (&r)[32]) {
+    if (row >= p.M) return;
+    const Epilogue& e = p.epi;
+    const bool full = col0 + CH <= p.N;
+    if (p.partials) {
+        // raw fp32 partial tile, stored densely in C's layout
+        const int64_t slice = static_cast<int64_t>(w.split) * p.batch + w.b;
+        float* P = p.partials + slice * static_cast<int64_t>(p.M) * p.N;
+        if (e.c_row_major) {
+            float* dst = P + row * p.N + col0;
+            if (full && (p.N & 3) == 0) {
+#pragma unroll
+                for (int q = 0; q < CH / 4; ++q)
+                    reinterpret_cast<float4*>(dst)[q] =
+                        make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < CH; ++c)
+                    if (col0 + c < p.N) dst[c] = __uint_as_float(r[c]);
+            }
+        } else {
+            float* dst = P + row;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                if (col0 + c < p.N) dst[static_cast<int64_t>(col0 + c) * p.M] = __uint_as_float(r[c]);
+        }
+        return;
+    }
+    if (e.c_row_major && full && e.c_vec_ok) {
+        float v[CH];
+#pragma unroll
+        for (int c = 0; c < CH; ++c) v[c] = e.alpha * __uint_as_float(r[c]);
+        char* c = c_addr(e, w.b, row, col0);
+        const float* bias_run = nullptr;
+        float bias_row = 0.0f;
+        if (e.bias) {
+            if (e.bias_on_rows)
+                bias_row = e.bias[row];
+            else if (e.bias_vec_ok)
+                bias_run = e.bias + col0;
+            else {
+#pragma unroll
+                for (int q = 0; q < CH; ++q) v[q] += e.bias[col0 + q];
+            }
+        }
+        epilogue_row_vec<CH>(e, c, bias_run, bias_row, v);
+        return;
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+        if (col0 + c < p.N) epilogue_store(e, w.b, row, col0 + c, __uint_as_float(r[c]));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sA0 = smem_u32(smem);
+    const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
+    const uint32_t full0 = bar0;
+    const uint32_t empty0 = bar0 + 8u * C::STAGES;
+    const uint32_t tfull0 = bar0 + 16u * C::STAGES;
+    const uint32_t tempty0 = tfull0 + 16u;
+    const uint32_t drain_bar = tempty0 + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8u * b, 1);
+            mbar_init(tempty0 + 8u * b, TC_EPI_THREADS);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&p.tmap_a);
+        prefetch_tmap(&p.tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_normal();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+                const Unit w = decode_unit(p, u);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (p.test_stall && armed == 0) {
+                        // test only: leave this stage unfilled; the MMA warp's bounded
+                        // wait on it must expire and report the timeout.
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8u * stage;
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t a_dst = sA0 + stage * C::A_BYTES;
+                    const uint32_t b_dst = sB0 + stage * C::B_BYTES;
+                    const int k0 = kb * BK;
+                    if (!p.a_mn) {
+                        load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < BM / 64; ++h)
+                            load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
+                                      w.b, p.a_3d, pol);
+                    }
+                    if (!p.b_mn) {
+                        load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol);
+                    } else {
+                        if constexpr (BN >= 64) {
+#pragma unroll
+                            for (int h = 0; h < BN / 64; ++h)
+                                load_tile(&p.tmap_b, b_dst + h * 8192u, fb, w.pid_n * BN + 64 * h,
+                                          k0, w.b, p.b_3d, pol);
+                        }
+                    }
+                    ++armed;
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every issued fill must land before the CTA may exit.
+            for (int s = 0; s < C::STAGES && static_cast<uint32_t>(s) < armed; ++s) {
+                const uint32_t fills = (armed - 1u - s) / C::STAGES + 1u;
+                wait_drain(full0 + 8u * s, (fills - 1u) & 1u, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int abuf = 0;
+            uint32_t aphase = 0;
+            bool issued = false;
+            bool ok = true;
+            // K-major operands advance 32 bytes per K=16 step inside the 128-byte
+            // swizzle row; MN-major ones advance two 8-row (1024-byte) groups.
+            const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
+            const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
+            const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+            const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+                const Unit w = decode_unit(p, u);
+                if (!mbar_wait(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.status,
+                               p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(abuf * BN);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (!mbar_wait(full0 + 8u * stage, phase, abort_flag, p.status,
+                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_base = sA0 + stage * C::A_BYTES;
+                    const uint32_t b_base = sB0 + stage * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = smem_desc_sw128(a_base + k * a_kstep, a_lbo, 1024u);
+                        const uint64_t bd = smem_desc_sw128(b_base + k * b_kstep, b_lbo, 1024u);
+                        umma_f16(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(empty0 + 8u * stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull0 + 8u * abuf);
+                if (++abuf == 2) {
+                    abuf = 0;
+                    aphase ^= 1u;
+                }
+            }
+            if (issued) {
+                // all MMAs of this CTA complete before TMEM is released
+                umma_commit(drain_bar);
+                wait_drain(drain_bar, 0u, p.timeout_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
+        int abuf = 0;
+        uint32_t aphase = 0;
+        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+            const Unit w = decode_unit(p, u);
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(tfull0 + 8u * abuf, aphase, abort_flag, p.status, p.timeout_ns) ? 1
+                                                                                               : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int64_t row = static_cast<int64_t>(w.pid_m) * BM + row_in_tile;
+            const int col_base = w.pid_n * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
+                uint32_t r[32];
+                const uint32_t taddr =
+                    tmem_base + lane_field + static_cast<uint32_t>(abuf * BN + c0);
+                if constexpr (C::CHUNK == 32)
+                    tmem_ld_x32(taddr, r);
+                else
+                    tmem_ld_x16(taddr, r);
+                tmem_ld_wait(r);
+                epilogue_chunk<C::CHUNK>(p, w, row, col_base + c0, r);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(tempty0 + 8u * abuf);
+            if (++abuf == 2) {
+                abuf = 0;
+                aphase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
+    tc_gemm_kernel<BN><<<grid, TC_THREADS, Cfg<BN>::SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t prepare_bn() {
+    return cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(Cfg<BN>::SMEM));
+}
+
+}  // namespace
+
+int tc_stages_for(int bn) {
+    switch (bn) {
+        case 16: return Cfg<16>::STAGES;
+        case 32: return Cfg<32>::STAGES;
+        case 64: return Cfg<64>::STAGES;
+        case 128: return Cfg<128>::STAGES;
+        case 256: return Cfg<256>::STAGES;
+    }
+    return 0;
+}
+
+size_t tc_smem_bytes(int bn) {
+    switch (bn) {
+        case 16: return Cfg<16>::SMEM;
+        case 32: return Cfg<32>::SMEM;
+        case 64: return Cfg<64>::SMEM;
+        case 128: return Cfg<128>::SMEM;
+        case 256: return Cfg<256>::SMEM;
+    }
+    return 0;
+}
+
+cudaError_t tc_prepare(int bn) {
+    switch (bn) {
+        case 16: return prepare_bn<16>();
+        case 32: return prepare_bn<32>();
+        case 64: return prepare_bn<64>();
+        case 128: return prepare_bn<128>();
+        case 256: return prepare_bn<256>();
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t tc_launch(int bn, const TcParams& p, int grid, cudaStream_t stream) {
+    switch (bn) {
+        case 16: return launch_bn<16>(p, grid, stream);
+        case 32: return launch_bn<32>(p, grid, stream);
+        case 64: return launch_bn<64>(p, grid, stream);
+        case 128: return launch_bn<128>(p, grid, stream);
+        case 256: return launch_bn<256>(p, grid, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace dg

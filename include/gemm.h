@@ -1,0 +1,239 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library (libdgemm_gb300.so).
+ *
+ * Operation (BLAS level-3 GEMM, "2 . La GEMM, de zero a cuBLAS", section 2.1,
+ * with the fused epilogue of "Skill: Write a Triton GEMM Kernel", Required
+ * reasoning process step 6):
+ *
+ *     C[b] <- act( alpha * A[b] @ B[b] + beta * C[b] + bias )      b = 0..batch-1
+ *
+ *   A[b] is M x K, B[b] is K x N, C[b] is M x N.  Products accumulate in fp32
+ *   ("GEMM Kernel Optimization", Core Technique and Tensor Core Utilization);
+ *   the downcast to the output type happens once, after accumulation
+ *   ("GEMM Kernel Optimization", Common Pitfalls).  bias is a length-N fp32
+ *   vector added to every row before the activation and not scaled by alpha.
+ *   act is the identity or GELU in its tanh form,
+ *   0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *
+ * Storage.  Every matrix is given by a pointer, a leading dimension and a
+ * layout flag: element (r, c) of a GEMM_ROW_MAJOR matrix sits at r*ld + c, of
+ * a GEMM_COL_MAJOR one at c*ld + r (elements, not bytes).  The inner stride is
+ * always 1; ld must be at least the inner extent ("Skill: Write a Triton GEMM
+ * Kernel", Kernel design rules: strides are arguments, never recomputed from
+ * shapes).  Batch b of an operand starts at ptr + b*stride; a stride of 0
+ * broadcasts one matrix to the whole batch (same page, Correctness
+ * requirements, batched GEMM).  C is read (when beta != 0) and written in
+ * place, in its own dtype.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers except the workspace and the return codes are DEVICE
+ *     pointers on the current CUDA device; the caller owns every buffer.  The
+ *     library allocates no device memory in any call and keeps no pointer
+ *     after return.  Work is enqueued on `stream` (NULL = legacy default
+ *     stream) and runs asynchronously: results are ready when the stream is.
+ *   - beta == 0 means C is not read (NaN or Inf in C does not propagate).
+ *     alpha == 0 or K == 0 means A and B are not read:
+ *     C <- act(beta*C + bias).  M == 0, N == 0 or batch == 0 is a no-op.
+ *   - Argument errors are detected before anything is enqueued and are
+ *     reported by the return code; nothing aborts, prints or throws.
+ *   - Any pointer alignment that the element type allows is accepted.  Fast
+ *     TMA paths need 16-byte aligned bases and leading dimensions that are a
+ *     multiple of 16 bytes; other operands are first copied into the
+ *     caller's workspace (see gemm_workspace_size).
+ *   - Calls are thread-safe.  The first call on a device queries device
+ *     attributes and may set kernel attributes (no allocation).
+ */
+#ifndef DGEMM_GB300_GEMM_H
+#define DGEMM_GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream); NULL is the legacy stream. */
+typedef void* gemm_stream_t;
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+
+typedef enum { GEMM_DT_BF16 = 0, GEMM_DT_F16 = 1, GEMM_DT_F32 = 2 } gemm_dtype_t;
+
+typedef enum {
+    GEMM_EPI_NONE = 0,           /* C = alpha*A@B + beta*C                    */
+    GEMM_EPI_BIAS = 1,           /* ... + bias[n]                             */
+    GEMM_EPI_GELU_TANH = 2,      /* gelu_tanh(alpha*A@B + beta*C)             */
+    GEMM_EPI_BIAS_GELU_TANH = 3  /* gelu_tanh(alpha*A@B + beta*C + bias[n])   */
+} gemm_epilogue_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* negative size, ld too small, bad enum, NULL pointer, misaligned element */
+    GEMM_ERR_UNSUPPORTED = 2,  /* well-formed request this library does not implement (e.g. dtype mix)  */
+    GEMM_ERR_WORKSPACE = 3,    /* workspace smaller than the plan needs                                   */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, attribute, tensor map)      */
+    GEMM_ERR_TIMEOUT = 5,      /* a kernel gave up a bounded wait (reported by gemm_check_device_status) */
+    GEMM_ERR_NO_DEVICE = 6     /* no usable sm_103 device is current                                      */
+} gemm_status_t;
+
+/*
+ * gemm_bf16 -- bf16 A and B, fp32 accumulation on the tcgen05 tensor cores.
+ *
+ *   M, N, K      problem size (>= 0, each below 2^31).
+ *   A, lda, la   M x K operand, bf16.           B, ldb, lb  K x N operand, bf16.
+ *   C, ldc, lc   M x N result, c_dtype GEMM_DT_BF16 or GEMM_DT_F32; read when beta != 0.
+ *   alpha, beta  fp32 scalars.
+ *   bias         length-N fp32 device vector, required iff epi uses a bias, else ignored.
+ *   epi          epilogue (gemm_epilogue_t).
+ *   split_k      0 = choose automatically, 1 = no split, s > 1 = split K into s
+ *                slices whose fp32 partial tiles are summed in a fixed order by a
+ *                second kernel ("Skill: Write a Triton GEMM Kernel", Kernel
+ *                design rules, split-K; "2 . La GEMM, de zero a cuBLAS", section 2.10).
+ *                s is clamped to the number of 64-wide K blocks.
+ *   workspace    device scratch of workspace_bytes bytes, 256-byte aligned (may be
+ *                NULL/0).  Needed
+ *                for split-K partials and for copies of operands that TMA cannot
+ *                address; gemm_workspace_size() gives a sufficient size.  With
+ *                split_k == 0 the plan never asks for more than is given
+ *                (it drops to fewer splits); split_k > 1 or an operand that needs
+ *                a copy with too small a workspace returns GEMM_ERR_WORKSPACE.
+ *   stream       CUDA stream.
+ */
+gemm_status_t gemm_bf16(int64_t M, int64_t N, int64_t K,
+                        const void* A, int64_t lda, gemm_layout_t la,
+                        const void* B, int64_t ldb, gemm_layout_t lb,
+                        void* C, int64_t ldc, gemm_layout_t lc, gemm_dtype_t c_dtype,
+                        float alpha, float beta, const float* bias, gemm_epilogue_t epi,
+                        int split_k, void* workspace, size_t workspace_bytes,
+                        gemm_stream_t stream);
+
+/* gemm_f16 -- as gemm_bf16 with fp16 A and B; c_dtype GEMM_DT_F16 or GEMM_DT_F32. */
+gemm_status_t gemm_f16(int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, gemm_layout_t la,
+                       const void* B, int64_t ldb, gemm_layout_t lb,
+                       void* C, int64_t ldc, gemm_layout_t lc, gemm_dtype_t c_dtype,
+                       float alpha, float beta, const float* bias, gemm_epilogue_t epi,
+                       int split_k, void* workspace, size_t workspace_bytes,
+                       gemm_stream_t stream);
+
+/*
+ * sgemm_f32 -- true fp32 GEMM on the CUDA cores (FFMA; no tensor cores, no TF32).
+ * Register-tiled outer-product kernel ("2 . La GEMM, de zero a cuBLAS",
+ * sections 2.6-2.8: 128x128x8 block tile, 8x8 accumulators per thread, float4
+ * loads, transposed A tile in shared memory, double buffering).
+ * Arguments as gemm_bf16, all matrices fp32; no workspace is used.
+ */
+gemm_status_t sgemm_f32(int64_t M, int64_t N, int64_t K,
+                        const float* A, int64_t lda, gemm_layout_t la,
+                        const float* B, int64_t ldb, gemm_layout_t lb,
+                        float* C, int64_t ldc, gemm_layout_t lc,
+                        float alpha, float beta, const float* bias, gemm_epilogue_t epi,
+                        gemm_stream_t stream);
+
+/*
+ * gemm_batched -- strided batched GEMM ("Skill: Write a Triton GEMM Kernel",
+ * Inputs step 6 and Correctness requirements).
+ *
+ *   ab_dtype     GEMM_DT_BF16 / GEMM_DT_F16 (tensor cores) or GEMM_DT_F32 (CUDA cores).
+ *   batch        number of products (>= 0).
+ *   stride_a/b   elements between consecutive A[b] / B[b]; 0 = broadcast.
+ *   stride_c     elements between consecutive C[b]; must be > 0 when batch > 1
+ *                and large enough that the C[b] do not overlap.
+ *   Other arguments as gemm_bf16 (c_dtype: ab_dtype or GEMM_DT_F32; an fp32
+ *   ab_dtype needs an fp32 C and ignores split_k and the workspace).
+ */
+gemm_status_t gemm_batched(gemm_dtype_t ab_dtype, int64_t batch,
+                           int64_t M, int64_t N, int64_t K,
+                           const void* A, int64_t lda, gemm_layout_t la, int64_t stride_a,
+                           const void* B, int64_t ldb, gemm_layout_t lb, int64_t stride_b,
+                           void* C, int64_t ldc, gemm_layout_t lc, int64_t stride_c,
+                           gemm_dtype_t c_dtype,
+                           float alpha, float beta, const float* bias, gemm_epilogue_t epi,
+                           int split_k, void* workspace, size_t workspace_bytes,
+                           gemm_stream_t stream);
+
+/*
+ * gemm_workspace_size -- bytes of workspace that suffice for any call with these
+ * sizes, whatever the layouts, leading dimensions and pointer alignment
+ * (an upper bound; 0 when no plan can need scratch).  Queries the current
+ * device's SM count.  Returns 0 for invalid sizes.
+ */
+size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N,
+                           int64_t K, int split_k);
+
+/* gemm_status_string -- static, human-readable name of a status code. */
+const char* gemm_status_string(gemm_status_t status);
+
+/*
+ * gemm_check_device_status -- synchronises `stream`, then reads and clears the
+ * current device's error word, which a kernel sets when one of its bounded
+ * waits expires.  Returns GEMM_ERR_TIMEOUT if it was set, GEMM_ERR_CUDA if the
+ * synchronisation failed, else GEMM_OK.  For tests and debugging; it blocks.
+ */
+gemm_status_t gemm_check_device_status(gemm_stream_t stream);
+
+/*
+ * Plan inspection (no launch): fills *plan with the kernel choice that
+ * gemm_batched would make for the same arguments.  Pointers are only
+ * inspected for alignment, never dereferenced.
+ */
+typedef struct {
+    int32_t kernel;          /* 0 none, 1 tcgen05 tensor-core, 2 CUDA-core fp32, 3 epilogue only */
+    int32_t block_m, block_n, block_k;
+    int32_t stages;
+    int32_t split_k;         /* K slices (1 = none)                                */
+    int32_t swap_ab;         /* 1: computed as C^T = B^T A^T                       */
+    int32_t pack_a, pack_b;  /* 1: operand copied into the workspace first         */
+    int32_t grid;            /* CTAs of the main kernel                            */
+    int32_t group_m;         /* tile-order grouping                                */
+    int32_t launches;        /* kernels enqueued by the call                       */
+    int64_t workspace_bytes; /* workspace the plan uses                            */
+} gemm_plan_t;
+
+gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
+                              int64_t M, int64_t N, int64_t K,
+                              const void* A, int64_t lda, gemm_layout_t la, int64_t stride_a,
+                              const void* B, int64_t ldb, gemm_layout_t lb, int64_t stride_b,
+                              void* C, int64_t ldc, gemm_layout_t lc, int64_t stride_c,
+                              gemm_dtype_t c_dtype, float alpha, float beta,
+                              const float* bias, gemm_epilogue_t epi,
+                              int split_k, size_t workspace_bytes, gemm_plan_t* plan);
+
+/*
+ * Process-wide tuning knobs (for measurements and tests; defaults are what the
+ * library ships with).  Returns GEMM_ERR_INVALID_ARG for an unknown option or
+ * value out of range.
+ *   GEMM_OPT_GROUP_M      tile-order group size ("Skill: Write a Triton GEMM
+ *                         Kernel", step 2; 1 = plain row-major tile order), 1..64.
+ *   GEMM_OPT_MAX_CTAS     cap on persistent CTAs (0 = one per SM).
+ *   GEMM_OPT_TIMEOUT_US   bound on any single in-kernel wait, microseconds (>= 1).
+ *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
+ *                         pipeline stage unfilled, so its consumer's bounded wait
+ *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
+ *                         knob resets itself after that launch.
+ */
+typedef enum {
+    GEMM_OPT_GROUP_M = 1,
+    GEMM_OPT_MAX_CTAS = 2,
+    GEMM_OPT_TIMEOUT_US = 3,
+    GEMM_OPT_TEST_STALL = 4
+} gemm_option_t;
+
+gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);
+int64_t gemm_get_option(gemm_option_t option);
+
+/*
+ * gemm_tile_order -- host copy of the kernels' tile order: writes, for every
+ * work index t in [0, num_pid_m*num_pid_n), the tile (pid_m[t], pid_n[t]) it
+ * computes, for grouping `group_m` ("Skill: Write a Triton GEMM Kernel",
+ * Required reasoning process step 2).  The caller sizes both arrays; invalid
+ * arguments write nothing.  Needs no GPU.
+ */
+void gemm_tile_order(int num_pid_m, int num_pid_n, int group_m, int* pid_m, int* pid_n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_GB300_GEMM_H */

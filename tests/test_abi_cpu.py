@@ -1,0 +1,141 @@
+"""The C-ABI library without a GPU: it loads, exports every function the header
+declares, rejects bad arguments before touching CUDA, and its host-side tile
+order is a bijection ("Skill: Write a Triton GEMM Kernel", Correctness
+requirements: every (pid_m, pid_n) exactly once)."""
+import os
+import re
+
+import pytest
+
+import dense_gemm_bf16_gb300 as dg
+from dense_gemm_bf16_gb300 import DType, Epi, Layout, Option, Status
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dg.build()
+    return dg.lib()
+
+
+def header_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", src, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#")):
+                names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding(lib):
+    declared = header_functions()
+    assert set(declared) == set(dg.EXPORTED), declared
+
+
+@pytest.mark.parametrize("name", header_functions())
+def test_symbol_exported(lib, name):
+    assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for s in Status:
+        assert dg.gemm_status_string(s) == "GEMM_" + s.name
+    assert dg.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def _bf16(M, N, K, **kw):
+    args = dict(M=M, N=N, K=K, A=16, lda=max(K, 1), la=Layout.ROW_MAJOR, B=16, ldb=max(N, 1),
+                lb=Layout.ROW_MAJOR, C=16, ldc=max(N, 1), lc=Layout.ROW_MAJOR,
+                c_dtype=DType.F32, alpha=1.0, beta=0.0, bias=None, epi=Epi.NONE, split_k=0,
+                workspace=None, workspace_bytes=0, stream=None)
+    args.update(kw)
+    return dg.gemm_bf16(**args)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=-1, N=4, K=4),
+    dict(M=4, N=-1, K=4),
+    dict(M=4, N=4, K=-1),
+    dict(M=4, N=4, K=4, lda=3),                        # lda < K
+    dict(M=4, N=4, K=4, ldb=3),                        # ldb < N
+    dict(M=4, N=4, K=4, ldc=3),                        # ldc < N
+    dict(M=4, N=4, K=4, la=7),                         # bad layout
+    dict(M=4, N=4, K=4, epi=9),                        # bad epilogue
+    dict(M=4, N=4, K=4, epi=Epi.BIAS),                 # bias missing
+    dict(M=4, N=4, K=4, A=None),                       # A missing
+    dict(M=4, N=4, K=4, C=None),                       # C missing
+    dict(M=4, N=4, K=4, A=17),                         # A not 2-byte aligned
+    dict(M=4, N=4, K=4, split_k=-2),
+    dict(M=1 << 31, N=4, K=4),
+])
+def test_invalid_arguments_rejected_without_gpu(lib, kw):
+    assert _bf16(**kw) == Status.ERR_INVALID_ARG
+
+
+def test_unsupported_dtype_mix(lib):
+    assert _bf16(4, 4, 4, c_dtype=DType.F16) == Status.ERR_UNSUPPORTED
+    st = dg.gemm_batched(DType.F32, 1, 4, 4, 4, 16, 4, 0, 0, 16, 4, 0, 0, 16, 4, 0, 0,
+                         DType.BF16, 1.0, 0.0, None, 0, 0, None, 0, None)
+    assert st == Status.ERR_UNSUPPORTED
+
+
+def test_empty_problems_are_noops(lib):
+    assert _bf16(0, 5, 5, A=None, B=None, C=None) == Status.OK
+    assert _bf16(5, 0, 5, A=None, B=None, C=None) == Status.OK
+    st = dg.gemm_batched(DType.BF16, 0, 4, 4, 4, None, 4, 0, 0, None, 4, 0, 0, None, 4, 0, 0,
+                         DType.F32, 1.0, 0.0, None, 0, 0, None, 0, None)
+    assert st == Status.OK
+
+
+def test_batched_overlapping_C_rejected(lib):
+    st = dg.gemm_batched(DType.BF16, 2, 4, 4, 4, 16, 4, 0, 16, 16, 4, 0, 16, 16, 4, 0, 8,
+                         DType.F32, 1.0, 0.0, None, 0, 0, None, 0, None)
+    assert st == Status.ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host has a GPU")
+def test_valid_call_without_gpu_reports_no_device(lib):
+    assert _bf16(4, 4, 4) == Status.ERR_NO_DEVICE
+    assert dg.gemm_workspace_size(DType.BF16, 1, 256, 256, 65536, 0) == 0
+
+
+def test_options(lib):
+    assert dg.gemm_get_option(Option.GROUP_M) == 8
+    assert dg.gemm_set_option(Option.GROUP_M, 0) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.GROUP_M, 65) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.GROUP_M, 3) == Status.OK
+    assert dg.gemm_get_option(Option.GROUP_M) == 3
+    assert dg.gemm_set_option(Option.GROUP_M, 8) == Status.OK
+    assert dg.gemm_set_option(Option.TIMEOUT_US, 0) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.TEST_STALL, 2) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(99, 1) == Status.ERR_INVALID_ARG
+    assert dg.gemm_get_option(99) == -1
+
+
+@pytest.mark.parametrize("group_m", [1, 2, 3, 5, 8, 64])
+def test_tile_order_is_a_bijection(lib, group_m):
+    for npm in (1, 2, 3, 7, 8, 9, 17, 33, 64):
+        for npn in (1, 2, 5, 12, 32):
+            pm, pn = dg.gemm_tile_order(npm, npn, group_m)
+            pairs = set(zip(pm, pn))
+            assert len(pairs) == npm * npn
+            assert all(0 <= a < npm for a in pm) and all(0 <= b < npn for b in pn)
+
+
+def test_tile_order_group_one_is_row_major(lib):
+    pm, pn = dg.gemm_tile_order(5, 7, 1)
+    assert pm == [t // 7 for t in range(35)]
+    assert pn == [t % 7 for t in range(35)]
+
+
+def test_tile_order_groups_walk_columns_of_tile_rows(lib):
+    # 8 tile-rows per group: the first 8 work items cover column 0 of rows 0..7
+    pm, pn = dg.gemm_tile_order(16, 4, 8)
+    assert pm[:8] == list(range(8)) and pn[:8] == [0] * 8
+    assert pm[8:16] == list(range(8)) and pn[8:16] == [1] * 8
+    assert pm[32:40] == list(range(8, 16)) and pn[32:40] == [0] * 8

@@ -1,0 +1,227 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Sizes span several tiles and ragged tails; every layout combination, the
+split-K and swap-AB plans, batched/broadcast strides, unaligned operands,
+fused epilogues and the degenerate cases are covered.  Small-integer inputs
+make every fp32 partial sum exact, so those cases must match the oracle
+bit for bit whatever the tile order, split or batch.
+"""
+import numpy as np
+import pytest
+
+from gemm_case import Case, check_close
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dense_gemm_bf16_gb300 as dg
+    dg.build()
+    dg.lib()
+    yield
+    dg.gemm_set_option(dg.Option.MAX_CTAS, 0)
+    dg.gemm_set_option(dg.Option.GROUP_M, 8)
+
+
+def run_exact(case):
+    st, out = case.run_gpu()
+    assert st == 0, f"status {st}"
+    got = case.result(out)
+    ref = case.oracle_full()
+    assert np.array_equal(got, ref), (
+        f"max |diff| {np.abs(got - ref).max()} plan={getattr(case, 'plan', None)}")
+    assert case.untouched_padding(out)
+    return case
+
+
+def run_close(case):
+    st, out = case.run_gpu()
+    assert st == 0, f"status {st}"
+    got = case.result(out)
+    ref = case.oracle_full()
+    check_close(case, got, ref)
+    assert case.untouched_padding(out)
+    return case
+
+
+# ---------------------------------------------------------------- exact integer cases
+
+@pytest.mark.parametrize("la", ["row", "col"])
+@pytest.mark.parametrize("lb", ["row", "col"])
+@pytest.mark.parametrize("ab", ["bf16", "f16"])
+def test_exact_layouts(la, lb, ab):
+    run_exact(Case(ab, 300, 520, 200, la=la, lb=lb, values="ints", pads=(3, 5, 7), seed=11))
+
+
+@pytest.mark.parametrize("lc", ["row", "col"])
+def test_exact_output_layout(lc):
+    run_exact(Case("bf16", 257, 130, 190, lc=lc, values="ints", pads=(0, 0, 3), seed=12))
+
+
+@pytest.mark.parametrize("N", [16, 24, 32, 48, 64, 100, 128, 200, 600])
+def test_exact_block_n_variants(N):
+    import dense_gemm_bf16_gb300 as dg
+    # few CTAs: every CTA walks several tiles, so the stage ring and both TMEM
+    # accumulators wrap many times
+    dg.gemm_set_option(dg.Option.MAX_CTAS, 6)
+    try:
+        c = run_exact(Case("bf16", 700, N, 333, values="ints", seed=13))
+    finally:
+        dg.gemm_set_option(dg.Option.MAX_CTAS, 0)
+    assert c.plan["kernel"] == 1
+
+
+@pytest.mark.parametrize("lb", ["row", "col"])
+@pytest.mark.parametrize("split", [2, 3, 7])
+def test_exact_split_k(lb, split):
+    c = run_exact(Case("bf16", 256, 384, 1000, lb=lb, values="ints", split_k=split, seed=14))
+    assert c.plan["split_k"] == split
+
+
+@pytest.mark.parametrize("la", ["row", "col"])
+@pytest.mark.parametrize("M", [1, 5, 16, 33, 64])
+def test_exact_swap_ab(la, M):
+    c = run_exact(Case("bf16", M, 1000, 300, la=la, values="ints", seed=15))
+    assert c.plan["swap_ab"] == 1
+
+
+def test_exact_batched_broadcast():
+    run_exact(Case("bf16", 130, 200, 150, batch=3, values="ints", broadcast_b=True, seed=16))
+    run_exact(Case("bf16", 130, 200, 150, batch=3, la="col", lb="col", values="ints", seed=17))
+
+
+def test_exact_persistent_many_tiles_group_orders():
+    import dense_gemm_bf16_gb300 as dg
+    for g in (1, 3, 8):
+        dg.gemm_set_option(dg.Option.GROUP_M, g)
+        dg.gemm_set_option(dg.Option.MAX_CTAS, 7)
+        try:
+            run_exact(Case("bf16", 1100, 900, 128, values="ints", seed=18))
+        finally:
+            dg.gemm_set_option(dg.Option.GROUP_M, 8)
+            dg.gemm_set_option(dg.Option.MAX_CTAS, 0)
+
+
+# ---------------------------------------------------------------- tolerance cases
+
+@pytest.mark.parametrize("act", ["none", "gelu_tanh"])
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+def test_epilogue_bias_alpha_beta(act, c_dtype):
+    run_close(Case("bf16", 333, 444, 555, c_dtype=c_dtype, alpha=0.75, beta=-0.5, bias=True,
+                   act=act, pads=(2, 2, 2), seed=21))
+
+
+@pytest.mark.parametrize("c_dtype", ["f16", "f32"])
+def test_f16_inputs(c_dtype):
+    run_close(Case("f16", 300, 260, 520, lb="col", c_dtype=c_dtype, alpha=1.5, beta=0.5,
+                   bias=True, seed=22))
+
+
+def test_long_k_fp32_accumulation():
+    # K = 8192: an fp16/bf16 accumulator would be far outside the fp32 bound
+    run_close(Case("bf16", 128, 256, 8192, c_dtype="f32", seed=23))
+
+
+def test_split_k_with_epilogue():
+    run_close(Case("bf16", 200, 300, 4096, c_dtype="bf16", alpha=2.0, beta=1.0, bias=True,
+                   act="gelu_tanh", split_k=5, seed=24))
+
+
+def test_swap_with_bias_col_major_c():
+    run_close(Case("bf16", 12, 700, 640, lc="col", c_dtype="f32", bias=True, beta=0.25, seed=25))
+
+
+def test_batched_in_place_beta_one():
+    run_close(Case("bf16", 256, 256, 256, batch=4, c_dtype="bf16", alpha=0.5, beta=1.0,
+                   broadcast_b=True, seed=26))
+
+
+# ---------------------------------------------------------------- unaligned operands
+
+@pytest.mark.parametrize("pads,offsets", [((1, 0, 0), (0, 0, 0)), ((0, 1, 0), (0, 0, 0)),
+                                          ((0, 0, 0), (1, 0, 0)), ((0, 0, 0), (0, 3, 0)),
+                                          ((0, 0, 1), (0, 0, 1)), ((1, 1, 1), (1, 1, 1))])
+def test_unaligned_operands(pads, offsets):
+    c = run_exact(Case("bf16", 190, 301, 157, values="ints", pads=pads, offsets=offsets, seed=31))
+    assert c.plan["pack_a"] or c.plan["pack_b"] or pads[:2] == (0, 0) and offsets[:2] == (0, 0)
+
+
+def test_unaligned_batched_and_broadcast():
+    run_exact(Case("bf16", 70, 90, 33, batch=3, values="ints", pads=(1, 3, 1), seed=32))
+    run_exact(Case("bf16", 70, 90, 33, batch=3, values="ints", pads=(1, 3, 1),
+                   broadcast_b=True, seed=33))
+
+
+# ---------------------------------------------------------------- degenerate cases
+
+def test_k_zero_and_alpha_zero():
+    run_close(Case("bf16", 50, 60, 0, c_dtype="f32", beta=0.5, bias=True, act="gelu_tanh",
+                   seed=41))
+    run_close(Case("bf16", 50, 60, 40, c_dtype="bf16", alpha=0.0, beta=2.0, seed=42))
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 7, 3), (3, 1, 5), (2, 3, 1), (129, 257, 17),
+                                   (128, 256, 64), (127, 255, 63)])
+def test_tiny_and_boundary_shapes(shape):
+    M, N, K = shape
+    run_exact(Case("bf16", M, N, K, values="ints", seed=43 + M))
+
+
+def test_beta_zero_ignores_nan_in_c():
+    c = Case("bf16", 100, 100, 100, c_dtype="f32", beta=0.0, seed=44)
+    st, out = c.run_gpu()
+    assert st == 0
+    assert np.all(np.isfinite(c.result(out)))
+
+
+# ---------------------------------------------------------------- fp32 CUDA-core SGEMM
+
+@pytest.mark.parametrize("la", ["row", "col"])
+@pytest.mark.parametrize("lb", ["row", "col"])
+def test_sgemm_exact_layouts(la, lb):
+    run_exact(Case("f32", 300, 260, 270, la=la, lb=lb, values="ints", pads=(1, 3, 2), seed=51))
+
+
+def test_sgemm_alpha_beta_bias_gelu():
+    run_close(Case("f32", 257, 129, 333, alpha=1.5, beta=0.5, bias=True, act="gelu_tanh",
+                   seed=52))
+
+
+def test_sgemm_batched_unaligned():
+    run_exact(Case("f32", 70, 90, 33, batch=3, values="ints", pads=(1, 1, 1),
+                   offsets=(1, 2, 3), seed=53))
+
+
+def test_sgemm_is_true_fp32():
+    # TF32 would keep 10 mantissa bits (rms error ~3e-4); fp32 FFMA gives ~1e-6.
+    c = Case("f32", 256, 256, 1024, seed=54)
+    st, out = c.run_gpu()
+    assert st == 0
+    got, ref = c.result(out), c.oracle_full()
+    assert np.sqrt(np.mean((got - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)) <= 1e-5
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_stalled_pipeline_reports_timeout_and_recovers():
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.TIMEOUT_US, 20000)
+    try:
+        dg.gemm_set_option(dg.Option.TEST_STALL, 1)
+        c = Case("bf16", 256, 256, 256, values="ints", seed=61)
+        st, _ = c.run_gpu()
+        assert st == 0
+        stream = torch.cuda.current_stream().cuda_stream
+        assert dg.gemm_check_device_status(stream) == dg.Status.ERR_TIMEOUT
+        assert dg.gemm_check_device_status(stream) == dg.Status.OK
+    finally:
+        dg.gemm_set_option(dg.Option.TEST_STALL, 0)
+        dg.gemm_set_option(dg.Option.TIMEOUT_US, 1000000)
+    # the context is still usable and the next GEMM is right
+    run_exact(Case("bf16", 256, 256, 256, values="ints", seed=62))
+    assert dg.gemm_check_device_status(torch.cuda.current_stream().cuda_stream) == 0
