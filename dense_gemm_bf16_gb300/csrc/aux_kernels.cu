@@ -19,21 +19,17 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// grid: x covers the contiguous dimension, y the rows (grid-stride), z the batch
 __global__ void __launch_bounds__(kThreads) pack16_kernel(const uint16_t* __restrict__ src,
                                                           int64_t ld, int64_t stride, int64_t rows,
-                                                          int64_t cols, int64_t batch,
-                                                          uint16_t* __restrict__ dst,
+                                                          int64_t cols, uint16_t* __restrict__ dst,
                                                           int64_t ld_dst) {
-    const int64_t per = rows * cols;
-    const int64_t total = batch * per;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t b = idx / per;
-        const int64_t rem = idx - b * per;
-        const int64_t r = rem / cols;
-        const int64_t c = rem - r * cols;
-        dst[b * rows * ld_dst + r * ld_dst + c] = src[b * stride + r * ld + c];
-    }
+    const int64_t b = blockIdx.z;
+    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (c >= cols) return;
+    const uint16_t* s = src + b * stride + c;
+    uint16_t* d = dst + b * rows * ld_dst + c;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) d[r * ld_dst] = s[r * ld];
 }
 
 __global__ void __launch_bounds__(kThreads) splitk_epi_kernel(const float* __restrict__ P,
@@ -70,11 +66,15 @@ int grid_for(int64_t total) {
 
 cudaError_t pack16_launch(const void* src, int64_t ld, int64_t stride, int64_t rows, int64_t cols,
                           int64_t batch, void* dst, int64_t ld_dst, cudaStream_t stream) {
-    const int64_t total = batch * rows * cols;
-    if (total <= 0) return cudaSuccess;
-    pack16_kernel<<<grid_for(total), kThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(src), ld, stride, rows, cols, batch,
-        static_cast<uint16_t*>(dst), ld_dst);
+    if (batch <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
+    if (batch > 65535) return cudaErrorInvalidValue;
+    const int64_t gx = (cols + kThreads - 1) / kThreads;
+    const int64_t gy = rows < 4096 ? rows : 4096;
+    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    pack16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
+                         static_cast<unsigned>(batch)),
+                    kThreads, 0, stream>>>(static_cast<const uint16_t*>(src), ld, stride, rows,
+                                           cols, static_cast<uint16_t*>(dst), ld_dst);
     return cudaGetLastError();
 }
 

@@ -65,92 +65,4 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int64_t b, int
     store_elem(c, e.c_dtype, x);
 }
 
-// 16-bit pack/unpack helpers for vectorised epilogues.
-__device__ __forceinline__ uint32_t pack2(int dt, float a, float b) {
-    if (dt == DT_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float2 unpack2(int dt, uint32_t v) {
-    if (dt == DT_BF16) {
-        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
-        return __bfloat1622float2(h);
-    }
-    __half2 h = *reinterpret_cast<__half2*>(&v);
-    return __half22float2(h);
-}
-
-// A contiguous run of W (a multiple of 8) elements of one row of a row-major
-// C, starting at a 16-byte aligned address: v holds alpha*acc on entry.
-template <int W>
-__device__ __forceinline__ void epilogue_row_vec(const Epilogue& e, char* c, const float* bias_run,
-                                                 float bias_row, float (&v)[W]) {
-    if (e.c_dtype == DT_F32) {
-        float4* c4 = reinterpret_cast<float4*>(c);
-        if (e.beta != 0.0f) {
-#pragma unroll
-            for (int q = 0; q < W / 4; ++q) {
-                const float4 o = c4[q];
-                v[4 * q + 0] = fmaf(e.beta, o.x, v[4 * q + 0]);
-                v[4 * q + 1] = fmaf(e.beta, o.y, v[4 * q + 1]);
-                v[4 * q + 2] = fmaf(e.beta, o.z, v[4 * q + 2]);
-                v[4 * q + 3] = fmaf(e.beta, o.w, v[4 * q + 3]);
-            }
-        }
-    } else {
-        const uint4* c4 = reinterpret_cast<const uint4*>(c);
-        if (e.beta != 0.0f) {
-#pragma unroll
-            for (int q = 0; q < W / 8; ++q) {
-                const uint4 o = c4[q];
-                const uint32_t w4[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float2 f = unpack2(e.c_dtype, w4[h]);
-                    v[8 * q + 2 * h + 0] = fmaf(e.beta, f.x, v[8 * q + 2 * h + 0]);
-                    v[8 * q + 2 * h + 1] = fmaf(e.beta, f.y, v[8 * q + 2 * h + 1]);
-                }
-            }
-        }
-    }
-    if (bias_run) {
-#pragma unroll
-        for (int q = 0; q < W / 4; ++q) {
-            const float4 bb = reinterpret_cast<const float4*>(bias_run)[q];
-            v[4 * q + 0] += bb.x;
-            v[4 * q + 1] += bb.y;
-            v[4 * q + 2] += bb.z;
-            v[4 * q + 3] += bb.w;
-        }
-    } else if (bias_row != 0.0f) {
-#pragma unroll
-        for (int q = 0; q < W; ++q) v[q] += bias_row;
-    }
-    if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-        for (int q = 0; q < W; ++q) v[q] = gelu_tanh(v[q]);
-    }
-    if (e.c_dtype == DT_F32) {
-        float4* c4 = reinterpret_cast<float4*>(c);
-#pragma unroll
-        for (int q = 0; q < W / 4; ++q)
-            c4[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-        uint4* c4 = reinterpret_cast<uint4*>(c);
-#pragma unroll
-        for (int q = 0; q < W / 8; ++q) {
-            uint4 o;
-            o.x = pack2(e.c_dtype, v[8 * q + 0], v[8 * q + 1]);
-            o.y = pack2(e.c_dtype, v[8 * q + 2], v[8 * q + 3]);
-            o.z = pack2(e.c_dtype, v[8 * q + 4], v[8 * q + 5]);
-            o.w = pack2(e.c_dtype, v[8 * q + 6], v[8 * q + 7]);
-            c4[q] = o;
-        }
-    }
-}
-
 }  // namespace dg

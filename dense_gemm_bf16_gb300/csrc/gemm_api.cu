@@ -314,7 +314,6 @@ Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
     const bool has_bias = c.epi == GEMM_EPI_BIAS || c.epi == GEMM_EPI_BIAS_GELU_TANH;
     e.bias = has_bias ? c.bias : nullptr;
     e.bias_on_rows = bias_on_rows ? 1 : 0;
-    e.bias_vec_ok = (e.bias && aligned(e.bias, 16)) ? 1 : 0;
     e.act = (c.epi == GEMM_EPI_GELU_TANH || c.epi == GEMM_EPI_BIAS_GELU_TANH) ? ACT_GELU_TANH
                                                                                : ACT_NONE;
     return e;

@@ -28,7 +28,6 @@ struct Epilogue {
     float alpha, beta;
     const float* bias;       // may be null
     int32_t bias_on_rows;    // 1: bias indexed by row i (swapped problem), 0: by column j
-    int32_t bias_vec_ok;     // bias pointer 16-byte aligned
     int32_t act;             // ACT_NONE / ACT_GELU_TANH
 };
 

@@ -36,17 +36,24 @@ constexpr int BM = TC_BLOCK_M;
 constexpr int BK = TC_BLOCK_K;
 constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
 
+// Per-warp staging tile of the row-major epilogue: 32 rows x 32 fp32 columns,
+// rows padded to 33 words so that the row-wise writes (one row per lane) and
+// the column-wise reads (one column per lane) each touch 32 distinct banks.
+constexpr int STAGE_LD = 33;
+constexpr uint32_t EPI_STAGE_FLOATS = 32 * STAGE_LD;
+constexpr uint32_t EPI_BYTES = 4 * EPI_STAGE_FLOATS * 4;  // four epilogue warps
+
 template <int BN>
 struct Cfg {
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = BN * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
     static constexpr int CHUNK = BN < 32 ? BN : 32;
-    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
@@ -87,62 +94,180 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, 
         tma_load_2d(dst, map, bar, x, y, pol);
 }
 
-// Epilogue of one CH-column chunk held by this thread (row `row` of the
-// computed problem, columns col0 .. col0+CH-1).
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+}
+template <>
+__device__ __forceinline__ float ld_f<__half>(const __half* p) { return __half2float(*p); }
+
+template <typename T>
+__device__ __forceinline__ void st_f(T* p, float x);
+template <>
+__device__ __forceinline__ void st_f<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void st_f<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+    *p = __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ void st_f<__half>(__half* p, float x) { *p = __float2half_rn(x); }
+
+__device__ __forceinline__ float finish(const Epilogue& e, float acc, float c_old, float bias) {
+    float x = e.alpha * acc;
+    if (e.beta != 0.0f) x = fmaf(e.beta, c_old, x);
+    x += bias;
+    if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
+    return x;
+}
+
+// Row-major C: lane t owns column col0 + t of the warp's 32 rows, read from
+// the staging tile.  All beta*C loads of the chunk are issued before any
+// store (C is read and written in place, so the compiler may not reorder a
+// load above an earlier store by itself).
+template <int CH, typename T>
+__device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M, int N,
+                                         int64_t row_base, int lane, int col0,
+                                         const float* stage) {
+    constexpr int H = 16;  // rows per half: bounds the registers held by in-flight loads
+    const int col = col0 + lane;
+    const bool col_ok = lane < CH && col < N;
+    const int64_t left = M - row_base;
+    const int nrows = left < 32 ? static_cast<int>(left) : 32;
+    const int64_t ldc = e.ldc;
+    const float bias_col = (e.bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
+    T* const c0 =
+        static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c + row_base * ldc + col;
+#pragma unroll 1
+    for (int h = 0; h < 32; h += H) {
+        float cv[H];
+        if (e.beta != 0.0f) {
+            const T* q = c0 + h * ldc;
+#pragma unroll
+            for (int i = 0; i < H; ++i, q += ldc)
+                cv[i] = (h + i < nrows && col_ok) ? ld_f(q) : 0.0f;
+        }
+        T* q = c0 + h * ldc;
+#pragma unroll
+        for (int i = 0; i < H; ++i, q += ldc) {
+            if (h + i < nrows && col_ok) {
+                const float b =
+                    (e.bias && e.bias_on_rows) ? e.bias[row_base + h + i] : bias_col;
+                st_f(q, finish(e, stage[(h + i) * STAGE_LD + lane],
+                               e.beta != 0.0f ? cv[i] : 0.0f, b));
+            }
+        }
+    }
+}
+
+// Column-major C: lane t owns row row_base + t; for a fixed column the 32
+// lanes address 32 consecutive elements, so the accesses are coalesced.
+template <int CH, typename T>
+__device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M, int N,
+                                         int64_t row_base, int lane, int col0,
+                                         const uint32_t (&r)[32]) {
+    constexpr int H = CH < 16 ? CH : 16;
+    const int64_t row = row_base + lane;
+    if (row >= M) return;
+    const int left = N - col0;
+    const int ncols = left < CH ? left : CH;
+    const int64_t ldc = e.ldc;
+    const float bias_row = (e.bias && e.bias_on_rows) ? e.bias[row] : 0.0f;
+    T* const c0 = static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c +
+                  static_cast<int64_t>(col0) * ldc + row;
+#pragma unroll
+    for (int h = 0; h < CH; h += H) {
+        float cv[H];
+        if (e.beta != 0.0f) {
+            const T* q = c0 + h * ldc;
+#pragma unroll
+            for (int i = 0; i < H; ++i, q += ldc) cv[i] = h + i < ncols ? ld_f(q) : 0.0f;
+        }
+        T* q = c0 + h * ldc;
+#pragma unroll
+        for (int i = 0; i < H; ++i, q += ldc) {
+            if (h + i < ncols) {
+                const float b = (e.bias && !e.bias_on_rows) ? e.bias[col0 + h + i] : bias_row;
+                st_f(q, finish(e, __uint_as_float(r[h + i]), e.beta != 0.0f ? cv[i] : 0.0f, b));
+            }
+        }
+    }
+}
+
+// Epilogue of one CH-column chunk of this warp's 32 rows.  On entry lane t
+// holds row row_base + t, columns col0 .. col0+CH-1 (fp32 accumulators).
 template <int CH>
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w, int64_t row,
-                                               int col0, const uint32_t (&r)[32]) {
-    if (row >= p.M) return;
+__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w, int64_t row_base,
+                                               int lane, int col0, const uint32_t (&r)[32],
+                                               float* stage) {
     const Epilogue& e = p.epi;
-    const bool full = col0 + CH <= p.N;
+    if (row_base >= p.M) return;
     if (p.partials) {
         // raw fp32 partial tile, stored densely in C's layout
         const int64_t slice = static_cast<int64_t>(w.split) * p.batch + w.b;
         float* P = p.partials + slice * static_cast<int64_t>(p.M) * p.N;
-        if (e.c_row_major) {
-            float* dst = P + row * p.N + col0;
-            if (full && (p.N & 3) == 0) {
-#pragma unroll
-                for (int q = 0; q < CH / 4; ++q)
-                    reinterpret_cast<float4*>(dst)[q] =
-                        make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < CH; ++c)
-                    if (col0 + c < p.N) dst[c] = __uint_as_float(r[c]);
-            }
-        } else {
-            float* dst = P + row;
+        if (!e.c_row_major) {
+            const int64_t row = row_base + lane;
+            if (row >= p.M) return;
 #pragma unroll
             for (int c = 0; c < CH; ++c)
-                if (col0 + c < p.N) dst[static_cast<int64_t>(col0 + c) * p.M] = __uint_as_float(r[c]);
+                if (col0 + c < p.N)
+                    P[static_cast<int64_t>(col0 + c) * p.M + row] = __uint_as_float(r[c]);
+            return;
         }
-        return;
-    }
-    if (e.c_row_major && full && e.c_vec_ok) {
-        float v[CH];
 #pragma unroll
-        for (int c = 0; c < CH; ++c) v[c] = e.alpha * __uint_as_float(r[c]);
-        char* c = c_addr(e, w.b, row, col0);
-        const float* bias_run = nullptr;
-        float bias_row = 0.0f;
-        if (e.bias) {
-            if (e.bias_on_rows)
-                bias_row = e.bias[row];
-            else if (e.bias_vec_ok)
-                bias_run = e.bias + col0;
-            else {
-#pragma unroll
-                for (int q = 0; q < CH; ++q) v[q] += e.bias[col0 + q];
+        for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
+        __syncwarp();
+        const int col = col0 + lane;
+        if (lane < CH && col < p.N) {
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int64_t row = row_base + rr;
+                if (row < p.M) P[row * p.N + col] = stage[rr * STAGE_LD + lane];
             }
         }
-        epilogue_row_vec<CH>(e, c, bias_run, bias_row, v);
+        __syncwarp();
         return;
     }
+    if (!e.c_row_major) {
+        if (e.c_dtype == DT_BF16)
+            cols_out<CH, __nv_bfloat16>(e, w, p.M, p.N, row_base, lane, col0, r);
+        else if (e.c_dtype == DT_F16)
+            cols_out<CH, __half>(e, w, p.M, p.N, row_base, lane, col0, r);
+        else
+            cols_out<CH, float>(e, w, p.M, p.N, row_base, lane, col0, r);
+        return;
+    }
+    // row-major output: transpose through shared memory so that each warp
+    // store covers consecutive columns of one row.
 #pragma unroll
-    for (int c = 0; c < CH; ++c)
-        if (col0 + c < p.N) epilogue_store(e, w.b, row, col0 + c, __uint_as_float(r[c]));
+    for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
+    __syncwarp();
+    if (e.c_dtype == DT_BF16)
+        rows_out<CH, __nv_bfloat16>(e, w, p.M, p.N, row_base, lane, col0, stage);
+    else if (e.c_dtype == DT_F16)
+        rows_out<CH, __half>(e, w, p.M, p.N, row_base, lane, col0, stage);
+    else
+        rows_out<CH, float>(e, w, p.M, p.N, row_base, lane, col0, stage);
+    __syncwarp();
+}
+
+// Pull this warp's rows of the C tile into L2 before the accumulator is ready
+// (beta != 0 only), so that the epilogue's reads of C hit L2.
+template <int BN>
+__device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w, int64_t row) {
+    const Epilogue& e = p.epi;
+    if (e.beta == 0.0f || p.partials || !e.c_row_major || row >= p.M) return;
+    const int col0 = w.pid_n * BN;
+    const int ncols = p.N - col0 < BN ? p.N - col0 : BN;
+    const int es = dt_size(e.c_dtype);
+    const char* base = static_cast<const char*>(e.C) +
+                       (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc + col0) * es;
+    for (int off = 0; off < ncols * es; off += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
 }
 
 template <int BN>
@@ -163,6 +288,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const uint32_t drain_bar = tempty0 + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* epi_stage0 =
+        reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -311,12 +438,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
         const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
+        float* stage = epi_stage0 + (warp - 2) * EPI_STAGE_FLOATS;
         int abuf = 0;
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
             const Unit w = decode_unit(p, u);
+            prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
             int ok = 1;
             if (lane == 0)
                 ok = mbar_wait(tfull0 + 8u * abuf, aphase, abort_flag, p.status, p.timeout_ns) ? 1
@@ -324,7 +452,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
-            const int64_t row = static_cast<int64_t>(w.pid_m) * BM + row_in_tile;
+            const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
@@ -336,7 +464,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 else
                     tmem_ld_x16(taddr, r);
                 tmem_ld_wait(r);
-                epilogue_chunk<C::CHUNK>(p, w, row, col_base + c0, r);
+                epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
             }
             tc_fence_before_sync();
             mbar_arrive(tempty0 + 8u * abuf);
