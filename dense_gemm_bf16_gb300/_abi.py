@@ -93,7 +93,11 @@ _SIGNATURES = {
     "gemm_get_option": ([_i32], _i64),
     "gemm_tile_order": ([_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int),
                          ctypes.POINTER(ctypes.c_int)], None),
+    "gemm_bf16_static_workspace": ([_i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp,
+                                    _i64, _i32, _i32, _f32, _f32, _vp, _i32, _i32, _vp], _i32),
 }
+# size of the library-owned scratch array used by gemm_bf16_static_workspace
+STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 EXPORTED = tuple(_SIGNATURES)
 
 
@@ -150,6 +154,14 @@ def gemm_batched(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, str
     return lib().gemm_batched(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb,
                               stride_b, C, ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi,
                               split_k, workspace, workspace_bytes, stream)
+
+
+def gemm_bf16_static_workspace(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta,
+                               bias, epi, split_k, stream) -> int:
+    """gemm_bf16 with the library's own scratch array instead of a caller
+    workspace (for callers that cannot allocate device memory)."""
+    return lib().gemm_bf16_static_workspace(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype,
+                                            alpha, beta, bias, epi, split_k, stream)
 
 
 def gemm_workspace_size(ab_dtype, batch, M, N, K, split_k) -> int:

@@ -232,6 +232,44 @@ int64_t gemm_get_option(gemm_option_t option);
  */
 void gemm_tile_order(int num_pid_m, int num_pid_n, int group_m, int* pid_m, int* pid_n);
 
+/*
+ * gemm_bf16_static_workspace -- gemm_bf16 for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this is an interface of
+ * this library only.)
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace: code that
+ * runs where a host framework has already reserved the device's memory for
+ * its own allocator, plugin hooks whose contract forbids allocation during
+ * execution, and latency-critical loops that must not enter the allocator
+ * (cudaMalloc can synchronise the device).  This entry point takes the same
+ * arguments as gemm_bf16 minus the workspace; its scratch (split-K partial
+ * tiles and aligned operand copies) is a library-owned device array of
+ * GEMM_STATIC_WORKSPACE_BYTES bytes that every GPU loading the library keeps
+ * until the process exits.  No call allocates anything.
+ *
+ *   - Limit: a plan that needs more than GEMM_STATIC_WORKSPACE_BYTES of
+ *     scratch is rejected with GEMM_ERR_WORKSPACE before anything is
+ *     enqueued (split_k > 1 too large for the array, or operand copies that
+ *     do not fit); with split_k == 0 the split is reduced to fit.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture begins.
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: every call writes each scratch
+ *     byte before reading it.  Calls whose work overlaps on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on the array and may produce wrong results: order them.
+ */
+#define GEMM_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+gemm_status_t gemm_bf16_static_workspace(int64_t M, int64_t N, int64_t K,
+                                         const void* A, int64_t lda, gemm_layout_t la,
+                                         const void* B, int64_t ldb, gemm_layout_t lb,
+                                         void* C, int64_t ldc, gemm_layout_t lc,
+                                         gemm_dtype_t c_dtype, float alpha, float beta,
+                                         const float* bias, gemm_epilogue_t epi, int split_k,
+                                         gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
