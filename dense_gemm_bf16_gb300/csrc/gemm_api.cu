@@ -342,6 +342,35 @@ gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const v
     return GEMM_OK;
 }
 
+// Tensor map of the epilogue's output boxes (32 columns x 32 rows): C itself
+// when TMA can address it, or the dense fp32 split-K partials.  Returns false
+// when the row-major TMA epilogue does not apply (the kernel then falls back
+// to st.global stores).
+bool encode_output_map(CUtensorMap* map, int dt, void* ptr, int64_t N, int64_t M, int64_t ld,
+                       int64_t depth, int64_t stride, bool* is3d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int es = dt_bytes(dt);
+    if (!aligned(ptr, 16) || (ld * es) % 16 != 0) return false;
+    const bool three = depth > 1;
+    if (three && (stride * es) % 16 != 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                          static_cast<cuuint64_t>(depth)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es), static_cast<cuuint64_t>(stride * es)};
+    cuuint32_t box[3] = {32u, 32u, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType t = dt == DT_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUresult r =
+        fn(map, t, three ? 3u : 2u, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    *is3d = three;
+    return true;
+}
+
 gemm_status_t run(const Call& c) {
     gemm_status_t st = validate(c);
     if (st != GEMM_OK) return st;
@@ -431,6 +460,17 @@ gemm_status_t run(const Call& c) {
     p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, TC_BLOCK_M, pl.bn);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
+    if (pl.c_row_major_c && pl.bn >= 32) {
+        bool c3 = false;
+        bool ok;
+        if (p.partials)
+            ok = encode_output_map(&p.tmap_c, DT_F32, p.partials, pl.Nc, pl.Mc, pl.Nc,
+                                   static_cast<int64_t>(pl.splits) * c.batch, pl.Mc * pl.Nc, &c3);
+        else
+            ok = encode_output_map(&p.tmap_c, c.cdt, c.C, pl.Nc, pl.Mc, c.ldc, c.batch, c.sc, &c3);
+        p.c_tma = ok ? 1 : 0;
+        p.c_tma_3d = c3 ? 1 : 0;
+    }
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;

@@ -46,6 +46,9 @@ struct TcParams {
     int32_t a_3d, b_3d;      // 1: tensor map carries the batch as its third dimension
     uint32_t idesc;          // tcgen05 instruction descriptor
     Epilogue epi;
+    CUtensorMap tmap_c;      // output (or split-K partials) for the TMA-store epilogue
+    int32_t c_tma;           // 1: epilogue stores through tmap_c
+    int32_t c_tma_3d;        // 1: tmap_c has a third (batch or slice) dimension
     float* partials;         // split-K: fp32 partial tiles [split][batch][M][N] in C's layout; else null
     int* status;             // device error word
     uint64_t timeout_ns;     // bound on every wait

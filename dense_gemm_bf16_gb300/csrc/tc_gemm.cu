@@ -36,12 +36,16 @@ constexpr int BM = TC_BLOCK_M;
 constexpr int BK = TC_BLOCK_K;
 constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
 
-// Per-warp staging tile of the row-major epilogue: 32 rows x 32 fp32 columns,
-// rows padded to 33 words so that the row-wise writes (one row per lane) and
-// the column-wise reads (one column per lane) each touch 32 distinct banks.
+// Shared memory of each epilogue warp: two 4 KB output boxes (32 rows x 128
+// bytes, 128-byte swizzled) for the TMA-store epilogue, or one staging tile
+// of 32 rows x 32 fp32 columns (rows padded to 33 words so that row-wise
+// writes and column-wise reads each touch 32 distinct banks) for the
+// st.global fallback.
 constexpr int STAGE_LD = 33;
-constexpr uint32_t EPI_STAGE_FLOATS = 32 * STAGE_LD;
-constexpr uint32_t EPI_BYTES = 4 * EPI_STAGE_FLOATS * 4;  // four epilogue warps
+constexpr uint32_t EPI_WARP_BYTES = 8192;
+constexpr uint32_t EPI_BOX_BYTES = 4096;
+constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;  // four epilogue warps
+static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 
 template <int BN>
 struct Cfg {
@@ -57,6 +61,8 @@ struct Cfg {
     static_assert(STAGES >= 2, "pipeline needs two stages");
     static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
+    static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
+                  "swizzled output boxes must be 1024-byte aligned");
 };
 
 struct Unit {
@@ -255,6 +261,148 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w,
     __syncwarp();
 }
 
+__device__ __forceinline__ uint32_t pack2_out(int dt, float lo, float hi) {
+    if (dt == DT_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2_in(int dt, uint32_t u) {
+    if (dt == DT_BF16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+}
+
+// TMA-store epilogue of one tile for this warp's 32 rows.  The tile is cut
+// into chunks of 32 columns.  Per chunk, lane t turns row t's accumulators
+// into output values (alpha, beta*C, bias, GELU, one rounding; or raw fp32
+// for split-K partials) and writes them as row t of a 32-row box in shared
+// memory, laid out as the tensor map's swizzle expects (rows of RB = 32*ES
+// bytes; 128-byte swizzle for fp32, 64-byte swizzle for 16-bit outputs);
+// lane 0 then stores the box with one TMA tensor store.  The TMA unit clips
+// rows >= M and columns >= N.  Two boxes per warp alternate, so the math of
+// a chunk overlaps the store of the previous one.
+template <int BN, int ES>
+__device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, int q, int lane,
+                                             uint32_t tmem_row, uint8_t* wbuf, uint32_t& nbox,
+                                             uint64_t pol) {
+    constexpr int EB = 32;             // columns per chunk
+    constexpr int RB = EB * ES;        // bytes per box row: 128 (fp32) or 64 (16-bit)
+    constexpr int NJ = RB / 16;        // 16-byte pieces per row
+    constexpr int NW = RB / 4;         // 32-bit words per row
+    const Epilogue& e = p.epi;
+    const bool partial = p.partials != nullptr;
+    const int dt = partial ? DT_F32 : e.c_dtype;
+    const int row0 = w.pid_m * BM + q * 32;
+    const int64_t row = static_cast<int64_t>(row0) + lane;
+    const bool row_ok = row < p.M;
+    const int zc = partial ? w.split * p.batch + w.b : w.b;
+    // swizzle: piece j of row r sits at piece j ^ ((r * RB / 128) % NJ)
+    const int swz = ((lane * RB) >> 7) & (NJ - 1);
+#pragma unroll 1
+    for (int c = 0; c < BN / EB; ++c) {
+        const int col0 = w.pid_n * BN + c * EB;
+        if (col0 >= p.N) break;
+        const bool full = col0 + EB <= p.N;
+        // beta*C of this thread's row segment (issued before the TMEM read)
+        uint32_t craw[NW];
+        const bool need_c = !partial && e.beta != 0.0f && row_ok;
+        if (need_c) {
+            const char* src = static_cast<const char*>(e.C) +
+                              (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc + col0) * ES;
+            if (full) {
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const uint4 t = reinterpret_cast<const uint4*>(src)[j];
+                    craw[4 * j + 0] = t.x;
+                    craw[4 * j + 1] = t.y;
+                    craw[4 * j + 2] = t.z;
+                    craw[4 * j + 3] = t.w;
+                }
+            } else {
+                const int nvalid = p.N - col0;
+#pragma unroll
+                for (int i = 0; i < NW; ++i) craw[i] = 0u;
+#pragma unroll
+                for (int i = 0; i < EB; ++i) {
+                    if (i < nvalid) {
+                        if (ES == 4) {
+                            craw[i] = reinterpret_cast<const uint32_t*>(src)[i];
+                        } else {
+                            const uint32_t h = reinterpret_cast<const uint16_t*>(src)[i];
+                            craw[i >> 1] |= (i & 1) ? (h << 16) : h;
+                        }
+                    }
+                }
+            }
+        }
+        // accumulators: 32 consecutive TMEM columns of this lane's row
+        uint32_t r[32];
+        tmem_ld_x32(tmem_row + static_cast<uint32_t>(c * EB), r);
+        tmem_ld_wait(r);
+        float v[EB];
+#pragma unroll
+        for (int i = 0; i < EB; ++i) v[i] = __uint_as_float(r[i]);
+        if (!partial) {
+            const float bias_row = (e.bias && e.bias_on_rows && row_ok) ? e.bias[row] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < EB; ++i) {
+                float x = e.alpha * v[i];
+                if (need_c) {
+                    float cval;
+                    if (ES == 4) {
+                        cval = __uint_as_float(craw[i]);
+                    } else {
+                        const float2 f = unpack2_in(dt, craw[i >> 1]);
+                        cval = (i & 1) ? f.y : f.x;
+                    }
+                    x = fmaf(e.beta, cval, x);
+                }
+                if (e.bias) {
+                    if (e.bias_on_rows)
+                        x += bias_row;
+                    else if (full || col0 + i < p.N)
+                        x += __ldg(e.bias + col0 + i);
+                }
+                if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
+                v[i] = x;
+            }
+        }
+        // the box written two chunks ago must have been read by its TMA store
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint8_t* box = wbuf + (nbox & 1u) * EPI_BOX_BYTES;
+        uint8_t* line = box + lane * RB;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            uint4 t;
+            if (ES == 4) {
+                t = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                               __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
+            } else {
+                t.x = pack2_out(dt, v[8 * j + 0], v[8 * j + 1]);
+                t.y = pack2_out(dt, v[8 * j + 2], v[8 * j + 3]);
+                t.z = pack2_out(dt, v[8 * j + 4], v[8 * j + 5]);
+                t.w = pack2_out(dt, v[8 * j + 6], v[8 * j + 7]);
+            }
+            *reinterpret_cast<uint4*>(line + ((j ^ swz) << 4)) = t;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (p.c_tma_3d)
+                tma_store_3d(&p.tmap_c, smem_u32(box), col0, row0, zc, pol);
+            else
+                tma_store_2d(&p.tmap_c, smem_u32(box), col0, row0, pol);
+            bulk_commit_group();
+        }
+        ++nbox;
+    }
+}
+
 // Pull this warp's rows of the C tile into L2 before the accumulator is ready
 // (beta != 0 only), so that the epilogue's reads of C hit L2.
 template <int BN>
@@ -278,7 +426,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][barriers]
+    uint8_t* epi_smem = smem + C::STAGES * C::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
     // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
     const uint32_t full0 = bar0;
@@ -288,8 +438,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const uint32_t drain_bar = tempty0 + 16u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* epi_stage0 =
-        reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -439,7 +587,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
-        float* stage = epi_stage0 + (warp - 2) * EPI_STAGE_FLOATS;
+        uint8_t* wbuf = epi_smem + (warp - 2) * EPI_WARP_BYTES;
+        float* stage = reinterpret_cast<float*>(wbuf);
+        uint32_t nbox = 0;
+        const uint64_t store_pol = l2_policy_evict_first();
         int abuf = 0;
         uint32_t aphase = 0;
         for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
@@ -454,17 +605,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             tc_fence_after_sync();
             const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
+            const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
+            if (p.c_tma) {
+                if constexpr (BN >= 32) {
+                    if (p.partials != nullptr || p.epi.c_dtype == DT_F32)
+                        tile_out_tma<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                    else
+                        tile_out_tma<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                }
+            } else {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
-                uint32_t r[32];
-                const uint32_t taddr =
-                    tmem_base + lane_field + static_cast<uint32_t>(abuf * BN + c0);
-                if constexpr (C::CHUNK == 32)
-                    tmem_ld_x32(taddr, r);
-                else
-                    tmem_ld_x16(taddr, r);
-                tmem_ld_wait(r);
-                epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
+                for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
+                    uint32_t r[32];
+                    const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
+                    if constexpr (C::CHUNK == 32)
+                        tmem_ld_x32(taddr, r);
+                    else
+                        tmem_ld_x16(taddr, r);
+                    tmem_ld_wait(r);
+                    epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
+                }
             }
             tc_fence_before_sync();
             mbar_arrive(tempty0 + 8u * abuf);
@@ -473,6 +633,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 aphase ^= 1u;
             }
         }
+        // the TMA stores must finish before the CTA exits
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
