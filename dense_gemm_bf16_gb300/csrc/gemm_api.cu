@@ -25,6 +25,7 @@ std::atomic<int64_t> g_opt_group_m{8};
 std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_timeout_us{1000000};
 std::atomic<int64_t> g_opt_test_stall{0};
+std::atomic<int64_t> g_opt_cluster_m{0};
 
 constexpr int kMaxDevices = 64;
 constexpr int kBlockN[] = {16, 32, 64, 128, 256};
@@ -35,6 +36,8 @@ struct DevState {
     int sm_count = 0;
     int cc = 0;
     int* status = nullptr;
+    int max_pairs128 = 0;  // co-resident two-CTA clusters, BN = 128 / 256
+    int max_pairs256 = 0;
 };
 DevState g_dev[kMaxDevices];
 
@@ -57,6 +60,10 @@ gemm_status_t device_state(DevState** out) {
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
             for (int bn : kBlockN)
                 if (e == cudaSuccess) e = tc_prepare(bn);
+            if (e == cudaSuccess) {
+                d.max_pairs128 = tc_max_pairs(128);
+                d.max_pairs256 = tc_max_pairs(256);
+            }
         }
         d.sm_count = sms;
         d.err = e;
@@ -134,7 +141,7 @@ struct Plan {
     int kernel = 0;  // 0 none, 1 tensor core, 2 CUDA-core fp32, 3 epilogue only
     bool swap = false;
     int64_t Mc = 0, Nc = 0;
-    int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0;
+    int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1;
     int64_t kblocks = 0, tiles = 0, units = 0;
     Operand a{}, b{};
     bool c_row_major_c = true;
@@ -211,7 +218,8 @@ int auto_splits(int64_t units, int64_t kblocks, int ctas, int64_t batch, int64_t
     return best;
 }
 
-gemm_status_t make_plan(const Call& c, int sm_count, Plan& pl) {
+gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
+    const int sm_count = d.sm_count;
     pl = Plan{};
     pl.group_m = static_cast<int>(g_opt_group_m.load());
     int ctas = sm_count;
@@ -288,9 +296,27 @@ gemm_status_t make_plan(const Call& c, int sm_count, Plan& pl) {
         pl.launches += 1;
     }
     pl.ws_need = off;
+    // Two-CTA clusters along M sharing B tiles, for problems with at least a
+    // full wave of tile pairs (GEMM_OPT_CLUSTER_M: 0 auto, 1 never, 2 when possible).
+    const int64_t want_cm = g_opt_cluster_m.load();
+    const int max_pairs = pl.bn == 256 ? d.max_pairs256 : (pl.bn == 128 ? d.max_pairs128 : 0);
+    const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
+    if (want_cm != 1 && tc_has_pair(pl.bn) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
+        (want_cm == 2 || pair_units >= max_pairs)) {
+        pl.cm = 2;
+        pl.tiles = cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
+        pl.units = pair_units;
+    }
     const int64_t total_units = pl.units * pl.splits;
     if (total_units > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED;
-    pl.grid = static_cast<int>(total_units < ctas ? total_units : ctas);
+    if (pl.cm == 2) {
+        int clusters = max_pairs;
+        if (cap > 0 && cap / 2 < clusters) clusters = static_cast<int>(cap / 2 > 0 ? cap / 2 : 1);
+        if (total_units < clusters) clusters = static_cast<int>(total_units);
+        pl.grid = 2 * clusters;
+    } else {
+        pl.grid = static_cast<int>(total_units < ctas ? total_units : ctas);
+    }
     pl.launches += 1;
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
     if (pl.ws_need > 0 && !aligned(c.ws, 256)) return GEMM_ERR_INVALID_ARG;
@@ -379,7 +405,7 @@ gemm_status_t run(const Call& c) {
     st = device_state(&d);
     if (st != GEMM_OK) return st;
     Plan pl;
-    st = make_plan(c, d->sm_count, pl);
+    st = make_plan(c, *d, pl);
     if (st != GEMM_OK) return st;
 
     if (pl.kernel == 3) {
@@ -440,13 +466,13 @@ gemm_status_t run(const Call& c) {
     st = encode_operand(&p.tmap_a, c.ab, pl.a, a_ptr, a_ld, a_stride, c.batch, TC_BLOCK_M, &a3);
     if (st != GEMM_OK) return st;
     st = encode_operand(&p.tmap_b, c.ab, pl.b, b_ptr, b_ld, b_stride, c.batch,
-                        static_cast<uint32_t>(pl.bn), &b3);
+                        static_cast<uint32_t>(pl.bn / pl.cm), &b3);
     if (st != GEMM_OK) return st;
     p.M = static_cast<int32_t>(pl.Mc);
     p.N = static_cast<int32_t>(pl.Nc);
     p.K = static_cast<int32_t>(c.K);
     p.batch = static_cast<int32_t>(c.batch);
-    p.num_pid_m = static_cast<int32_t>(cdiv(pl.Mc, TC_BLOCK_M));
+    p.num_pid_m = static_cast<int32_t>(cdiv(pl.Mc, TC_BLOCK_M * pl.cm));
     p.num_pid_n = static_cast<int32_t>(cdiv(pl.Nc, pl.bn));
     p.tiles_per_batch = static_cast<int32_t>(pl.tiles);
     p.splits = pl.splits;
@@ -474,7 +500,7 @@ gemm_status_t run(const Call& c) {
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
-    if (tc_launch(pl.bn, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (tc_launch(pl.bn, pl.cm, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
                                    c.stream) != cudaSuccess)
@@ -595,7 +621,7 @@ size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int6
                                    0.0f, nullptr, GEMM_EPI_NONE, split_k,
                                    const_cast<char*>(dummy), SIZE_MAX / 2, nullptr);
                 Plan pl;
-                if (make_plan(c, d->sm_count, pl) == GEMM_OK && pl.part_bytes > worst_part)
+                if (make_plan(c, *d, pl) == GEMM_OK && pl.part_bytes > worst_part)
                     worst_part = pl.part_bytes;
             }
     return static_cast<size_t>(round_up(pa * 2, 256) + round_up(pb * 2, 256)) +
@@ -655,7 +681,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     st = device_state(&d);
     if (st != GEMM_OK) return st;
     Plan pl;
-    st = make_plan(c, d->sm_count, pl);
+    st = make_plan(c, *d, pl);
     plan->kernel = pl.kernel;
     plan->block_m = pl.kernel == 1 ? TC_BLOCK_M : (pl.kernel == 2 ? 128 : 0);
     plan->block_n = pl.bn;
@@ -669,6 +695,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->group_m = pl.group_m;
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
+    plan->cluster_m = pl.cm;
     return st;
 }
 
@@ -690,6 +717,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_opt_test_stall.store(value);
             return GEMM_OK;
+        case GEMM_OPT_CLUSTER_M:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_cluster_m.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -700,6 +731,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_MAX_CTAS: return g_opt_max_ctas.load();
         case GEMM_OPT_TIMEOUT_US: return g_opt_timeout_us.load();
         case GEMM_OPT_TEST_STALL: return g_opt_test_stall.load();
+        case GEMM_OPT_CLUSTER_M: return g_opt_cluster_m.load();
     }
     return -1;
 }

@@ -59,7 +59,9 @@ struct TcParams {
 int tc_stages_for(int block_n);
 size_t tc_smem_bytes(int block_n);
 cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
-cudaError_t tc_launch(int block_n, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc_launch(int block_n, int cluster_m, const TcParams& p, int grid, cudaStream_t stream);
+bool tc_has_pair(int block_n);     // a two-CTA (cluster along M) variant exists
+int tc_max_pairs(int block_n);     // two-CTA clusters resident at once on this device
 
 struct SgemmParams {
     const float* A; int64_t lda; int64_t stride_a; int32_t a_row;

@@ -69,7 +69,11 @@ struct Unit {
     int b, split, pid_m, pid_n, kb0, kb1;
 };
 
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+// Work unit u -> (batch, K slice, tile).  With clusters of CM CTAs along M the
+// unit is a CM-tile-high slab and CTA `rank` of the cluster takes tile-row
+// pid_m * CM + rank of it.
+template <int CM>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, uint32_t rank) {
     const int per_batch = p.splits * p.tiles_per_batch;
     Unit w;
     w.b = u / per_batch;
@@ -77,6 +81,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
     w.split = r / p.tiles_per_batch;
     const int t = r - w.split * p.tiles_per_batch;
     tile_coord(t, p.num_pid_m, p.num_pid_n, p.group_m, w.pid_m, w.pid_n);
+    w.pid_m = w.pid_m * CM + static_cast<int>(rank);
     w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
     w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
     return w;
@@ -347,11 +352,14 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
 #pragma unroll
         for (int i = 0; i < EB; ++i) v[i] = __uint_as_float(r[i]);
         if (!partial) {
-            const float bias_row = (e.bias && e.bias_on_rows && row_ok) ? e.bias[row] : 0.0f;
+            // one pass per epilogue term, each branch taken once per chunk
+            if (e.alpha != 1.0f) {
 #pragma unroll
-            for (int i = 0; i < EB; ++i) {
-                float x = e.alpha * v[i];
-                if (need_c) {
+                for (int i = 0; i < EB; ++i) v[i] *= e.alpha;
+            }
+            if (need_c) {
+#pragma unroll
+                for (int i = 0; i < EB; ++i) {
                     float cval;
                     if (ES == 4) {
                         cval = __uint_as_float(craw[i]);
@@ -359,16 +367,26 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
                         const float2 f = unpack2_in(dt, craw[i >> 1]);
                         cval = (i & 1) ? f.y : f.x;
                     }
-                    x = fmaf(e.beta, cval, x);
+                    v[i] = fmaf(e.beta, cval, v[i]);
                 }
-                if (e.bias) {
-                    if (e.bias_on_rows)
-                        x += bias_row;
-                    else if (full || col0 + i < p.N)
-                        x += __ldg(e.bias + col0 + i);
+            }
+            if (e.bias) {
+                if (e.bias_on_rows) {
+                    const float bias_row = row_ok ? e.bias[row] : 0.0f;
+#pragma unroll
+                    for (int i = 0; i < EB; ++i) v[i] += bias_row;
+                } else if (full) {
+#pragma unroll
+                    for (int i = 0; i < EB; ++i) v[i] += __ldg(e.bias + col0 + i);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < EB; ++i)
+                        if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
                 }
-                if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
-                v[i] = x;
+            }
+            if (e.act == ACT_GELU_TANH) {
+#pragma unroll
+                for (int i = 0; i < EB; ++i) v[i] = gelu_tanh(v[i]);
             }
         }
         // the box written two chunks ago must have been read by its TMA store
@@ -418,9 +436,19 @@ __device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w
         asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
 }
 
-template <int BN>
+// CM = 1: one CTA per tile.  CM = 2: clusters of two CTAs stacked along M
+// share the B tile: each loads one half of it and multicasts that half into
+// both CTAs' shared memory, halving the B traffic from L2 per CTA.  A stage
+// is refilled only when both CTAs' MMAs have released it (the commits are
+// multicast to both CTAs' stage barriers).
+template <int BN, int CM>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<BN>;
+    static_assert(CM == 1 || CM == 2, "cluster of one or two CTAs along M");
+    const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
+    const int cta0 = static_cast<int>(blockIdx.x) / CM;  // cluster index
+    const int ncta = static_cast<int>(gridDim.x) / CM;   // clusters in the grid
+    constexpr uint16_t kPair = (1u << CM) - 1u;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -445,7 +473,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, CM);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8u * b, 1);
@@ -462,7 +490,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CM > 1)
+        cluster_sync();  // the peer's barriers are initialised before any multicast
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -474,8 +505,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             uint32_t phase = 0;
             uint32_t armed = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-                const Unit w = decode_unit(p, u);
+            for (int u = cta0; ok && u < p.total_units; u += ncta) {
+                const Unit w = decode_unit<CM>(p, u, rank);
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status,
                                    p.timeout_ns)) {
@@ -501,14 +532,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
                                       w.b, p.a_3d, pol);
                     }
-                    if (!p.b_mn) {
-                        load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol);
-                    } else {
-                        if constexpr (BN >= 64) {
+                    if constexpr (CM == 1) {
+                        if (!p.b_mn) {
+                            load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol);
+                        } else {
+                            if constexpr (BN >= 64) {
 #pragma unroll
-                            for (int h = 0; h < BN / 64; ++h)
-                                load_tile(&p.tmap_b, b_dst + h * 8192u, fb, w.pid_n * BN + 64 * h,
-                                          k0, w.b, p.b_3d, pol);
+                                for (int h = 0; h < BN / 64; ++h)
+                                    load_tile(&p.tmap_b, b_dst + h * 8192u, fb,
+                                              w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol);
+                            }
+                        }
+                    } else {
+                        // this CTA's half of the B tile, multicast to the pair
+                        constexpr int HALF = BN / CM;
+                        if (!p.b_mn) {
+                            const uint32_t dst = b_dst + rank * (HALF * 128u);
+                            const int y = w.pid_n * BN + static_cast<int>(rank) * HALF;
+                            if (p.b_3d)
+                                tma_load_3d_mc(dst, &p.tmap_b, fb, k0, y, w.b, kPair, pol);
+                            else
+                                tma_load_2d_mc(dst, &p.tmap_b, fb, k0, y, kPair, pol);
+                        } else {
+#pragma unroll
+                            for (int hh = 0; hh < HALF / 64; ++hh) {
+                                const int h = static_cast<int>(rank) * (HALF / 64) + hh;
+                                const uint32_t dst = b_dst + h * 8192u;
+                                const int x = w.pid_n * BN + 64 * h;
+                                if (p.b_3d)
+                                    tma_load_3d_mc(dst, &p.tmap_b, fb, x, k0, w.b, kPair, pol);
+                                else
+                                    tma_load_2d_mc(dst, &p.tmap_b, fb, x, k0, kPair, pol);
+                            }
                         }
                     }
                     ++armed;
@@ -539,8 +594,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
             const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
             const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
-            for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-                const Unit w = decode_unit(p, u);
+            for (int u = cta0; ok && u < p.total_units; u += ncta) {
+                const Unit w = decode_unit<CM>(p, u, rank);
                 if (!mbar_wait(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.status,
                                p.timeout_ns)) {
                     ok = false;
@@ -564,7 +619,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         umma_f16(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
-                    umma_commit(empty0 + 8u * stage);
+                    if constexpr (CM > 1)
+                        umma_commit_mc(empty0 + 8u * stage, kPair);
+                    else
+                        umma_commit(empty0 + 8u * stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -593,8 +651,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const uint64_t store_pol = l2_policy_evict_first();
         int abuf = 0;
         uint32_t aphase = 0;
-        for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
-            const Unit w = decode_unit(p, u);
+        for (int u = cta0; u < p.total_units; u += ncta) {
+            const Unit w = decode_unit<CM>(p, u, rank);
             prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
             int ok = 1;
             if (lane == 0)
@@ -640,22 +698,62 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (CM > 1)
+        cluster_sync();  // no CTA leaves while its peer may still write its shared memory
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
-template <int BN>
+template <int BN, int CM>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
-    tc_gemm_kernel<BN><<<grid, TC_THREADS, Cfg<BN>::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    if constexpr (CM == 1) {
+        tc_gemm_kernel<BN, 1><<<grid, TC_THREADS, Cfg<BN>::SMEM, stream>>>(p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, CM>, p);
+    }
 }
 
-template <int BN>
+template <int BN, int CM>
 cudaError_t prepare_bn() {
-    return cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(tc_gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(Cfg<BN>::SMEM));
+}
+
+// Clusters of CM CTAs that can be resident at once (0 on error).
+template <int BN, int CM>
+int max_clusters_bn() {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CM * 64);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, CM>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 }  // namespace
@@ -684,22 +782,45 @@ size_t tc_smem_bytes(int bn) {
 
 cudaError_t tc_prepare(int bn) {
     switch (bn) {
-        case 16: return prepare_bn<16>();
-        case 32: return prepare_bn<32>();
-        case 64: return prepare_bn<64>();
-        case 128: return prepare_bn<128>();
-        case 256: return prepare_bn<256>();
+        case 16: return prepare_bn<16, 1>();
+        case 32: return prepare_bn<32, 1>();
+        case 64: return prepare_bn<64, 1>();
+        case 128: {
+            const cudaError_t e = prepare_bn<128, 1>();
+            return e != cudaSuccess ? e : prepare_bn<128, 2>();
+        }
+        case 256: {
+            const cudaError_t e = prepare_bn<256, 1>();
+            return e != cudaSuccess ? e : prepare_bn<256, 2>();
+        }
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t tc_launch(int bn, const TcParams& p, int grid, cudaStream_t stream) {
+bool tc_has_pair(int bn) { return bn == 128 || bn == 256; }
+
+int tc_max_pairs(int bn) {
     switch (bn) {
-        case 16: return launch_bn<16>(p, grid, stream);
-        case 32: return launch_bn<32>(p, grid, stream);
-        case 64: return launch_bn<64>(p, grid, stream);
-        case 128: return launch_bn<128>(p, grid, stream);
-        case 256: return launch_bn<256>(p, grid, stream);
+        case 128: return max_clusters_bn<128, 2>();
+        case 256: return max_clusters_bn<256, 2>();
+    }
+    return 0;
+}
+
+cudaError_t tc_launch(int bn, int cm, const TcParams& p, int grid, cudaStream_t stream) {
+    if (cm == 2) {
+        switch (bn) {
+            case 128: return launch_bn<128, 2>(p, grid, stream);
+            case 256: return launch_bn<256, 2>(p, grid, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
+    switch (bn) {
+        case 16: return launch_bn<16, 1>(p, grid, stream);
+        case 32: return launch_bn<32, 1>(p, grid, stream);
+        case 64: return launch_bn<64, 1>(p, grid, stream);
+        case 128: return launch_bn<128, 1>(p, grid, stream);
+        case 256: return launch_bn<256, 1>(p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }
