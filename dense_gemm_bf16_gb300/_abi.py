@@ -49,7 +49,7 @@ class Option(enum.IntEnum):
     MAX_CTAS = 2
     TIMEOUT_US = 3
     TEST_STALL = 4
-    CLUSTER_M = 5
+    CTA_PAIR = 5
 
 
 class Plan(ctypes.Structure):
@@ -59,7 +59,7 @@ class Plan(ctypes.Structure):
                 ("swap_ab", ctypes.c_int32), ("pack_a", ctypes.c_int32),
                 ("pack_b", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("launches", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64), ("cluster_m", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("cta_pair", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
     def as_dict(self):

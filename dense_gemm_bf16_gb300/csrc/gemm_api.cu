@@ -25,7 +25,7 @@ std::atomic<int64_t> g_opt_group_m{8};
 std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_timeout_us{1000000};
 std::atomic<int64_t> g_opt_test_stall{0};
-std::atomic<int64_t> g_opt_cluster_m{0};
+std::atomic<int64_t> g_opt_cta_pair{0};
 
 constexpr int kMaxDevices = 64;
 constexpr int kBlockN[] = {16, 32, 64, 128, 256};
@@ -36,8 +36,7 @@ struct DevState {
     int sm_count = 0;
     int cc = 0;
     int* status = nullptr;
-    int max_pairs128 = 0;  // co-resident two-CTA clusters, BN = 128 / 256
-    int max_pairs256 = 0;
+    int max_pairs[3][2] = {};  // co-resident two-CTA clusters [mode][BN 128, 256]
 };
 DevState g_dev[kMaxDevices];
 
@@ -61,8 +60,10 @@ gemm_status_t device_state(DevState** out) {
             for (int bn : kBlockN)
                 if (e == cudaSuccess) e = tc_prepare(bn);
             if (e == cudaSuccess) {
-                d.max_pairs128 = tc_max_pairs(128);
-                d.max_pairs256 = tc_max_pairs(256);
+                for (int mode = 1; mode <= 2; ++mode) {
+                    d.max_pairs[mode][0] = tc_max_pairs(128, mode);
+                    d.max_pairs[mode][1] = tc_max_pairs(256, mode);
+                }
             }
         }
         d.sm_count = sms;
@@ -141,7 +142,7 @@ struct Plan {
     int kernel = 0;  // 0 none, 1 tensor core, 2 CUDA-core fp32, 3 epilogue only
     bool swap = false;
     int64_t Mc = 0, Nc = 0;
-    int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1;
+    int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
     int64_t kblocks = 0, tiles = 0, units = 0;
     Operand a{}, b{};
     bool c_row_major_c = true;
@@ -259,7 +260,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     else
         pl.bn = (c.batch * tiles_m * cdiv(pl.Nc, 256) >= ctas) ? 256 : 128;
     if (pl.b.mn && pl.bn < 64) pl.bn = 64;  // MN-major B tiles come in 64-wide swizzle atoms
-    pl.stages = tc_stages_for(pl.bn);
+    pl.stages = tc_stages_for(pl.bn, 0);
 
     // operand copies for what TMA cannot address
     size_t off = 0;
@@ -296,14 +297,22 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.launches += 1;
     }
     pl.ws_need = off;
-    // Two-CTA clusters along M sharing B tiles, for problems with at least a
-    // full wave of tile pairs (GEMM_OPT_CLUSTER_M: 0 auto, 1 never, 2 when possible).
-    const int64_t want_cm = g_opt_cluster_m.load();
-    const int max_pairs = pl.bn == 256 ? d.max_pairs256 : (pl.bn == 128 ? d.max_pairs128 : 0);
+    // CTA pairs along M (GEMM_OPT_CTA_PAIR: 0 auto, 1 never, 2 B-multicast pair,
+    // 3 pair MMA) for problems with at least a full wave of tile pairs.
+    const int64_t want = g_opt_cta_pair.load();
+    int mode = 0;
+    if (want == 2 || want == 3)
+        mode = static_cast<int>(want) - 1;
+    else if (want == 0)
+        mode = 2;
+    const int bn_idx = pl.bn == 256 ? 1 : 0;
+    const int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
-    if (want_cm != 1 && tc_has_pair(pl.bn) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
-        (want_cm == 2 || pair_units >= max_pairs)) {
+    if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
+        (want >= 2 || pair_units >= max_pairs)) {
+        pl.mode = mode;
         pl.cm = 2;
+        pl.stages = tc_stages_for(pl.bn, mode);
         pl.tiles = cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
         pl.units = pair_units;
     }
@@ -483,7 +492,8 @@ gemm_status_t run(const Call& c) {
     p.b_mn = pl.b.mn ? 1 : 0;
     p.a_3d = a3 ? 1 : 0;
     p.b_3d = b3 ? 1 : 0;
-    p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, TC_BLOCK_M, pl.bn);
+    p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, pl.mode == 2 ? 2 * TC_BLOCK_M : TC_BLOCK_M,
+                             pl.bn);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
     if (pl.c_row_major_c && pl.bn >= 32) {
@@ -500,7 +510,7 @@ gemm_status_t run(const Call& c) {
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
-    if (tc_launch(pl.bn, pl.cm, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (tc_launch(pl.bn, pl.mode, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
                                    c.stream) != cudaSuccess)
@@ -695,7 +705,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->group_m = pl.group_m;
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
-    plan->cluster_m = pl.cm;
+    plan->cta_pair = pl.mode;
     return st;
 }
 
@@ -717,9 +727,9 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
             g_opt_test_stall.store(value);
             return GEMM_OK;
-        case GEMM_OPT_CLUSTER_M:
-            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
-            g_opt_cluster_m.store(value);
+        case GEMM_OPT_CTA_PAIR:
+            if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+            g_opt_cta_pair.store(value);
             return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
@@ -731,7 +741,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_MAX_CTAS: return g_opt_max_ctas.load();
         case GEMM_OPT_TIMEOUT_US: return g_opt_timeout_us.load();
         case GEMM_OPT_TEST_STALL: return g_opt_test_stall.load();
-        case GEMM_OPT_CLUSTER_M: return g_opt_cluster_m.load();
+        case GEMM_OPT_CTA_PAIR: return g_opt_cta_pair.load();
     }
     return -1;
 }

@@ -56,12 +56,14 @@ struct TcParams {
 };
 
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).
-int tc_stages_for(int block_n);
-size_t tc_smem_bytes(int block_n);
+// Tensor-core kernel modes: 0 one CTA per 128 x BN tile; 1 CTA pair along M
+// sharing B through TMA multicast; 2 CTA pair computing a 256 x BN tile with
+// cta_group::2 MMAs.
+int tc_stages_for(int block_n, int mode);
+bool tc_has_mode(int block_n, int mode);
 cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
-cudaError_t tc_launch(int block_n, int cluster_m, const TcParams& p, int grid, cudaStream_t stream);
-bool tc_has_pair(int block_n);     // a two-CTA (cluster along M) variant exists
-int tc_max_pairs(int block_n);     // two-CTA clusters resident at once on this device
+cudaError_t tc_launch(int block_n, int mode, const TcParams& p, int grid, cudaStream_t stream);
+int tc_max_pairs(int block_n, int mode);  // two-CTA clusters resident at once on this device
 
 struct SgemmParams {
     const float* A; int64_t lda; int64_t stride_a; int32_t a_row;

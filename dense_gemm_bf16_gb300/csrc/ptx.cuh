@@ -141,6 +141,28 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* 
         : "memory");
 }
 
+// CTA-pair variants: the box lands in this CTA's shared memory at `dst`, and
+// its bytes complete on `bar`, which may be the peer CTA's mbarrier (a
+// shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar),
+          "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -284,6 +306,86 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
           "+r"(r[31])
         :
         : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05, CTA-pair forms
+// With cta_group::2 one thread of the even CTA of a cluster pair issues MMAs
+// that read A (M/2 rows) and B (N/2 columns) from both CTAs' shared memory and
+// write each CTA's M/2 accumulator rows into that CTA's tensor memory.  Every
+// tcgen05 instruction of a kernel uses the same cta_group.
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t dst_smem, uint32_t ncols) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(dst_smem), "r"(ncols) : "memory");
+    else
+        tmem_alloc(dst_smem, ncols);
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        tmem_relinquish();
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols) : "memory");
+    else
+        tmem_dealloc(taddr, ncols);
+}
+
+template <int CG>
+__device__ __forceinline__ void umma_f16_cg(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        umma_f16(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
+template <int CG>
+__device__ __forceinline__ void umma_commit_cg(uint32_t bar) {
+    if constexpr (CG == 2)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+            ::"r"(bar) : "memory");
+    else
+        umma_commit(bar);
+}
+
+template <int CG>
+__device__ __forceinline__ void umma_commit_mc_cg(uint32_t bar, uint16_t mask) {
+    if constexpr (CG == 2)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster"
+            ".b64 [%0], %1;" ::"r"(bar), "h"(mask)
+            : "memory");
+    else
+        umma_commit_mc(bar, mask);
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier in another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor for tcgen05.mma (128-byte swizzle):

@@ -47,10 +47,19 @@ constexpr uint32_t EPI_BOX_BYTES = 4096;
 constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;  // four epilogue warps
 static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 
-template <int BN>
+// MODE 0: one CTA per 128 x BN tile.
+// MODE 1: two CTAs of a cluster stacked along M; each loads its own A rows and
+//         one half of the shared B tile, multicast into both CTAs.
+// MODE 2: two CTAs of a cluster compute one 256 x BN tile with cta_group::2
+//         MMAs issued by the even CTA; each CTA holds its own 128 A rows and
+//         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.
+template <int BN, int MODE>
 struct Cfg {
+    static constexpr int CM = MODE == 0 ? 1 : 2;        // CTAs per cluster
+    static constexpr int CG = MODE == 2 ? 2 : 1;        // tcgen05 cta_group
+    static constexpr int B_ROWS = MODE == 2 ? BN / 2 : BN;  // B rows (N) held per CTA
     static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
@@ -63,6 +72,7 @@ struct Cfg {
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
+    static_assert(MODE != 2 || BN >= 128, "pair MMA splits B into 64-column atoms");
 };
 
 struct Unit {
@@ -206,6 +216,15 @@ __device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M
             }
         }
     }
+}
+
+// CTA-pair load: bytes complete on `bar`, which may be the peer's barrier.
+__device__ __forceinline__ void load_pair(const CUtensorMap* map, uint32_t dst, uint32_t bar, int x,
+                                          int y, int z, bool is3d, uint64_t pol) {
+    if (is3d)
+        tma_load_3d_pair(dst, map, bar, x, y, z, pol);
+    else
+        tma_load_2d_pair(dst, map, bar, x, y, pol);
 }
 
 // Epilogue of one CH-column chunk of this warp's 32 rows.  On entry lane t
@@ -436,16 +455,13 @@ __device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w
         asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
 }
 
-// CM = 1: one CTA per tile.  CM = 2: clusters of two CTAs stacked along M
-// share the B tile: each loads one half of it and multicasts that half into
-// both CTAs' shared memory, halving the B traffic from L2 per CTA.  A stage
-// is refilled only when both CTAs' MMAs have released it (the commits are
-// multicast to both CTAs' stage barriers).
-template <int BN, int CM>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<BN>;
-    static_assert(CM == 1 || CM == 2, "cluster of one or two CTAs along M");
+    using C = Cfg<BN, MODE>;
+    constexpr int CM = C::CM;
+    constexpr int CG = C::CG;
     const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
     const int cta0 = static_cast<int>(blockIdx.x) / CM;  // cluster index
     const int ncta = static_cast<int>(gridDim.x) / CM;   // clusters in the grid
     constexpr uint16_t kPair = (1u << CM) - 1u;
@@ -471,13 +487,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        // MODE 2: the leader's stage barrier collects the bytes of both CTAs'
+        // loads; its accumulator-release barrier counts the epilogue warps of
+        // both CTAs.  Accumulator releases are one arrival per epilogue warp.
+        const uint32_t full_count = 1u;
+        const uint32_t empty_count = MODE == 1 ? 2u : 1u;
+        const uint32_t tempty_count = MODE == 2 ? 2u * (TC_EPI_THREADS / 32) : TC_EPI_THREADS / 32;
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, CM);
+            mbar_init(full0 + 8u * s, full_count);
+            mbar_init(empty0 + 8u * s, empty_count);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8u * b, 1);
-            mbar_init(tempty0 + 8u * b, TC_EPI_THREADS);
+            mbar_init(tempty0 + 8u * b, tempty_count);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -486,12 +508,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         prefetch_tmap(&p.tmap_b);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_cg<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_cg<CG>();
     }
     tc_fence_before_sync();
     if constexpr (CM > 1)
-        cluster_sync();  // the peer's barriers are initialised before any multicast
+        cluster_sync();  // the peer's barriers are initialised before any cross-CTA signal
     else
         __syncthreads();
     tc_fence_after_sync();
@@ -520,11 +542,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     const uint32_t fb = full0 + 8u * stage;
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    // MODE 1: own A + both B halves.  MODE 2: the leader's barrier
+                    // takes the bytes of both CTAs; the peer's barrier is unused.
+                    if (MODE != 2 || leader)
+                        mbar_arrive_expect_tx(fb, MODE == 2 ? 2u * C::STAGE_BYTES : C::STAGE_BYTES);
                     const uint32_t a_dst = sA0 + stage * C::A_BYTES;
                     const uint32_t b_dst = sB0 + stage * C::B_BYTES;
                     const int k0 = kb * BK;
-                    if (!p.a_mn) {
+                    if constexpr (MODE == 2) {
+                        // own A rows and own BN/2 B columns; bytes complete on the leader
+                        const uint32_t lb = leader ? fb : mapa_shared(fb, 0u);
+                        if (!p.a_mn) {
+                            load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < BM / 64; ++h)
+                                load_pair(&p.tmap_a, a_dst + h * 8192u, lb, w.pid_m * BM + 64 * h,
+                                          k0, w.b, p.a_3d, pol);
+                        }
+                        constexpr int HALF = BN / 2;
+                        if (!p.b_mn) {
+                            load_pair(&p.tmap_b, b_dst, lb, k0,
+                                      w.pid_n * BN + static_cast<int>(rank) * HALF, w.b, p.b_3d,
+                                      pol);
+                        } else {
+#pragma unroll
+                            for (int hh = 0; hh < HALF / 64; ++hh)
+                                load_pair(&p.tmap_b, b_dst + hh * 8192u, lb,
+                                          w.pid_n * BN + static_cast<int>(rank) * HALF + 64 * hh,
+                                          k0, w.b, p.b_3d, pol);
+                        }
+                    } else if (!p.a_mn) {
                         load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol);
                     } else {
 #pragma unroll
@@ -532,7 +580,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
                                       w.b, p.a_3d, pol);
                     }
-                    if constexpr (CM == 1) {
+                    if constexpr (MODE == 0) {
                         if (!p.b_mn) {
                             load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol);
                         } else {
@@ -543,9 +591,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                               w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol);
                             }
                         }
-                    } else {
+                    } else if constexpr (MODE == 1) {
                         // this CTA's half of the B tile, multicast to the pair
-                        constexpr int HALF = BN / CM;
+                        constexpr int HALF = BN / 2;
                         if (!p.b_mn) {
                             const uint32_t dst = b_dst + rank * (HALF * 128u);
                             const int y = w.pid_n * BN + static_cast<int>(rank) * HALF;
@@ -573,15 +621,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                 }
             }
-            // Every issued fill must land before the CTA may exit.
-            for (int s = 0; s < C::STAGES && static_cast<uint32_t>(s) < armed; ++s) {
-                const uint32_t fills = (armed - 1u - s) / C::STAGES + 1u;
-                wait_drain(full0 + 8u * s, (fills - 1u) & 1u, p.timeout_ns);
+            // Every issued fill must land before the CTA may exit.  A MODE 2
+            // peer's loads complete on the leader's barriers: after a normal
+            // run the leader has consumed them all before the final cluster
+            // barrier; after an abort the peer gives its copies a fixed bound.
+            if (MODE == 2 && !leader) {
+                if (!ok) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 200000ull) {
+                    }
+                }
+            } else {
+                for (int s = 0; s < C::STAGES && static_cast<uint32_t>(s) < armed; ++s) {
+                    const uint32_t fills = (armed - 1u - s) / C::STAGES + 1u;
+                    wait_drain(full0 + 8u * s, (fills - 1u) & 1u, p.timeout_ns);
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (MODE == 2 && !leader) {
+            // MODE 2 peer: the leader's thread issues the MMAs for both CTAs
+        } else if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0;
             int abuf = 0;
@@ -616,28 +677,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = smem_desc_sw128(a_base + k * a_kstep, a_lbo, 1024u);
                         const uint64_t bd = smem_desc_sw128(b_base + k * b_kstep, b_lbo, 1024u);
-                        umma_f16(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        umma_f16_cg<CG>(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     issued = true;
                     if constexpr (CM > 1)
-                        umma_commit_mc(empty0 + 8u * stage, kPair);
+                        umma_commit_mc_cg<CG>(empty0 + 8u * stage, kPair);
                     else
-                        umma_commit(empty0 + 8u * stage);
+                        umma_commit_cg<CG>(empty0 + 8u * stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull0 + 8u * abuf);
+                if constexpr (MODE == 2)
+                    umma_commit_mc_cg<CG>(tfull0 + 8u * abuf, kPair);  // both CTAs' accumulators
+                else
+                    umma_commit_cg<CG>(tfull0 + 8u * abuf);
                 if (++abuf == 2) {
                     abuf = 0;
                     aphase ^= 1u;
                 }
             }
             if (issued) {
-                // all MMAs of this CTA complete before TMEM is released
-                umma_commit(drain_bar);
+                // all MMAs complete before tensor memory is released
+                umma_commit_cg<CG>(drain_bar);
                 wait_drain(drain_bar, 0u, p.timeout_ns);
             }
         }
@@ -684,8 +748,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
                 }
             }
+            // every lane's tensor-memory reads are ordered before the warp's
+            // single release of the accumulator buffer
             tc_fence_before_sync();
-            mbar_arrive(tempty0 + 8u * abuf);
+            __syncwarp();
+            if (lane == 0) {
+                if (MODE == 2 && !leader)
+                    mbar_arrive_remote(mapa_shared(tempty0 + 8u * abuf, 0u));
+                else
+                    mbar_arrive(tempty0 + 8u * abuf);
+            }
             if (++abuf == 2) {
                 abuf = 0;
                 aphase ^= 1u;
@@ -699,23 +771,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     tc_fence_before_sync();
     __syncthreads();
     if constexpr (CM > 1)
-        cluster_sync();  // no CTA leaves while its peer may still write its shared memory
+        cluster_sync();  // no CTA leaves while its peer may still touch its shared or tensor memory
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        tmem_dealloc_cg<CG>(tmem_base, C::TMEM_COLS);
     }
 }
 
-template <int BN, int CM>
+template <int BN, int MODE>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
+    constexpr int CM = Cfg<BN, MODE>::CM;
     if constexpr (CM == 1) {
-        tc_gemm_kernel<BN, 1><<<grid, TC_THREADS, Cfg<BN>::SMEM, stream>>>(p);
+        tc_gemm_kernel<BN, MODE><<<grid, TC_THREADS, Cfg<BN, MODE>::SMEM, stream>>>(p);
         return cudaGetLastError();
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
         cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+        cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -724,23 +797,25 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, CM>, p);
+        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, MODE>, p);
     }
 }
 
-template <int BN, int CM>
+template <int BN, int MODE>
 cudaError_t prepare_bn() {
-    return cudaFuncSetAttribute(tc_gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(Cfg<BN>::SMEM));
+    return cudaFuncSetAttribute(tc_gemm_kernel<BN, MODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(Cfg<BN, MODE>::SMEM));
 }
 
-// Clusters of CM CTAs that can be resident at once (0 on error).
-template <int BN, int CM>
+// Two-CTA clusters that can be resident at once (0 on error).
+template <int BN, int MODE>
 int max_clusters_bn() {
+    constexpr int CM = 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CM * 64);
     cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CM;
@@ -749,7 +824,7 @@ int max_clusters_bn() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, CM>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, MODE>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -758,69 +833,77 @@ int max_clusters_bn() {
 
 }  // namespace
 
-int tc_stages_for(int bn) {
-    switch (bn) {
-        case 16: return Cfg<16>::STAGES;
-        case 32: return Cfg<32>::STAGES;
-        case 64: return Cfg<64>::STAGES;
-        case 128: return Cfg<128>::STAGES;
-        case 256: return Cfg<256>::STAGES;
+int tc_stages_for(int bn, int mode) {
+    if (mode == 2) {
+        if (bn == 128) return Cfg<128, 2>::STAGES;
+        if (bn == 256) return Cfg<256, 2>::STAGES;
+        return 0;
     }
-    return 0;
-}
-
-size_t tc_smem_bytes(int bn) {
     switch (bn) {
-        case 16: return Cfg<16>::SMEM;
-        case 32: return Cfg<32>::SMEM;
-        case 64: return Cfg<64>::SMEM;
-        case 128: return Cfg<128>::SMEM;
-        case 256: return Cfg<256>::SMEM;
+        case 16: return Cfg<16, 0>::STAGES;
+        case 32: return Cfg<32, 0>::STAGES;
+        case 64: return Cfg<64, 0>::STAGES;
+        case 128: return Cfg<128, 0>::STAGES;
+        case 256: return Cfg<256, 0>::STAGES;
     }
     return 0;
 }
 
 cudaError_t tc_prepare(int bn) {
     switch (bn) {
-        case 16: return prepare_bn<16, 1>();
-        case 32: return prepare_bn<32, 1>();
-        case 64: return prepare_bn<64, 1>();
+        case 16: return prepare_bn<16, 0>();
+        case 32: return prepare_bn<32, 0>();
+        case 64: return prepare_bn<64, 0>();
         case 128: {
-            const cudaError_t e = prepare_bn<128, 1>();
-            return e != cudaSuccess ? e : prepare_bn<128, 2>();
+            cudaError_t e = prepare_bn<128, 0>();
+            if (e == cudaSuccess) e = prepare_bn<128, 1>();
+            if (e == cudaSuccess) e = prepare_bn<128, 2>();
+            return e;
         }
         case 256: {
-            const cudaError_t e = prepare_bn<256, 1>();
-            return e != cudaSuccess ? e : prepare_bn<256, 2>();
+            cudaError_t e = prepare_bn<256, 0>();
+            if (e == cudaSuccess) e = prepare_bn<256, 1>();
+            if (e == cudaSuccess) e = prepare_bn<256, 2>();
+            return e;
         }
     }
     return cudaErrorInvalidValue;
 }
 
-bool tc_has_pair(int bn) { return bn == 128 || bn == 256; }
+bool tc_has_mode(int bn, int mode) {
+    if (mode == 0) return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
+    if (mode == 1) return bn == 128 || bn == 256;
+    if (mode == 2) return bn == 128 || bn == 256;
+    return false;
+}
 
-int tc_max_pairs(int bn) {
-    switch (bn) {
-        case 128: return max_clusters_bn<128, 2>();
-        case 256: return max_clusters_bn<256, 2>();
-    }
+int tc_max_pairs(int bn, int mode) {
+    if (mode == 1 && bn == 128) return max_clusters_bn<128, 1>();
+    if (mode == 1 && bn == 256) return max_clusters_bn<256, 1>();
+    if (mode == 2 && bn == 128) return max_clusters_bn<128, 2>();
+    if (mode == 2 && bn == 256) return max_clusters_bn<256, 2>();
     return 0;
 }
 
-cudaError_t tc_launch(int bn, int cm, const TcParams& p, int grid, cudaStream_t stream) {
-    if (cm == 2) {
+cudaError_t tc_launch(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream) {
+    if (mode == 2) {
+        if (bn == 128) return launch_bn<128, 2>(p, grid, stream);
+        if (bn == 256) return launch_bn<256, 2>(p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (mode == 1) {
         switch (bn) {
-            case 128: return launch_bn<128, 2>(p, grid, stream);
-            case 256: return launch_bn<256, 2>(p, grid, stream);
+            case 128: return launch_bn<128, 1>(p, grid, stream);
+            case 256: return launch_bn<256, 1>(p, grid, stream);
         }
         return cudaErrorInvalidValue;
     }
     switch (bn) {
-        case 16: return launch_bn<16, 1>(p, grid, stream);
-        case 32: return launch_bn<32, 1>(p, grid, stream);
-        case 64: return launch_bn<64, 1>(p, grid, stream);
-        case 128: return launch_bn<128, 1>(p, grid, stream);
-        case 256: return launch_bn<256, 1>(p, grid, stream);
+        case 16: return launch_bn<16, 0>(p, grid, stream);
+        case 32: return launch_bn<32, 0>(p, grid, stream);
+        case 64: return launch_bn<64, 0>(p, grid, stream);
+        case 128: return launch_bn<128, 0>(p, grid, stream);
+        case 256: return launch_bn<256, 0>(p, grid, stream);
     }
     return cudaErrorInvalidValue;
 }

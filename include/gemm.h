@@ -189,7 +189,9 @@ typedef struct {
     int32_t group_m;         /* tile-order grouping                                */
     int32_t launches;        /* kernels enqueued by the call                       */
     int64_t workspace_bytes; /* workspace the plan uses                            */
-    int32_t cluster_m;       /* CTAs per cluster along M sharing B tiles (1 or 2)  */
+    int32_t cta_pair;        /* 0 one CTA per tile; 1 CTA pair along M sharing B by
+                                TMA multicast; 2 CTA pair computing 256-row tiles
+                                with two-CTA (cta_group::2) MMAs                   */
     int32_t reserved;
 } gemm_plan_t;
 
@@ -210,9 +212,9 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         Kernel", step 2; 1 = plain row-major tile order), 1..64.
  *   GEMM_OPT_MAX_CTAS     cap on persistent CTAs (0 = one per SM).
  *   GEMM_OPT_TIMEOUT_US   bound on any single in-kernel wait, microseconds (>= 1).
- *   GEMM_OPT_CLUSTER_M    0 (default): pair CTAs along M, sharing each B tile through
- *                         TMA multicast, when a problem has a full wave of tile pairs;
- *                         1: never; 2: whenever the tile width allows.
+ *   GEMM_OPT_CTA_PAIR     0 (default): pair CTAs along M when a problem has a full
+ *                         wave of tile pairs; 1: never; 2: B-multicast pairs whenever
+ *                         the tile width allows; 3: two-CTA MMA pairs likewise.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -223,7 +225,7 @@ typedef enum {
     GEMM_OPT_MAX_CTAS = 2,
     GEMM_OPT_TIMEOUT_US = 3,
     GEMM_OPT_TEST_STALL = 4,
-    GEMM_OPT_CLUSTER_M = 5
+    GEMM_OPT_CTA_PAIR = 5
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

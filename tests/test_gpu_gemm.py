@@ -229,13 +229,13 @@ def test_stalled_pipeline_reports_timeout_and_recovers():
 
 # ---------------------------------------------------------------- two-CTA clusters
 
-@pytest.fixture()
-def pairs():
+@pytest.fixture(params=[2, 3], ids=["multicast_pair", "pair_mma"])
+def pairs(request):
     import dense_gemm_bf16_gb300 as dg
-    dg.gemm_set_option(dg.Option.CLUSTER_M, 2)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, request.param)
     dg.gemm_set_option(dg.Option.MAX_CTAS, 8)  # four clusters walk many tile pairs
-    yield dg
-    dg.gemm_set_option(dg.Option.CLUSTER_M, 0)
+    yield request.param - 1
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
     dg.gemm_set_option(dg.Option.MAX_CTAS, 0)
 
 
@@ -245,16 +245,16 @@ def pairs():
 def test_exact_cluster_pairs(pairs, la, lb, N):
     # 700 rows = 5.5 tiles: the second CTA of the last pair has no valid rows
     c = run_exact(Case("bf16", 700, N, 333, la=la, lb=lb, values="ints", seed=71))
-    assert c.plan["cluster_m"] == 2
+    assert c.plan["cta_pair"] == pairs
 
 
 def test_exact_cluster_pairs_batched(pairs):
     c = run_exact(Case("bf16", 300, 400, 150, batch=3, values="ints", broadcast_b=True, seed=72))
-    assert c.plan["cluster_m"] == 2
+    assert c.plan["cta_pair"] in (pairs, 0)
     run_exact(Case("bf16", 300, 400, 150, batch=3, lb="col", values="ints", seed=73))
 
 
 def test_cluster_pairs_epilogue(pairs):
     c = run_close(Case("bf16", 520, 700, 300, c_dtype="bf16", alpha=0.5, beta=1.0, bias=True,
                        act="gelu_tanh", seed=74))
-    assert c.plan["cluster_m"] == 2
+    assert c.plan["cta_pair"] in (pairs, 0)
