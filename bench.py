@@ -7,13 +7,14 @@ fp32 N(0,1), fp32 accumulation, bf16 output; one call of the library's C ABI
 (``gemm_batched``) on the current stream.  Metric: TFLOPS = 2MNK / time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--rows FILE]
+                    [--rows FILE] [--row NAME]
 
 --impl reference times the CPU oracle (plain fp64 C, one host core) on a
 bounded slice of the same workload: the deliberately slow baseline.
 --rows FILE additionally measures the other library paths (SGEMM 4096^3,
 ragged 4097x3001x1000, split-K 256x256x65536, skinny 16x8192x8192, batched
-64x1024^3) and writes one JSON object per path to FILE.
+64x1024^3) and writes one JSON object per path to FILE; --row NAME runs only
+that path (--steps launches) and prints its JSON object.
 Multi-GPU runs (torchrun) run one independent replica per GPU (weak scaling).
 """
 from __future__ import annotations
@@ -49,6 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--rows", default=None, help="also measure the other paths into this file")
+    ap.add_argument("--row", default=None, choices=ROW_NAMES,
+                    help="run only this other path (--steps launches) and print its timing")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     a = ap.parse_args()
@@ -297,6 +300,9 @@ def main():
     device = torch.device("cuda", local if world > 1 else 0)
     dg.build()
     dg.lib()
+    if args.row:
+        print(json.dumps(measure_rows([args.row], device, reps=args.steps)[0]), flush=True)
+        return
 
     a, b_cm, bias = c3_host_inputs()
     hA = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -356,11 +362,9 @@ def main():
                                                                peaks["bf16_tflops"]),
                 "kernel": "tc_gemm_kernel<256>"}
 
-    rows_out = None
     if args.rows and rank == 0:
-        rows_out = measure_rows(args, device)
         with open(args.rows, "w") as f:
-            json.dump(rows_out, f, indent=1)
+            json.dump(measure_rows(ROW_NAMES, device), f, indent=1)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -387,132 +391,115 @@ def main():
 
 # ----------------------------------------------------------------------------- other paths
 
-def measure_rows(args, device):
-    """Times each other library path once (median of repeats), with its roofline."""
+ROW_NAMES = ("sgemm_4096", "ragged_4097x3001x1000", "splitk_256x256x65536",
+             "skinny_16x8192x8192", "batched_64x1024", "batched_64x1024_bcast")
+
+
+def build_row(name, device):
+    """Inputs and one call of a non-headline path.  Returns
+    (fn, flops, algorithmic_bytes, bound, plan, keepalive)."""
     import numpy as np
     import torch
 
     import datagen
     import dense_gemm_bf16_gb300 as dg
     peaks, _ = measured_peaks()
-    bw = peaks["hbm_gbs"]
-    out = []
     stream = torch.cuda.current_stream(device).cuda_stream
 
     def dev(x):
         return torch.from_numpy(np.ascontiguousarray(x)).to(device)
 
-    def bf16(seed, shape, scale=1.0):
-        return dev(datagen.to_bf16_bits(datagen.uniform(seed, shape) * scale).view(np.int16))
+    def bf16(seed, shape):
+        return dev(datagen.to_bf16_bits(datagen.uniform(seed, shape)).view(np.int16))
 
-    def timeit(fn, reps=20):
-        ts = []
+    def call16(batch, m, n, k, A, lda, sa, B, ldb, sb, C, ldc, sc, cdt, alpha, beta):
+        args_ = [0, batch, m, n, k, A.data_ptr(), lda, 0, sa, B.data_ptr(), ldb, 0, sb,
+                 C.data_ptr(), ldc, 0, sc, cdt, alpha, beta, None, 0, 0]
+        st, plan = dg.gemm_plan_query(*args_, 1 << 62)
+        if st != 0:
+            raise RuntimeError(dg.gemm_status_string(st))
+        wst = torch.empty(max(int(plan.workspace_bytes), 256), dtype=torch.uint8, device=device)
+
+        def fn():
+            s_ = dg.gemm_batched(*args_, wst.data_ptr(), wst.numel(), stream)
+            if s_ != 0:
+                raise RuntimeError(dg.gemm_status_string(s_))
+        return fn, plan.as_dict(), wst
+
+    if name == "sgemm_4096":
+        n = 4096
+        A = dev(datagen.to_f32(datagen.uniform(2001, (n, n))))
+        B = dev(datagen.to_f32(datagen.uniform(2002, (n, n))))
+        C = dev(datagen.to_f32(datagen.uniform(2003, (n, n))))
+
+        def fn():
+            s_ = dg.sgemm_f32(n, n, n, A.data_ptr(), n, 0, B.data_ptr(), n, 0, C.data_ptr(), n, 0,
+                              1.5, 0.5, None, 0, stream)
+            if s_ != 0:
+                raise RuntimeError(dg.gemm_status_string(s_))
+        return fn, 2.0 * n ** 3, 4 * n * n * 4, "alu", {"kernel": 2}, (A, B, C)
+    if name in ("ragged_4097x3001x1000", "splitk_256x256x65536", "skinny_16x8192x8192"):
+        m_, n_, k_ = {"ragged_4097x3001x1000": (4097, 3001, 1000),
+                      "splitk_256x256x65536": (256, 256, 65536),
+                      "skinny_16x8192x8192": (16, 8192, 8192)}[name]
+        seed = {"ragged_4097x3001x1000": 4001, "splitk_256x256x65536": 4011,
+                "skinny_16x8192x8192": 4021}[name]
+        A = bf16(seed, (m_, k_))
+        B = bf16(seed + 1, (k_, n_))
+        C = torch.empty((m_, n_), dtype=torch.float32, device=device)
+        fn, plan, wst = call16(1, m_, n_, k_, A, k_, 0, B, n_, 0, C, n_, 0, 2, 1.0, 0.0)
+        nbytes = (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4
+        flops = 2.0 * m_ * n_ * k_
+        bound = "tensor" if name.startswith("ragged") else "hbm"
+        return fn, flops, nbytes, bound, plan, (A, B, C, wst)
+    if name in ("batched_64x1024", "batched_64x1024_bcast"):
+        bt, s_ = 64, 1024
+        A = bf16(5001, (bt, s_, s_))
+        B = bf16(5002, (bt, s_, s_))
+        C = dev(datagen.to_bf16_bits(datagen.normal(5003, (bt, s_, s_))).view(np.int16))
+        sb = 0 if name.endswith("bcast") else s_ * s_
+        fn, plan, wst = call16(bt, s_, s_, s_, A, s_, s_ * s_, B, s_, sb, C, s_, s_ * s_, 0, 0.5,
+                               1.0)
+        nbytes = (bt * s_ * s_ + (bt if sb else 1) * s_ * s_ + 2 * bt * s_ * s_) * 2
+        flops = 2.0 * bt * s_ ** 3
+        t_comp = flops / (peaks["bf16_tflops"] * 1e12)
+        t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
+        return fn, flops, nbytes, "hbm" if t_mem > t_comp else "tensor", plan, (A, B, C, wst)
+    raise ValueError(f"unknown row {name!r}")
+
+
+def measure_rows(names, device, reps=20):
+    """Times each named path (median of `reps` launches after 3 warm-ups, CUDA
+    events on the launching stream) with its roofline fraction."""
+    import torch
+    peaks, _ = measured_peaks()
+    out = []
+    for name in names:
+        fn, flops, nbytes, bound, plan, keep = build_row(name, device)
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
+        ts = []
         for _ in range(reps):
-            s = torch.cuda.Event(enable_timing=True)
-            e = torch.cuda.Event(enable_timing=True)
-            s.record()
+            s_ = torch.cuda.Event(enable_timing=True)
+            e_ = torch.cuda.Event(enable_timing=True)
+            s_.record()
             fn()
-            e.record()
+            e_.record()
             torch.cuda.synchronize()
-            ts.append(s.elapsed_time(e))
-        return statistics.median(ts), min(ts)
-
-    def record(name, flops, bytes_, med, mn, bound, plan, extra=None):
+            ts.append(s_.elapsed_time(e_))
+        med, mn = statistics.median(ts), min(ts)
         r = {"path": name, "ms_median": med, "ms_min": mn, "tflops": flops / (med * 1e-3) / 1e12,
-             "gbs": bytes_ / (med * 1e-3) / 1e9, "algorithmic_bytes": bytes_, "flops": flops,
+             "gbs": nbytes / (med * 1e-3) / 1e9, "algorithmic_bytes": nbytes, "flops": flops,
              "bound": bound, "plan": plan}
         if bound == "hbm":
-            r["frac"] = r["gbs"] / bw
-            r["peak"] = bw
-        elif bound == "alu":
-            r["peak"] = None
+            r["peak"], r["frac"] = peaks["hbm_gbs"], r["gbs"] / peaks["hbm_gbs"]
+        elif bound == "tensor":
+            r["peak"], r["frac"] = peaks["bf16_tflops"], r["tflops"] / peaks["bf16_tflops"]
         else:
-            r["frac"] = r["tflops"] / peaks["bf16_tflops"]
-            r["peak"] = peaks["bf16_tflops"]
-        if extra:
-            r.update(extra)
+            r["peak"] = None  # fp32 FMA pipe: peak from SM count x 128 FFMA x 2 x clock
         out.append(r)
-
-    def call16(batch, m, n, k, A, lda, la, sa, B, ldb, lb, sb, C, ldc, sc, cdt, alpha, beta,
-               ws=None):
-        args_ = [0, batch, m, n, k, A.data_ptr(), lda, la, sa, B.data_ptr(), ldb, lb, sb,
-                 C.data_ptr(), ldc, 0, sc, cdt, alpha, beta, None, 0, 0]
-        st, plan = dg.gemm_plan_query(*args_, 1 << 62)
-        need = int(plan.workspace_bytes)
-        wst = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-
-        def fn():
-            s = dg.gemm_batched(*args_, wst.data_ptr(), wst.numel(), stream)
-            if s != 0:
-                raise RuntimeError(dg.gemm_status_string(s))
-        return fn, plan.as_dict()
-
-    # SGEMM 4096^3, alpha 1.5, beta 0.5
-    n = 4096
-    A = dev(datagen.to_f32(datagen.uniform(2001, (n, n))))
-    B = dev(datagen.to_f32(datagen.uniform(2002, (n, n))))
-    C = dev(datagen.to_f32(datagen.uniform(2003, (n, n))))
-
-    def sg():
-        s = dg.sgemm_f32(n, n, n, A.data_ptr(), n, 0, B.data_ptr(), n, 0, C.data_ptr(), n, 0, 1.5,
-                         0.5, None, 0, stream)
-        if s != 0:
-            raise RuntimeError(dg.gemm_status_string(s))
-    med, mn = timeit(sg)
-    record("sgemm_f32 4096^3", 2.0 * n ** 3, 4 * n * n * 4, med, mn, "alu",
-           {"kernel": 2, "block": "128x128x8"})
-    del A, B, C
-
-    # ragged 4097 x 3001 x 1000, unaligned ldb / ldc, fp32 out
-    m_, n_, k_ = 4097, 3001, 1000
-    A = bf16(4001, (m_, k_))
-    B = bf16(4002, (k_, n_))
-    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
-    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
-    med, mn = timeit(fn)
-    record("bf16 4097x3001x1000 -> f32", 2.0 * m_ * n_ * k_,
-           (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4, med, mn, "tensor", plan)
-    del A, B, C
-
-    # split-K 256 x 256 x 65536, fp32 out
-    m_, n_, k_ = 256, 256, 65536
-    A = bf16(4011, (m_, k_))
-    B = bf16(4012, (k_, n_))
-    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
-    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
-    med, mn = timeit(fn)
-    record("bf16 256x256x65536 split-K -> f32", 2.0 * m_ * n_ * k_,
-           (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4, med, mn, "hbm", plan)
-    del A, B, C
-
-    # skinny 16 x 8192 x 8192, fp32 out
-    m_, n_, k_ = 16, 8192, 8192
-    A = bf16(4021, (m_, k_))
-    B = bf16(4022, (k_, n_))
-    C = torch.empty((m_, n_), dtype=torch.float32, device=device)
-    fn, plan = call16(1, m_, n_, k_, A, k_, 0, 0, B, n_, 0, 0, C, n_, 0, 2, 1.0, 0.0)
-    med, mn = timeit(fn)
-    record("bf16 16x8192x8192 -> f32", 2.0 * m_ * n_ * k_, (m_ * k_ + k_ * n_) * 2 + m_ * n_ * 4,
-           med, mn, "hbm", plan)
-    del A, B, C
-
-    # batched 64 x 1024^3, alpha 0.5, beta 1, bf16 C in place; per-batch and broadcast B
-    bt, s = 64, 1024
-    A = bf16(5001, (bt, s, s))
-    Bp = bf16(5002, (bt, s, s))
-    C = dev(datagen.to_bf16_bits(datagen.normal(5003, (bt, s, s))).view(np.int16))
-    for label, Bt, sb in (("per-batch B", Bp, s * s), ("broadcast B", Bp, 0)):
-        fn, plan = call16(bt, s, s, s, A, s, 0, s * s, Bt, s, 0, sb, C, s, s * s, 0, 0.5, 1.0)
-        med, mn = timeit(fn)
-        nbytes = (bt * s * s + (bt if sb else 1) * s * s + 2 * bt * s * s) * 2
-        flops = 2.0 * bt * s ** 3
-        t_comp = flops / (peaks["bf16_tflops"] * 1e12)
-        t_mem = nbytes / (bw * 1e9)
-        record(f"batched 64x1024^3 {label}", flops, nbytes, med, mn,
-               "hbm" if t_mem > t_comp else "tensor", plan)
+        del keep
     return out
 
 

@@ -137,16 +137,32 @@ __device__ __forceinline__ void st_f<__nv_bfloat16>(__nv_bfloat16* p, float x) {
 template <>
 __device__ __forceinline__ void st_f<__half>(__half* p, float x) { *p = __float2half_rn(x); }
 
-__device__ __forceinline__ float finish(const Epilogue& e, float acc, float c_old, float bias) {
-    float x = e.alpha * acc;
-    if (e.beta != 0.0f) x = fmaf(e.beta, c_old, x);
-    x += bias;
-    if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
-    return x;
+// Epilogue terms on a run of H values (each branch taken once per run, so
+// unrequested terms never enter the unrolled loops).  cv: beta*C inputs,
+// bias_v: per-value bias (already 0 where there is none).
+template <int H>
+__device__ __forceinline__ void finish_run(const Epilogue& e, float (&v)[H], const float (&cv)[H],
+                                           const float (&bias_v)[H], bool has_c, bool has_bias) {
+    if (e.alpha != 1.0f) {
+#pragma unroll
+        for (int i = 0; i < H; ++i) v[i] *= e.alpha;
+    }
+    if (has_c) {
+#pragma unroll
+        for (int i = 0; i < H; ++i) v[i] = fmaf(e.beta, cv[i], v[i]);
+    }
+    if (has_bias) {
+#pragma unroll
+        for (int i = 0; i < H; ++i) v[i] += bias_v[i];
+    }
+    if (e.act == ACT_GELU_TANH) {
+#pragma unroll
+        for (int i = 0; i < H; ++i) v[i] = gelu_tanh(v[i]);
+    }
 }
 
 // Row-major C: lane t owns column col0 + t of the warp's 32 rows, read from
-// the staging tile.  All beta*C loads of the chunk are issued before any
+// the staging tile.  All beta*C loads of a half-chunk are issued before any
 // store (C is read and written in place, so the compiler may not reorder a
 // load above an earlier store by itself).
 template <int CH, typename T>
@@ -159,28 +175,32 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
     const int64_t left = M - row_base;
     const int nrows = left < 32 ? static_cast<int>(left) : 32;
     const int64_t ldc = e.ldc;
-    const float bias_col = (e.bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
+    const bool has_c = e.beta != 0.0f;
+    const bool has_bias = e.bias != nullptr;
+    const float bias_col = (has_bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
     T* const c0 =
         static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c + row_base * ldc + col;
 #pragma unroll 1
     for (int h = 0; h < 32; h += H) {
-        float cv[H];
-        if (e.beta != 0.0f) {
-            const T* q = c0 + h * ldc;
-#pragma unroll
-            for (int i = 0; i < H; ++i, q += ldc)
-                cv[i] = (h + i < nrows && col_ok) ? ld_f(q) : 0.0f;
-        }
-        T* q = c0 + h * ldc;
+        float v[H], cv[H], bv[H];
+        const T* q = c0 + h * ldc;
 #pragma unroll
         for (int i = 0; i < H; ++i, q += ldc) {
-            if (h + i < nrows && col_ok) {
-                const float b =
-                    (e.bias && e.bias_on_rows) ? e.bias[row_base + h + i] : bias_col;
-                st_f(q, finish(e, stage[(h + i) * STAGE_LD + lane],
-                               e.beta != 0.0f ? cv[i] : 0.0f, b));
-            }
+            const bool ok = h + i < nrows && col_ok;
+            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
+            v[i] = stage[(h + i) * STAGE_LD + lane];
+            bv[i] = bias_col;
         }
+        if (has_bias && e.bias_on_rows) {
+#pragma unroll
+            for (int i = 0; i < H; ++i)
+                bv[i] = h + i < nrows ? e.bias[row_base + h + i] : 0.0f;
+        }
+        finish_run<H>(e, v, cv, bv, has_c, has_bias);
+        T* o = c0 + h * ldc;
+#pragma unroll
+        for (int i = 0; i < H; ++i, o += ldc)
+            if (h + i < nrows && col_ok) st_f(o, v[i]);
     }
 }
 
@@ -196,25 +216,31 @@ __device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M
     const int left = N - col0;
     const int ncols = left < CH ? left : CH;
     const int64_t ldc = e.ldc;
-    const float bias_row = (e.bias && e.bias_on_rows) ? e.bias[row] : 0.0f;
+    const bool has_c = e.beta != 0.0f;
+    const bool has_bias = e.bias != nullptr;
+    const float bias_row = (has_bias && e.bias_on_rows) ? e.bias[row] : 0.0f;
     T* const c0 = static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c +
                   static_cast<int64_t>(col0) * ldc + row;
 #pragma unroll
     for (int h = 0; h < CH; h += H) {
-        float cv[H];
-        if (e.beta != 0.0f) {
-            const T* q = c0 + h * ldc;
-#pragma unroll
-            for (int i = 0; i < H; ++i, q += ldc) cv[i] = h + i < ncols ? ld_f(q) : 0.0f;
-        }
-        T* q = c0 + h * ldc;
+        float v[H], cv[H], bv[H];
+        const T* q = c0 + h * ldc;
 #pragma unroll
         for (int i = 0; i < H; ++i, q += ldc) {
-            if (h + i < ncols) {
-                const float b = (e.bias && !e.bias_on_rows) ? e.bias[col0 + h + i] : bias_row;
-                st_f(q, finish(e, __uint_as_float(r[h + i]), e.beta != 0.0f ? cv[i] : 0.0f, b));
-            }
+            const bool ok = h + i < ncols;
+            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
+            v[i] = __uint_as_float(r[h + i]);
+            bv[i] = bias_row;
         }
+        if (has_bias && !e.bias_on_rows) {
+#pragma unroll
+            for (int i = 0; i < H; ++i) bv[i] = h + i < ncols ? e.bias[col0 + h + i] : 0.0f;
+        }
+        finish_run<H>(e, v, cv, bv, has_c, has_bias);
+        T* o = c0 + h * ldc;
+#pragma unroll
+        for (int i = 0; i < H; ++i, o += ldc)
+            if (h + i < ncols) st_f(o, v[i]);
     }
 }
 
