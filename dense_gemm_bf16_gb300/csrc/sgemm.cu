@@ -2,8 +2,9 @@
 //
 // The register-tiled design of "2 . La GEMM, de zero a cuBLAS", sections
 // 2.3-2.8, for sm_103a:
-//   - a 128 x 128 output tile per CTA of 256 threads, K consumed 8 at a time
-//     (section 2.6: BM = BN = 128, BK = 8, TM = TN = 8);
+//   - a 128 x 128 output tile per CTA of 256 threads (section 2.6: BM = BN =
+//     128, TM = TN = 8), K consumed 16 at a time (the page's BK = 8 doubled
+//     to halve the synchronisations and tile loads per FMA);
 //   - each thread accumulates an 8 x 8 block as outer products of 8 values of
 //     A and 8 values of B per k: 16 shared-memory reads for 64 FMAs
 //     (section 2.6); its rows are {4ty..4ty+3, 64+4ty..64+4ty+3} and its
@@ -13,7 +14,10 @@
 //     contiguous and vectorisable (section 2.7);
 //   - global loads are float4 (LDG.128) when alignment allows (section 2.7)
 //     and land in the second of two shared buffers while the first is
-//     consumed (section 2.8), one __syncthreads per K step;
+//     consumed (section 2.8), one __syncthreads per K step; the operand
+//     fragments of step k+1 are also read while step k computes;
+//   - one CTA per SM (up to 255 registers, no spills), which also gives more
+//     waves and a smaller tail at 4096^2;
 //   - consecutive threads read consecutive addresses of each operand row
 //     (coalescing, section 2.3);
 //   - ragged M / N / K edges are masked with zero fill, and the store is
@@ -29,114 +33,82 @@
 namespace dg {
 namespace {
 
-constexpr int SBM = 128, SBN = 128, SBK = 8, STHREADS = 256;
+constexpr int SBM = 128, SBN = 128, SBK = 16, STHREADS = 256;
 
-template <bool A_ROW>
-__device__ __forceinline__ float4 load_a(const SgemmParams& p, const float* A, int m0, int k0,
-                                         int tid) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (A_ROW) {
-        // 128 rows x 8 k: thread -> row tid/2, k offset 4*(tid%2), float4 along k
-        const int m = m0 + (tid >> 1);
-        const int k = k0 + ((tid & 1) << 2);
-        if (m < p.M) {
-            const float* src = A + static_cast<int64_t>(m) * p.lda + k;
-            if (p.a_vec_ok && k + 3 < p.K) {
-                v = *reinterpret_cast<const float4*>(src);
-            } else {
-                if (k + 0 < p.K) v.x = src[0];
-                if (k + 1 < p.K) v.y = src[1];
-                if (k + 2 < p.K) v.z = src[2];
-                if (k + 3 < p.K) v.w = src[3];
+// Global -> register staging of one 128 x 16 A tile and one 16 x 128 B tile:
+// two float4 of each per thread.  Mapping (thread t):
+//   K-contiguous operand (row-major A, column-major B): row r = t % 64 (+64),
+//     k offset 4 * (t / 64); a warp covers 32 consecutive rows at one k
+//     offset, so the transposed shared-memory stores hit 32 distinct banks.
+//   MN-contiguous operand: k = t / 32 (+8), mn offset 4 * (t % 32); a warp
+//     reads 512 contiguous bytes and stores one float4 each.
+struct Frag4 {
+    float4 v[2];
+};
+
+template <bool KCONTIG>
+__device__ __forceinline__ Frag4 load_tile(const float* __restrict__ X, int64_t ld, int mn0,
+                                           int mn_ext, int k0, int K, bool vec_ok, int tid) {
+    Frag4 f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (KCONTIG) {
+            const int r = mn0 + (tid & 63) + 64 * h;
+            const int k = k0 + ((tid >> 6) << 2);
+            if (r < mn_ext) {
+                const float* src = X + static_cast<int64_t>(r) * ld + k;
+                if (vec_ok && k + 3 < K) {
+                    v = *reinterpret_cast<const float4*>(src);
+                } else {
+                    if (k + 0 < K) v.x = src[0];
+                    if (k + 1 < K) v.y = src[1];
+                    if (k + 2 < K) v.z = src[2];
+                    if (k + 3 < K) v.w = src[3];
+                }
+            }
+        } else {
+            const int k = k0 + (tid >> 5) + 8 * h;
+            const int r = mn0 + ((tid & 31) << 2);
+            if (k < K) {
+                const float* src = X + static_cast<int64_t>(k) * ld + r;
+                if (vec_ok && r + 3 < mn_ext) {
+                    v = *reinterpret_cast<const float4*>(src);
+                } else {
+                    if (r + 0 < mn_ext) v.x = src[0];
+                    if (r + 1 < mn_ext) v.y = src[1];
+                    if (r + 2 < mn_ext) v.z = src[2];
+                    if (r + 3 < mn_ext) v.w = src[3];
+                }
             }
         }
-    } else {
-        // column-major A: 8 k x 128 m, thread -> k tid/32, m offset 4*(tid%32), float4 along m
-        const int k = k0 + (tid >> 5);
-        const int m = m0 + ((tid & 31) << 2);
-        if (k < p.K) {
-            const float* src = A + static_cast<int64_t>(k) * p.lda + m;
-            if (p.a_vec_ok && m + 3 < p.M) {
-                v = *reinterpret_cast<const float4*>(src);
-            } else {
-                if (m + 0 < p.M) v.x = src[0];
-                if (m + 1 < p.M) v.y = src[1];
-                if (m + 2 < p.M) v.z = src[2];
-                if (m + 3 < p.M) v.w = src[3];
-            }
-        }
+        f.v[h] = v;
     }
-    return v;
+    return f;
 }
 
-template <bool B_ROW>
-__device__ __forceinline__ float4 load_b(const SgemmParams& p, const float* B, int n0, int k0,
-                                         int tid) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (B_ROW) {
-        // 8 k x 128 n: thread -> k tid/32, n offset 4*(tid%32), float4 along n
-        const int k = k0 + (tid >> 5);
-        const int n = n0 + ((tid & 31) << 2);
-        if (k < p.K) {
-            const float* src = B + static_cast<int64_t>(k) * p.ldb + n;
-            if (p.b_vec_ok && n + 3 < p.N) {
-                v = *reinterpret_cast<const float4*>(src);
-            } else {
-                if (n + 0 < p.N) v.x = src[0];
-                if (n + 1 < p.N) v.y = src[1];
-                if (n + 2 < p.N) v.z = src[2];
-                if (n + 3 < p.N) v.w = src[3];
-            }
+// Store a staged tile as S[k][mn] (k-major rows of 128 floats).
+template <bool KCONTIG>
+__device__ __forceinline__ void store_tile(float (*S)[SBM], const Frag4& f, int tid) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (KCONTIG) {
+            const int r = (tid & 63) + 64 * h;
+            const int k = (tid >> 6) << 2;
+            S[k + 0][r] = f.v[h].x;
+            S[k + 1][r] = f.v[h].y;
+            S[k + 2][r] = f.v[h].z;
+            S[k + 3][r] = f.v[h].w;
+        } else {
+            const int k = (tid >> 5) + 8 * h;
+            const int r = (tid & 31) << 2;
+            *reinterpret_cast<float4*>(&S[k][r]) = f.v[h];
         }
-    } else {
-        // column-major B: thread -> column n tid/2, k offset 4*(tid%2), float4 along k
-        const int n = n0 + (tid >> 1);
-        const int k = k0 + ((tid & 1) << 2);
-        if (n < p.N) {
-            const float* src = B + static_cast<int64_t>(n) * p.ldb + k;
-            if (p.b_vec_ok && k + 3 < p.K) {
-                v = *reinterpret_cast<const float4*>(src);
-            } else {
-                if (k + 0 < p.K) v.x = src[0];
-                if (k + 1 < p.K) v.y = src[1];
-                if (k + 2 < p.K) v.z = src[2];
-                if (k + 3 < p.K) v.w = src[3];
-            }
-        }
-    }
-    return v;
-}
-
-template <bool A_ROW>
-__device__ __forceinline__ void store_a(float (*As)[SBM], float4 v, int tid) {
-    if (A_ROW) {
-        const int m = tid >> 1, k = (tid & 1) << 2;
-        As[k + 0][m] = v.x;
-        As[k + 1][m] = v.y;
-        As[k + 2][m] = v.z;
-        As[k + 3][m] = v.w;
-    } else {
-        const int k = tid >> 5, m = (tid & 31) << 2;
-        *reinterpret_cast<float4*>(&As[k][m]) = v;
-    }
-}
-
-template <bool B_ROW>
-__device__ __forceinline__ void store_b(float (*Bs)[SBN], float4 v, int tid) {
-    if (B_ROW) {
-        const int k = tid >> 5, n = (tid & 31) << 2;
-        *reinterpret_cast<float4*>(&Bs[k][n]) = v;
-    } else {
-        const int n = tid >> 1, k = (tid & 1) << 2;
-        Bs[k + 0][n] = v.x;
-        Bs[k + 1][n] = v.y;
-        Bs[k + 2][n] = v.z;
-        Bs[k + 3][n] = v.w;
     }
 }
 
 template <bool A_ROW, bool B_ROW>
-__global__ void __launch_bounds__(STHREADS, 2) sgemm_kernel(const __grid_constant__ SgemmParams p) {
+__global__ void __launch_bounds__(STHREADS, 1) sgemm_kernel(const __grid_constant__ SgemmParams p) {
     __shared__ __align__(16) float As[2][SBK][SBM];
     __shared__ __align__(16) float Bs[2][SBK][SBN];
 
@@ -147,8 +119,8 @@ __global__ void __launch_bounds__(STHREADS, 2) sgemm_kernel(const __grid_constan
     int pid_m, pid_n;
     tile_coord(blockIdx.x - b * tiles, p.num_pid_m, p.num_pid_n, p.group_m, pid_m, pid_n);
     const int m0 = pid_m * SBM, n0 = pid_n * SBN;
-    const float* A = p.A + static_cast<int64_t>(b) * p.stride_a;
-    const float* B = p.B + static_cast<int64_t>(b) * p.stride_b;
+    const float* __restrict__ A = p.A + static_cast<int64_t>(b) * p.stride_a;
+    const float* __restrict__ B = p.B + static_cast<int64_t>(b) * p.stride_b;
 
     float acc[8][8];
 #pragma unroll
@@ -157,35 +129,48 @@ __global__ void __launch_bounds__(STHREADS, 2) sgemm_kernel(const __grid_constan
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     const int nk = (p.K + SBK - 1) / SBK;
-    float4 ra = load_a<A_ROW>(p, A, m0, 0, tid);
-    float4 rb = load_b<B_ROW>(p, B, n0, 0, tid);
-    store_a<A_ROW>(As[0], ra, tid);
-    store_b<B_ROW>(Bs[0], rb, tid);
+    // A is K-contiguous when row-major; B is K-contiguous when column-major
+    Frag4 fa = load_tile<A_ROW>(A, p.lda, m0, p.M, 0, p.K, p.a_vec_ok, tid);
+    Frag4 fb = load_tile<!B_ROW>(B, p.ldb, n0, p.N, 0, p.K, p.b_vec_ok, tid);
+    store_tile<A_ROW>(As[0], fa, tid);
+    store_tile<!B_ROW>(Bs[0], fb, tid);
     __syncthreads();
 
     for (int kt = 0; kt < nk; ++kt) {
         const int cur = kt & 1;
         const bool more = kt + 1 < nk;
         if (more) {
-            ra = load_a<A_ROW>(p, A, m0, (kt + 1) * SBK, tid);
-            rb = load_b<B_ROW>(p, B, n0, (kt + 1) * SBK, tid);
+            fa = load_tile<A_ROW>(A, p.lda, m0, p.M, (kt + 1) * SBK, p.K, p.a_vec_ok, tid);
+            fb = load_tile<!B_ROW>(B, p.ldb, n0, p.N, (kt + 1) * SBK, p.K, p.b_vec_ok, tid);
         }
+        // outer products; the float4 fragments of step k+1 are read while step
+        // k computes and are used in place (no copies between the load and the FMAs)
+        float4 xa0[2], xa1[2], xb0[2], xb1[2];
+        xa0[0] = *reinterpret_cast<const float4*>(&As[cur][0][ty * 4]);
+        xa1[0] = *reinterpret_cast<const float4*>(&As[cur][0][64 + ty * 4]);
+        xb0[0] = *reinterpret_cast<const float4*>(&Bs[cur][0][tx * 4]);
+        xb1[0] = *reinterpret_cast<const float4*>(&Bs[cur][0][64 + tx * 4]);
 #pragma unroll
         for (int k = 0; k < SBK; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
-            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
-            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][64 + tx * 4]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const int c = k & 1;
+            if (k + 1 < SBK) {
+                xa0[c ^ 1] = *reinterpret_cast<const float4*>(&As[cur][k + 1][ty * 4]);
+                xa1[c ^ 1] = *reinterpret_cast<const float4*>(&As[cur][k + 1][64 + ty * 4]);
+                xb0[c ^ 1] = *reinterpret_cast<const float4*>(&Bs[cur][k + 1][tx * 4]);
+                xb1[c ^ 1] = *reinterpret_cast<const float4*>(&Bs[cur][k + 1][64 + tx * 4]);
+            }
+            const float a[8] = {xa0[c].x, xa0[c].y, xa0[c].z, xa0[c].w,
+                                xa1[c].x, xa1[c].y, xa1[c].z, xa1[c].w};
+            const float bb[8] = {xb0[c].x, xb0[c].y, xb0[c].z, xb0[c].w,
+                                 xb1[c].x, xb1[c].y, xb1[c].z, xb1[c].w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
         }
         if (more) {
-            store_a<A_ROW>(As[cur ^ 1], ra, tid);
-            store_b<B_ROW>(Bs[cur ^ 1], rb, tid);
+            store_tile<A_ROW>(As[cur ^ 1], fa, tid);
+            store_tile<!B_ROW>(Bs[cur ^ 1], fb, tid);
         }
         __syncthreads();
     }
