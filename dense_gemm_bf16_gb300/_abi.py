@@ -50,6 +50,7 @@ class Option(enum.IntEnum):
     TIMEOUT_US = 3
     TEST_STALL = 4
     CTA_PAIR = 5
+    SWAP_AB = 6
 
 
 class Plan(ctypes.Structure):

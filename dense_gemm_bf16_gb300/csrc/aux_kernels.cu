@@ -19,7 +19,8 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// grid: x covers the contiguous dimension, y the rows (grid-stride), z the batch
+// grid: x covers the contiguous dimension, y groups of 8 rows (grid-stride), z the
+// batch.  Each thread issues the loads of its 8 rows before any store.
 __global__ void __launch_bounds__(kThreads) pack16_kernel(const uint16_t* __restrict__ src,
                                                           int64_t ld, int64_t stride, int64_t rows,
                                                           int64_t cols, uint16_t* __restrict__ dst,
@@ -29,7 +30,14 @@ __global__ void __launch_bounds__(kThreads) pack16_kernel(const uint16_t* __rest
     if (c >= cols) return;
     const uint16_t* s = src + b * stride + c;
     uint16_t* d = dst + b * rows * ld_dst + c;
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) d[r * ld_dst] = s[r * ld];
+    for (int64_t r0 = 8 * static_cast<int64_t>(blockIdx.y); r0 < rows; r0 += 8 * gridDim.y) {
+        uint16_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = r0 + u < rows ? s[(r0 + u) * ld] : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (r0 + u < rows) d[(r0 + u) * ld_dst] = v[u];
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) splitk_epi_kernel(const float* __restrict__ P,
@@ -56,6 +64,51 @@ __global__ void __launch_bounds__(kThreads) splitk_epi_kernel(const float* __res
     }
 }
 
+// Four consecutive elements of one row per thread (row-major C, N % 4 == 0):
+// 16-byte partial loads, eight slices in flight at a time, summed in slice order.
+__global__ void __launch_bounds__(kThreads) splitk_epi_vec4_kernel(const float* __restrict__ P,
+                                                                   int splits, int64_t batch,
+                                                                   int64_t M, int64_t N,
+                                                                   Epilogue e) {
+    const int64_t mn = M * N;
+    const int64_t total = batch * mn;
+    const int64_t total4 = total >> 2;
+    const float4* __restrict__ P4 = reinterpret_cast<const float4*>(P);
+    for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < total4;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int s = 0;
+        for (; s + 8 <= splits; s += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = P4[static_cast<int64_t>(s + u) * total4 + q];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                acc.x += v[u].x;
+                acc.y += v[u].y;
+                acc.z += v[u].z;
+                acc.w += v[u].w;
+            }
+        }
+        for (; s < splits; ++s) {
+            const float4 v = P4[static_cast<int64_t>(s) * total4 + q];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const int64_t idx = q << 2;
+        const int64_t b = idx / mn;
+        const int64_t rem = idx - b * mn;
+        const int64_t i = rem / N;
+        const int64_t j = rem - i * N;
+        epilogue_store(e, b, i, j + 0, acc.x);
+        epilogue_store(e, b, i, j + 1, acc.y);
+        epilogue_store(e, b, i, j + 2, acc.z);
+        epilogue_store(e, b, i, j + 3, acc.w);
+    }
+}
+
 int grid_for(int64_t total) {
     int64_t g = (total + kThreads - 1) / kThreads;
     if (g > 152 * 32) g = 152 * 32;  // grid-stride beyond a few waves of the 152 SMs
@@ -69,7 +122,8 @@ cudaError_t pack16_launch(const void* src, int64_t ld, int64_t stride, int64_t r
     if (batch <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
     if (batch > 65535) return cudaErrorInvalidValue;
     const int64_t gx = (cols + kThreads - 1) / kThreads;
-    const int64_t gy = rows < 4096 ? rows : 4096;
+    const int64_t groups = (rows + 7) / 8;
+    const int64_t gy = groups < 4096 ? groups : 4096;
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     pack16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
                          static_cast<unsigned>(batch)),
@@ -82,7 +136,13 @@ cudaError_t splitk_epilogue_launch(const float* partials, int splits, int64_t ba
                                    int64_t N, const Epilogue& e, cudaStream_t stream) {
     const int64_t total = batch * M * N;
     if (total <= 0) return cudaSuccess;
-    splitk_epi_kernel<<<grid_for(total), kThreads, 0, stream>>>(partials, splits, batch, M, N, e);
+    if (partials && e.c_row_major && (N & 3) == 0) {
+        splitk_epi_vec4_kernel<<<grid_for(total >> 2), kThreads, 0, stream>>>(partials, splits, batch,
+                                                                              M, N, e);
+    } else {
+        splitk_epi_kernel<<<grid_for(total), kThreads, 0, stream>>>(partials, splits, batch, M, N,
+                                                                    e);
+    }
     return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ std::atomic<int64_t> g_opt_max_ctas{0};
 std::atomic<int64_t> g_opt_timeout_us{1000000};
 std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cta_pair{0};
+std::atomic<int64_t> g_opt_swap_ab{0};
 
 constexpr int kMaxDevices = 64;
 constexpr int kBlockN[] = {16, 32, 64, 128, 256};
@@ -241,7 +242,8 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         return GEMM_OK;
     }
     pl.kernel = 1;
-    pl.swap = c.M <= 64 && c.N > c.M;
+    const int64_t swap_opt = g_opt_swap_ab.load();
+    pl.swap = swap_opt == 2 || (swap_opt == 0 && c.M <= 64 && c.N > c.M);
     const Operand opA{c.A, c.lda, c.sa, c.la == GEMM_COL_MAJOR, c.M, c.K};
     const Operand opB{c.B, c.ldb, c.sb, c.lb == GEMM_ROW_MAJOR, c.N, c.K};
     pl.a = pl.swap ? opB : opA;
@@ -731,6 +733,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
             g_opt_cta_pair.store(value);
             return GEMM_OK;
+        case GEMM_OPT_SWAP_AB:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_swap_ab.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -742,6 +748,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_TIMEOUT_US: return g_opt_timeout_us.load();
         case GEMM_OPT_TEST_STALL: return g_opt_test_stall.load();
         case GEMM_OPT_CTA_PAIR: return g_opt_cta_pair.load();
+        case GEMM_OPT_SWAP_AB: return g_opt_swap_ab.load();
     }
     return -1;
 }

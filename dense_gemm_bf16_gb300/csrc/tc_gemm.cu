@@ -738,7 +738,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         uint8_t* wbuf = epi_smem + (warp - 2) * EPI_WARP_BYTES;
         float* stage = reinterpret_cast<float*>(wbuf);
         uint32_t nbox = 0;
-        const uint64_t store_pol = l2_policy_evict_first();
+        // outputs leave L2 first; split-K partials stay for the reduction that follows
+        const uint64_t store_pol = p.partials ? l2_policy_evict_last() : l2_policy_evict_first();
         int abuf = 0;
         uint32_t aphase = 0;
         for (int u = cta0; u < p.total_units; u += ncta) {

@@ -215,6 +215,8 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *   GEMM_OPT_CTA_PAIR     0 (default): pair CTAs along M when a problem has a full
  *                         wave of tile pairs; 1: never; 2: B-multicast pairs whenever
  *                         the tile width allows; 3: two-CTA MMA pairs likewise.
+ *   GEMM_OPT_SWAP_AB      0 (default): compute C^T = B^T A^T when M <= 64 < N;
+ *                         1: never; 2: always.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -225,7 +227,8 @@ typedef enum {
     GEMM_OPT_MAX_CTAS = 2,
     GEMM_OPT_TIMEOUT_US = 3,
     GEMM_OPT_TEST_STALL = 4,
-    GEMM_OPT_CTA_PAIR = 5
+    GEMM_OPT_CTA_PAIR = 5,
+    GEMM_OPT_SWAP_AB = 6
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);
