@@ -52,6 +52,9 @@ def parse_args():
     ap.add_argument("--rows", default=None, help="also measure the other paths into this file")
     ap.add_argument("--row", default=None, choices=ROW_NAMES,
                     help="run only this other path (--steps launches) and print its timing")
+    ap.add_argument("--ablation", default=None,
+                    help="interleaved GROUP_M / L2-hint / CTA-pair ablation of the headline "
+                         "into this file (JSON)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     a = ap.parse_args()
@@ -303,6 +306,9 @@ def main():
     if args.row:
         print(json.dumps(measure_rows([args.row], device, reps=args.steps)[0]), flush=True)
         return
+    if args.ablation:
+        run_ablation(args, device)
+        return
 
     a, b_cm, bias = c3_host_inputs()
     hA = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -387,6 +393,63 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- ablation
+
+ABLATION = [  # (label, GEMM options)
+    ("group_m=8 (default)", {}),
+    ("group_m=1 (row-major tile order)", {"GROUP_M": 1}),
+    ("group_m=4", {"GROUP_M": 4}),
+    ("group_m=16", {"GROUP_M": 16}),
+    ("group_m=32", {"GROUP_M": 32}),
+    ("L2 hints: A evict-first, B evict-last", {"L2_HINTS": 1}),
+    ("L2 hints: A evict-last, B evict-first", {"L2_HINTS": 2}),
+    ("single-CTA tiles (no CTA pairs)", {"CTA_PAIR": 1}),
+    ("CTA pairs sharing B by multicast", {"CTA_PAIR": 2}),
+]
+
+
+def run_ablation(args, device, reps=None, launches=20):
+    """Headline workload under each setting.  Every repetition runs all
+    settings back to back, and the order rotates by one each repetition (a
+    Latin square): each setting takes each position once, so the power-cap
+    ramp within a repetition hits all settings alike."""
+    import numpy as np
+    import torch
+
+    import dense_gemm_bf16_gb300 as dg
+    a, b_cm, bias = c3_host_inputs()
+    dA = torch.from_numpy(a.view(np.int16)).to(device)
+    dB = torch.from_numpy(b_cm.view(np.int16)).to(device)
+    dbias = torch.from_numpy(bias).to(device)
+    dC = torch.empty((M, N), dtype=torch.int16, device=device)
+    gemm = Gemm(dA, dB, dbias, dC, torch.cuda.current_stream(device).cuda_stream)
+    defaults = {name: dg.gemm_get_option(dg.Option[name])
+                for name in ("GROUP_M", "L2_HINTS", "CTA_PAIR")}
+    times = {label: [] for label, _ in ABLATION}
+    reps = reps or len(ABLATION)
+    sampler = ClockSampler(device.index)
+    for r in range(reps):
+        order = ABLATION[r % len(ABLATION):] + ABLATION[:r % len(ABLATION)]
+        for label, opts in order:
+            for name, val in defaults.items():
+                dg.gemm_set_option(dg.Option[name], opts.get(name, val))
+            ms = time_steps(gemm, launches, 3)
+            times[label].append(ms / launches)
+    clocks = sampler.stop()
+    for name, val in defaults.items():
+        dg.gemm_set_option(dg.Option[name], val)
+    flops = 2.0 * M * N * K
+    out = {"workload": WORKLOAD, "reps": reps, "launches_per_rep": launches, "clocks": clocks,
+           "results": [{"setting": label, "ms_median": statistics.median(times[label]),
+                        "ms_all": times[label],
+                        "tflops": flops / (statistics.median(times[label]) * 1e-3) / 1e12}
+                       for label, _ in ABLATION]}
+    with open(args.ablation, "w") as f:
+        json.dump(out, f, indent=1)
+    for r in out["results"]:
+        print(f"{r['setting']:40s} {r['ms_median'] * 1000:8.1f} us {r['tflops']:8.1f} TFLOPS")
 
 
 # ----------------------------------------------------------------------------- other paths

@@ -51,6 +51,7 @@ class Option(enum.IntEnum):
     TEST_STALL = 4
     CTA_PAIR = 5
     SWAP_AB = 6
+    L2_HINTS = 7
 
 
 class Plan(ctypes.Structure):

@@ -27,6 +27,7 @@ std::atomic<int64_t> g_opt_timeout_us{1000000};
 std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cta_pair{0};
 std::atomic<int64_t> g_opt_swap_ab{0};
+std::atomic<int64_t> g_opt_l2_hints{0};
 
 constexpr int kMaxDevices = 64;
 constexpr int kBlockN[] = {16, 32, 64, 128, 256};
@@ -512,6 +513,7 @@ gemm_status_t run(const Call& c) {
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
+    p.l2_hints = static_cast<int32_t>(g_opt_l2_hints.load());
     if (tc_launch(pl.bn, pl.mode, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
@@ -737,6 +739,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_opt_swap_ab.store(value);
             return GEMM_OK;
+        case GEMM_OPT_L2_HINTS:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_l2_hints.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -749,6 +755,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_TEST_STALL: return g_opt_test_stall.load();
         case GEMM_OPT_CTA_PAIR: return g_opt_cta_pair.load();
         case GEMM_OPT_SWAP_AB: return g_opt_swap_ab.load();
+        case GEMM_OPT_L2_HINTS: return g_opt_l2_hints.load();
     }
     return -1;
 }

@@ -53,6 +53,7 @@ struct TcParams {
     int* status;             // device error word
     uint64_t timeout_ns;     // bound on every wait
     int32_t test_stall;      // test only: leave one stage unfilled
+    int32_t l2_hints;        // operand L2 policy: 0 normal; 1 A evict-first, B evict-last; 2 the reverse
 };
 
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).

@@ -548,7 +548,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_normal();
+            // L2 policies of the two operands ("Skill: Write a Triton GEMM Kernel",
+            // Kernel design rules: keep the operand reused across the tile group)
+            const uint64_t pol_normal = l2_policy_evict_normal();
+            const uint64_t pol_first = l2_policy_evict_first();
+            const uint64_t pol_last = l2_policy_evict_last();
+            const uint64_t pol_a = p.l2_hints == 1 ? pol_first : (p.l2_hints == 2 ? pol_last : pol_normal);
+            const uint64_t pol_b = p.l2_hints == 1 ? pol_last : (p.l2_hints == 2 ? pol_first : pol_normal);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0;
@@ -579,42 +585,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         // own A rows and own BN/2 B columns; bytes complete on the leader
                         const uint32_t lb = leader ? fb : mapa_shared(fb, 0u);
                         if (!p.a_mn) {
-                            load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol);
+                            load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
                         } else {
 #pragma unroll
                             for (int h = 0; h < BM / 64; ++h)
                                 load_pair(&p.tmap_a, a_dst + h * 8192u, lb, w.pid_m * BM + 64 * h,
-                                          k0, w.b, p.a_3d, pol);
+                                          k0, w.b, p.a_3d, pol_a);
                         }
                         constexpr int HALF = BN / 2;
                         if (!p.b_mn) {
                             load_pair(&p.tmap_b, b_dst, lb, k0,
                                       w.pid_n * BN + static_cast<int>(rank) * HALF, w.b, p.b_3d,
-                                      pol);
+                                      pol_b);
                         } else {
 #pragma unroll
                             for (int hh = 0; hh < HALF / 64; ++hh)
                                 load_pair(&p.tmap_b, b_dst + hh * 8192u, lb,
                                           w.pid_n * BN + static_cast<int>(rank) * HALF + 64 * hh,
-                                          k0, w.b, p.b_3d, pol);
+                                          k0, w.b, p.b_3d, pol_b);
                         }
                     } else if (!p.a_mn) {
-                        load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol);
+                        load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
                     } else {
 #pragma unroll
                         for (int h = 0; h < BM / 64; ++h)
                             load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
-                                      w.b, p.a_3d, pol);
+                                      w.b, p.a_3d, pol_a);
                     }
                     if constexpr (MODE == 0) {
                         if (!p.b_mn) {
-                            load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol);
+                            load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol_b);
                         } else {
                             if constexpr (BN >= 64) {
 #pragma unroll
                                 for (int h = 0; h < BN / 64; ++h)
                                     load_tile(&p.tmap_b, b_dst + h * 8192u, fb,
-                                              w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol);
+                                              w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol_b);
                             }
                         }
                     } else if constexpr (MODE == 1) {
@@ -624,9 +630,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             const uint32_t dst = b_dst + rank * (HALF * 128u);
                             const int y = w.pid_n * BN + static_cast<int>(rank) * HALF;
                             if (p.b_3d)
-                                tma_load_3d_mc(dst, &p.tmap_b, fb, k0, y, w.b, kPair, pol);
+                                tma_load_3d_mc(dst, &p.tmap_b, fb, k0, y, w.b, kPair, pol_b);
                             else
-                                tma_load_2d_mc(dst, &p.tmap_b, fb, k0, y, kPair, pol);
+                                tma_load_2d_mc(dst, &p.tmap_b, fb, k0, y, kPair, pol_b);
                         } else {
 #pragma unroll
                             for (int hh = 0; hh < HALF / 64; ++hh) {
@@ -634,9 +640,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                 const uint32_t dst = b_dst + h * 8192u;
                                 const int x = w.pid_n * BN + 64 * h;
                                 if (p.b_3d)
-                                    tma_load_3d_mc(dst, &p.tmap_b, fb, x, k0, w.b, kPair, pol);
+                                    tma_load_3d_mc(dst, &p.tmap_b, fb, x, k0, w.b, kPair, pol_b);
                                 else
-                                    tma_load_2d_mc(dst, &p.tmap_b, fb, x, k0, kPair, pol);
+                                    tma_load_2d_mc(dst, &p.tmap_b, fb, x, k0, kPair, pol_b);
                             }
                         }
                     }

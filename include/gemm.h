@@ -217,6 +217,8 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         the tile width allows; 3: two-CTA MMA pairs likewise.
  *   GEMM_OPT_SWAP_AB      0 (default): compute C^T = B^T A^T when M <= 64 < N;
  *                         1: never; 2: always.
+ *   GEMM_OPT_L2_HINTS     L2 policy of the tensor-core operand loads: 0 (default) normal;
+ *                         1: A evict-first, B evict-last; 2: A evict-last, B evict-first.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -228,7 +230,8 @@ typedef enum {
     GEMM_OPT_TIMEOUT_US = 3,
     GEMM_OPT_TEST_STALL = 4,
     GEMM_OPT_CTA_PAIR = 5,
-    GEMM_OPT_SWAP_AB = 6
+    GEMM_OPT_SWAP_AB = 6,
+    GEMM_OPT_L2_HINTS = 7
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);
