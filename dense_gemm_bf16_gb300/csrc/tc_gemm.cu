@@ -352,42 +352,51 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
     const int zc = partial ? w.split * p.batch + w.b : w.b;
     // swizzle: piece j of row r sits at piece j ^ ((r * RB / 128) % NJ)
     const int swz = ((lane * RB) >> 7) & (NJ - 1);
+    const bool need_c = !partial && e.beta != 0.0f && row_ok;
+    const char* crow =
+        need_c ? static_cast<const char*>(e.C) + (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc) * ES
+               : nullptr;
+    // beta*C of this thread's row segment for one chunk, as raw output words
+    auto load_c = [&](int col0, uint32_t (&craw)[NW]) {
+        if (col0 + EB <= p.N) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const uint4 t = reinterpret_cast<const uint4*>(crow + static_cast<int64_t>(col0) * ES)[j];
+                craw[4 * j + 0] = t.x;
+                craw[4 * j + 1] = t.y;
+                craw[4 * j + 2] = t.z;
+                craw[4 * j + 3] = t.w;
+            }
+        } else {
+            const char* src = crow + static_cast<int64_t>(col0) * ES;
+            const int nvalid = p.N - col0;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) craw[i] = 0u;
+#pragma unroll
+            for (int i = 0; i < EB; ++i) {
+                if (i < nvalid) {
+                    if (ES == 4) {
+                        craw[i] = reinterpret_cast<const uint32_t*>(src)[i];
+                    } else {
+                        const uint32_t h = reinterpret_cast<const uint16_t*>(src)[i];
+                        craw[i >> 1] |= (i & 1) ? (h << 16) : h;
+                    }
+                }
+            }
+        }
+    };
+    // the loads for chunk c+1 are issued before chunk c is computed
+    uint32_t craw[NW], craw_next[NW];
+    if (need_c) load_c(w.pid_n * BN, craw_next);
 #pragma unroll 1
     for (int c = 0; c < BN / EB; ++c) {
         const int col0 = w.pid_n * BN + c * EB;
         if (col0 >= p.N) break;
         const bool full = col0 + EB <= p.N;
-        // beta*C of this thread's row segment (issued before the TMEM read)
-        uint32_t craw[NW];
-        const bool need_c = !partial && e.beta != 0.0f && row_ok;
         if (need_c) {
-            const char* src = static_cast<const char*>(e.C) +
-                              (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc + col0) * ES;
-            if (full) {
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) {
-                    const uint4 t = reinterpret_cast<const uint4*>(src)[j];
-                    craw[4 * j + 0] = t.x;
-                    craw[4 * j + 1] = t.y;
-                    craw[4 * j + 2] = t.z;
-                    craw[4 * j + 3] = t.w;
-                }
-            } else {
-                const int nvalid = p.N - col0;
-#pragma unroll
-                for (int i = 0; i < NW; ++i) craw[i] = 0u;
-#pragma unroll
-                for (int i = 0; i < EB; ++i) {
-                    if (i < nvalid) {
-                        if (ES == 4) {
-                            craw[i] = reinterpret_cast<const uint32_t*>(src)[i];
-                        } else {
-                            const uint32_t h = reinterpret_cast<const uint16_t*>(src)[i];
-                            craw[i >> 1] |= (i & 1) ? (h << 16) : h;
-                        }
-                    }
-                }
-            }
+            for (int i = 0; i < NW; ++i) craw[i] = craw_next[i];
+            if (c + 1 < BN / EB && col0 + EB < p.N) load_c(col0 + EB, craw_next);
         }
         // accumulators: 32 consecutive TMEM columns of this lane's row
         uint32_t r[32];
@@ -750,7 +759,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         uint32_t aphase = 0;
         for (int u = cta0; u < p.total_units; u += ncta) {
             const Unit w = decode_unit<CM>(p, u, rank);
-            prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
+            if (u == cta0)  // first unit: its own C; afterwards one unit ahead
+                prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
+            if (u + ncta < p.total_units) {
+                const Unit wn = decode_unit<CM>(p, u + ncta, rank);
+                prefetch_c_tile<BN>(p, wn, static_cast<int64_t>(wn.pid_m) * BM + q * 32 + lane);
+            }
             int ok = 1;
             if (lane == 0)
                 ok = mbar_wait(tfull0 + 8u * abuf, aphase, abort_flag, p.status, p.timeout_ns) ? 1
