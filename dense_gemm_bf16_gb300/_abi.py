@@ -52,6 +52,7 @@ class Option(enum.IntEnum):
     CTA_PAIR = 5
     SWAP_AB = 6
     L2_HINTS = 7
+    STREAM_K = 8
 
 
 class Plan(ctypes.Structure):
@@ -62,7 +63,7 @@ class Plan(ctypes.Structure):
                 ("pack_b", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("cta_pair", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -28,6 +28,12 @@ std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cta_pair{0};
 std::atomic<int64_t> g_opt_swap_ab{0};
 std::atomic<int64_t> g_opt_l2_hints{0};
+std::atomic<int64_t> g_opt_stream_k{0};
+// stream-K flag values: one fresh 64-bit value per launch (stale or garbage
+// workspace contents never equal it)
+std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
+                                           static_cast<unsigned long long>(
+                                               reinterpret_cast<uintptr_t>(&g_opt_group_m))};
 
 constexpr int kMaxDevices = 64;
 constexpr int kBlockN[] = {16, 32, 64, 128, 256};
@@ -145,6 +151,10 @@ struct Plan {
     bool swap = false;
     int64_t Mc = 0, Nc = 0;
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
+    int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
+    int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
+    int64_t dp_units = 0, sk_iters = 0;
+    size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0;
     int64_t kblocks = 0, tiles = 0, units = 0;
     Operand a{}, b{};
     bool c_row_major_c = true;
@@ -328,6 +338,68 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.grid = 2 * clusters;
     } else {
         pl.grid = static_cast<int>(total_units < ctas ? total_units : ctas);
+    }
+    // Stream-K ("2 . La GEMM, de zero a cuBLAS", section 2.10): when whole-unit
+    // waves would leave clusters idle in the last one, the last units are cut
+    // along K.  GEMM_OPT_STREAM_K: 0 auto, 1 never, 2 contiguous form, 3 split form
+    // (both forced whenever a partial last wave follows at least one full wave).
+    const int64_t want_sk = g_opt_stream_k.load();
+    const int64_t P = pl.grid / pl.cm;
+    if (want_sk != 1 && pl.splits == 1 && P > 0 && pl.units > P && pl.units % P != 0 &&
+        pl.kblocks >= 2) {
+        const int64_t W = pl.units / P, r = pl.units % P;
+        // split form: each of the r last units becomes S pieces of at least
+        // kMinPiece K blocks, one per cluster, all starting together so that
+        // concurrent clusters keep reading the same K slices of A and B; the
+        // piece that finishes a unit adds the others' partials one by one, so
+        // S stays small
+        constexpr int64_t kMinPiece = 4, kMaxSplit = 4;
+        int64_t S = P / r;
+        if (S > kMaxSplit) S = kMaxSplit;
+        if (S > pl.kblocks / kMinPiece) S = pl.kblocks / kMinPiece;
+        int form = 0;
+        if (want_sk == 2) {
+            form = 1;
+        } else if (want_sk == 3) {
+            form = S >= 2 ? 2 : 0;
+        } else if (S >= 2) {
+            // Cost model in K-block times: the last wave shrinks from kblocks to
+            // kblocks / S; each cut unit costs one extra epilogue for the partial
+            // and half of one per partial added.  An epilogue is about 10 K
+            // blocks of main loop with 128 x 256 tiles; kEpi = 20 also covers
+            // what the measured gains fell short of that (a partial last wave
+            // of whole tiles runs faster than a full one), so that auto picks
+            // the split form only where it measured a gain (K >= 4096).
+            constexpr double kEpi = 20.0;
+            const double gain = static_cast<double>(pl.kblocks) * (1.0 - 1.0 / S);
+            const double cost = kEpi * (1.0 + 0.5 * static_cast<double>(S - 1));
+            if (gain > cost) form = 2;
+        }
+        if (form != 0) {
+            const int64_t nslots = form == 1 ? P : r * (S - 1);
+            const size_t slots = static_cast<size_t>(nslots) * pl.cm * TC_BLOCK_M * pl.bn * 4;
+            const size_t flags = static_cast<size_t>(nslots) * pl.cm * 4 * 8;
+            const size_t need = static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256)) +
+                                static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
+            if (c.ws != nullptr && off + need <= c.ws_bytes) {
+                pl.sk = form;
+                if (form == 1) {
+                    pl.dp_per_cluster = static_cast<int>(W - 1);
+                    pl.dp_units = (W - 1) * P;
+                    pl.sk_iters = (pl.units - pl.dp_units) * pl.kblocks;
+                } else {
+                    pl.dp_per_cluster = static_cast<int>(W);
+                    pl.dp_units = W * P;
+                    pl.sk_split = static_cast<int>(S);
+                    pl.sk_tiles = static_cast<int>(r);
+                }
+                pl.sk_off = off;
+                pl.sk_bytes = slots;
+                pl.sk_flags_off = off + static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256));
+                off += need;
+                pl.ws_need = off;
+            }
+        }
     }
     pl.launches += 1;
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
@@ -514,6 +586,16 @@ gemm_status_t run(const Call& c) {
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
     p.l2_hints = static_cast<int32_t>(g_opt_l2_hints.load());
+    if (pl.sk) {
+        p.dp_per_cluster = pl.dp_per_cluster;
+        p.dp_units = static_cast<int32_t>(pl.dp_units);
+        p.sk_iters = pl.sk_iters;
+        p.sk_split = pl.sk_split;
+        p.sk_tiles = pl.sk_tiles;
+        p.sk_partials = reinterpret_cast<float*>(ws + pl.sk_off);
+        p.sk_flags = reinterpret_cast<unsigned long long*>(ws + pl.sk_flags_off);
+        p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
+    }
     if (tc_launch(pl.bn, pl.mode, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
@@ -638,8 +720,12 @@ size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int6
                 if (make_plan(c, *d, pl) == GEMM_OK && pl.part_bytes > worst_part)
                     worst_part = pl.part_bytes;
             }
+    // stream-K slots and flags: one 128 x 256 fp32 tile per CTA of the grid, plus flags
+    const int64_t sk = round_up(static_cast<int64_t>(d->sm_count) * TC_BLOCK_M * 256 * 4, 256) +
+                       round_up(static_cast<int64_t>(d->sm_count) * 4 * 8, 256);
     return static_cast<size_t>(round_up(pa * 2, 256) + round_up(pb * 2, 256)) +
-           static_cast<size_t>(round_up(static_cast<int64_t>(worst_part), 256));
+           static_cast<size_t>(round_up(static_cast<int64_t>(worst_part), 256)) +
+           static_cast<size_t>(sk);
 }
 
 const char* gemm_status_string(gemm_status_t s) {
@@ -710,6 +796,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
     plan->cta_pair = pl.mode;
+    plan->stream_k = pl.sk;
     return st;
 }
 
@@ -743,6 +830,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_opt_l2_hints.store(value);
             return GEMM_OK;
+        case GEMM_OPT_STREAM_K:
+            if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+            g_opt_stream_k.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -756,6 +847,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_CTA_PAIR: return g_opt_cta_pair.load();
         case GEMM_OPT_SWAP_AB: return g_opt_swap_ab.load();
         case GEMM_OPT_L2_HINTS: return g_opt_l2_hints.load();
+        case GEMM_OPT_STREAM_K: return g_opt_stream_k.load();
     }
     return -1;
 }

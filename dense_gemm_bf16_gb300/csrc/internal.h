@@ -54,6 +54,23 @@ struct TcParams {
     uint64_t timeout_ns;     // bound on every wait
     int32_t test_stall;      // test only: leave one stage unfilled
     int32_t l2_hints;        // operand L2 policy: 0 normal; 1 A evict-first, B evict-last; 2 the reverse
+    // Stream-K.  Every cluster first takes dp_per_cluster whole units round
+    // robin; the units from dp_units on are then cut along K, in one of two forms.
+    // Contiguous (sk_iters > 0): their K blocks are split evenly over the
+    // clusters, each taking one contiguous range; a unit cut at a cluster
+    // boundary is finished by the cluster that holds its first K blocks, after
+    // the next cluster has left its fp32 partial in the slot of that boundary.
+    // Split (sk_split > 0): each of the sk_tiles last units is cut into sk_split
+    // equal K pieces, one per cluster, so that all pieces start together; piece 0
+    // finishes the tile after the other sk_split - 1 have left their partials.
+    int32_t dp_per_cluster;
+    int32_t dp_units;
+    int64_t sk_iters;        // K blocks of the contiguous form (0: off)
+    int32_t sk_split;        // pieces per unit of the split form (0: off)
+    int32_t sk_tiles;        // units cut in the split form
+    float* sk_partials;      // [slot][cta rank][128][BN] fp32, lane-interleaved per warp
+    unsigned long long* sk_flags;  // [slot][cta rank][epilogue warp]: epoch when published
+    unsigned long long sk_epoch;   // this launch's flag value
 };
 
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).

@@ -77,7 +77,13 @@ struct Cfg {
 
 struct Unit {
     int b, split, pid_m, pid_n, kb0, kb1;
+    int kind;  // UNIT_FULL, or a stream-K piece: UNIT_HEAD (finishes the tile) / UNIT_TAIL
+    // stream-K partial slots: a TAIL publishes into slot `slot`; a HEAD adds the
+    // `nslots` partials in slots slot .. slot + nslots - 1
+    int slot, nslots;
 };
+
+enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
 
 // Work unit u -> (batch, K slice, tile).  With clusters of CM CTAs along M the
 // unit is a CM-tile-high slab and CTA `rank` of the cluster takes tile-row
@@ -95,6 +101,86 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, uint32_t r
     w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
     w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
     return w;
+}
+
+// The sequence of work items of one cluster; every role of the CTA walks it.
+struct WorkIter {
+    int cluster;      // this cluster's index
+    int unit_rr;      // next round-robin unit
+    int rr_left;      // round-robin units left
+    int64_t it, end;  // stream-K K-block range (contiguous form)
+    int piece;        // split form: this cluster's piece of the last wave, or -1
+};
+
+__device__ __forceinline__ WorkIter work_begin(const TcParams& p, int cta0, int ncta) {
+    WorkIter s;
+    s.cluster = cta0;
+    s.unit_rr = cta0;
+    s.it = s.end = 0;
+    s.piece = -1;
+    if (p.sk_iters > 0) {
+        s.rr_left = p.dp_per_cluster;
+        s.it = p.sk_iters * cta0 / ncta;
+        s.end = p.sk_iters * (cta0 + 1) / ncta;
+    } else if (p.sk_split > 0) {
+        s.rr_left = p.dp_per_cluster;
+        if (cta0 < p.sk_split * p.sk_tiles) s.piece = cta0;
+    } else {
+        s.rr_left = cta0 < p.total_units ? (p.total_units - 1 - cta0) / ncta + 1 : 0;
+    }
+    return s;
+}
+
+template <int CM>
+__device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int ncta, uint32_t rank,
+                                          Unit& w) {
+    if (s.rr_left > 0) {
+        w = decode_unit<CM>(p, s.unit_rr, rank);
+        w.kind = UNIT_FULL;
+        s.unit_rr += ncta;
+        --s.rr_left;
+        return true;
+    }
+    if (s.piece >= 0) {
+        // split form: piece j of last-wave tile t covers K blocks
+        // [j * kblocks / S, (j + 1) * kblocks / S); piece 0 finishes the tile
+        const int S = p.sk_split;
+        const int j = s.piece / p.sk_tiles;
+        const int t = s.piece - j * p.sk_tiles;
+        w = decode_unit<CM>(p, p.dp_units + t, rank);
+        w.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kblocks / S);
+        w.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kblocks / S);
+        w.kind = j == 0 ? UNIT_HEAD : UNIT_TAIL;
+        w.slot = t * (S - 1) + (j > 0 ? j - 1 : 0);
+        w.nslots = S - 1;
+        s.piece = -1;
+        return true;
+    }
+    if (s.it >= s.end) return false;
+    const int64_t kb_unit = p.kblocks;
+    const int64_t u_off = s.it / kb_unit;
+    const int kb0 = static_cast<int>(s.it - u_off * kb_unit);
+    int64_t lim = (u_off + 1) * kb_unit;
+    if (lim > s.end) lim = s.end;
+    w = decode_unit<CM>(p, static_cast<int>(p.dp_units + u_off), rank);
+    w.kb0 = kb0;
+    w.kb1 = kb0 + static_cast<int>(lim - s.it);
+    w.kind = (kb0 == 0 && w.kb1 == p.kblocks) ? UNIT_FULL : (kb0 == 0 ? UNIT_HEAD : UNIT_TAIL);
+    // contiguous form: the partial crosses the boundary before this cluster
+    w.slot = w.kind == UNIT_TAIL ? s.cluster - 1 : s.cluster;
+    w.nslots = 1;
+    s.it = lim;
+    return true;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* ptr, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* ptr) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+    return v;
 }
 
 // Bounded wait used while draining: ignores the abort flag.
@@ -326,6 +412,49 @@ __device__ __forceinline__ float2 unpack2_in(int dt, uint32_t u) {
     return __half22float2(h);
 }
 
+// Stream-K fix-up: add the other cluster's fp32 partial of this warp's 32 rows
+// into the accumulator in tensor memory, before the ordinary output pass.
+// The partial is lane-interleaved (float4 k of lane l at k * 32 + l), so each
+// load instruction of the warp reads 512 contiguous bytes; the loads of chunk
+// c + 1 are in flight while chunk c is added.
+template <int BN, int CHUNK>
+__device__ __forceinline__ void add_partial_to_tmem(uint32_t tmem_row, const float* slab,
+                                                    int lane) {
+    constexpr int NV = CHUNK / 4;
+    const float4* a4 = reinterpret_cast<const float4*>(slab) + lane;
+    float4 cur[NV], nxt[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) cur[j] = __ldcg(a4 + j * 32);
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += CHUNK) {
+        if (c0 + CHUNK < BN) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) nxt[j] = __ldcg(a4 + ((c0 + CHUNK) / 4 + j) * 32);
+        }
+        uint32_t r[32];
+        const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
+        if constexpr (CHUNK == 32)
+            tmem_ld_x32(taddr, r);
+        else
+            tmem_ld_x16(taddr, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            r[4 * j + 0] = __float_as_uint(__uint_as_float(r[4 * j + 0]) + cur[j].x);
+            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + cur[j].y);
+            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + cur[j].z);
+            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + cur[j].w);
+        }
+        if constexpr (CHUNK == 32)
+            tmem_st_x32(taddr, r);
+        else
+            tmem_st_x16(taddr, r);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) cur[j] = nxt[j];
+    }
+    tmem_st_wait();
+}
+
 // TMA-store epilogue of one tile for this warp's 32 rows.  The tile is cut
 // into chunks of 32 columns.  Per chunk, lane t turns row t's accumulators
 // into output values (alpha, beta*C, bias, GELU, one rounding; or raw fp32
@@ -388,6 +517,7 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
     // the loads for chunk c+1 are issued before chunk c is computed
     uint32_t craw[NW], craw_next[NW];
     if (need_c) load_c(w.pid_n * BN, craw_next);
+
 #pragma unroll 1
     for (int c = 0; c < BN / EB; ++c) {
         const int col0 = w.pid_n * BN + c * EB;
@@ -568,8 +698,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             uint32_t phase = 0;
             uint32_t armed = 0;
             bool ok = true;
-            for (int u = cta0; ok && u < p.total_units; u += ncta) {
-                const Unit w = decode_unit<CM>(p, u, rank);
+            WorkIter wi = work_begin(p, cta0, ncta);
+            Unit w;
+            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status,
                                    p.timeout_ns)) {
@@ -696,8 +827,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
             const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
             const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
-            for (int u = cta0; ok && u < p.total_units; u += ncta) {
-                const Unit w = decode_unit<CM>(p, u, rank);
+            WorkIter wi = work_begin(p, cta0, ncta);
+            Unit w;
+            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
                 if (!mbar_wait(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.status,
                                p.timeout_ns)) {
                     ok = false;
@@ -757,13 +889,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const uint64_t store_pol = p.partials ? l2_policy_evict_last() : l2_policy_evict_first();
         int abuf = 0;
         uint32_t aphase = 0;
-        for (int u = cta0; u < p.total_units; u += ncta) {
-            const Unit w = decode_unit<CM>(p, u, rank);
-            if (u == cta0)  // first unit: its own C; afterwards one unit ahead
-                prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
-            if (u + ncta < p.total_units) {
-                const Unit wn = decode_unit<CM>(p, u + ncta, rank);
-                prefetch_c_tile<BN>(p, wn, static_cast<int64_t>(wn.pid_m) * BM + q * 32 + lane);
+        WorkIter wi = work_begin(p, cta0, ncta);
+        Unit w;
+        bool first = true;
+        while (work_next<CM>(p, wi, ncta, rank, w)) {
+            {
+                // C tile of the next item into L2 (and of this one, the first time)
+                if (first)
+                    prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
+                first = false;
+                WorkIter peek = wi;
+                Unit wn;
+                if (work_next<CM>(p, peek, ncta, rank, wn))
+                    prefetch_c_tile<BN>(p, wn, static_cast<int64_t>(wn.pid_m) * BM + q * 32 + lane);
             }
             int ok = 1;
             if (lane == 0)
@@ -775,14 +913,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
             const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
-            if (p.c_tma) {
-                if constexpr (BN >= 32) {
-                    if (p.partials != nullptr || p.epi.c_dtype == DT_F32)
-                        tile_out_tma<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
-                    else
-                        tile_out_tma<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
-                }
-            } else {
+            if (w.kind == UNIT_TAIL) {
+                // stream-K tail: publish this CTA's raw fp32 partial for the cluster
+                // that finishes the tile
+                const int64_t slot = static_cast<int64_t>(w.slot) * CM + rank;
+                float4* dst = reinterpret_cast<float4*>(p.sk_partials + (slot * BM + q * 32) * BN) + lane;
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
                     uint32_t r[32];
@@ -792,7 +927,65 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     else
                         tmem_ld_x16(taddr, r);
                     tmem_ld_wait(r);
-                    epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
+#pragma unroll
+                    for (int i = 0; i < C::CHUNK / 4; ++i)
+                        __stcg(dst + (c0 / 4 + i) * 32,
+                               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                           __uint_as_float(r[4 * i + 2]),
+                                           __uint_as_float(r[4 * i + 3])));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_u64(p.sk_flags + slot * 4 + q, p.sk_epoch);
+            } else {
+                // stream-K head: wait (bounded) for each other piece's partial of
+                // this tile and add it to the accumulator
+                int got = 1;
+                for (int ps = 0; w.kind == UNIT_HEAD && ps < w.nslots; ++ps) {
+                    const int64_t slot = static_cast<int64_t>(w.slot + ps) * CM + rank;
+                    if (lane == 0) {
+                        const unsigned long long* flag = p.sk_flags + slot * 4 + q;
+                        if (ld_acquire_u64(flag) != p.sk_epoch) {
+                            const uint64_t t0 = globaltimer_ns();
+                            for (uint32_t it = 1;; ++it) {
+                                if (ld_acquire_u64(flag) == p.sk_epoch) break;
+                                if ((it & 15u) == 0) {
+                                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                                        *abort_flag = 1;
+                                        if (p.status) atomicExch(p.status, 1);
+                                        got = 0;
+                                        break;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) break;
+                    __syncwarp();  // lane 0's acquire orders the whole warp's reads below
+                    add_partial_to_tmem<BN, C::CHUNK>(tmem_row, p.sk_partials + (slot * BM + q * 32) * BN,
+                                                      lane);
+                }
+                if (!got) break;
+                if (p.c_tma) {
+                    if constexpr (BN >= 32) {
+                        if (p.partials != nullptr || p.epi.c_dtype == DT_F32)
+                            tile_out_tma<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                        else
+                            tile_out_tma<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
+                        uint32_t r[32];
+                        const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
+                        if constexpr (C::CHUNK == 32)
+                            tmem_ld_x32(taddr, r);
+                        else
+                            tmem_ld_x16(taddr, r);
+                        tmem_ld_wait(r);
+                        epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
+                    }
                 }
             }
             // every lane's tensor-memory reads are ordered before the warp's

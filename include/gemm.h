@@ -192,7 +192,10 @@ typedef struct {
     int32_t cta_pair;        /* 0 one CTA per tile; 1 CTA pair along M sharing B by
                                 TMA multicast; 2 CTA pair computing 256-row tiles
                                 with two-CTA (cta_group::2) MMAs                   */
-    int32_t reserved;
+    int32_t stream_k;        /* stream-K: 0 off; 1 the K blocks of the last one-to-two
+                                waves split evenly over all CTAs in contiguous ranges;
+                                2 each unit of the last partial wave cut into equal
+                                K pieces that run side by side                     */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
@@ -219,6 +222,14 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         1: never; 2: always.
  *   GEMM_OPT_L2_HINTS     L2 policy of the tensor-core operand loads: 0 (default) normal;
  *                         1: A evict-first, B evict-last; 2: A evict-last, B evict-first.
+ *   GEMM_OPT_STREAM_K     stream-K ("2 . La GEMM, de zero a cuBLAS", section 2.10) for a
+ *                         partial last wave after at least one whole wave of tiles:
+ *                         0 (default): cut each of the r last tiles into S = P / r
+ *                         equal K pieces (P: CTAs or CTA pairs of the grid) when a
+ *                         cost model says the shorter last wave outweighs the extra
+ *                         partial-tile traffic and the workspace holds the partials;
+ *                         1: never; 2: force the contiguous form (plan stream_k 1);
+ *                         3: force the split form (plan stream_k 2) when S >= 2.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -231,7 +242,8 @@ typedef enum {
     GEMM_OPT_TEST_STALL = 4,
     GEMM_OPT_CTA_PAIR = 5,
     GEMM_OPT_SWAP_AB = 6,
-    GEMM_OPT_L2_HINTS = 7
+    GEMM_OPT_L2_HINTS = 7,
+    GEMM_OPT_STREAM_K = 8
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -258,3 +258,64 @@ def test_cluster_pairs_epilogue(pairs):
     c = run_close(Case("bf16", 520, 700, 300, c_dtype="bf16", alpha=0.5, beta=1.0, bias=True,
                        act="gelu_tanh", seed=74))
     assert c.plan["cta_pair"] in (pairs, 0)
+
+
+# ---------------------------------------------------------------- stream-K
+
+# GEMM_OPT_STREAM_K 2 forces the contiguous form (plan stream_k 1), 3 the split
+# form (plan stream_k 2); each with one CTA per tile and with pair MMA
+@pytest.fixture(params=[(2, 1), (2, 3), (3, 1), (3, 3)],
+                ids=["contiguous-single_cta", "contiguous-pair_mma", "split-single_cta",
+                     "split-pair_mma"])
+def streamk(request):
+    import dense_gemm_bf16_gb300 as dg
+    form, pair = request.param
+    dg.gemm_set_option(dg.Option.STREAM_K, form)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, pair)
+    dg.gemm_set_option(dg.Option.MAX_CTAS, 8)  # few clusters: several whole units, then a cut tail
+    yield form - 1
+    dg.gemm_set_option(dg.Option.STREAM_K, 0)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
+    dg.gemm_set_option(dg.Option.MAX_CTAS, 0)
+
+
+# On 8 CTAs and on 4 CTA pairs each shape leaves a last wave of 1 to 3 units
+# after whole ones, cut into 2 or 4 pieces by the split form (pieces of 4, 5 or
+# 5 and 6 K blocks).
+@pytest.mark.parametrize("shape", [(700, 600, 1000), (700, 600, 600), (700, 600, 700)])
+def test_exact_stream_k(streamk, shape):
+    M, N, K = shape
+    c = run_exact(Case("bf16", M, N, K, values="ints", seed=81 + K))
+    assert c.plan["stream_k"] == streamk
+
+
+# contiguous form only: partial last waves the split form leaves alone
+@pytest.mark.parametrize("shape", [(700, 600, 333), (1100, 700, 1000), (300, 1200, 130),
+                                   (1300, 1100, 257)])
+def test_exact_stream_k_contiguous(streamk, shape):
+    M, N, K = shape
+    c = run_exact(Case("bf16", M, N, K, values="ints", seed=91 + M))
+    if streamk == 1:
+        assert c.plan["stream_k"] == 1
+
+
+def test_exact_stream_k_batched(streamk):
+    c = run_exact(Case("bf16", 300, 520, 600, batch=3, values="ints", seed=85))
+    assert c.plan["stream_k"] == streamk
+
+
+def test_stream_k_epilogue(streamk):
+    c = run_close(Case("bf16", 700, 600, 600, c_dtype="bf16", alpha=0.5, beta=1.0, bias=True,
+                       act="gelu_tanh", seed=86))
+    assert c.plan["stream_k"] == streamk
+
+
+def test_stream_k_fp32_out(streamk):
+    c = run_close(Case("bf16", 700, 600, 1000, c_dtype="f32", beta=-1.0, seed=88))
+    assert c.plan["stream_k"] == streamk
+
+
+def test_stream_k_unaligned_c(streamk):
+    # st.global epilogue path (ldc not a multiple of 16 bytes)
+    c = run_exact(Case("bf16", 700, 601, 1000, values="ints", pads=(0, 0, 1), seed=87))
+    assert c.plan["stream_k"] == streamk
