@@ -40,7 +40,8 @@ WORKLOAD = ("bf16 GEMM M=N=K=8192, A row-major, B column-major, fused bias + GEL
             "fp32 accumulate, bf16 output")
 WORKLOAD_ID = 3  # seeds 3001 (A), 3002 (B), 3004 (bias)
 L2_NOTE = "inputs larger than L2: A + B = 256 MiB and C = 128 MiB vs a 126.5 MiB L2; no flush"
-TC_SOURCES = ["tc_gemm.cu", "ptx.cuh", "epilogue.cuh", "tile_order.h", "internal.h"]
+TC_SOURCES = ["tc_kernel.cuh", "tc_gemm.cu", "tc_gemm_fast.cu", "tc_gemm_general.cu", "ptx.cuh",
+              "epilogue.cuh", "tile_order.h", "internal.h"]
 
 
 def parse_args():
@@ -366,7 +367,7 @@ def main():
                 "traffic": profiled_traffic(), "peak_source": peak_src + " (bf16 burst)",
                 "frac_vs_sustained_peak": achieved / peaks.get("bf16_tflops_sustained",
                                                                peaks["bf16_tflops"]),
-                "kernel": "tc_gemm_kernel<256>"}
+                "kernel": "tc_gemm_kernel<256, 2, 1>"}
 
     if args.rows and rank == 0:
         with open(args.rows, "w") as f:
@@ -455,7 +456,11 @@ def run_ablation(args, device, reps=None, launches=20):
 # ----------------------------------------------------------------------------- other paths
 
 ROW_NAMES = ("sgemm_4096", "ragged_4097x3001x1000", "splitk_256x256x65536",
-             "skinny_16x8192x8192", "batched_64x1024", "batched_64x1024_bcast")
+             "skinny_16x8192x8192", "batched_64x1024", "batched_64x1024_bcast",
+             "streamk_2560x2560x16384", "streamk_off_2560x2560x16384",
+             "flat_4096x4096x16", "flat_4096x4096x16_f32")
+# library options a row runs under (restored afterwards)
+ROW_OPTIONS = {"streamk_off_2560x2560x16384": {"STREAM_K": 1}}
 
 
 def build_row(name, device):
@@ -528,29 +533,64 @@ def build_row(name, device):
         t_comp = flops / (peaks["bf16_tflops"] * 1e12)
         t_mem = nbytes / (peaks["hbm_gbs"] * 1e9)
         return fn, flops, nbytes, "hbm" if t_mem > t_comp else "tensor", plan, (A, B, C, wst)
+    if name in ("streamk_2560x2560x16384", "streamk_off_2560x2560x16384"):
+        # 10 x 10 tiles of 256 x 256: one whole wave on the GPU's CTA pairs and a
+        # partial one, which stream-K cuts along K
+        m_ = n_ = 2560
+        k_ = 16384
+        A = bf16(6001, (m_, k_))
+        B = bf16(6002, (k_, n_))
+        C = torch.empty((m_, n_), dtype=torch.int16, device=device)
+        fn, plan, wst = call16(1, m_, n_, k_, A, k_, 0, B, n_, 0, C, n_, 0, 0, 1.0, 0.0)
+        nbytes = (m_ * k_ + k_ * n_ + m_ * n_) * 2
+        return fn, 2.0 * m_ * n_ * k_, nbytes, "tensor", plan, (A, B, C, wst)
+    if name in ("flat_4096x4096x16", "flat_4096x4096x16_f32"):
+        # flat product ("2 . La GEMM, de zero a cuBLAS", small-K exercise): the
+        # output write is nearly all of the traffic
+        m_ = n_ = 4096
+        k_ = 16
+        f32 = name.endswith("f32")
+        A = bf16(7001, (m_, k_))
+        B = bf16(7002, (k_, n_))
+        C = torch.empty((m_, n_), dtype=torch.float32 if f32 else torch.int16, device=device)
+        fn, plan, wst = call16(1, m_, n_, k_, A, k_, 0, B, n_, 0, C, n_, 0, 2 if f32 else 0, 1.0,
+                               0.0)
+        nbytes = (m_ * k_ + k_ * n_) * 2 + m_ * n_ * (4 if f32 else 2)
+        return fn, 2.0 * m_ * n_ * k_, nbytes, "hbm", plan, (A, B, C, wst)
     raise ValueError(f"unknown row {name!r}")
 
 
 def measure_rows(names, device, reps=20):
-    """Times each named path (median of `reps` launches after 3 warm-ups, CUDA
-    events on the launching stream) with its roofline fraction."""
+    """Times each named path with its roofline fraction: `reps` launches after
+    3 warm-ups, each preceded by a write of a buffer larger than L2 (so every
+    launch starts with a cold L2) and bracketed by CUDA events on the
+    launching stream.  All launches are queued before the first is waited
+    for, so the host's time to issue a call (about 6 us) stays outside the
+    events; the median per-launch time is reported."""
     import torch
+    import dense_gemm_bf16_gb300 as dg
     peaks, _ = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     out = []
     for name in names:
+        saved = {k: dg.gemm_get_option(dg.Option[k]) for k in ROW_OPTIONS.get(name, {})}
+        for k, v in ROW_OPTIONS.get(name, {}).items():
+            dg.gemm_set_option(dg.Option[k], v)
         fn, flops, nbytes, bound, plan, keep = build_row(name, device)
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        ts = []
+        evs = []
         for _ in range(reps):
+            flush.zero_()
             s_ = torch.cuda.Event(enable_timing=True)
             e_ = torch.cuda.Event(enable_timing=True)
             s_.record()
             fn()
             e_.record()
-            torch.cuda.synchronize()
-            ts.append(s_.elapsed_time(e_))
+            evs.append((s_, e_))
+        torch.cuda.synchronize()
+        ts = [s_.elapsed_time(e_) for s_, e_ in evs]
         med, mn = statistics.median(ts), min(ts)
         r = {"path": name, "ms_median": med, "ms_min": mn, "tflops": flops / (med * 1e-3) / 1e12,
              "gbs": nbytes / (med * 1e-3) / 1e9, "algorithmic_bytes": nbytes, "flops": flops,
@@ -563,6 +603,8 @@ def measure_rows(names, device, reps=20):
             r["peak"] = None  # fp32 FMA pipe: peak from SM count x 128 FFMA x 2 x clock
         out.append(r)
         del keep
+        for k, v in saved.items():
+            dg.gemm_set_option(dg.Option[k], v)
     return out
 
 

@@ -53,6 +53,7 @@ class Option(enum.IntEnum):
     SWAP_AB = 6
     L2_HINTS = 7
     STREAM_K = 8
+    FAST_EPILOGUE = 9
 
 
 class Plan(ctypes.Structure):
@@ -63,7 +64,7 @@ class Plan(ctypes.Structure):
                 ("pack_b", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("group_m", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("cta_pair", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("fast_epilogue", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -29,6 +29,7 @@ std::atomic<int64_t> g_opt_cta_pair{0};
 std::atomic<int64_t> g_opt_swap_ab{0};
 std::atomic<int64_t> g_opt_l2_hints{0};
 std::atomic<int64_t> g_opt_stream_k{0};
+std::atomic<int64_t> g_opt_fast_epilogue{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -151,6 +152,7 @@ struct Plan {
     bool swap = false;
     int64_t Mc = 0, Nc = 0;
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
+    bool fast_epi = false;  // TMA-store-only epilogue form
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
     int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
     int64_t dp_units = 0, sk_iters = 0;
@@ -311,7 +313,12 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     }
     pl.ws_need = off;
     // CTA pairs along M (GEMM_OPT_CTA_PAIR: 0 auto, 1 never, 2 B-multicast pair,
-    // 3 pair MMA) for problems with at least a full wave of tile pairs.
+    // 3 pair MMA) for problems with at least a full wave of tile pairs and a
+    // main loop of at least kPairMinKBlocks K blocks: with shorter ones the
+    // pair's shared epilogue hand-off costs more than the halved B traffic
+    // saves (measured: K <= 256 ran 10-25 % slower paired, K = 512 even,
+    // K >= 1024 5-20 % faster).
+    constexpr int64_t kPairMinKBlocks = 12;
     const int64_t want = g_opt_cta_pair.load();
     int mode = 0;
     if (want == 2 || want == 3)
@@ -322,7 +329,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     const int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
     if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
-        (want >= 2 || pair_units >= max_pairs)) {
+        (want >= 2 || (pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
         pl.mode = mode;
         pl.cm = 2;
         pl.stages = tc_stages_for(pl.bn, mode);
@@ -402,6 +409,17 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         }
     }
     pl.launches += 1;
+    // epilogue form: the TMA-store-only one when the output (C, or the split-K
+    // partials) takes TMA stores and no beta * C has to be read
+    if (g_opt_fast_epilogue.load() == 0 && tc_has_fast(pl.bn) && pl.c_row_major_c) {
+        if (pl.splits > 1) {
+            pl.fast_epi = (pl.Nc * 4) % 16 == 0;
+        } else if (c.beta == 0.0f) {
+            const int64_t es = dt_bytes(c.cdt);
+            pl.fast_epi = aligned(c.C, 16) && (c.ldc * es) % 16 == 0 &&
+                          (c.batch == 1 || (c.sc * es) % 16 == 0);
+        }
+    }
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
     if (pl.ws_need > 0 && !aligned(c.ws, 256)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
@@ -456,8 +474,11 @@ gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const v
 // when TMA can address it, or the dense fp32 split-K partials.  Returns false
 // when the row-major TMA epilogue does not apply (the kernel then falls back
 // to st.global stores).
+// Output map of the tensor-core epilogue: boxes of 32 rows by 32 columns, or,
+// with `wide`, by 128 bytes of columns (64 for a 16-bit C), 128-byte swizzled
+// when a box row is 128 bytes and 64-byte swizzled otherwise.
 bool encode_output_map(CUtensorMap* map, int dt, void* ptr, int64_t N, int64_t M, int64_t ld,
-                       int64_t depth, int64_t stride, bool* is3d) {
+                       int64_t depth, int64_t stride, bool wide, bool* is3d) {
     auto fn = encode_fn();
     if (!fn) return false;
     const int es = dt_bytes(dt);
@@ -467,14 +488,15 @@ bool encode_output_map(CUtensorMap* map, int dt, void* ptr, int64_t N, int64_t M
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
                           static_cast<cuuint64_t>(depth)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * es), static_cast<cuuint64_t>(stride * es)};
-    cuuint32_t box[3] = {32u, 32u, 1u};
+    const cuuint32_t box_cols = wide ? static_cast<cuuint32_t>(128 / es) : 32u;
+    cuuint32_t box[3] = {box_cols, 32u, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapDataType t = dt == DT_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                   : dt == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const CUresult r =
         fn(map, t, three ? 3u : 2u, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           box_cols * es == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     *is3d = three;
@@ -571,16 +593,21 @@ gemm_status_t run(const Call& c) {
                              pl.bn);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
+    const bool want_fast = pl.fast_epi;
+    int epi_form = 0;
     if (pl.c_row_major_c && pl.bn >= 32) {
         bool c3 = false;
         bool ok;
         if (p.partials)
             ok = encode_output_map(&p.tmap_c, DT_F32, p.partials, pl.Nc, pl.Mc, pl.Nc,
-                                   static_cast<int64_t>(pl.splits) * c.batch, pl.Mc * pl.Nc, &c3);
+                                   static_cast<int64_t>(pl.splits) * c.batch, pl.Mc * pl.Nc,
+                                   want_fast, &c3);
         else
-            ok = encode_output_map(&p.tmap_c, c.cdt, c.C, pl.Nc, pl.Mc, c.ldc, c.batch, c.sc, &c3);
+            ok = encode_output_map(&p.tmap_c, c.cdt, c.C, pl.Nc, pl.Mc, c.ldc, c.batch, c.sc,
+                                   want_fast, &c3);
         p.c_tma = ok ? 1 : 0;
         p.c_tma_3d = c3 ? 1 : 0;
+        epi_form = ok && want_fast ? 1 : 0;
     }
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
@@ -596,7 +623,8 @@ gemm_status_t run(const Call& c) {
         p.sk_flags = reinterpret_cast<unsigned long long*>(ws + pl.sk_flags_off);
         p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
     }
-    if (tc_launch(pl.bn, pl.mode, p, pl.grid, c.stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (tc_launch(pl.bn, pl.mode, epi_form, p, pl.grid, c.stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
                                    c.stream) != cudaSuccess)
@@ -796,6 +824,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
     plan->cta_pair = pl.mode;
+    plan->fast_epilogue = pl.fast_epi ? 1 : 0;
     plan->stream_k = pl.sk;
     return st;
 }
@@ -834,6 +863,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
             g_opt_stream_k.store(value);
             return GEMM_OK;
+        case GEMM_OPT_FAST_EPILOGUE:
+            if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+            g_opt_fast_epilogue.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -848,6 +881,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_SWAP_AB: return g_opt_swap_ab.load();
         case GEMM_OPT_L2_HINTS: return g_opt_l2_hints.load();
         case GEMM_OPT_STREAM_K: return g_opt_stream_k.load();
+        case GEMM_OPT_FAST_EPILOGUE: return g_opt_fast_epilogue.load();
     }
     return -1;
 }

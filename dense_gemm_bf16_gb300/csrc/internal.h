@@ -76,11 +76,15 @@ struct TcParams {
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).
 // Tensor-core kernel modes: 0 one CTA per 128 x BN tile; 1 CTA pair along M
 // sharing B through TMA multicast; 2 CTA pair computing a 256 x BN tile with
-// cta_group::2 MMAs.
+// cta_group::2 MMAs.  Epilogue forms: 0 general; 1 TMA store only, for
+// beta == 0 or split-K partials, with tmap_c boxes of 128-byte rows
+// (tc_has_fast tells the tile widths that have it).
 int tc_stages_for(int block_n, int mode);
 bool tc_has_mode(int block_n, int mode);
+bool tc_has_fast(int block_n);
 cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
-cudaError_t tc_launch(int block_n, int mode, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc_launch(int block_n, int mode, int epi, const TcParams& p, int grid,
+                      cudaStream_t stream);
 int tc_max_pairs(int block_n, int mode);  // two-CTA clusters resident at once on this device
 
 struct SgemmParams {

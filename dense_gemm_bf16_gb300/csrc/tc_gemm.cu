@@ -1,1077 +1,15 @@
-// Persistent, warp-specialised tcgen05 GEMM for sm_103a (bf16 / fp16 in, fp32 accumulate).
-//
-// The tiled algorithm of "GEMM Kernel Optimization", Core Technique (one
-// BLOCK_M x BLOCK_N output tile per work unit, K consumed in BLOCK_K slices,
-// fp32 accumulator, cast after the loop) mapped onto GB300:
-//
-//   warp 0 (one lane)  TMA producer: fills a ring of STAGES shared-memory
-//                      stages with the A tile [128 x 64] and the B tile
-//                      [BN x 64], 128-byte swizzled, out-of-range elements
-//                      zero-filled by the TMA unit (the K / M / N masks of
-//                      "Skill: Write a Triton GEMM Kernel", step 5).
-//   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16,
-//                      four per stage, into one of two TMEM accumulators;
-//                      tcgen05.commit frees the stage / publishes the tile.
-//   warps 2-5          epilogue: tcgen05.ld of the accumulator (one TMEM lane =
-//                      one output row per thread), alpha/beta/bias/GELU in fp32,
-//                      one rounding to the output type, masked global stores;
-//                      or, for split-K, the raw fp32 partial tile.
-//
-// The two TMEM accumulators let the epilogue of tile i overlap the main loop
-// of tile i+1.  Work units (batch, K slice, tile) are dealt to CTAs round
-// robin (persistent grid, one CTA per SM); tiles follow the grouped order of
-// tile_order.h.  Every mbarrier wait is bounded: on expiry the kernel records an
-// error word, lets its own copies and MMAs drain, frees TMEM and returns.
-#include <stdint.h>
-
-#include "epilogue.cuh"
-#include "internal.h"
-#include "ptx.cuh"
-#include "tile_order.h"
+// Host dispatch of the tensor-core GEMM kernel over tile width, CTA mode and
+// epilogue form; the instantiations live in tc_gemm_general.cu and
+// tc_gemm_fast.cu.
+#include "tc_kernel.cuh"
 
 namespace dg {
-namespace {
 
-constexpr int BM = TC_BLOCK_M;
-constexpr int BK = TC_BLOCK_K;
-constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
-
-// Shared memory of each epilogue warp: two 4 KB output boxes (32 rows x 128
-// bytes, 128-byte swizzled) for the TMA-store epilogue, or one staging tile
-// of 32 rows x 32 fp32 columns (rows padded to 33 words so that row-wise
-// writes and column-wise reads each touch 32 distinct banks) for the
-// st.global fallback.
-constexpr int STAGE_LD = 33;
-constexpr uint32_t EPI_WARP_BYTES = 8192;
-constexpr uint32_t EPI_BOX_BYTES = 4096;
-constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;  // four epilogue warps
-static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
-
-// MODE 0: one CTA per 128 x BN tile.
-// MODE 1: two CTAs of a cluster stacked along M; each loads its own A rows and
-//         one half of the shared B tile, multicast into both CTAs.
-// MODE 2: two CTAs of a cluster compute one 256 x BN tile with cta_group::2
-//         MMAs issued by the even CTA; each CTA holds its own 128 A rows and
-//         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.
-template <int BN, int MODE>
-struct Cfg {
-    static constexpr int CM = MODE == 0 ? 1 : 2;        // CTAs per cluster
-    static constexpr int CG = MODE == 2 ? 2 : 1;        // tcgen05 cta_group
-    static constexpr int B_ROWS = MODE == 2 ? BN / 2 : BN;  // B rows (N) held per CTA
-    static constexpr uint32_t A_BYTES = BM * BK * 2;
-    static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
-    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
-    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int CHUNK = BN < 32 ? BN : 32;
-    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_BYTES;
-    static_assert(STAGES >= 2, "pipeline needs two stages");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
-    static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
-    static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
-                  "swizzled output boxes must be 1024-byte aligned");
-    static_assert(MODE != 2 || BN >= 128, "pair MMA splits B into 64-column atoms");
-};
-
-struct Unit {
-    int b, split, pid_m, pid_n, kb0, kb1;
-    int kind;  // UNIT_FULL, or a stream-K piece: UNIT_HEAD (finishes the tile) / UNIT_TAIL
-    // stream-K partial slots: a TAIL publishes into slot `slot`; a HEAD adds the
-    // `nslots` partials in slots slot .. slot + nslots - 1
-    int slot, nslots;
-};
-
-enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
-
-// Work unit u -> (batch, K slice, tile).  With clusters of CM CTAs along M the
-// unit is a CM-tile-high slab and CTA `rank` of the cluster takes tile-row
-// pid_m * CM + rank of it.
-template <int CM>
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, uint32_t rank) {
-    const int per_batch = p.splits * p.tiles_per_batch;
-    Unit w;
-    w.b = u / per_batch;
-    const int r = u - w.b * per_batch;
-    w.split = r / p.tiles_per_batch;
-    const int t = r - w.split * p.tiles_per_batch;
-    tile_coord(t, p.num_pid_m, p.num_pid_n, p.group_m, w.pid_m, w.pid_n);
-    w.pid_m = w.pid_m * CM + static_cast<int>(rank);
-    w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
-    w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
-    return w;
-}
-
-// The sequence of work items of one cluster; every role of the CTA walks it.
-struct WorkIter {
-    int cluster;      // this cluster's index
-    int unit_rr;      // next round-robin unit
-    int rr_left;      // round-robin units left
-    int64_t it, end;  // stream-K K-block range (contiguous form)
-    int piece;        // split form: this cluster's piece of the last wave, or -1
-};
-
-__device__ __forceinline__ WorkIter work_begin(const TcParams& p, int cta0, int ncta) {
-    WorkIter s;
-    s.cluster = cta0;
-    s.unit_rr = cta0;
-    s.it = s.end = 0;
-    s.piece = -1;
-    if (p.sk_iters > 0) {
-        s.rr_left = p.dp_per_cluster;
-        s.it = p.sk_iters * cta0 / ncta;
-        s.end = p.sk_iters * (cta0 + 1) / ncta;
-    } else if (p.sk_split > 0) {
-        s.rr_left = p.dp_per_cluster;
-        if (cta0 < p.sk_split * p.sk_tiles) s.piece = cta0;
-    } else {
-        s.rr_left = cta0 < p.total_units ? (p.total_units - 1 - cta0) / ncta + 1 : 0;
-    }
-    return s;
-}
-
-template <int CM>
-__device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int ncta, uint32_t rank,
-                                          Unit& w) {
-    if (s.rr_left > 0) {
-        w = decode_unit<CM>(p, s.unit_rr, rank);
-        w.kind = UNIT_FULL;
-        s.unit_rr += ncta;
-        --s.rr_left;
-        return true;
-    }
-    if (s.piece >= 0) {
-        // split form: piece j of last-wave tile t covers K blocks
-        // [j * kblocks / S, (j + 1) * kblocks / S); piece 0 finishes the tile
-        const int S = p.sk_split;
-        const int j = s.piece / p.sk_tiles;
-        const int t = s.piece - j * p.sk_tiles;
-        w = decode_unit<CM>(p, p.dp_units + t, rank);
-        w.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kblocks / S);
-        w.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kblocks / S);
-        w.kind = j == 0 ? UNIT_HEAD : UNIT_TAIL;
-        w.slot = t * (S - 1) + (j > 0 ? j - 1 : 0);
-        w.nslots = S - 1;
-        s.piece = -1;
-        return true;
-    }
-    if (s.it >= s.end) return false;
-    const int64_t kb_unit = p.kblocks;
-    const int64_t u_off = s.it / kb_unit;
-    const int kb0 = static_cast<int>(s.it - u_off * kb_unit);
-    int64_t lim = (u_off + 1) * kb_unit;
-    if (lim > s.end) lim = s.end;
-    w = decode_unit<CM>(p, static_cast<int>(p.dp_units + u_off), rank);
-    w.kb0 = kb0;
-    w.kb1 = kb0 + static_cast<int>(lim - s.it);
-    w.kind = (kb0 == 0 && w.kb1 == p.kblocks) ? UNIT_FULL : (kb0 == 0 ? UNIT_HEAD : UNIT_TAIL);
-    // contiguous form: the partial crosses the boundary before this cluster
-    w.slot = w.kind == UNIT_TAIL ? s.cluster - 1 : s.cluster;
-    w.nslots = 1;
-    s.it = lim;
-    return true;
-}
-
-__device__ __forceinline__ void st_release_u64(unsigned long long* ptr, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* ptr) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
-    return v;
-}
-
-// Bounded wait used while draining: ignores the abort flag.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, int x,
-                                          int y, int z, bool is3d, uint64_t pol) {
-    if (is3d)
-        tma_load_3d(dst, map, bar, x, y, z, pol);
-    else
-        tma_load_2d(dst, map, bar, x, y, pol);
-}
-
-template <typename T>
-__device__ __forceinline__ float ld_f(const T* p);
-template <>
-__device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16* p) {
-    return __bfloat162float(*p);
-}
-template <>
-__device__ __forceinline__ float ld_f<__half>(const __half* p) { return __half2float(*p); }
-
-template <typename T>
-__device__ __forceinline__ void st_f(T* p, float x);
-template <>
-__device__ __forceinline__ void st_f<float>(float* p, float x) { *p = x; }
-template <>
-__device__ __forceinline__ void st_f<__nv_bfloat16>(__nv_bfloat16* p, float x) {
-    *p = __float2bfloat16_rn(x);
-}
-template <>
-__device__ __forceinline__ void st_f<__half>(__half* p, float x) { *p = __float2half_rn(x); }
-
-// Epilogue terms on a run of H values (each branch taken once per run, so
-// unrequested terms never enter the unrolled loops).  cv: beta*C inputs,
-// bias_v: per-value bias (already 0 where there is none).
-template <int H>
-__device__ __forceinline__ void finish_run(const Epilogue& e, float (&v)[H], const float (&cv)[H],
-                                           const float (&bias_v)[H], bool has_c, bool has_bias) {
-    if (e.alpha != 1.0f) {
-#pragma unroll
-        for (int i = 0; i < H; ++i) v[i] *= e.alpha;
-    }
-    if (has_c) {
-#pragma unroll
-        for (int i = 0; i < H; ++i) v[i] = fmaf(e.beta, cv[i], v[i]);
-    }
-    if (has_bias) {
-#pragma unroll
-        for (int i = 0; i < H; ++i) v[i] += bias_v[i];
-    }
-    if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-        for (int i = 0; i < H; ++i) v[i] = gelu_tanh(v[i]);
-    }
-}
-
-// Row-major C: lane t owns column col0 + t of the warp's 32 rows, read from
-// the staging tile.  All beta*C loads of a half-chunk are issued before any
-// store (C is read and written in place, so the compiler may not reorder a
-// load above an earlier store by itself).
-template <int CH, typename T>
-__device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M, int N,
-                                         int64_t row_base, int lane, int col0,
-                                         const float* stage) {
-    constexpr int H = 16;  // rows per half: bounds the registers held by in-flight loads
-    const int col = col0 + lane;
-    const bool col_ok = lane < CH && col < N;
-    const int64_t left = M - row_base;
-    const int nrows = left < 32 ? static_cast<int>(left) : 32;
-    const int64_t ldc = e.ldc;
-    const bool has_c = e.beta != 0.0f;
-    const bool has_bias = e.bias != nullptr;
-    const float bias_col = (has_bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
-    T* const c0 =
-        static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c + row_base * ldc + col;
-#pragma unroll 1
-    for (int h = 0; h < 32; h += H) {
-        float v[H], cv[H], bv[H];
-        const T* q = c0 + h * ldc;
-#pragma unroll
-        for (int i = 0; i < H; ++i, q += ldc) {
-            const bool ok = h + i < nrows && col_ok;
-            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
-            v[i] = stage[(h + i) * STAGE_LD + lane];
-            bv[i] = bias_col;
-        }
-        if (has_bias && e.bias_on_rows) {
-#pragma unroll
-            for (int i = 0; i < H; ++i)
-                bv[i] = h + i < nrows ? e.bias[row_base + h + i] : 0.0f;
-        }
-        finish_run<H>(e, v, cv, bv, has_c, has_bias);
-        T* o = c0 + h * ldc;
-#pragma unroll
-        for (int i = 0; i < H; ++i, o += ldc)
-            if (h + i < nrows && col_ok) st_f(o, v[i]);
-    }
-}
-
-// Column-major C: lane t owns row row_base + t; for a fixed column the 32
-// lanes address 32 consecutive elements, so the accesses are coalesced.
-template <int CH, typename T>
-__device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M, int N,
-                                         int64_t row_base, int lane, int col0,
-                                         const uint32_t (&r)[32]) {
-    constexpr int H = CH < 16 ? CH : 16;
-    const int64_t row = row_base + lane;
-    if (row >= M) return;
-    const int left = N - col0;
-    const int ncols = left < CH ? left : CH;
-    const int64_t ldc = e.ldc;
-    const bool has_c = e.beta != 0.0f;
-    const bool has_bias = e.bias != nullptr;
-    const float bias_row = (has_bias && e.bias_on_rows) ? e.bias[row] : 0.0f;
-    T* const c0 = static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c +
-                  static_cast<int64_t>(col0) * ldc + row;
-#pragma unroll
-    for (int h = 0; h < CH; h += H) {
-        float v[H], cv[H], bv[H];
-        const T* q = c0 + h * ldc;
-#pragma unroll
-        for (int i = 0; i < H; ++i, q += ldc) {
-            const bool ok = h + i < ncols;
-            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
-            v[i] = __uint_as_float(r[h + i]);
-            bv[i] = bias_row;
-        }
-        if (has_bias && !e.bias_on_rows) {
-#pragma unroll
-            for (int i = 0; i < H; ++i) bv[i] = h + i < ncols ? e.bias[col0 + h + i] : 0.0f;
-        }
-        finish_run<H>(e, v, cv, bv, has_c, has_bias);
-        T* o = c0 + h * ldc;
-#pragma unroll
-        for (int i = 0; i < H; ++i, o += ldc)
-            if (h + i < ncols) st_f(o, v[i]);
-    }
-}
-
-// CTA-pair load: bytes complete on `bar`, which may be the peer's barrier.
-__device__ __forceinline__ void load_pair(const CUtensorMap* map, uint32_t dst, uint32_t bar, int x,
-                                          int y, int z, bool is3d, uint64_t pol) {
-    if (is3d)
-        tma_load_3d_pair(dst, map, bar, x, y, z, pol);
-    else
-        tma_load_2d_pair(dst, map, bar, x, y, pol);
-}
-
-// Epilogue of one CH-column chunk of this warp's 32 rows.  On entry lane t
-// holds row row_base + t, columns col0 .. col0+CH-1 (fp32 accumulators).
-template <int CH>
-__device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w, int64_t row_base,
-                                               int lane, int col0, const uint32_t (&r)[32],
-                                               float* stage) {
-    const Epilogue& e = p.epi;
-    if (row_base >= p.M) return;
-    if (p.partials) {
-        // raw fp32 partial tile, stored densely in C's layout
-        const int64_t slice = static_cast<int64_t>(w.split) * p.batch + w.b;
-        float* P = p.partials + slice * static_cast<int64_t>(p.M) * p.N;
-        if (!e.c_row_major) {
-            const int64_t row = row_base + lane;
-            if (row >= p.M) return;
-#pragma unroll
-            for (int c = 0; c < CH; ++c)
-                if (col0 + c < p.N)
-                    P[static_cast<int64_t>(col0 + c) * p.M + row] = __uint_as_float(r[c]);
-            return;
-        }
-#pragma unroll
-        for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
-        __syncwarp();
-        const int col = col0 + lane;
-        if (lane < CH && col < p.N) {
-#pragma unroll 8
-            for (int rr = 0; rr < 32; ++rr) {
-                const int64_t row = row_base + rr;
-                if (row < p.M) P[row * p.N + col] = stage[rr * STAGE_LD + lane];
-            }
-        }
-        __syncwarp();
-        return;
-    }
-    if (!e.c_row_major) {
-        if (e.c_dtype == DT_BF16)
-            cols_out<CH, __nv_bfloat16>(e, w, p.M, p.N, row_base, lane, col0, r);
-        else if (e.c_dtype == DT_F16)
-            cols_out<CH, __half>(e, w, p.M, p.N, row_base, lane, col0, r);
-        else
-            cols_out<CH, float>(e, w, p.M, p.N, row_base, lane, col0, r);
-        return;
-    }
-    // row-major output: transpose through shared memory so that each warp
-    // store covers consecutive columns of one row.
-#pragma unroll
-    for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
-    __syncwarp();
-    if (e.c_dtype == DT_BF16)
-        rows_out<CH, __nv_bfloat16>(e, w, p.M, p.N, row_base, lane, col0, stage);
-    else if (e.c_dtype == DT_F16)
-        rows_out<CH, __half>(e, w, p.M, p.N, row_base, lane, col0, stage);
-    else
-        rows_out<CH, float>(e, w, p.M, p.N, row_base, lane, col0, stage);
-    __syncwarp();
-}
-
-__device__ __forceinline__ uint32_t pack2_out(int dt, float lo, float hi) {
-    if (dt == DT_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float2 unpack2_in(int dt, uint32_t u) {
-    if (dt == DT_BF16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-    __half2 h = *reinterpret_cast<__half2*>(&u);
-    return __half22float2(h);
-}
-
-// Stream-K fix-up: add the other cluster's fp32 partial of this warp's 32 rows
-// into the accumulator in tensor memory, before the ordinary output pass.
-// The partial is lane-interleaved (float4 k of lane l at k * 32 + l), so each
-// load instruction of the warp reads 512 contiguous bytes; the loads of chunk
-// c + 1 are in flight while chunk c is added.
-template <int BN, int CHUNK>
-__device__ __forceinline__ void add_partial_to_tmem(uint32_t tmem_row, const float* slab,
-                                                    int lane) {
-    constexpr int NV = CHUNK / 4;
-    const float4* a4 = reinterpret_cast<const float4*>(slab) + lane;
-    float4 cur[NV], nxt[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) cur[j] = __ldcg(a4 + j * 32);
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += CHUNK) {
-        if (c0 + CHUNK < BN) {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) nxt[j] = __ldcg(a4 + ((c0 + CHUNK) / 4 + j) * 32);
-        }
-        uint32_t r[32];
-        const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
-        if constexpr (CHUNK == 32)
-            tmem_ld_x32(taddr, r);
-        else
-            tmem_ld_x16(taddr, r);
-        tmem_ld_wait(r);
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            r[4 * j + 0] = __float_as_uint(__uint_as_float(r[4 * j + 0]) + cur[j].x);
-            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + cur[j].y);
-            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + cur[j].z);
-            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + cur[j].w);
-        }
-        if constexpr (CHUNK == 32)
-            tmem_st_x32(taddr, r);
-        else
-            tmem_st_x16(taddr, r);
-#pragma unroll
-        for (int j = 0; j < NV; ++j) cur[j] = nxt[j];
-    }
-    tmem_st_wait();
-}
-
-// TMA-store epilogue of one tile for this warp's 32 rows.  The tile is cut
-// into chunks of 32 columns.  Per chunk, lane t turns row t's accumulators
-// into output values (alpha, beta*C, bias, GELU, one rounding; or raw fp32
-// for split-K partials) and writes them as row t of a 32-row box in shared
-// memory, laid out as the tensor map's swizzle expects (rows of RB = 32*ES
-// bytes; 128-byte swizzle for fp32, 64-byte swizzle for 16-bit outputs);
-// lane 0 then stores the box with one TMA tensor store.  The TMA unit clips
-// rows >= M and columns >= N.  Two boxes per warp alternate, so the math of
-// a chunk overlaps the store of the previous one.
-template <int BN, int ES>
-__device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, int q, int lane,
-                                             uint32_t tmem_row, uint8_t* wbuf, uint32_t& nbox,
-                                             uint64_t pol) {
-    constexpr int EB = 32;             // columns per chunk
-    constexpr int RB = EB * ES;        // bytes per box row: 128 (fp32) or 64 (16-bit)
-    constexpr int NJ = RB / 16;        // 16-byte pieces per row
-    constexpr int NW = RB / 4;         // 32-bit words per row
-    const Epilogue& e = p.epi;
-    const bool partial = p.partials != nullptr;
-    const int dt = partial ? DT_F32 : e.c_dtype;
-    const int row0 = w.pid_m * BM + q * 32;
-    const int64_t row = static_cast<int64_t>(row0) + lane;
-    const bool row_ok = row < p.M;
-    const int zc = partial ? w.split * p.batch + w.b : w.b;
-    // swizzle: piece j of row r sits at piece j ^ ((r * RB / 128) % NJ)
-    const int swz = ((lane * RB) >> 7) & (NJ - 1);
-    const bool need_c = !partial && e.beta != 0.0f && row_ok;
-    const char* crow =
-        need_c ? static_cast<const char*>(e.C) + (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc) * ES
-               : nullptr;
-    // beta*C of this thread's row segment for one chunk, as raw output words
-    auto load_c = [&](int col0, uint32_t (&craw)[NW]) {
-        if (col0 + EB <= p.N) {
-#pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const uint4 t = reinterpret_cast<const uint4*>(crow + static_cast<int64_t>(col0) * ES)[j];
-                craw[4 * j + 0] = t.x;
-                craw[4 * j + 1] = t.y;
-                craw[4 * j + 2] = t.z;
-                craw[4 * j + 3] = t.w;
-            }
-        } else {
-            const char* src = crow + static_cast<int64_t>(col0) * ES;
-            const int nvalid = p.N - col0;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) craw[i] = 0u;
-#pragma unroll
-            for (int i = 0; i < EB; ++i) {
-                if (i < nvalid) {
-                    if (ES == 4) {
-                        craw[i] = reinterpret_cast<const uint32_t*>(src)[i];
-                    } else {
-                        const uint32_t h = reinterpret_cast<const uint16_t*>(src)[i];
-                        craw[i >> 1] |= (i & 1) ? (h << 16) : h;
-                    }
-                }
-            }
-        }
-    };
-    // the loads for chunk c+1 are issued before chunk c is computed
-    uint32_t craw[NW], craw_next[NW];
-    if (need_c) load_c(w.pid_n * BN, craw_next);
-
-#pragma unroll 1
-    for (int c = 0; c < BN / EB; ++c) {
-        const int col0 = w.pid_n * BN + c * EB;
-        if (col0 >= p.N) break;
-        const bool full = col0 + EB <= p.N;
-        if (need_c) {
-#pragma unroll
-            for (int i = 0; i < NW; ++i) craw[i] = craw_next[i];
-            if (c + 1 < BN / EB && col0 + EB < p.N) load_c(col0 + EB, craw_next);
-        }
-        // accumulators: 32 consecutive TMEM columns of this lane's row
-        uint32_t r[32];
-        tmem_ld_x32(tmem_row + static_cast<uint32_t>(c * EB), r);
-        tmem_ld_wait(r);
-        float v[EB];
-#pragma unroll
-        for (int i = 0; i < EB; ++i) v[i] = __uint_as_float(r[i]);
-        if (!partial) {
-            // one pass per epilogue term, each branch taken once per chunk
-            if (e.alpha != 1.0f) {
-#pragma unroll
-                for (int i = 0; i < EB; ++i) v[i] *= e.alpha;
-            }
-            if (need_c) {
-#pragma unroll
-                for (int i = 0; i < EB; ++i) {
-                    float cval;
-                    if (ES == 4) {
-                        cval = __uint_as_float(craw[i]);
-                    } else {
-                        const float2 f = unpack2_in(dt, craw[i >> 1]);
-                        cval = (i & 1) ? f.y : f.x;
-                    }
-                    v[i] = fmaf(e.beta, cval, v[i]);
-                }
-            }
-            if (e.bias) {
-                if (e.bias_on_rows) {
-                    const float bias_row = row_ok ? e.bias[row] : 0.0f;
-#pragma unroll
-                    for (int i = 0; i < EB; ++i) v[i] += bias_row;
-                } else if (full) {
-#pragma unroll
-                    for (int i = 0; i < EB; ++i) v[i] += __ldg(e.bias + col0 + i);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < EB; ++i)
-                        if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
-                }
-            }
-            if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-                for (int i = 0; i < EB; ++i) v[i] = gelu_tanh(v[i]);
-            }
-        }
-        // the box written two chunks ago must have been read by its TMA store
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-        uint8_t* box = wbuf + (nbox & 1u) * EPI_BOX_BYTES;
-        uint8_t* line = box + lane * RB;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            uint4 t;
-            if (ES == 4) {
-                t = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
-                               __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3]));
-            } else {
-                t.x = pack2_out(dt, v[8 * j + 0], v[8 * j + 1]);
-                t.y = pack2_out(dt, v[8 * j + 2], v[8 * j + 3]);
-                t.z = pack2_out(dt, v[8 * j + 4], v[8 * j + 5]);
-                t.w = pack2_out(dt, v[8 * j + 6], v[8 * j + 7]);
-            }
-            *reinterpret_cast<uint4*>(line + ((j ^ swz) << 4)) = t;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            if (p.c_tma_3d)
-                tma_store_3d(&p.tmap_c, smem_u32(box), col0, row0, zc, pol);
-            else
-                tma_store_2d(&p.tmap_c, smem_u32(box), col0, row0, pol);
-            bulk_commit_group();
-        }
-        ++nbox;
-    }
-}
-
-// Pull this warp's rows of the C tile into L2 before the accumulator is ready
-// (beta != 0 only), so that the epilogue's reads of C hit L2.
-template <int BN>
-__device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w, int64_t row) {
-    const Epilogue& e = p.epi;
-    if (e.beta == 0.0f || p.partials || !e.c_row_major || row >= p.M) return;
-    const int col0 = w.pid_n * BN;
-    const int ncols = p.N - col0 < BN ? p.N - col0 : BN;
-    const int es = dt_size(e.c_dtype);
-    const char* base = static_cast<const char*>(e.C) +
-                       (static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc + col0) * es;
-    for (int off = 0; off < ncols * es; off += 128)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
-}
-
-template <int BN, int MODE>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<BN, MODE>;
-    constexpr int CM = C::CM;
-    constexpr int CG = C::CG;
-    const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
-    const bool leader = rank == 0;
-    const int cta0 = static_cast<int>(blockIdx.x) / CM;  // cluster index
-    const int ncta = static_cast<int>(gridDim.x) / CM;   // clusters in the grid
-    constexpr uint16_t kPair = (1u << CM) - 1u;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sA0 = smem_u32(smem);
-    const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
-    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][barriers]
-    uint8_t* epi_smem = smem + C::STAGES * C::STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + EPI_BYTES);
-    const uint32_t bar0 = smem_u32(bars);
-    // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
-    const uint32_t full0 = bar0;
-    const uint32_t empty0 = bar0 + 8u * C::STAGES;
-    const uint32_t tfull0 = bar0 + 16u * C::STAGES;
-    const uint32_t tempty0 = tfull0 + 16u;
-    const uint32_t drain_bar = tempty0 + 16u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        // MODE 2: the leader's stage barrier collects the bytes of both CTAs'
-        // loads; its accumulator-release barrier counts the epilogue warps of
-        // both CTAs.  Accumulator releases are one arrival per epilogue warp.
-        const uint32_t full_count = 1u;
-        const uint32_t empty_count = MODE == 1 ? 2u : 1u;
-        const uint32_t tempty_count = MODE == 2 ? 2u * (TC_EPI_THREADS / 32) : TC_EPI_THREADS / 32;
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full0 + 8u * s, full_count);
-            mbar_init(empty0 + 8u * s, empty_count);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull0 + 8u * b, 1);
-            mbar_init(tempty0 + 8u * b, tempty_count);
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        prefetch_tmap(&p.tmap_a);
-        prefetch_tmap(&p.tmap_b);
-    }
-    if (warp == 1) {
-        tmem_alloc_cg<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish_cg<CG>();
-    }
-    tc_fence_before_sync();
-    if constexpr (CM > 1)
-        cluster_sync();  // the peer's barriers are initialised before any cross-CTA signal
-    else
-        __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            // L2 policies of the two operands ("Skill: Write a Triton GEMM Kernel",
-            // Kernel design rules: keep the operand reused across the tile group)
-            const uint64_t pol_normal = l2_policy_evict_normal();
-            const uint64_t pol_first = l2_policy_evict_first();
-            const uint64_t pol_last = l2_policy_evict_last();
-            const uint64_t pol_a = p.l2_hints == 1 ? pol_first : (p.l2_hints == 2 ? pol_last : pol_normal);
-            const uint64_t pol_b = p.l2_hints == 1 ? pol_last : (p.l2_hints == 2 ? pol_first : pol_normal);
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t armed = 0;
-            bool ok = true;
-            WorkIter wi = work_begin(p, cta0, ncta);
-            Unit w;
-            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status,
-                                   p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    if (p.test_stall && armed == 0) {
-                        // test only: leave this stage unfilled; the MMA warp's bounded
-                        // wait on it must expire and report the timeout.
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full0 + 8u * stage;
-                    // MODE 1: own A + both B halves.  MODE 2: the leader's barrier
-                    // takes the bytes of both CTAs; the peer's barrier is unused.
-                    if (MODE != 2 || leader)
-                        mbar_arrive_expect_tx(fb, MODE == 2 ? 2u * C::STAGE_BYTES : C::STAGE_BYTES);
-                    const uint32_t a_dst = sA0 + stage * C::A_BYTES;
-                    const uint32_t b_dst = sB0 + stage * C::B_BYTES;
-                    const int k0 = kb * BK;
-                    if constexpr (MODE == 2) {
-                        // own A rows and own BN/2 B columns; bytes complete on the leader
-                        const uint32_t lb = leader ? fb : mapa_shared(fb, 0u);
-                        if (!p.a_mn) {
-                            load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
-                        } else {
-#pragma unroll
-                            for (int h = 0; h < BM / 64; ++h)
-                                load_pair(&p.tmap_a, a_dst + h * 8192u, lb, w.pid_m * BM + 64 * h,
-                                          k0, w.b, p.a_3d, pol_a);
-                        }
-                        constexpr int HALF = BN / 2;
-                        if (!p.b_mn) {
-                            load_pair(&p.tmap_b, b_dst, lb, k0,
-                                      w.pid_n * BN + static_cast<int>(rank) * HALF, w.b, p.b_3d,
-                                      pol_b);
-                        } else {
-#pragma unroll
-                            for (int hh = 0; hh < HALF / 64; ++hh)
-                                load_pair(&p.tmap_b, b_dst + hh * 8192u, lb,
-                                          w.pid_n * BN + static_cast<int>(rank) * HALF + 64 * hh,
-                                          k0, w.b, p.b_3d, pol_b);
-                        }
-                    } else if (!p.a_mn) {
-                        load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < BM / 64; ++h)
-                            load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
-                                      w.b, p.a_3d, pol_a);
-                    }
-                    if constexpr (MODE == 0) {
-                        if (!p.b_mn) {
-                            load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol_b);
-                        } else {
-                            if constexpr (BN >= 64) {
-#pragma unroll
-                                for (int h = 0; h < BN / 64; ++h)
-                                    load_tile(&p.tmap_b, b_dst + h * 8192u, fb,
-                                              w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol_b);
-                            }
-                        }
-                    } else if constexpr (MODE == 1) {
-                        // this CTA's half of the B tile, multicast to the pair
-                        constexpr int HALF = BN / 2;
-                        if (!p.b_mn) {
-                            const uint32_t dst = b_dst + rank * (HALF * 128u);
-                            const int y = w.pid_n * BN + static_cast<int>(rank) * HALF;
-                            if (p.b_3d)
-                                tma_load_3d_mc(dst, &p.tmap_b, fb, k0, y, w.b, kPair, pol_b);
-                            else
-                                tma_load_2d_mc(dst, &p.tmap_b, fb, k0, y, kPair, pol_b);
-                        } else {
-#pragma unroll
-                            for (int hh = 0; hh < HALF / 64; ++hh) {
-                                const int h = static_cast<int>(rank) * (HALF / 64) + hh;
-                                const uint32_t dst = b_dst + h * 8192u;
-                                const int x = w.pid_n * BN + 64 * h;
-                                if (p.b_3d)
-                                    tma_load_3d_mc(dst, &p.tmap_b, fb, x, k0, w.b, kPair, pol_b);
-                                else
-                                    tma_load_2d_mc(dst, &p.tmap_b, fb, x, k0, kPair, pol_b);
-                            }
-                        }
-                    }
-                    ++armed;
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Every issued fill must land before the CTA may exit.  A MODE 2
-            // peer's loads complete on the leader's barriers: after a normal
-            // run the leader has consumed them all before the final cluster
-            // barrier; after an abort the peer gives its copies a fixed bound.
-            if (MODE == 2 && !leader) {
-                if (!ok) {
-                    const uint64_t t0 = globaltimer_ns();
-                    while (globaltimer_ns() - t0 < 200000ull) {
-                    }
-                }
-            } else {
-                for (int s = 0; s < C::STAGES && static_cast<uint32_t>(s) < armed; ++s) {
-                    const uint32_t fills = (armed - 1u - s) / C::STAGES + 1u;
-                    wait_drain(full0 + 8u * s, (fills - 1u) & 1u, p.timeout_ns);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (MODE == 2 && !leader) {
-            // MODE 2 peer: the leader's thread issues the MMAs for both CTAs
-        } else if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            int stage = 0;
-            uint32_t phase = 0;
-            int abuf = 0;
-            uint32_t aphase = 0;
-            bool issued = false;
-            bool ok = true;
-            // K-major operands advance 32 bytes per K=16 step inside the 128-byte
-            // swizzle row; MN-major ones advance two 8-row (1024-byte) groups.
-            const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
-            const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
-            const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
-            const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
-            WorkIter wi = work_begin(p, cta0, ncta);
-            Unit w;
-            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
-                if (!mbar_wait(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.status,
-                               p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(abuf * BN);
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(full0 + 8u * stage, phase, abort_flag, p.status,
-                                   p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t a_base = sA0 + stage * C::A_BYTES;
-                    const uint32_t b_base = sB0 + stage * C::B_BYTES;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = smem_desc_sw128(a_base + k * a_kstep, a_lbo, 1024u);
-                        const uint64_t bd = smem_desc_sw128(b_base + k * b_kstep, b_lbo, 1024u);
-                        umma_f16_cg<CG>(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
-                    }
-                    issued = true;
-                    if constexpr (CM > 1)
-                        umma_commit_mc_cg<CG>(empty0 + 8u * stage, kPair);
-                    else
-                        umma_commit_cg<CG>(empty0 + 8u * stage);
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                if constexpr (MODE == 2)
-                    umma_commit_mc_cg<CG>(tfull0 + 8u * abuf, kPair);  // both CTAs' accumulators
-                else
-                    umma_commit_cg<CG>(tfull0 + 8u * abuf);
-                if (++abuf == 2) {
-                    abuf = 0;
-                    aphase ^= 1u;
-                }
-            }
-            if (issued) {
-                // all MMAs complete before tensor memory is released
-                umma_commit_cg<CG>(drain_bar);
-                wait_drain(drain_bar, 0u, p.timeout_ns);
-            }
-        }
-    } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* wbuf = epi_smem + (warp - 2) * EPI_WARP_BYTES;
-        float* stage = reinterpret_cast<float*>(wbuf);
-        uint32_t nbox = 0;
-        // outputs leave L2 first; split-K partials stay for the reduction that follows
-        const uint64_t store_pol = p.partials ? l2_policy_evict_last() : l2_policy_evict_first();
-        int abuf = 0;
-        uint32_t aphase = 0;
-        WorkIter wi = work_begin(p, cta0, ncta);
-        Unit w;
-        bool first = true;
-        while (work_next<CM>(p, wi, ncta, rank, w)) {
-            {
-                // C tile of the next item into L2 (and of this one, the first time)
-                if (first)
-                    prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
-                first = false;
-                WorkIter peek = wi;
-                Unit wn;
-                if (work_next<CM>(p, peek, ncta, rank, wn))
-                    prefetch_c_tile<BN>(p, wn, static_cast<int64_t>(wn.pid_m) * BM + q * 32 + lane);
-            }
-            int ok = 1;
-            if (lane == 0)
-                ok = mbar_wait(tfull0 + 8u * abuf, aphase, abort_flag, p.status, p.timeout_ns) ? 1
-                                                                                               : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
-            const int col_base = w.pid_n * BN;
-            const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
-            if (w.kind == UNIT_TAIL) {
-                // stream-K tail: publish this CTA's raw fp32 partial for the cluster
-                // that finishes the tile
-                const int64_t slot = static_cast<int64_t>(w.slot) * CM + rank;
-                float4* dst = reinterpret_cast<float4*>(p.sk_partials + (slot * BM + q * 32) * BN) + lane;
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
-                    uint32_t r[32];
-                    const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
-                    if constexpr (C::CHUNK == 32)
-                        tmem_ld_x32(taddr, r);
-                    else
-                        tmem_ld_x16(taddr, r);
-                    tmem_ld_wait(r);
-#pragma unroll
-                    for (int i = 0; i < C::CHUNK / 4; ++i)
-                        __stcg(dst + (c0 / 4 + i) * 32,
-                               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                           __uint_as_float(r[4 * i + 2]),
-                                           __uint_as_float(r[4 * i + 3])));
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) st_release_u64(p.sk_flags + slot * 4 + q, p.sk_epoch);
-            } else {
-                // stream-K head: wait (bounded) for each other piece's partial of
-                // this tile and add it to the accumulator
-                int got = 1;
-                for (int ps = 0; w.kind == UNIT_HEAD && ps < w.nslots; ++ps) {
-                    const int64_t slot = static_cast<int64_t>(w.slot + ps) * CM + rank;
-                    if (lane == 0) {
-                        const unsigned long long* flag = p.sk_flags + slot * 4 + q;
-                        if (ld_acquire_u64(flag) != p.sk_epoch) {
-                            const uint64_t t0 = globaltimer_ns();
-                            for (uint32_t it = 1;; ++it) {
-                                if (ld_acquire_u64(flag) == p.sk_epoch) break;
-                                if ((it & 15u) == 0) {
-                                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
-                                        *abort_flag = 1;
-                                        if (p.status) atomicExch(p.status, 1);
-                                        got = 0;
-                                        break;
-                                    }
-                                }
-                            }
-                        }
-                    }
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) break;
-                    __syncwarp();  // lane 0's acquire orders the whole warp's reads below
-                    add_partial_to_tmem<BN, C::CHUNK>(tmem_row, p.sk_partials + (slot * BM + q * 32) * BN,
-                                                      lane);
-                }
-                if (!got) break;
-                if (p.c_tma) {
-                    if constexpr (BN >= 32) {
-                        if (p.partials != nullptr || p.epi.c_dtype == DT_F32)
-                            tile_out_tma<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
-                        else
-                            tile_out_tma<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
-                    }
-                } else {
-#pragma unroll 1
-                    for (int c0 = 0; c0 < BN; c0 += C::CHUNK) {
-                        uint32_t r[32];
-                        const uint32_t taddr = tmem_row + static_cast<uint32_t>(c0);
-                        if constexpr (C::CHUNK == 32)
-                            tmem_ld_x32(taddr, r);
-                        else
-                            tmem_ld_x16(taddr, r);
-                        tmem_ld_wait(r);
-                        epilogue_chunk<C::CHUNK>(p, w, row_base, lane, col_base + c0, r, stage);
-                    }
-                }
-            }
-            // every lane's tensor-memory reads are ordered before the warp's
-            // single release of the accumulator buffer
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                if (MODE == 2 && !leader)
-                    mbar_arrive_remote(mapa_shared(tempty0 + 8u * abuf, 0u));
-                else
-                    mbar_arrive(tempty0 + 8u * abuf);
-            }
-            if (++abuf == 2) {
-                abuf = 0;
-                aphase ^= 1u;
-            }
-        }
-        // the TMA stores must finish before the CTA exits
-        if (lane == 0) bulk_wait_group_all();
-        __syncwarp();
-    }
-
-    tc_fence_before_sync();
-    __syncthreads();
-    if constexpr (CM > 1)
-        cluster_sync();  // no CTA leaves while its peer may still touch its shared or tensor memory
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc_cg<CG>(tmem_base, C::TMEM_COLS);
-    }
-}
-
-template <int BN, int MODE>
-cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
-    constexpr int CM = Cfg<BN, MODE>::CM;
-    if constexpr (CM == 1) {
-        tc_gemm_kernel<BN, MODE><<<grid, TC_THREADS, Cfg<BN, MODE>::SMEM, stream>>>(p);
-        return cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CM;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, MODE>, p);
-    }
-}
-
-template <int BN, int MODE>
-cudaError_t prepare_bn() {
-    return cudaFuncSetAttribute(tc_gemm_kernel<BN, MODE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(Cfg<BN, MODE>::SMEM));
-}
-
-// Two-CTA clusters that can be resident at once (0 on error).
-template <int BN, int MODE>
-int max_clusters_bn() {
-    constexpr int CM = 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CM * 64);
-    cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, MODE>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-}  // namespace
+cudaError_t tc_prepare_general(int bn);
+cudaError_t tc_prepare_fast(int bn);
+int tc_max_pairs_general(int bn, int mode);
+cudaError_t tc_launch_general(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc_launch_fast(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 
 int tc_stages_for(int bn, int mode) {
     if (mode == 2) {
@@ -1090,24 +28,9 @@ int tc_stages_for(int bn, int mode) {
 }
 
 cudaError_t tc_prepare(int bn) {
-    switch (bn) {
-        case 16: return prepare_bn<16, 0>();
-        case 32: return prepare_bn<32, 0>();
-        case 64: return prepare_bn<64, 0>();
-        case 128: {
-            cudaError_t e = prepare_bn<128, 0>();
-            if (e == cudaSuccess) e = prepare_bn<128, 1>();
-            if (e == cudaSuccess) e = prepare_bn<128, 2>();
-            return e;
-        }
-        case 256: {
-            cudaError_t e = prepare_bn<256, 0>();
-            if (e == cudaSuccess) e = prepare_bn<256, 1>();
-            if (e == cudaSuccess) e = prepare_bn<256, 2>();
-            return e;
-        }
-    }
-    return cudaErrorInvalidValue;
+    cudaError_t e = tc_prepare_general(bn);
+    if (e == cudaSuccess) e = tc_prepare_fast(bn);
+    return e;
 }
 
 bool tc_has_mode(int bn, int mode) {
@@ -1117,35 +40,13 @@ bool tc_has_mode(int bn, int mode) {
     return false;
 }
 
-int tc_max_pairs(int bn, int mode) {
-    if (mode == 1 && bn == 128) return max_clusters_bn<128, 1>();
-    if (mode == 1 && bn == 256) return max_clusters_bn<256, 1>();
-    if (mode == 2 && bn == 128) return max_clusters_bn<128, 2>();
-    if (mode == 2 && bn == 256) return max_clusters_bn<256, 2>();
-    return 0;
-}
+int tc_max_pairs(int bn, int mode) { return tc_max_pairs_general(bn, mode); }
 
-cudaError_t tc_launch(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream) {
-    if (mode == 2) {
-        if (bn == 128) return launch_bn<128, 2>(p, grid, stream);
-        if (bn == 256) return launch_bn<256, 2>(p, grid, stream);
-        return cudaErrorInvalidValue;
-    }
-    if (mode == 1) {
-        switch (bn) {
-            case 128: return launch_bn<128, 1>(p, grid, stream);
-            case 256: return launch_bn<256, 1>(p, grid, stream);
-        }
-        return cudaErrorInvalidValue;
-    }
-    switch (bn) {
-        case 16: return launch_bn<16, 0>(p, grid, stream);
-        case 32: return launch_bn<32, 0>(p, grid, stream);
-        case 64: return launch_bn<64, 0>(p, grid, stream);
-        case 128: return launch_bn<128, 0>(p, grid, stream);
-        case 256: return launch_bn<256, 0>(p, grid, stream);
-    }
-    return cudaErrorInvalidValue;
+bool tc_has_fast(int bn) { return bn == 64 || bn == 128 || bn == 256; }
+
+cudaError_t tc_launch(int bn, int mode, int epi, const TcParams& p, int grid, cudaStream_t stream) {
+    if (epi == 1 && tc_has_fast(bn)) return tc_launch_fast(bn, mode, p, grid, stream);
+    return tc_launch_general(bn, mode, p, grid, stream);
 }
 
 }  // namespace dg

@@ -196,6 +196,7 @@ typedef struct {
                                 waves split evenly over all CTAs in contiguous ranges;
                                 2 each unit of the last partial wave cut into equal
                                 K pieces that run side by side                     */
+    int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue (GEMM_OPT_FAST_EPILOGUE) */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
@@ -215,9 +216,10 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         Kernel", step 2; 1 = plain row-major tile order), 1..64.
  *   GEMM_OPT_MAX_CTAS     cap on persistent CTAs (0 = one per SM).
  *   GEMM_OPT_TIMEOUT_US   bound on any single in-kernel wait, microseconds (>= 1).
- *   GEMM_OPT_CTA_PAIR     0 (default): pair CTAs along M when a problem has a full
- *                         wave of tile pairs; 1: never; 2: B-multicast pairs whenever
- *                         the tile width allows; 3: two-CTA MMA pairs likewise.
+ *   GEMM_OPT_CTA_PAIR     0 (default): two-CTA MMA pairs along M when a problem has a
+ *                         full wave of tile pairs and K >= 768; 1: never; 2: B-multicast
+ *                         pairs whenever the tile width allows; 3: two-CTA MMA pairs
+ *                         likewise.
  *   GEMM_OPT_SWAP_AB      0 (default): compute C^T = B^T A^T when M <= 64 < N;
  *                         1: never; 2: always.
  *   GEMM_OPT_L2_HINTS     L2 policy of the tensor-core operand loads: 0 (default) normal;
@@ -230,6 +232,10 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         partial-tile traffic and the workspace holds the partials;
  *                         1: never; 2: force the contiguous form (plan stream_k 1);
  *                         3: force the split form (plan stream_k 2) when S >= 2.
+ *   GEMM_OPT_FAST_EPILOGUE 0 (default): when no beta * C is read (beta == 0, or split-K
+ *                         partials) and C takes TMA stores, use the epilogue built for
+ *                         that case alone (64-column steps, fewer registers); 1: always
+ *                         the general epilogue.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -243,7 +249,8 @@ typedef enum {
     GEMM_OPT_CTA_PAIR = 5,
     GEMM_OPT_SWAP_AB = 6,
     GEMM_OPT_L2_HINTS = 7,
-    GEMM_OPT_STREAM_K = 8
+    GEMM_OPT_STREAM_K = 8,
+    GEMM_OPT_FAST_EPILOGUE = 9
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -319,3 +319,81 @@ def test_stream_k_unaligned_c(streamk):
     # st.global epilogue path (ldc not a multiple of 16 bytes)
     c = run_exact(Case("bf16", 700, 601, 1000, values="ints", pads=(0, 0, 1), seed=87))
     assert c.plan["stream_k"] == streamk
+
+
+# ---------------------------------------------------------------- epilogue forms
+
+@pytest.fixture
+def general_epilogue():
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.FAST_EPILOGUE, 1)
+    yield
+    dg.gemm_set_option(dg.Option.FAST_EPILOGUE, 0)
+
+
+# The TMA-store-only epilogue (beta == 0 or split-K partials) and the general
+# one do the same fp32 arithmetic in the same order, so they agree bit for bit;
+# each case also meets the oracle.  Shapes leave a ragged last 64-column step
+# (N % 64 != 0, with C rows still 16-byte aligned for TMA) and a ragged last
+# row block.
+FORM_CASES = {
+    "bf16_bias_gelu": dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", alpha=0.5, bias=True,
+                           act="gelu_tanh"),
+    "f16_out": dict(ab="f16", M=300, N=520, K=200, c_dtype="f16", alpha=2.0),
+    "f32_out_bias": dict(ab="bf16", M=260, N=332, K=450, c_dtype="f32", bias=True),
+    "batched_bf16": dict(ab="bf16", M=200, N=264, K=130, batch=3, c_dtype="bf16", bias=True),
+    "splitk_partials": dict(ab="bf16", M=130, N=200, K=2048, c_dtype="bf16", split_k=4,
+                            bias=True, act="gelu_tanh"),
+    # swap-AB computes C^T: a column-major C makes it row-major, and the bias
+    # runs along its rows
+    "swap_row_bias": dict(ab="bf16", M=40, N=900, K=256, lc="col", c_dtype="f32", bias=True),
+    "pair_mma": dict(ab="bf16", M=1100, N=1304, K=320, c_dtype="bf16", alpha=0.25, bias=True,
+                     opts={"CTA_PAIR": 3}),
+    "pair_multicast": dict(ab="bf16", M=700, N=600, K=200, c_dtype="f32", opts={"CTA_PAIR": 2}),
+}
+
+
+def _form_run(name, seed):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(FORM_CASES[name])
+    opts = kw.pop("opts", {})
+    for k, v in opts.items():
+        dg.gemm_set_option(dg.Option[k], v)
+    try:
+        c = Case(seed=seed, **kw)
+        st, out = c.run_gpu()
+    finally:
+        for k in opts:
+            dg.gemm_set_option(dg.Option[k], 0)
+    assert st == 0, f"status {st}"
+    return c, out
+
+
+@pytest.mark.parametrize("name", sorted(FORM_CASES))
+def test_fast_epilogue_matches_general(name):
+    import dense_gemm_bf16_gb300 as dg
+    fast, out_fast = _form_run(name, 301)
+    assert fast.plan["fast_epilogue"] == 1, fast.plan
+    if "opts" in FORM_CASES[name]:
+        assert fast.plan["cta_pair"] == FORM_CASES[name]["opts"]["CTA_PAIR"] - 1, fast.plan
+    check_close(fast, fast.result(out_fast), fast.oracle_full())
+    assert fast.untouched_padding(out_fast)
+    dg.gemm_set_option(dg.Option.FAST_EPILOGUE, 1)
+    try:
+        gen, out_gen = _form_run(name, 301)
+    finally:
+        dg.gemm_set_option(dg.Option.FAST_EPILOGUE, 0)
+    assert gen.plan["fast_epilogue"] == 0
+    assert np.array_equal(out_fast.view(np.uint8), out_gen.view(np.uint8))
+
+
+def test_beta_uses_general_epilogue():
+    c = run_close(Case("bf16", 300, 520, 200, c_dtype="bf16", beta=0.5, seed=311))
+    assert c.plan["fast_epilogue"] == 0
+
+
+@pytest.mark.parametrize("shape", [(700, 600, 333), (4097, 700, 64)])
+def test_exact_general_epilogue_forced(general_epilogue, shape):
+    M, N, K = shape
+    c = run_exact(Case("bf16", M, N, K, values="ints", seed=321 + M))
+    assert c.plan["fast_epilogue"] == 0
