@@ -54,6 +54,7 @@ class Option(enum.IntEnum):
     L2_HINTS = 7
     STREAM_K = 8
     FAST_EPILOGUE = 9
+    SGEMM_KERNEL = 10
 
 
 class Plan(ctypes.Structure):

@@ -30,6 +30,7 @@ std::atomic<int64_t> g_opt_swap_ab{0};
 std::atomic<int64_t> g_opt_l2_hints{0};
 std::atomic<int64_t> g_opt_stream_k{0};
 std::atomic<int64_t> g_opt_fast_epilogue{0};
+std::atomic<int64_t> g_opt_sgemm_kernel{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -68,6 +69,7 @@ gemm_status_t device_state(DevState** out) {
             e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word);
             for (int bn : kBlockN)
                 if (e == cudaSuccess) e = tc_prepare(bn);
+            if (e == cudaSuccess) e = sgemm_prepare();
             if (e == cudaSuccess) {
                 for (int mode = 1; mode <= 2; ++mode) {
                     d.max_pairs[mode][0] = tc_max_pairs(128, mode);
@@ -536,8 +538,14 @@ gemm_status_t run(const Call& c) {
         p.batch = static_cast<int32_t>(c.batch);
         p.a_vec_ok = aligned(c.A, 16) && c.lda % 4 == 0 && p.stride_a % 4 == 0;
         p.b_vec_ok = aligned(c.B, 16) && c.ldb % 4 == 0 && p.stride_b % 4 == 0;
+        // the cp.async kernel (128 x 64 tiles) for row-major, 16-byte aligned A
+        // and B; the register-staged one (128 x 128 tiles) for everything else
+        p.kernel = g_opt_sgemm_kernel.load() == 0 && p.a_row && p.b_row && p.a_vec_ok &&
+                           p.b_vec_ok
+                       ? 0
+                       : 1;
         p.num_pid_m = static_cast<int32_t>(cdiv(c.M, 128));
-        p.num_pid_n = static_cast<int32_t>(cdiv(c.N, 128));
+        p.num_pid_n = static_cast<int32_t>(cdiv(c.N, p.kernel == 0 ? 64 : 128));
         p.group_m = pl.group_m;
         p.epi = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
         return sgemm_launch(p, c.stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -867,6 +875,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
             g_opt_fast_epilogue.store(value);
             return GEMM_OK;
+        case GEMM_OPT_SGEMM_KERNEL:
+            if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+            g_opt_sgemm_kernel.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -882,6 +894,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_L2_HINTS: return g_opt_l2_hints.load();
         case GEMM_OPT_STREAM_K: return g_opt_stream_k.load();
         case GEMM_OPT_FAST_EPILOGUE: return g_opt_fast_epilogue.load();
+        case GEMM_OPT_SGEMM_KERNEL: return g_opt_sgemm_kernel.load();
     }
     return -1;
 }

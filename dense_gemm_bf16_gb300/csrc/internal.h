@@ -92,10 +92,12 @@ struct SgemmParams {
     const float* B; int64_t ldb; int64_t stride_b; int32_t b_row;
     int32_t M, N, K, batch;
     int32_t a_vec_ok, b_vec_ok;   // float4 global loads allowed
+    int32_t kernel;               // 0 cp.async packed-FMA kernel (row-major A and B); 1 register-staged
     int32_t num_pid_m, num_pid_n, group_m;
     Epilogue epi;
 };
 cudaError_t sgemm_launch(const SgemmParams& p, cudaStream_t stream);
+cudaError_t sgemm_prepare();  // dynamic shared memory attributes (per device)
 
 // Dense copy of a rows x cols 16-bit matrix stored with (ld, batch stride) into
 // dst with leading dimension ld_dst and batch stride rows*ld_dst.

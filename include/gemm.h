@@ -236,6 +236,13 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         partials) and C takes TMA stores, use the epilogue built for
  *                         that case alone (64-column steps, fewer registers); 1: always
  *                         the general epilogue.
+ *   GEMM_OPT_SGEMM_KERNEL 0 (default): the fp32 CUDA-core path with row-major A and B
+ *                         whose rows are 16-byte aligned uses the kernel that copies
+ *                         tiles with cp.async and issues packed fp32 FMAs (128 x 64
+ *                         tiles, three CTAs per SM); other layouts use the register-
+ *                         staged kernel (128 x 128 tiles); 1: always the register-staged
+ *                         kernel.  Both add each output's products in ascending k with
+ *                         one rounding per FMA, so their results are identical.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -250,7 +257,8 @@ typedef enum {
     GEMM_OPT_SWAP_AB = 6,
     GEMM_OPT_L2_HINTS = 7,
     GEMM_OPT_STREAM_K = 8,
-    GEMM_OPT_FAST_EPILOGUE = 9
+    GEMM_OPT_FAST_EPILOGUE = 9,
+    GEMM_OPT_SGEMM_KERNEL = 10
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -197,6 +197,37 @@ def test_sgemm_batched_unaligned():
                    offsets=(1, 2, 3), seed=53))
 
 
+# Row-major A and B with 16-byte aligned rows take the cp.async kernel; the
+# padding keeps lda = 272 and ldb = 260 multiples of 4 while K = 270 and N = 258
+# end inside a 16-byte copy, so the zero-filled tails are exercised.
+def test_sgemm_async_exact_ragged():
+    c = run_exact(Case("f32", 300, 258, 270, values="ints", pads=(2, 2, 0), seed=55))
+    assert c.lda % 4 == 0 and c.ldb % 4 == 0
+
+
+def test_sgemm_async_batched():
+    run_exact(Case("f32", 70, 92, 36, batch=3, values="ints", seed=56))
+
+
+@pytest.mark.parametrize("shape", [(300, 258, 270), (129, 260, 1000)])
+def test_sgemm_async_matches_register_staged(shape):
+    # both kernels add the products of each output in ascending k with fmaf
+    import dense_gemm_bf16_gb300 as dg
+    M, N, K = shape
+    kw = dict(alpha=1.5, beta=0.5, bias=True, act="gelu_tanh", pads=(2, 2, 0), seed=57)
+    fast = Case("f32", M, N, K, **kw)
+    st, out_a = fast.run_gpu()
+    assert st == 0
+    check_close(fast, fast.result(out_a), fast.oracle_full())
+    dg.gemm_set_option(dg.Option.SGEMM_KERNEL, 1)
+    try:
+        st, out_b = Case("f32", M, N, K, **kw).run_gpu()
+    finally:
+        dg.gemm_set_option(dg.Option.SGEMM_KERNEL, 0)
+    assert st == 0
+    assert np.array_equal(out_a.view(np.uint8), out_b.view(np.uint8))
+
+
 def test_sgemm_is_true_fp32():
     # TF32 would keep 10 mantissa bits (rms error ~3e-4); fp32 FFMA gives ~1e-6.
     c = Case("f32", 256, 256, 1024, seed=54)
