@@ -560,6 +560,23 @@ def build_row(name, device):
     raise ValueError(f"unknown row {name!r}")
 
 
+def fp32_peak_tflops(device):
+    """FP32 CUDA-core peak from unit counts and the clock: SMs x 128 FMA lanes x
+    2 FLOP x the maximum SM clock (nvidia-smi), in TFLOP/s; None if unknown."""
+    import subprocess
+
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(torch.cuda.current_device()),
+                              "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=20).stdout
+        mhz = float(out.strip().splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        return None, None
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, mhz
+
+
 def measure_rows(names, device, reps=20):
     """Times each named path with its roofline fraction: `reps` launches after
     3 warm-ups, each preceded by a write of a buffer larger than L2 (so every
@@ -600,7 +617,11 @@ def measure_rows(names, device, reps=20):
         elif bound == "tensor":
             r["peak"], r["frac"] = peaks["bf16_tflops"], r["tflops"] / peaks["bf16_tflops"]
         else:
-            r["peak"] = None  # fp32 FMA pipe: peak from SM count x 128 FFMA x 2 x clock
+            # fp32 FMA pipe: SM count x 128 lanes x 2 FLOP x the maximum SM clock
+            pk, mhz = fp32_peak_tflops(device)
+            r["peak"] = pk
+            r["peak_source"] = f"derived: SMs x 128 FMA lanes x 2 x {mhz} MHz" if pk else None
+            r["frac"] = r["tflops"] / pk if pk else None
         out.append(r)
         del keep
         for k, v in saved.items():
