@@ -24,7 +24,7 @@ _lib = None
 
 DT = {"bf16": 0, "f16": 1, "f32": 2, "f64": 3}
 LAYOUT = {"row": 0, "col": 1}
-ACT = {"none": 0, "gelu_tanh": 1}
+ACT = {"none": 0, "gelu_tanh": 1, "relu": 2, "gelu_erf": 3}
 
 
 def build(force: bool = False) -> str:
@@ -53,13 +53,23 @@ def _load():
                       vp, i64, i32, i64,
                       vp, i64, i32, i64,
                       vp, i64, i32, i64,
-                      dbl, dbl, vp, i32]
+                      dbl, dbl, vp, i32, i32]
+            strided = [i32, i32, i64, i64, i64, i64,
+                       vp, i64, i64, i64,
+                       vp, i64, i64, i64,
+                       vp, i64, i64, i64,
+                       dbl, dbl, vp, i32, i32]
             lib.oracle_gemm.argtypes = common + [vp]
             lib.oracle_gemm.restype = i32
             lib.oracle_gemm_sampled.argtypes = common + [i64, vp, vp, vp, vp]
             lib.oracle_gemm_sampled.restype = i32
-            lib.oracle_gelu_tanh.argtypes = [dbl]
-            lib.oracle_gelu_tanh.restype = dbl
+            lib.oracle_gemm_strided.argtypes = strided + [vp]
+            lib.oracle_gemm_strided.restype = i32
+            lib.oracle_gemm_strided_sampled.argtypes = strided + [i64, vp, vp, vp, vp]
+            lib.oracle_gemm_strided_sampled.restype = i32
+            for fn in ("oracle_gelu_tanh", "oracle_gelu_erf", "oracle_relu"):
+                getattr(lib, fn).argtypes = [dbl]
+                getattr(lib, fn).restype = dbl
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_bf16.restype = dbl
             lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
@@ -87,12 +97,14 @@ class Problem:
 
     Buffers are flat numpy arrays holding the storage (uint16 bit patterns for
     bf16/f16, float32 for f32); ``ld``/``layout``/``stride`` give the indexing.
+    With ``strides`` = ((rs, cs) of A, of B, of C) every element (r, c) is at
+    r*rs + c*cs instead, and ld/layout are not used.
     """
 
-    def __init__(self, *, ab_dtype, M, N, K, A, lda, la, B, ldb, lb,
+    def __init__(self, *, ab_dtype, M, N, K, A, B, lda=0, la="row", ldb=0, lb="row",
                  c_dtype="f32", C0=None, ldc=None, lc="row", batch=1,
                  stride_a=0, stride_b=0, stride_c=0, alpha=1.0, beta=0.0,
-                 bias=None, act="none"):
+                 bias=None, act="none", bias_rows=False, strides=None):
         self.ab_dtype, self.c_dtype = ab_dtype, c_dtype
         self.M, self.N, self.K, self.batch = int(M), int(N), int(K), int(batch)
         self.A, self.B = _storage(A, ab_dtype), _storage(B, ab_dtype)
@@ -104,19 +116,34 @@ class Problem:
         self.alpha, self.beta = float(alpha), float(beta)
         self.bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
         self.act = act
+        self.bias_rows = 1 if bias_rows else 0
+        self.strides = None if strides is None else [tuple(int(v) for v in st) for st in strides]
 
     def _args(self):
+        if self.strides is not None:
+            (ars, acs), (brs, bcs), (crs, ccs) = self.strides
+            return [DT[self.ab_dtype], DT[self.c_dtype], self.batch, self.M, self.N, self.K,
+                    _ptr(self.A), ars, acs, self.stride_a,
+                    _ptr(self.B), brs, bcs, self.stride_b,
+                    _ptr(self.C0), crs, ccs, self.stride_c,
+                    self.alpha, self.beta, _ptr(self.bias), self.bias_rows, ACT[self.act]]
         return [DT[self.ab_dtype], DT[self.c_dtype], self.batch, self.M, self.N, self.K,
                 _ptr(self.A), self.lda, LAYOUT[self.la], self.stride_a,
                 _ptr(self.B), self.ldb, LAYOUT[self.lb], self.stride_b,
                 _ptr(self.C0), self.ldc, LAYOUT[self.lc], self.stride_c,
-                self.alpha, self.beta, _ptr(self.bias), ACT[self.act]]
+                self.alpha, self.beta, _ptr(self.bias), self.bias_rows, ACT[self.act]]
+
+    def _fns(self):
+        lib = _load()
+        if self.strides is not None:
+            return lib.oracle_gemm_strided, lib.oracle_gemm_strided_sampled
+        return lib.oracle_gemm, lib.oracle_gemm_sampled
 
 
 def gemm(p: Problem) -> np.ndarray:
     """Full fp64 result, shape [batch, M, N]."""
     out = np.empty((p.batch, p.M, p.N), dtype=np.float64)
-    rc = _load().oracle_gemm(*p._args(), _ptr(out))
+    rc = p._fns()[0](*p._args(), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle_gemm rejected its arguments (rc={rc})")
     return out
@@ -131,8 +158,7 @@ def gemm_sampled(p: Problem, b_idx, i_idx, j_idx) -> np.ndarray:
     if not (len(b_idx) == len(i_idx) == len(j_idx)):
         raise ValueError("index arrays differ in length")
     out = np.empty(len(i_idx), dtype=np.float64)
-    rc = _load().oracle_gemm_sampled(*p._args(), len(i_idx), _ptr(b_idx), _ptr(i_idx),
-                                     _ptr(j_idx), _ptr(out))
+    rc = p._fns()[1](*p._args(), len(i_idx), _ptr(b_idx), _ptr(i_idx), _ptr(j_idx), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle_gemm_sampled rejected its arguments (rc={rc})")
     return out
@@ -140,6 +166,14 @@ def gemm_sampled(p: Problem, b_idx, i_idx, j_idx) -> np.ndarray:
 
 def gelu_tanh(x: float) -> float:
     return _load().oracle_gelu_tanh(float(x))
+
+
+def gelu_erf(x: float) -> float:
+    return _load().oracle_gelu_erf(float(x))
+
+
+def relu(x: float) -> float:
+    return _load().oracle_relu(float(x))
 
 
 def decode_bf16(bits: int) -> float:

@@ -18,19 +18,23 @@ SRC = os.path.join(ROOT, "oracle", "oracle_gemm.c")
 MUTANTS = {
     "drop_first_k_term": ("for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 1; k < K; ++k) {"),
     "wrong_beta_sign": ("v += beta * mat(", "v -= beta * mat("),
-    "transposed_index": ("r * ld + c : c * ld + r", "c * ld + r : r * ld + c"),
+    "transposed_index": ("*rs = layout == OR_ROW ? ld : 1;", "*rs = layout == OR_ROW ? 1 : ld;"),
     "batch_stride_ignored": ("int64_t idx = b * stride + ", "int64_t idx = 0 * stride + "),
     "alpha_dropped": ("double v = alpha * acc;", "double v = acc;"),
     "beta_zero_reads_C": ("if (beta != 0.0) v += beta", "v += beta"),
     "gelu_cubic_constant": ("0.044715 * x * x * x", "0.04715 * x * x * x"),
     "gelu_scale_constant": ("sqrt(2.0 / M_PI)", "sqrt(1.0 / M_PI)"),
     "bias_after_activation": (
-        "    if (bias) v += (double)bias[j];\n    if (act == OR_ACT_GELU_TANH) v = oracle_gelu_tanh(v);",
-        "    if (act == OR_ACT_GELU_TANH) v = oracle_gelu_tanh(v);\n    if (bias) v += (double)bias[j];"),
+        "    if (bias) v += (double)bias[bias_rows ? i : j];\n    if (act == OR_ACT_GELU_TANH) v = oracle_gelu_tanh(v);",
+        "    if (act == OR_ACT_GELU_TANH) v = oracle_gelu_tanh(v);\n    if (bias) v += (double)bias[bias_rows ? i : j];"),
     "bf16_shift": ("(uint32_t)h << 16", "(uint32_t)h << 15"),
     "f16_exponent_bias": ("e - 25", "e - 24"),
     "f16_subnormal_scale": ("ldexp((double)m, -24)", "ldexp((double)m, -25)"),
-    "k_loop_reversed_operands": ("mat(B, ab_dt, lb, ldb, sb, b, k, j)", "mat(B, ab_dt, lb, ldb, sb, b, j, k)"),
+    "k_loop_reversed_operands": ("mat(B, ab_dt, brs, bcs, sb, b, k, j);", "mat(B, ab_dt, brs, bcs, sb, b, j, k);"),
+    "relu_passes_negatives": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : -x;"),
+    "gelu_erf_scale": ("erf(x / sqrt(2.0))", "erf(x / 2.0)"),
+    "bias_orientation_swapped": ("bias[bias_rows ? i : j]", "bias[bias_rows ? j : i]"),
+    "strided_column_stride_dropped": ("int64_t idx = b * stride + r * rs + c * cs;", "int64_t idx = b * stride + r * rs + c;"),
 }
 
 

@@ -17,7 +17,14 @@ itself:
   beta == 0 does not read C, K == 0;
 * GELU(tanh): odd-part identity, value at 0, the Taylor coefficients of the
   closed form (which pin sqrt(2/pi) and 0.044715), the large-|x| limits, and
-  closeness to the exact erf GELU of the same paper.
+  closeness to the exact erf GELU of the same paper;
+* GELU(erf) = x Phi(x): standard normal table values of Phi, the odd-part
+  identity, and its curvature at 0 (2 phi(0) = sqrt(2/pi), which pins the
+  sqrt(2) inside erf); ReLU on signed values and NaN;
+* the epilogue's wiring of each activation (equal to the activation applied
+  to the identity-activation result), bias along columns or rows (closed
+  form with identity B on non-square shapes), and storage by arbitrary
+  (row, column) strides (closed form, and equal to the row-major result).
 """
 from __future__ import annotations
 
@@ -85,7 +92,7 @@ def representable(x, dt):
 
 
 def make_problem(oracle, A, B, dt, la, lb, *, C0=None, c_dt="f32", lc="row", alpha=1.0,
-                 beta=0.0, bias=None, act="none", pad=0, bstride_a=None, bstride_b=None):
+                 beta=0.0, bias=None, act="none", pad=0, bstride_a=None, bstride_b=None, bias_rows=False):
     A = np.asarray(A, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     if A.ndim == 2:
@@ -114,7 +121,7 @@ def make_problem(oracle, A, B, dt, la, lb, *, C0=None, c_dt="f32", lc="row", alp
     return oracle.Problem(ab_dtype=dt, M=M, N=N, K=K, A=fa, lda=lda, la=la, B=fb, ldb=ldb,
                           lb=lb, c_dtype=c_dt, C0=fc, ldc=ldc, lc=lc, batch=nb,
                           stride_a=sa, stride_b=sb, stride_c=sc, alpha=alpha, beta=beta,
-                          bias=bias, act=act)
+                          bias=bias, act=act, bias_rows=bias_rows)
 
 
 # ---------------------------------------------------------------------------
@@ -442,3 +449,112 @@ def test_gelu_applied_after_bias(oracle_mod):
     for i in range(M):
         for j in range(N):
             assert got[i, j] == oracle_mod.gelu_tanh(2.0 * C0[i, j] + float(bias[j]))
+
+
+# ---------------------------------------------------------------------------
+# GELU (erf form), ReLU, bias orientation, general strides
+# ---------------------------------------------------------------------------
+
+# Phi(x) of the standard normal distribution, from standard normal tables
+# (values to 16 digits, e.g. Abramowitz & Stegun, table 26.1).
+PHI_TABLE = {1.0: 0.8413447460685429, 1.96: 0.9750021048517795, -0.5: 0.3085375387259869,
+             2.5: 0.9937903346742238}
+
+
+@pytest.mark.parametrize("x", sorted(PHI_TABLE))
+def test_gelu_erf_is_x_phi(oracle_mod, x):
+    assert oracle_mod.gelu_erf(x) == pytest.approx(x * PHI_TABLE[x], rel=1e-14)
+
+
+def test_gelu_erf_odd_part_and_curvature(oracle_mod):
+    g = oracle_mod.gelu_erf
+    assert g(0.0) == 0.0
+    for x in (0.1, 0.7, 1.3, 4.0):
+        # Phi(x) + Phi(-x) = 1  =>  g(x) - g(-x) = x
+        assert g(x) - g(-x) == pytest.approx(x, rel=1e-14)
+    # g'(0) = Phi(0) = 1/2 and g''(0) = 2 phi(0) = sqrt(2/pi): central differences
+    h = 1e-4
+    assert (g(h) - g(-h)) / (2 * h) == pytest.approx(0.5, abs=1e-9)
+    assert (g(h) - 2 * g(0.0) + g(-h)) / h ** 2 == pytest.approx(math.sqrt(2 / math.pi), rel=1e-5)
+
+
+def test_relu_definition(oracle_mod):
+    r = oracle_mod.relu
+    assert [r(x) for x in (-2.0, -0.0, 0.0, 3.5, 1e-300)] == [0.0, 0.0, 0.0, 3.5, 1e-300]
+    assert r(float("nan")) == 0.0
+
+
+def _wiring_case(oracle_mod, act, bias_rows=False):
+    M, N, K = 7, 5, 9
+    A = representable(datagen.uniform(71, (M, K)), "bf16")
+    B = representable(datagen.uniform(72, (K, N)), "bf16")
+    bias = representable(datagen.normal(73, (M if bias_rows else N,)), "f32")
+    p = make_problem(oracle_mod, A, B, "bf16", "row", "row", alpha=1.5, bias=bias,
+                     act=act, bias_rows=bias_rows)
+    return oracle_mod.gemm(p)[0], A, B, bias
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu_erf", "gelu_tanh"])
+@pytest.mark.parametrize("bias_rows", [False, True])
+def test_activation_applied_to_identity_result(oracle_mod, act, bias_rows):
+    got, *_ = _wiring_case(oracle_mod, act, bias_rows)
+    ident, *_ = _wiring_case(oracle_mod, "none", bias_rows)
+    fn = {"relu": oracle_mod.relu, "gelu_erf": oracle_mod.gelu_erf,
+          "gelu_tanh": oracle_mod.gelu_tanh}[act]
+    want = np.vectorize(fn)(ident)
+    assert np.array_equal(got, want)
+    if act == "relu":
+        assert np.array_equal(got, np.maximum(ident, 0.0))
+
+
+@pytest.mark.parametrize("M,N", [(9, 4), (4, 9)])
+def test_bias_orientation_closed_form(oracle_mod, M, N):
+    # B = identity (N = K): R = alpha * A + bias, bias along columns (length N)
+    # or along rows (length M); non-square so that the orientations differ
+    A = representable(datagen.uniform(74, (M, N)), "bf16")
+    bias_c = representable(datagen.normal(75, (N,)), "f32")
+    bias_r = representable(datagen.normal(76, (M,)), "f32")
+    pc = make_problem(oracle_mod, A, np.eye(N), "bf16", "row", "row", alpha=0.5, bias=bias_c)
+    pr = make_problem(oracle_mod, A, np.eye(N), "bf16", "row", "row", alpha=0.5, bias=bias_r,
+                      bias_rows=True)
+    assert np.array_equal(oracle_mod.gemm(pc)[0], 0.5 * A + bias_c[None, :])
+    assert np.array_equal(oracle_mod.gemm(pr)[0], 0.5 * A + bias_r[:, None])
+
+
+def _store_strided(vals, rs, cs, dt, size):
+    """Logical [R, C] values placed at r*rs + c*cs in a NaN-filled buffer."""
+    R, C = vals.shape
+    buf = np.zeros(size)
+    used = np.zeros(size, dtype=bool)
+    for r in range(R):
+        for c in range(C):
+            buf[r * rs + c * cs] = vals[r, c]
+            used[r * rs + c * cs] = True
+    assert used.sum() == R * C  # the map is injective
+    out = datagen.encode(buf, dt)
+    out[~used] = np.nan if dt == "f32" else NAN_BITS[dt]
+    return out
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_strided_storage(oracle_mod, dt):
+    M, N, K = 5, 6, 7
+    A = representable(datagen.uniform(77, (M, K)), dt)
+    B = representable(datagen.uniform(78, (K, N)), dt)
+    C0 = representable(datagen.normal(79, (M, N)), "f32")
+    # A with row stride 3 and column stride 17, B transposed with a gap, C
+    # interleaved: every map is injective and none is row- or column-major
+    fa = _store_strided(A, 3, 17, dt, 3 * M + 17 * K)
+    fb = _store_strided(B, 2, 2 * K + 3, dt, 2 * K + (2 * K + 3) * N)
+    fc = _store_strided(C0, 2 * N + 1, 2, "f32", (2 * N + 1) * M + 2 * N)
+    strided = oracle_mod.Problem(ab_dtype=dt, M=M, N=N, K=K, A=fa, B=fb, c_dtype="f32", C0=fc,
+                                 alpha=1.25, beta=-0.5,
+                                 strides=[(3, 17), (2, 2 * K + 3), (2 * N + 1, 2)])
+    dense = make_problem(oracle_mod, A, B, dt, "row", "row", C0=C0, alpha=1.25, beta=-0.5)
+    got = oracle_mod.gemm(strided)
+    assert np.array_equal(got, oracle_mod.gemm(dense))
+    # closed form with B = identity, stored with strides
+    fi = _store_strided(np.eye(K), 1, K + 2, dt, (K + 2) * K)
+    pid = oracle_mod.Problem(ab_dtype=dt, M=M, N=K, K=K, A=fa, B=fi, c_dtype="f32",
+                             alpha=2.0, strides=[(3, 17), (1, K + 2), (K, 1)])
+    assert np.array_equal(oracle_mod.gemm(pid)[0], 2.0 * A)
