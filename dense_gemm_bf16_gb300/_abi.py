@@ -42,6 +42,14 @@ class Epi(enum.IntEnum):
     BIAS = 1
     GELU_TANH = 2
     BIAS_GELU_TANH = 3
+    RELU = 4
+    BIAS_RELU = 5
+    GELU_ERF = 6
+    BIAS_GELU_ERF = 7
+    ROW_BIAS = 9
+    ROW_BIAS_GELU_TANH = 11
+    ROW_BIAS_RELU = 13
+    ROW_BIAS_GELU_ERF = 15
 
 
 class Option(enum.IntEnum):

@@ -1,6 +1,8 @@
 // Element-wise epilogue shared by the tensor-core kernel, the CUDA-core
 // SGEMM and the split-K reduction:
 //     x = act(alpha * acc + beta * C + bias)
+// with act the identity, GELU (tanh form or erf form) or ReLU, and the bias
+// indexed by column or by row.
 // applied once, after accumulation ("Skill: Write a Triton GEMM Kernel",
 // Required reasoning process step 6 and Common failure modes on beta*C),
 // then rounded once to the output type ("GEMM Kernel Optimization", Common
@@ -29,6 +31,37 @@ __device__ __forceinline__ float gelu_tanh(float x) {
     const float e = __expf(2.0f * y);
     const float t = 1.0f - __fdividef(2.0f, e + 1.0f);
     return 0.5f * x * (1.0f + t);
+}
+
+// GELU itself (the same paper): gelu(x) = x Phi(x) = 0.5 x (1 + erf(x / sqrt(2))),
+// with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float x) {
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+// Rectifier: x for x > 0, else 0 (a NaN gives 0).
+__device__ __forceinline__ float relu(float x) { return x > 0.0f ? x : 0.0f; }
+
+__device__ __forceinline__ float apply_act(float x, int act) {
+    if (act == ACT_GELU_TANH) return gelu_tanh(x);
+    if (act == ACT_RELU) return relu(x);
+    if (act == ACT_GELU_ERF) return gelu_erf(x);
+    return x;
+}
+
+// The activation over NV values held in registers, the branch taken once.
+template <int NV>
+__device__ __forceinline__ void act_inplace(float* v, int act) {
+    if (act == ACT_GELU_TANH) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = gelu_tanh(v[i]);
+    } else if (act == ACT_RELU) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = relu(v[i]);
+    } else if (act == ACT_GELU_ERF) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) v[i] = gelu_erf(v[i]);
+    }
 }
 
 __device__ __forceinline__ float load_elem(const void* p, int dt) {
@@ -61,7 +94,7 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int64_t b, int
     float x = e.alpha * acc;
     if (e.beta != 0.0f) x = fmaf(e.beta, load_elem(c, e.c_dtype), x);
     if (e.bias) x += e.bias_on_rows ? e.bias[i] : e.bias[j];
-    if (e.act == ACT_GELU_TANH) x = gelu_tanh(x);
+    x = apply_act(x, e.act);
     store_elem(c, e.c_dtype, x);
 }
 

@@ -106,6 +106,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 inline int dt_bytes(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+// gemm_epilogue_t fields: bit 0 bias, bits 1-2 activation, bit 3 bias along rows
+inline bool epi_valid(int epi) { return epi >= 0 && epi <= 15 && !((epi & 8) && !(epi & 1)); }
+inline bool epi_bias(int epi) { return (epi & 1) != 0; }
+inline bool epi_row_bias(int epi) { return (epi & 8) != 0; }
+inline int epi_act(int epi) {
+    switch ((epi >> 1) & 3) {
+        case 1: return ACT_GELU_TANH;
+        case 2: return ACT_RELU;
+        case 3: return ACT_GELU_ERF;
+    }
+    return ACT_NONE;
+}
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct Call {
@@ -172,7 +185,7 @@ gemm_status_t validate(const Call& c) {
     if (c.ab != DT_F32 && c.cdt != DT_F32 && c.cdt != c.ab) return GEMM_ERR_UNSUPPORTED;
     for (int l : {c.la, c.lb, c.lc})
         if (l != GEMM_ROW_MAJOR && l != GEMM_COL_MAJOR) return GEMM_ERR_INVALID_ARG;
-    if (c.epi < GEMM_EPI_NONE || c.epi > GEMM_EPI_BIAS_GELU_TANH) return GEMM_ERR_INVALID_ARG;
+    if (!epi_valid(c.epi)) return GEMM_ERR_INVALID_ARG;
     if (c.batch < 0 || c.M < 0 || c.N < 0 || c.K < 0 || c.split_k < 0) return GEMM_ERR_INVALID_ARG;
     const int64_t lim = 0x7FFFFFFF;
     if (c.batch > lim || c.M > lim || c.N > lim || c.K > lim) return GEMM_ERR_INVALID_ARG;
@@ -186,8 +199,7 @@ gemm_status_t validate(const Call& c) {
         // C[b] must not overlap
         if (c.sc < (c_outer - 1) * c.ldc + c_inner) return GEMM_ERR_INVALID_ARG;
     }
-    const bool has_bias = c.epi == GEMM_EPI_BIAS || c.epi == GEMM_EPI_BIAS_GELU_TANH;
-    if (has_bias && (!c.bias || !aligned(c.bias, 4))) return GEMM_ERR_INVALID_ARG;
+    if (epi_bias(c.epi) && (!c.bias || !aligned(c.bias, 4))) return GEMM_ERR_INVALID_ARG;
     if (c.K > 0 && c.alpha != 0.0f) {
         if (!c.A || !c.B) return GEMM_ERR_INVALID_ARG;
         if (!aligned(c.A, dt_bytes(c.ab)) || !aligned(c.B, dt_bytes(c.ab)))
@@ -427,6 +439,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     return GEMM_OK;
 }
 
+// bias_on_rows: the computed problem is the caller's transposed (swap-AB).
 Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
     Epilogue e{};
     e.C = c.C;
@@ -441,11 +454,10 @@ Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
                      : 0;
     e.alpha = c.alpha;
     e.beta = c.beta;
-    const bool has_bias = c.epi == GEMM_EPI_BIAS || c.epi == GEMM_EPI_BIAS_GELU_TANH;
-    e.bias = has_bias ? c.bias : nullptr;
-    e.bias_on_rows = bias_on_rows ? 1 : 0;
-    e.act = (c.epi == GEMM_EPI_GELU_TANH || c.epi == GEMM_EPI_BIAS_GELU_TANH) ? ACT_GELU_TANH
-                                                                               : ACT_NONE;
+    e.bias = epi_bias(c.epi) ? c.bias : nullptr;
+    // a row bias of the caller's problem runs along the columns of a swapped one
+    e.bias_on_rows = (bias_on_rows != epi_row_bias(c.epi)) ? 1 : 0;
+    e.act = epi_act(c.epi);
     return e;
 }
 

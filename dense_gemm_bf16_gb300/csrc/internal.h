@@ -8,7 +8,7 @@
 namespace dg {
 
 enum : int { DT_BF16 = 0, DT_F16 = 1, DT_F32 = 2 };
-enum : int { ACT_NONE = 0, ACT_GELU_TANH = 1 };
+enum : int { ACT_NONE = 0, ACT_GELU_TANH = 1, ACT_RELU = 2, ACT_GELU_ERF = 3 };
 
 // Tile of the tensor-core kernel: BLOCK_M x BLOCK_N output, K consumed in
 // BLOCK_K = 64 slices (64 bf16 = one 128-byte swizzle row).
@@ -28,7 +28,7 @@ struct Epilogue {
     float alpha, beta;
     const float* bias;       // may be null
     int32_t bias_on_rows;    // 1: bias indexed by row i (swapped problem), 0: by column j
-    int32_t act;             // ACT_NONE / ACT_GELU_TANH
+    int32_t act;             // ACT_NONE / ACT_GELU_TANH / ACT_RELU / ACT_GELU_ERF
 };
 
 // Parameters of the persistent tcgen05 kernel (passed as a __grid_constant__).

@@ -134,13 +134,16 @@ __device__ __forceinline__ void sgemm_store(const SgemmParams& p, int b, int m0,
                     v[3] = fmaf(e.beta, o.w, v[3]);
                 }
                 if (e.bias) {
+                    if (e.bias_on_rows) {
+                        const float br = e.bias[m];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] += e.bias[n + j];
-                }
-                if (e.act == ACT_GELU_TANH) {
+                        for (int j = 0; j < 4; ++j) v[j] += br;
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = gelu_tanh(v[j]);
+                        for (int j = 0; j < 4; ++j) v[j] += e.bias[n + j];
+                    }
                 }
+                act_inplace<4>(v, e.act);
                 *c = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
@@ -457,13 +460,16 @@ __global__ void __launch_bounds__(NT, (RrCfg<NT, BK, STAGES>::MIN_BLOCKS))
                     v[3] = fmaf(e.beta, o4.w, v[3]);
                 }
                 if (e.bias) {
+                    if (e.bias_on_rows) {
+                        const float br = e.bias[m];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] += e.bias[n + j];
-                }
-                if (e.act == ACT_GELU_TANH) {
+                        for (int j = 0; j < 4; ++j) v[j] += br;
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = gelu_tanh(v[j]);
+                        for (int j = 0; j < 4; ++j) v[j] += e.bias[n + j];
+                    }
                 }
+                act_inplace<4>(v, e.act);
                 *c = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll

@@ -249,10 +249,7 @@ __device__ __forceinline__ void finish_run(const Epilogue& e, float (&v)[H], con
 #pragma unroll
         for (int i = 0; i < H; ++i) v[i] += bias_v[i];
     }
-    if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-        for (int i = 0; i < H; ++i) v[i] = gelu_tanh(v[i]);
-    }
+    act_inplace<H>(v, e.act);
 }
 
 // Row-major C: lane t owns column col0 + t of the warp's 32 rows, read from
@@ -576,10 +573,7 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
                         if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
                 }
             }
-            if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-                for (int i = 0; i < EB; ++i) v[i] = gelu_tanh(v[i]);
-            }
+            act_inplace<EB>(v, e.act);
         }
         // the box written two chunks ago must have been read by its TMA store
         if (lane == 0) bulk_wait_group_read<1>();
@@ -668,10 +662,7 @@ __device__ __forceinline__ void tile_out_fast(const TcParams& p, const Unit& w, 
                         if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
                 }
             }
-            if (e.act == ACT_GELU_TANH) {
-#pragma unroll
-                for (int i = 0; i < 64; ++i) v[i] = gelu_tanh(v[i]);
-            }
+            act_inplace<64>(v, e.act);
         }
         // the box(es) written before must have been read by their TMA stores:
         // 16-bit C alternates two boxes, fp32 fills both every step

@@ -10,10 +10,10 @@
  *   A[b] is M x K, B[b] is K x N, C[b] is M x N.  Products accumulate in fp32
  *   ("GEMM Kernel Optimization", Core Technique and Tensor Core Utilization);
  *   the downcast to the output type happens once, after accumulation
- *   ("GEMM Kernel Optimization", Common Pitfalls).  bias is a length-N fp32
- *   vector added to every row before the activation and not scaled by alpha.
- *   act is the identity or GELU in its tanh form,
- *   0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   ("GEMM Kernel Optimization", Common Pitfalls).  bias is an fp32 vector,
+ *   along columns (length N) or rows (length M), added before the activation
+ *   and not scaled by alpha.  act is the identity, GELU (tanh or erf form) or
+ *   ReLU; see gemm_epilogue_t.
  *
  * Storage.  Every matrix is given by a pointer, a leading dimension and a
  * layout flag: element (r, c) of a GEMM_ROW_MAJOR matrix sits at r*ld + c, of
@@ -60,11 +60,31 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
 
 typedef enum { GEMM_DT_BF16 = 0, GEMM_DT_F16 = 1, GEMM_DT_F32 = 2 } gemm_dtype_t;
 
+/*
+ * Epilogue: C = act(alpha*A@B + beta*C + bias), applied once after the K loop
+ * ("Skill: Write a Triton GEMM Kernel", Required reasoning process step 6;
+ * Inputs the agent should gather first, item 5).  The value is a bit field:
+ *   bit 0     add the bias vector (fp32, device memory);
+ *   bits 1-2  activation: 0 none, 1 GELU tanh form
+ *             0.5x(1 + tanh(sqrt(2/pi)(x + 0.044715x^3))), 2 ReLU (x > 0 ? x : 0,
+ *             NaN gives 0), 3 GELU erf form 0.5x(1 + erf(x/sqrt(2)));
+ *   bit 3     the bias runs along rows: bias[m], length M (requires bit 0);
+ *             without it bias[n], length N.
+ * The bias is added before the activation and is not scaled by alpha.
+ */
 typedef enum {
-    GEMM_EPI_NONE = 0,           /* C = alpha*A@B + beta*C                    */
-    GEMM_EPI_BIAS = 1,           /* ... + bias[n]                             */
-    GEMM_EPI_GELU_TANH = 2,      /* gelu_tanh(alpha*A@B + beta*C)             */
-    GEMM_EPI_BIAS_GELU_TANH = 3  /* gelu_tanh(alpha*A@B + beta*C + bias[n])   */
+    GEMM_EPI_NONE = 0,                /* C = alpha*A@B + beta*C              */
+    GEMM_EPI_BIAS = 1,                /* ... + bias[n]                       */
+    GEMM_EPI_GELU_TANH = 2,           /* gelu_tanh(alpha*A@B + beta*C)       */
+    GEMM_EPI_BIAS_GELU_TANH = 3,      /* gelu_tanh(... + bias[n])            */
+    GEMM_EPI_RELU = 4,                /* relu(alpha*A@B + beta*C)            */
+    GEMM_EPI_BIAS_RELU = 5,           /* relu(... + bias[n])                 */
+    GEMM_EPI_GELU_ERF = 6,            /* gelu_erf(alpha*A@B + beta*C)        */
+    GEMM_EPI_BIAS_GELU_ERF = 7,       /* gelu_erf(... + bias[n])             */
+    GEMM_EPI_ROW_BIAS = 9,            /* ... + bias[m]                       */
+    GEMM_EPI_ROW_BIAS_GELU_TANH = 11, /* gelu_tanh(... + bias[m])            */
+    GEMM_EPI_ROW_BIAS_RELU = 13,      /* relu(... + bias[m])                 */
+    GEMM_EPI_ROW_BIAS_GELU_ERF = 15   /* gelu_erf(... + bias[m])             */
 } gemm_epilogue_t;
 
 typedef enum {
@@ -84,7 +104,8 @@ typedef enum {
  *   A, lda, la   M x K operand, bf16.           B, ldb, lb  K x N operand, bf16.
  *   C, ldc, lc   M x N result, c_dtype GEMM_DT_BF16 or GEMM_DT_F32; read when beta != 0.
  *   alpha, beta  fp32 scalars.
- *   bias         length-N fp32 device vector, required iff epi uses a bias, else ignored.
+ *   bias         fp32 device vector of length N (length M for a row bias), 4-byte
+ *                aligned; required iff epi uses a bias, else ignored.
  *   epi          epilogue (gemm_epilogue_t).
  *   split_k      0 = choose automatically, 1 = no split, s > 1 = split K into s
  *                slices whose fp32 partial tiles are summed in a fixed order by a

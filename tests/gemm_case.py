@@ -13,7 +13,12 @@ ES = {"bf16": 2, "f16": 2, "f32": 4}
 NAN_BITS = {"bf16": 0x7FC0, "f16": 0x7E00}
 DT_CODE = {"bf16": 0, "f16": 1, "f32": 2}
 LAYOUT = {"row": 0, "col": 1}
-EPI = {(False, "none"): 0, (True, "none"): 1, (False, "gelu_tanh"): 2, (True, "gelu_tanh"): 3}
+ACT_CODE = {"none": 0, "gelu_tanh": 1, "relu": 2, "gelu_erf": 3}
+
+
+def epi_code(use_bias, act, row_bias=False):
+    """gemm_epilogue_t: bit 0 bias, bits 1-2 activation, bit 3 bias along rows."""
+    return (1 if use_bias else 0) | (ACT_CODE[act] << 1) | (8 if row_bias else 0)
 
 
 def _values(kind, seed, shape, K):
@@ -69,12 +74,14 @@ def read(flat, dt, layout, ld, stride, offset, nb, R, C):
 class Case:
     def __init__(self, ab="bf16", M=64, N=64, K=64, *, batch=1, la="row", lb="row", lc="row",
                  c_dtype="f32", pads=(0, 0, 0), offsets=(0, 0, 0), alpha=1.0, beta=0.0,
-                 bias=False, act="none", broadcast_b=False, values="uniform", c_values="normal",
+                 bias=False, act="none", row_bias=False, broadcast_b=False, values="uniform",
+                 c_values="normal",
                  seed=1, split_k=0):
         self.ab, self.M, self.N, self.K, self.batch = ab, M, N, K, batch
         self.la, self.lb, self.lc, self.c_dtype = la, lb, lc, c_dtype
         self.alpha, self.beta, self.act, self.split_k = alpha, beta, act, split_k
         self.use_bias = bias
+        self.row_bias = bool(row_bias and bias)
         sa, sb, sc, sbias = (seed * 10 + r for r in range(4))
         nb_b = 1 if broadcast_b else batch
         A = datagen.encode(_values(values, sa, (batch, M, K), K), ab)
@@ -89,7 +96,8 @@ class Case:
             C0 = _poison(batch * M * N, c_dtype).reshape(batch, M, N)  # must not be read
         self.C0, self.ldc, self.stride_c, self.off_c = store(C0, c_dtype, lc, pads[2], offsets[2],
                                                             batch)
-        self.bias = datagen.to_f32(datagen.normal(sbias, (N,))) if bias else None
+        self.bias = (datagen.to_f32(datagen.normal(sbias, (M if self.row_bias else N,)))
+                     if bias else None)
 
     # ------------------------------------------------------------------ oracle
     def problem(self):
@@ -99,7 +107,7 @@ class Case:
             B=self.B[self.off_b:], ldb=self.ldb, lb=self.lb, stride_b=self.stride_b,
             c_dtype=self.c_dtype, C0=self.C0[self.off_c:] if self.beta != 0.0 else None,
             ldc=self.ldc, lc=self.lc, stride_c=self.stride_c, alpha=self.alpha, beta=self.beta,
-            bias=self.bias, act=self.act)
+            bias=self.bias, act=self.act, bias_rows=self.row_bias)
 
     def oracle_full(self):
         return oracle.gemm(self.problem())
@@ -122,7 +130,7 @@ class Case:
         pa = dA.data_ptr() + self.off_a * es
         pb = dB.data_ptr() + self.off_b * es
         pc = dC.data_ptr() + self.off_c * ES[self.c_dtype]
-        epi = EPI[(self.use_bias, self.act)]
+        epi = epi_code(self.use_bias, self.act, self.row_bias)
         args = [DT_CODE[self.ab], self.batch, self.M, self.N, self.K,
                 pa, self.lda, LAYOUT[self.la], self.stride_a if self.batch > 1 else 0,
                 pb, self.ldb, LAYOUT[self.lb], self.stride_b if self.batch > 1 else 0,

@@ -65,7 +65,8 @@ def _bf16(M, N, K, **kw):
     dict(M=4, N=4, K=4, ldb=3),                        # ldb < N
     dict(M=4, N=4, K=4, ldc=3),                        # ldc < N
     dict(M=4, N=4, K=4, la=7),                         # bad layout
-    dict(M=4, N=4, K=4, epi=9),                        # bad epilogue
+    dict(M=4, N=4, K=4, epi=8),                        # row-bias flag without a bias
+    dict(M=4, N=4, K=4, epi=16),                       # bad epilogue
     dict(M=4, N=4, K=4, epi=Epi.BIAS),                 # bias missing
     dict(M=4, N=4, K=4, A=None),                       # A missing
     dict(M=4, N=4, K=4, C=None),                       # C missing

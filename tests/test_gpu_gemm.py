@@ -428,3 +428,58 @@ def test_exact_general_epilogue_forced(general_epilogue, shape):
     M, N, K = shape
     c = run_exact(Case("bf16", M, N, K, values="ints", seed=321 + M))
     assert c.plan["fast_epilogue"] == 0
+
+
+# ---------------------------------------------------------------- activations and bias orientation
+
+# Every route the epilogue can take, with each activation and the bias along
+# columns or rows.  Each entry: Case keyword arguments, options to set, and the
+# plan fields the route must show.
+EPI_ROUTES = {
+    "tc_fast": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", alpha=0.5), {},
+                {"fast_epilogue": 1}),
+    "tc_general_beta": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", beta=0.75), {},
+                        {"fast_epilogue": 0}),
+    "tc_unaligned_ldc": (dict(ab="bf16", M=260, N=701, K=200, c_dtype="f32"), {},
+                         {"fast_epilogue": 0}),
+    "tc_col_major_c": (dict(ab="f16", M=200, N=300, K=160, lc="col", c_dtype="f32",
+                            beta=-0.5), {}, {"swap_ab": 0}),
+    "swap_ab": (dict(ab="bf16", M=40, N=900, K=256, c_dtype="f32"), {}, {"swap_ab": 1}),
+    "split_k": (dict(ab="bf16", M=130, N=200, K=2048, c_dtype="bf16", split_k=4), {},
+                {"split_k": 4}),
+    "pair_mma": (dict(ab="bf16", M=1100, N=1304, K=320, c_dtype="bf16", alpha=0.25),
+                 {"CTA_PAIR": 3}, {"cta_pair": 2}),
+    "sgemm_cp_async": (dict(ab="f32", M=300, N=260, K=272, alpha=1.5, beta=0.5), {}, {}),
+    "sgemm_staged": (dict(ab="f32", M=300, N=260, K=270, la="col", beta=0.5), {}, {}),
+    "k_zero": (dict(ab="bf16", M=70, N=90, K=0, c_dtype="f32", beta=0.5), {}, {}),
+}
+
+
+@pytest.mark.parametrize("row_bias", [False, True], ids=["col_bias", "row_bias"])
+@pytest.mark.parametrize("act", ["relu", "gelu_erf", "gelu_tanh"])
+@pytest.mark.parametrize("route", sorted(EPI_ROUTES))
+def test_epilogue_activation_routes(route, act, row_bias):
+    import dense_gemm_bf16_gb300 as dg
+    kw, opts, want = EPI_ROUTES[route]
+    for k, v in opts.items():
+        dg.gemm_set_option(dg.Option[k], v)
+    try:
+        c = run_close(Case(bias=True, act=act, row_bias=row_bias, seed=401, **kw))
+    finally:
+        for k in opts:
+            dg.gemm_set_option(dg.Option[k], 0)
+    for k, v in want.items():
+        assert c.plan[k] == v, (k, c.plan)
+
+
+@pytest.mark.parametrize("shape", [(333, 712, 300), (40, 900, 256), (300, 260, 272)])
+@pytest.mark.parametrize("row_bias", [False, True], ids=["col_bias", "row_bias"])
+def test_exact_relu(shape, row_bias):
+    # small integers: the accumulator is exact, so is ReLU of it plus an
+    # integer-valued bias
+    M, N, K = shape
+    ab = "f32" if shape == (300, 260, 272) else "bf16"
+    c = Case(ab, M, N, K, values="ints", bias=True, act="relu", row_bias=row_bias, seed=411)
+    c.bias = np.round(c.bias * 4).astype(np.float32)
+    run_exact(c)
+
