@@ -2,21 +2,22 @@
 
 The compute lives in the CUDA library libdgemm_gb300.so (C ABI:
 include/gemm.h): a persistent tcgen05/TMA tensor-core kernel for bf16/fp16,
-a register-tiled CUDA-core SGEMM for fp32, and their split-K / operand-copy
-helpers.  This package is its binding: ``_abi`` mirrors the C entry points
+a CUDA-core SGEMM for fp32, their split-K / operand-copy helpers, and the
+general-stride entry point.  This package is its binding: ``_abi`` mirrors the C entry points
 one to one; ``api.gemm`` is the tensor-level convenience.
 """
 from ._abi import (EXPORTED, STATIC_WORKSPACE_BYTES, DType, Epi, GemmError, Layout, Option, Plan,
                    Status, build, gemm_batched, gemm_bf16, gemm_bf16_static_workspace,
-                   gemm_check_device_status, gemm_f16,
-                   gemm_get_option, gemm_plan_query, gemm_set_option, gemm_status_string,
+                   gemm_check_device_status, gemm_f16, gemm_get_option, gemm_plan_query,
+                   gemm_set_option, gemm_status_string, gemm_strided, gemm_strided_workspace_size,
                    gemm_tile_order, gemm_workspace_size, lib, library_path, sgemm_f32)
 
 __all__ = [
     "EXPORTED", "STATIC_WORKSPACE_BYTES", "DType", "Epi", "GemmError", "Layout", "Option", "Plan",
     "Status", "build", "gemm_batched", "gemm_bf16", "gemm_bf16_static_workspace",
-    "gemm_check_device_status", "gemm_f16", "gemm_get_option", "gemm_plan_query", "gemm_set_option", "gemm_status_string", "gemm_tile_order",
-    "gemm_workspace_size", "lib", "library_path", "sgemm_f32", "gemm", "plan",
+    "gemm_check_device_status", "gemm_f16", "gemm_get_option", "gemm_plan_query",
+    "gemm_set_option", "gemm_status_string", "gemm_strided", "gemm_strided_workspace_size",
+    "gemm_tile_order", "gemm_workspace_size", "lib", "library_path", "sgemm_f32", "gemm", "plan",
 ]
 
 

@@ -99,6 +99,11 @@ _SIGNATURES = {
                       _vp, _i64, _i32, _i64, _i32, _f32, _f32, _vp, _i32, _i32, _vp, _sz, _vp],
                      _i32),
     "gemm_workspace_size": ([_i32, _i64, _i64, _i64, _i64, _i32], _sz),
+    "gemm_strided": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64,
+                      _vp, _i64, _i64, _i64, _i32, _f32, _f32, _vp, _i32, _i32, _vp, _sz, _vp],
+                     _i32),
+    "gemm_strided_workspace_size": ([_i32, _i32, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _i64,
+                                     _i64, _i64, _i64, _i64, _i64, _i32], _sz),
     "gemm_status_string": ([_i32], ctypes.c_char_p),
     "gemm_check_device_status": ([_vp], _i32),
     "gemm_plan_query": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp, _i64, _i32,
@@ -181,6 +186,21 @@ def gemm_bf16_static_workspace(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dt
 
 def gemm_workspace_size(ab_dtype, batch, M, N, K, split_k) -> int:
     return lib().gemm_workspace_size(ab_dtype, batch, M, N, K, split_k)
+
+
+def gemm_strided(ab_dtype, batch, M, N, K, A, a_rs, a_cs, stride_a, B, b_rs, b_cs, stride_b, C,
+                 c_rs, c_cs, stride_c, c_dtype, alpha, beta, bias, epi, split_k, workspace,
+                 workspace_bytes, stream) -> int:
+    return lib().gemm_strided(ab_dtype, batch, M, N, K, A, a_rs, a_cs, stride_a, B, b_rs, b_cs,
+                              stride_b, C, c_rs, c_cs, stride_c, c_dtype, alpha, beta, bias, epi,
+                              split_k, workspace, workspace_bytes, stream)
+
+
+def gemm_strided_workspace_size(ab_dtype, c_dtype, batch, M, N, K, a_rs, a_cs, stride_a, b_rs,
+                                b_cs, stride_b, c_rs, c_cs, stride_c, split_k) -> int:
+    return lib().gemm_strided_workspace_size(ab_dtype, c_dtype, batch, M, N, K, a_rs, a_cs,
+                                             stride_a, b_rs, b_cs, stride_b, c_rs, c_cs,
+                                             stride_c, split_k)
 
 
 def gemm_status_string(status) -> str:

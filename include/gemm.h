@@ -183,6 +183,47 @@ gemm_status_t gemm_batched(gemm_dtype_t ab_dtype, int64_t batch,
 size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N,
                            int64_t K, int split_k);
 
+/*
+ * gemm_strided -- gemm_batched with every matrix given by element strides:
+ * element (r, c) of batch b of A sits at A + b*stride_a + r*a_rs + c*a_cs, and
+ * likewise for B (K x N) and C (M x N) ("Skill: Write a Triton GEMM Kernel",
+ * Kernel design rules: strides are arguments, so non-contiguous tensors work).
+ *
+ *   Strides are in elements and >= 0.  An input stride of 0 repeats a row, a
+ *   column or (batch stride) a whole matrix.  C's strides must give distinct
+ *   elements distinct addresses; r*c_rs + c*c_cs is not checked for
+ *   overlaps beyond c_rs, c_cs > 0 (when M, N > 1) and stride_c > 0 (batch > 1).
+ *   A matrix whose strides are a row-major (cs == 1, rs >= columns) or
+ *   column-major (rs == 1, cs >= rows) layout is used in place.  Any other A
+ *   or B is first gathered into a dense row-major copy in the workspace, and
+ *   any other C is computed in a dense row-major buffer in the workspace
+ *   (gathered from C first when beta != 0) and then scattered into C.  All of
+ *   it is enqueued on `stream`.
+ *   The other arguments are those of gemm_batched.  The workspace must hold
+ *   gemm_strided_workspace_size() bytes when a copy is needed
+ *   (GEMM_ERR_WORKSPACE otherwise) and be 256-byte aligned.
+ */
+gemm_status_t gemm_strided(gemm_dtype_t ab_dtype, int64_t batch,
+                           int64_t M, int64_t N, int64_t K,
+                           const void* A, int64_t a_rs, int64_t a_cs, int64_t stride_a,
+                           const void* B, int64_t b_rs, int64_t b_cs, int64_t stride_b,
+                           void* C, int64_t c_rs, int64_t c_cs, int64_t stride_c,
+                           gemm_dtype_t c_dtype,
+                           float alpha, float beta, const float* bias, gemm_epilogue_t epi,
+                           int split_k, void* workspace, size_t workspace_bytes,
+                           gemm_stream_t stream);
+
+/*
+ * gemm_strided_workspace_size -- bytes of workspace that suffice for
+ * gemm_strided with these sizes and strides: the dense copies it needs plus
+ * gemm_workspace_size() for the GEMM itself.  Returns 0 for invalid arguments.
+ */
+size_t gemm_strided_workspace_size(gemm_dtype_t ab_dtype, gemm_dtype_t c_dtype, int64_t batch,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int64_t a_rs, int64_t a_cs, int64_t stride_a,
+                                   int64_t b_rs, int64_t b_cs, int64_t stride_b,
+                                   int64_t c_rs, int64_t c_cs, int64_t stride_c, int split_k);
+
 /* gemm_status_string -- static, human-readable name of a status code. */
 const char* gemm_status_string(gemm_status_t status);
 
