@@ -6,9 +6,13 @@
 //              coalesced along the contiguous dimension.
 //  splitk_epi  the second pass of split-K ("Skill: Write a Triton GEMM
 //              Kernel", Kernel design rules, split-K): sums the fp32 partial
-//              tiles of all K slices in slice order (deterministic), then
+//              tiles of all K slices in a fixed order (deterministic), then
 //              applies the epilogue and the single downcast.  With zero
 //              slices it is the K == 0 / alpha == 0 path: C = act(beta*C + bias).
+//              With 8 or more slices and a row-major C, eight lanes share
+//              each group of four outputs: lane g sums slices g, g + 8, ...,
+//              and the eight sums combine by a fixed shuffle tree, so that a
+//              small output still spreads over the whole GPU.
 #include <stdint.h>
 
 #include "epilogue.cuh"
@@ -109,6 +113,66 @@ __global__ void __launch_bounds__(kThreads) splitk_epi_vec4_kernel(const float* 
     }
 }
 
+// Eight lanes per float4 of outputs: lane g of the group adds slices
+// g, g + 8, g + 16, ... in ascending order, then the group adds its eight sums
+// pairwise (distance 4, 2, 1), and lane 0 writes the four results.
+__global__ void __launch_bounds__(kThreads) splitk_epi_group8_kernel(const float* __restrict__ P,
+                                                                     int splits, int64_t batch,
+                                                                     int64_t M, int64_t N,
+                                                                     Epilogue e) {
+    const int64_t mn = M * N;
+    const int64_t total4 = (batch * mn) >> 2;
+    const float4* __restrict__ P4 = reinterpret_cast<const float4*>(P);
+    const int g = threadIdx.x & 7;
+    const int64_t groups = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 3);
+    for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x >> 3) + (threadIdx.x >> 3);
+         q - (threadIdx.x >> 3) < total4; q += groups) {
+        // every lane of the warp stays in the loop for the shuffles
+        const bool live = q < total4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+            int s = g;
+            for (; s + 24 < splits; s += 32) {
+                float4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = P4[static_cast<int64_t>(s + 8 * u) * total4 + q];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
+            }
+            for (; s < splits; s += 8) {
+                const float4 v = P4[static_cast<int64_t>(s) * total4 + q];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+        }
+#pragma unroll
+        for (int d = 4; d >= 1; d >>= 1) {
+            acc.x += __shfl_down_sync(0xffffffffu, acc.x, d, 8);
+            acc.y += __shfl_down_sync(0xffffffffu, acc.y, d, 8);
+            acc.z += __shfl_down_sync(0xffffffffu, acc.z, d, 8);
+            acc.w += __shfl_down_sync(0xffffffffu, acc.w, d, 8);
+        }
+        if (live && g == 0) {
+            const int64_t idx = q << 2;
+            const int64_t b = idx / mn;
+            const int64_t rem = idx - b * mn;
+            const int64_t i = rem / N;
+            const int64_t j = rem - i * N;
+            epilogue_store(e, b, i, j + 0, acc.x);
+            epilogue_store(e, b, i, j + 1, acc.y);
+            epilogue_store(e, b, i, j + 2, acc.z);
+            epilogue_store(e, b, i, j + 3, acc.w);
+        }
+    }
+}
+
 int grid_for(int64_t total) {
     int64_t g = (total + kThreads - 1) / kThreads;
     if (g > 152 * 32) g = 152 * 32;  // grid-stride beyond a few waves of the 152 SMs
@@ -136,7 +200,10 @@ cudaError_t splitk_epilogue_launch(const float* partials, int splits, int64_t ba
                                    int64_t N, const Epilogue& e, cudaStream_t stream) {
     const int64_t total = batch * M * N;
     if (total <= 0) return cudaSuccess;
-    if (partials && e.c_row_major && (N & 3) == 0) {
+    if (partials && e.c_row_major && (N & 3) == 0 && splits >= 8) {
+        splitk_epi_group8_kernel<<<grid_for(total << 1), kThreads, 0, stream>>>(partials, splits,
+                                                                               batch, M, N, e);
+    } else if (partials && e.c_row_major && (N & 3) == 0) {
         splitk_epi_vec4_kernel<<<grid_for(total >> 2), kThreads, 0, stream>>>(partials, splits, batch,
                                                                               M, N, e);
     } else {

@@ -313,10 +313,13 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.splits = static_cast<int>(c.split_k < pl.kblocks ? c.split_k : pl.kblocks);
     } else {
         pl.splits = auto_splits(pl.units, pl.kblocks, ctas, c.batch, pl.Mc, pl.Nc, pl.bn);
-        // never ask for more workspace than was given
-        const size_t avail = c.ws_bytes > off + 256 ? c.ws_bytes - off - 256 : 0;
-        if (pl.splits > 1 && per_split * pl.splits > avail)
-            pl.splits = static_cast<int>(per_split ? avail / per_split : 1);
+        // never ask for more workspace than was given: the partials start at
+        // `off` (256-aligned) and take per_split * splits rounded up to 256
+        const size_t avail = c.ws_bytes > off ? c.ws_bytes - off : 0;
+        auto need = [&](int s) {
+            return static_cast<size_t>(round_up(static_cast<int64_t>(per_split) * s, 256));
+        };
+        while (pl.splits > 1 && need(pl.splits) > avail) --pl.splits;
         if (pl.splits < 2) pl.splits = 1;
     }
     if (pl.splits > 1) {

@@ -483,3 +483,18 @@ def test_exact_relu(shape, row_bias):
     c.bias = np.round(c.bias * 4).astype(np.float32)
     run_exact(c)
 
+
+
+@pytest.mark.parametrize("shape", [(16, 8192, 8192), (256, 256, 65536), (128, 256, 8192)])
+def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
+    # a call given exactly the workspace its plan reported must make the same plan
+    import dense_gemm_bf16_gb300 as dg
+    M, N, K = shape
+    args = [0, 1, M, N, K, 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0, 2, 1.0, 0.0,
+            None, 0, 0]
+    st, big = dg.gemm_plan_query(*args, 1 << 40)
+    assert st == 0 and big.split_k > 1
+    st, exact = dg.gemm_plan_query(*args, int(big.workspace_bytes))
+    assert st == 0
+    assert exact.split_k == big.split_k
+    assert exact.workspace_bytes == big.workspace_bytes
