@@ -71,6 +71,49 @@ def env_rank():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+class Replicas:
+    """Host side of an N-process run: one independent replica of the workload per
+    rank, one GPU each, and no collective on the data path (tiles are
+    independent).  Barriers bracket the timed regions, a time is the maximum
+    over ranks, and whole-job throughput counts every rank's work."""
+
+    def __init__(self, backend, device=None):
+        rank, world, local = env_rank()
+        self.rank, self.world, self.local = rank, world, local
+        self.dist = None
+        self.device = device
+        if world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        """The maximum of x over the ranks."""
+        if self.dist is None:
+            return x
+        import torch
+        dev = self.device if self.dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def throughput(self, work_per_rank, ms):
+        """Whole-job rate: every rank's work over the slowest rank's time."""
+        return self.world * work_per_rank / (ms * 1e-3)
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.barrier()
+            self.dist.destroy_process_group()
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -355,15 +398,9 @@ def main():
 
     import dense_gemm_bf16_gb300 as dg
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_mod
-        dist = dist_mod
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
+    torch.cuda.set_device(local if world > 1 else 0)
     device = torch.device("cuda", local if world > 1 else 0)
+    reps = Replicas("nccl", device)
     dg.build()
     dg.lib()
     if args.row:
@@ -385,16 +422,8 @@ def main():
     stream = torch.cuda.current_stream(device).cuda_stream
     gemm = Gemm(dA, dB, dbias, dC, stream)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier = reps.barrier
+    max_over_ranks = reps.max
 
     # device-resident throughput (clocks sampled during the timed region)
     sampler = ClockSampler(device.index)
@@ -404,7 +433,7 @@ def main():
     ms_total = max_over_ranks(ms_total)
     ms_step = ms_total / args.steps
     flops = 2.0 * M * N * K
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = reps.throughput(flops, ms_step) / 1e12
 
     # end to end through the C ABI with host buffers: every step H2D inputs, GEMM,
     # D2H result.  Reported: the copies overlapped across steps (three streams);
@@ -421,12 +450,12 @@ def main():
         ms_serial = max_over_ranks(time_steps(e2e_step, e2e_steps, 3, barrier)) / e2e_steps
         ms_e2e = max_over_ranks(e2e_pipelined(hA, hB, hbias, hC, device, e2e_steps, 3, barrier))
         h2d = hA.numel() * 2 + hB.numel() * 2 + hbias.numel() * 4
-        e2e = {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": reps.throughput(flops, ms_e2e) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hC.numel() * 2,
                "ms_per_step": ms_e2e,
                "overlap": "inputs of step i+1 up and result of step i-1 down while step i "
                           "computes (three streams, two device copies of each buffer)",
-               "serial_value": world * flops / (ms_serial * 1e-3) / 1e12,
+               "serial_value": reps.throughput(flops, ms_serial) / 1e12,
                "serial_ms_per_step": ms_serial}
 
     peaks, peak_src = measured_peaks()
@@ -460,9 +489,7 @@ def main():
                 "gpu_launches": args.steps * gemm.plan["launches"],
                 "clocks": clocks}
         print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
+    reps.close()
 
 
 # ----------------------------------------------------------------------------- ablation
