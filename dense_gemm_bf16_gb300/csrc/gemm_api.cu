@@ -169,6 +169,7 @@ struct Plan {
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
     bool fast_epi = false;  // TMA-store-only epilogue form
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
+    int inkernel_split = 0;  // automatic split-K done in one kernel by the split form
     int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
     int64_t dp_units = 0, sk_iters = 0;
     size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0;
@@ -312,15 +313,37 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     if (c.split_k >= 1) {
         pl.splits = static_cast<int>(c.split_k < pl.kblocks ? c.split_k : pl.kblocks);
     } else {
-        pl.splits = auto_splits(pl.units, pl.kblocks, ctas, c.batch, pl.Mc, pl.Nc, pl.bn);
-        // never ask for more workspace than was given: the partials start at
-        // `off` (256-aligned) and take per_split * splits rounded up to 256
-        const size_t avail = c.ws_bytes > off ? c.ws_bytes - off : 0;
-        auto need = [&](int s) {
-            return static_cast<size_t>(round_up(static_cast<int64_t>(per_split) * s, 256));
-        };
-        while (pl.splits > 1 && need(pl.splits) > avail) --pl.splits;
-        if (pl.splits < 2) pl.splits = 1;
+        const int s_auto = auto_splits(pl.units, pl.kblocks, ctas, c.batch, pl.Mc, pl.Nc, pl.bn);
+        // A small automatic split runs in one kernel, as the split form of
+        // stream-K below: the S K pieces of each unit go to S CTAs that start
+        // together, and piece 0 adds the others' fp32 partials in tensor memory
+        // before writing the output, so there is no reduction pass and no
+        // second launch.  It needs a CTA per piece and at most kMaxInKernel
+        // pieces (piece 0 adds the others one by one).
+        constexpr int kMaxInKernel = 4;
+        int s_in = s_auto;
+        if (pl.units > 0 && s_in > ctas / pl.units) s_in = static_cast<int>(ctas / pl.units);
+        if (s_in > pl.kblocks / 4) s_in = static_cast<int>(pl.kblocks / 4);
+        if (g_opt_stream_k.load() != 1 && s_auto >= 2 && s_auto <= kMaxInKernel && s_in >= 2) {
+            const size_t nslots = static_cast<size_t>(pl.units) * (s_in - 1);
+            const size_t need = static_cast<size_t>(round_up(
+                                    static_cast<int64_t>(nslots * TC_BLOCK_M * pl.bn * 4), 256)) +
+                                static_cast<size_t>(round_up(static_cast<int64_t>(nslots * 4 * 8), 256));
+            if (c.ws != nullptr && off + need <= c.ws_bytes) pl.inkernel_split = s_in;
+        }
+        if (pl.inkernel_split > 0) {
+            pl.splits = 1;
+        } else {
+            pl.splits = s_auto;
+            // never ask for more workspace than was given: the partials start at
+            // `off` (256-aligned) and take per_split * splits rounded up to 256
+            const size_t avail = c.ws_bytes > off ? c.ws_bytes - off : 0;
+            auto need = [&](int s) {
+                return static_cast<size_t>(round_up(static_cast<int64_t>(per_split) * s, 256));
+            };
+            while (pl.splits > 1 && need(pl.splits) > avail) --pl.splits;
+            if (pl.splits < 2) pl.splits = 1;
+        }
     }
     if (pl.splits > 1) {
         pl.part_off = off;
@@ -346,6 +369,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     const int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
     if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
+        pl.inkernel_split == 0 &&
         (want >= 2 || (pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
         pl.mode = mode;
         pl.cm = 2;
@@ -369,8 +393,27 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     // (both forced whenever a partial last wave follows at least one full wave).
     const int64_t want_sk = g_opt_stream_k.load();
     const int64_t P = pl.grid / pl.cm;
-    if (want_sk != 1 && pl.splits == 1 && P > 0 && pl.units > P && pl.units % P != 0 &&
-        pl.kblocks >= 2) {
+    if (pl.inkernel_split > 0) {
+        // the automatic split-K above, in one kernel: no whole units first, every
+        // unit cut into inkernel_split pieces, one CTA each
+        const int64_t S = pl.inkernel_split, r = pl.units;
+        const size_t nslots = static_cast<size_t>(r * (S - 1));
+        const size_t slots = nslots * TC_BLOCK_M * pl.bn * 4;
+        const size_t flags = nslots * 4 * 8;
+        pl.sk = 2;
+        pl.dp_per_cluster = 0;
+        pl.dp_units = 0;
+        pl.sk_split = static_cast<int>(S);
+        pl.sk_tiles = static_cast<int>(r);
+        pl.sk_off = off;
+        pl.sk_bytes = slots;
+        pl.sk_flags_off = off + static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256));
+        off += static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256)) +
+               static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
+        pl.ws_need = off;
+        pl.grid = static_cast<int>(S * r);
+    } else if (want_sk != 1 && pl.splits == 1 && P > 0 && pl.units > P && pl.units % P != 0 &&
+               pl.kblocks >= 2) {
         const int64_t W = pl.units / P, r = pl.units % P;
         // split form: each of the r last units becomes S pieces of at least
         // kMinPiece K blocks, one per cluster, all starting together so that

@@ -493,8 +493,46 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
     args = [0, 1, M, N, K, 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0, 2, 1.0, 0.0,
             None, 0, 0]
     st, big = dg.gemm_plan_query(*args, 1 << 40)
-    assert st == 0 and big.split_k > 1
+    assert st == 0 and (big.split_k > 1 or big.stream_k == 2)
     st, exact = dg.gemm_plan_query(*args, int(big.workspace_bytes))
     assert st == 0
-    assert exact.split_k == big.split_k
+    assert (exact.split_k, exact.stream_k, exact.grid) == (big.split_k, big.stream_k, big.grid)
     assert exact.workspace_bytes == big.workspace_bytes
+
+
+# ---------------------------------------------------------------- automatic split-K in one kernel
+
+# An automatic split of 2-4 pieces per unit, with a CTA for every piece, runs
+# as the split form of stream-K (plan: split_k 1, stream_k 2, no reduction
+# launch); GEMM_OPT_STREAM_K = 1 falls back to the two-pass split-K.
+INKERNEL_CASES = {
+    "skinny_swap": dict(M=16, N=8192, K=4096),
+    "three_pieces": dict(M=1024, N=640, K=4096),
+}
+
+
+@pytest.mark.parametrize("name", sorted(INKERNEL_CASES))
+def test_exact_inkernel_split(name):
+    import dense_gemm_bf16_gb300 as dg
+    kw = INKERNEL_CASES[name]
+    c = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
+    assert c.plan["stream_k"] == 2 and c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
+    dg.gemm_set_option(dg.Option.STREAM_K, 1)
+    try:
+        c2 = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
+    finally:
+        dg.gemm_set_option(dg.Option.STREAM_K, 0)
+    assert c2.plan["stream_k"] == 0 and c2.plan["split_k"] > 1
+
+
+def test_inkernel_split_epilogue_and_beta():
+    c = run_close(Case("bf16", 1024, 640, 4096, c_dtype="bf16", alpha=0.5, beta=0.75, bias=True,
+                       act="gelu_tanh", seed=502))
+    assert c.plan["stream_k"] == 2
+
+
+def test_inkernel_split_unaligned_c():
+    # fp32 C with ldc = 641: the head's output goes through the st.global path
+    c = run_close(Case("bf16", 1024, 641, 4096, c_dtype="f32", bias=True, act="relu",
+                       row_bias=True, seed=503))
+    assert c.plan["stream_k"] == 2
