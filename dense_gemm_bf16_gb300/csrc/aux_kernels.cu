@@ -23,24 +23,40 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// grid: x covers the contiguous dimension, y groups of 8 rows (grid-stride), z the
-// batch.  Each thread issues the loads of its 8 rows before any store.
+// grid: x covers the contiguous dimension in groups of 8 elements, y groups of
+// 4 rows (grid-stride), z the batch.  A thread copies 8 consecutive elements
+// of each of its rows: 2-byte loads (the source rows need only be 2-byte
+// aligned; a warp's loads still cover 512 contiguous bytes) and one 16-byte
+// store (the destination pitch is a multiple of 8 elements and its base
+// 256-byte aligned).  Columns past `cols` in the last group are written as 0.
 __global__ void __launch_bounds__(kThreads) pack16_kernel(const uint16_t* __restrict__ src,
                                                           int64_t ld, int64_t stride, int64_t rows,
                                                           int64_t cols, uint16_t* __restrict__ dst,
                                                           int64_t ld_dst) {
     const int64_t b = blockIdx.z;
-    const int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    if (c >= cols) return;
-    const uint16_t* s = src + b * stride + c;
-    uint16_t* d = dst + b * rows * ld_dst + c;
-    for (int64_t r0 = 8 * static_cast<int64_t>(blockIdx.y); r0 < rows; r0 += 8 * gridDim.y) {
-        uint16_t v[8];
+    const int64_t c0 = 8 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x);
+    if (c0 >= cols) return;
+    const uint16_t* s = src + b * stride + c0;
+    uint16_t* d = dst + b * rows * ld_dst + c0;
+    const int nc = cols - c0 < 8 ? static_cast<int>(cols - c0) : 8;
+    for (int64_t r0 = 4 * static_cast<int64_t>(blockIdx.y); r0 < rows; r0 += 4 * gridDim.y) {
+        uint32_t w[4][4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = r0 + u < rows ? s[(r0 + u) * ld] : 0;
+        for (int u = 0; u < 4; ++u) {
+            const uint16_t* sr = s + (r0 + u) * ld;
+            const bool row_ok = r0 + u < rows;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (r0 + u < rows) d[(r0 + u) * ld_dst] = v[u];
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t lo = row_ok && 2 * h < nc ? __ldg(sr + 2 * h) : 0u;
+                const uint32_t hi = row_ok && 2 * h + 1 < nc ? __ldg(sr + 2 * h + 1) : 0u;
+                w[u][h] = lo | (hi << 16);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (r0 + u < rows)
+                *reinterpret_cast<uint4*>(d + (r0 + u) * ld_dst) =
+                    make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
     }
 }
 
@@ -185,8 +201,10 @@ cudaError_t pack16_launch(const void* src, int64_t ld, int64_t stride, int64_t r
                           int64_t batch, void* dst, int64_t ld_dst, cudaStream_t stream) {
     if (batch <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
     if (batch > 65535) return cudaErrorInvalidValue;
-    const int64_t gx = (cols + kThreads - 1) / kThreads;
-    const int64_t groups = (rows + 7) / 8;
+    if ((ld_dst & 7) != 0 || (reinterpret_cast<uintptr_t>(dst) & 15) != 0)
+        return cudaErrorInvalidValue;  // the 16-byte stores need an aligned destination
+    const int64_t gx = ((cols + 7) / 8 + kThreads - 1) / kThreads;
+    const int64_t groups = (rows + 3) / 4;
     const int64_t gy = groups < 4096 ? groups : 4096;
     if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
     pack16_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy),
