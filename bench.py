@@ -504,6 +504,7 @@ ABLATION = [  # (label, GEMM options)
     ("L2 hints: A evict-last, B evict-first", {"L2_HINTS": 2}),
     ("single-CTA tiles (no CTA pairs)", {"CTA_PAIR": 1}),
     ("CTA pairs sharing B by multicast", {"CTA_PAIR": 2}),
+    ("256 x 512 pair tiles (one accumulator)", {"WIDE_TILE": 2}),
 ]
 
 
@@ -523,7 +524,7 @@ def run_ablation(args, device, reps=None, launches=20):
     dC = torch.empty((M, N), dtype=torch.int16, device=device)
     gemm = Gemm(dA, dB, dbias, dC, torch.cuda.current_stream(device).cuda_stream)
     defaults = {name: dg.gemm_get_option(dg.Option[name])
-                for name in ("GROUP_M", "L2_HINTS", "CTA_PAIR")}
+                for name in ("GROUP_M", "L2_HINTS", "CTA_PAIR", "WIDE_TILE")}
     times = {label: [] for label, _ in ABLATION}
     reps = reps or len(ABLATION)
     sampler = ClockSampler(device.index)
@@ -551,7 +552,7 @@ def run_ablation(args, device, reps=None, launches=20):
 
 # ----------------------------------------------------------------------------- other paths
 
-ROW_NAMES = ("sgemm_4096", "ragged_4097x3001x1000", "splitk_256x256x65536",
+ROW_NAMES = ("small_256", "sgemm_4096", "ragged_4097x3001x1000", "splitk_256x256x65536",
              "skinny_16x8192x8192", "batched_64x1024", "batched_64x1024_bcast",
              "streamk_2560x2560x16384", "streamk_off_2560x2560x16384",
              "flat_4096x4096x16", "flat_4096x4096x16_f32")
@@ -590,6 +591,16 @@ def build_row(name, device):
                 raise RuntimeError(dg.gemm_status_string(s_))
         return fn, plan.as_dict(), wst
 
+    if name == "small_256":
+        # bf16 256^3, row-major A and B, bf16 out, no epilogue: launch-latency bound
+        n = 256
+        A = dev(datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(1, datagen.ROLE_A),
+                                                     (n, n))).view(np.int16))
+        B = dev(datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(1, datagen.ROLE_B),
+                                                     (n, n))).view(np.int16))
+        C = torch.empty((n, n), dtype=torch.int16, device=device)
+        fn, plan, wst = call16(1, n, n, n, A, n, 0, B, n, 0, C, n, 0, 0, 1.0, 0.0)
+        return fn, 2.0 * n ** 3, 4 * n * n * 2, "hbm", plan, (A, B, C, wst)
     if name == "sgemm_4096":
         n = 4096
         A = dev(datagen.to_f32(datagen.uniform(2001, (n, n))))

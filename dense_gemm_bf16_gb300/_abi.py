@@ -63,6 +63,7 @@ class Option(enum.IntEnum):
     STREAM_K = 8
     FAST_EPILOGUE = 9
     SGEMM_KERNEL = 10
+    WIDE_TILE = 11
 
 
 class Plan(ctypes.Structure):

@@ -31,6 +31,7 @@ std::atomic<int64_t> g_opt_l2_hints{0};
 std::atomic<int64_t> g_opt_stream_k{0};
 std::atomic<int64_t> g_opt_fast_epilogue{0};
 std::atomic<int64_t> g_opt_sgemm_kernel{0};
+std::atomic<int64_t> g_opt_wide_tile{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -38,7 +39,7 @@ std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
                                                reinterpret_cast<uintptr_t>(&g_opt_group_m))};
 
 constexpr int kMaxDevices = 64;
-constexpr int kBlockN[] = {16, 32, 64, 128, 256};
+constexpr int kBlockN[] = {16, 32, 64, 128, 256, 512};
 
 struct DevState {
     std::once_flag once;
@@ -46,7 +47,7 @@ struct DevState {
     int sm_count = 0;
     int cc = 0;
     int* status = nullptr;
-    int max_pairs[3][2] = {};  // co-resident two-CTA clusters [mode][BN 128, 256]
+    int max_pairs[3][3] = {};  // co-resident two-CTA clusters [mode][BN 128, 256, 512]
 };
 DevState g_dev[kMaxDevices];
 
@@ -74,6 +75,7 @@ gemm_status_t device_state(DevState** out) {
                 for (int mode = 1; mode <= 2; ++mode) {
                     d.max_pairs[mode][0] = tc_max_pairs(128, mode);
                     d.max_pairs[mode][1] = tc_max_pairs(256, mode);
+                    d.max_pairs[mode][2] = tc_max_pairs(512, mode);
                 }
             }
         }
@@ -366,7 +368,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     else if (want == 0)
         mode = 2;
     const int bn_idx = pl.bn == 256 ? 1 : 0;
-    const int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
+    int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
     if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
         pl.inkernel_split == 0 &&
@@ -376,6 +378,18 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.stages = tc_stages_for(pl.bn, mode);
         pl.tiles = cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
         pl.units = pair_units;
+        // wide pair tile, 256 x 512 (GEMM_OPT_WIDE_TILE: 0 auto, 1 never, 2 whenever
+        // the pair MMA runs with BN = 256 and N >= 512)
+        const int64_t wide = g_opt_wide_tile.load();
+        const int mp_wide = d.max_pairs[2][2];
+        if (pl.mode == 2 && (pl.bn == 256 || (pl.bn == 128 && wide == 2)) && pl.Nc >= 512 &&
+            mp_wide > 0 && wide == 2) {
+            pl.bn = 512;
+            pl.stages = tc_stages_for(512, 2);
+            pl.tiles = cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, 512);
+            pl.units = c.batch * pl.tiles;
+            max_pairs = mp_wide;
+        }
     }
     const int64_t total_units = pl.units * pl.splits;
     if (total_units > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED;
@@ -413,7 +427,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.ws_need = off;
         pl.grid = static_cast<int>(S * r);
     } else if (want_sk != 1 && pl.splits == 1 && P > 0 && pl.units > P && pl.units % P != 0 &&
-               pl.kblocks >= 2) {
+               pl.kblocks >= 2 && pl.bn <= 256) {
         const int64_t W = pl.units / P, r = pl.units % P;
         // split form: each of the r last units becomes S pieces of at least
         // kMinPiece K blocks, one per cluster, all starting together so that
@@ -637,8 +651,10 @@ gemm_status_t run(const Call& c) {
     bool a3 = false, b3 = false;
     st = encode_operand(&p.tmap_a, c.ab, pl.a, a_ptr, a_ld, a_stride, c.batch, TC_BLOCK_M, &a3);
     if (st != GEMM_OK) return st;
+    // B box: the rows (N) one load brings, half of an N <= 256 MMA per CTA of a pair
+    const int sub_n = pl.bn < 256 ? pl.bn : 256;
     st = encode_operand(&p.tmap_b, c.ab, pl.b, b_ptr, b_ld, b_stride, c.batch,
-                        static_cast<uint32_t>(pl.bn / pl.cm), &b3);
+                        static_cast<uint32_t>(pl.cm == 2 ? sub_n / 2 : pl.bn), &b3);
     if (st != GEMM_OK) return st;
     p.M = static_cast<int32_t>(pl.Mc);
     p.N = static_cast<int32_t>(pl.Nc);
@@ -656,7 +672,7 @@ gemm_status_t run(const Call& c) {
     p.a_3d = a3 ? 1 : 0;
     p.b_3d = b3 ? 1 : 0;
     p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, pl.mode == 2 ? 2 * TC_BLOCK_M : TC_BLOCK_M,
-                             pl.bn);
+                             sub_n);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
     const bool want_fast = pl.fast_epi;
@@ -937,6 +953,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
             g_opt_sgemm_kernel.store(value);
             return GEMM_OK;
+        case GEMM_OPT_WIDE_TILE:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_wide_tile.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -953,6 +973,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_STREAM_K: return g_opt_stream_k.load();
         case GEMM_OPT_FAST_EPILOGUE: return g_opt_fast_epilogue.load();
         case GEMM_OPT_SGEMM_KERNEL: return g_opt_sgemm_kernel.load();
+        case GEMM_OPT_WIDE_TILE: return g_opt_wide_tile.load();
     }
     return -1;
 }

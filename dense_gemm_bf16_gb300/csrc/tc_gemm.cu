@@ -15,6 +15,7 @@ int tc_stages_for(int bn, int mode) {
     if (mode == 2) {
         if (bn == 128) return Cfg<128, 2>::STAGES;
         if (bn == 256) return Cfg<256, 2>::STAGES;
+        if (bn == 512) return Cfg<512, 2>::STAGES;
         return 0;
     }
     switch (bn) {
@@ -36,13 +37,13 @@ cudaError_t tc_prepare(int bn) {
 bool tc_has_mode(int bn, int mode) {
     if (mode == 0) return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
     if (mode == 1) return bn == 128 || bn == 256;
-    if (mode == 2) return bn == 128 || bn == 256;
+    if (mode == 2) return bn == 128 || bn == 256 || bn == 512;
     return false;
 }
 
 int tc_max_pairs(int bn, int mode) { return tc_max_pairs_general(bn, mode); }
 
-bool tc_has_fast(int bn) { return bn == 64 || bn == 128 || bn == 256; }
+bool tc_has_fast(int bn) { return bn == 64 || bn == 128 || bn == 256 || bn == 512; }
 
 cudaError_t tc_launch(int bn, int mode, int epi, const TcParams& p, int grid, cudaStream_t stream) {
     if (epi == 1 && tc_has_fast(bn)) return tc_launch_fast(bn, mode, p, grid, stream);

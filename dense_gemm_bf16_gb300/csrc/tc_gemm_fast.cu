@@ -19,6 +19,7 @@ cudaError_t tc_prepare_fast(int bn) {
             if (e == cudaSuccess) e = prepare_bn<256, 2, 1>();
             return e;
         }
+        case 512: return prepare_bn<512, 2, 1>();
     }
     return cudaSuccess;  // no fast instantiation for narrower tiles
 }
@@ -27,6 +28,7 @@ cudaError_t tc_launch_fast(int bn, int mode, const TcParams& p, int grid, cudaSt
     if (mode == 2) {
         if (bn == 128) return launch_bn<128, 2, 1>(p, grid, stream);
         if (bn == 256) return launch_bn<256, 2, 1>(p, grid, stream);
+        if (bn == 512) return launch_bn<512, 2, 1>(p, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (mode == 1) {

@@ -20,6 +20,7 @@ cudaError_t tc_prepare_general(int bn) {
             if (e == cudaSuccess) e = prepare_bn<256, 2, 0>();
             return e;
         }
+        case 512: return prepare_bn<512, 2, 0>();
     }
     return cudaErrorInvalidValue;
 }
@@ -29,6 +30,7 @@ int tc_max_pairs_general(int bn, int mode) {
     if (mode == 1 && bn == 256) return max_clusters_bn<256, 1, 0>();
     if (mode == 2 && bn == 128) return max_clusters_bn<128, 2, 0>();
     if (mode == 2 && bn == 256) return max_clusters_bn<256, 2, 0>();
+    if (mode == 2 && bn == 512) return max_clusters_bn<512, 2, 0>();
     return 0;
 }
 
@@ -36,6 +38,7 @@ cudaError_t tc_launch_general(int bn, int mode, const TcParams& p, int grid, cud
     if (mode == 2) {
         if (bn == 128) return launch_bn<128, 2, 0>(p, grid, stream);
         if (bn == 256) return launch_bn<256, 2, 0>(p, grid, stream);
+        if (bn == 512) return launch_bn<512, 2, 0>(p, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (mode == 1) {

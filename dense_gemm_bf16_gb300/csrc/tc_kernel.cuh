@@ -60,19 +60,27 @@ static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 //         one half of the shared B tile, multicast into both CTAs.
 // MODE 2: two CTAs of a cluster compute one 256 x BN tile with cta_group::2
 //         MMAs issued by the even CTA; each CTA holds its own 128 A rows and
-//         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.
+//         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.  With
+//         BN = 512 the tile is two N = 256 MMAs per K step into the two halves
+//         of tensor memory (one accumulator, no double buffering): every CTA
+//         takes in 48 KB per 64-deep K block for twice the work of BN = 256,
+//         which matters because an SM's TMA intake, not the tensor pipe, bounds
+//         the BN = 256 main loop.
 template <int BN, int MODE>
 struct Cfg {
     static constexpr int CM = MODE == 0 ? 1 : 2;        // CTAs per cluster
     static constexpr int CG = MODE == 2 ? 2 : 1;        // tcgen05 cta_group
     static constexpr int B_ROWS = MODE == 2 ? BN / 2 : BN;  // B rows (N) held per CTA
+    static constexpr int NSUB = BN > 256 ? BN / 256 : 1;    // MMAs (N <= 256 each) per K step
+    static constexpr int SUB_N = BN / NSUB;
+    static constexpr int ACC_BUFS = 2 * BN <= 512 ? 2 : 1;  // accumulators in tensor memory
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t BAR_BYTES = 256;
     static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
-    static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr uint32_t TMEM_COLS = ACC_BUFS * BN < 32 ? 32 : ACC_BUFS * BN;
     static constexpr int CHUNK = BN < 32 ? BN : 32;
     static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
@@ -81,6 +89,7 @@ struct Cfg {
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
     static_assert(MODE != 2 || BN >= 128, "pair MMA splits B into 64-column atoms");
+    static_assert(BN <= 256 || MODE == 2, "N > 256 only as two pair MMAs");
 };
 
 struct Unit {
@@ -840,17 +849,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                 load_pair(&p.tmap_a, a_dst + h * 8192u, lb, w.pid_m * BM + 64 * h,
                                           k0, w.b, p.a_3d, pol_a);
                         }
-                        constexpr int HALF = BN / 2;
-                        if (!p.b_mn) {
-                            load_pair(&p.tmap_b, b_dst, lb, k0,
-                                      w.pid_n * BN + static_cast<int>(rank) * HALF, w.b, p.b_3d,
-                                      pol_b);
-                        } else {
+                        // per N = SUB_N MMA, this CTA's half of its columns
+                        constexpr int HALF = C::SUB_N / 2;
 #pragma unroll
-                            for (int hh = 0; hh < HALF / 64; ++hh)
-                                load_pair(&p.tmap_b, b_dst + hh * 8192u, lb,
-                                          w.pid_n * BN + static_cast<int>(rank) * HALF + 64 * hh,
-                                          k0, w.b, p.b_3d, pol_b);
+                        for (int sn = 0; sn < C::NSUB; ++sn) {
+                            const uint32_t bs = b_dst + sn * (HALF * 128u);
+                            const int n0 = w.pid_n * BN + sn * C::SUB_N + static_cast<int>(rank) * HALF;
+                            if (!p.b_mn) {
+                                load_pair(&p.tmap_b, bs, lb, k0, n0, w.b, p.b_3d, pol_b);
+                            } else {
+#pragma unroll
+                                for (int hh = 0; hh < HALF / 64; ++hh)
+                                    load_pair(&p.tmap_b, bs + hh * 8192u, lb, n0 + 64 * hh, k0, w.b,
+                                              p.b_3d, pol_b);
+                            }
                         }
                     } else if (!p.a_mn) {
                         load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
@@ -957,8 +969,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = smem_desc_sw128(a_base + k * a_kstep, a_lbo, 1024u);
-                        const uint64_t bd = smem_desc_sw128(b_base + k * b_kstep, b_lbo, 1024u);
-                        umma_f16_cg<CG>(d_tmem, ad, bd, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int sn = 0; sn < C::NSUB; ++sn) {
+                            // sub-tile sn: its B rows from (SUB_N / 2) * 128 bytes on, its
+                            // accumulator SUB_N columns on (one 64-wide atom column is 8 KB
+                            // for MN-major B, the same offset)
+                            const uint32_t bsub = b_base + sn * (C::SUB_N / 2) * 128u;
+                            const uint64_t bd = smem_desc_sw128(bsub + k * b_kstep, b_lbo, 1024u);
+                            umma_f16_cg<CG>(d_tmem + sn * C::SUB_N, ad, bd, p.idesc,
+                                            (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     issued = true;
                     if constexpr (CM > 1)
@@ -975,7 +995,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     umma_commit_mc_cg<CG>(tfull0 + 8u * abuf, kPair);  // both CTAs' accumulators
                 else
                     umma_commit_cg<CG>(tfull0 + 8u * abuf);
-                if (++abuf == 2) {
+                if (++abuf == C::ACC_BUFS) {
                     abuf = 0;
                     aphase ^= 1u;
                 }
@@ -1111,7 +1131,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 else
                     mbar_arrive(tempty0 + 8u * abuf);
             }
-            if (++abuf == 2) {
+            if (++abuf == C::ACC_BUFS) {
                 abuf = 0;
                 aphase ^= 1u;
             }

@@ -305,6 +305,10 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         staged kernel (128 x 128 tiles); 1: always the register-staged
  *                         kernel.  Both add each output's products in ascending k with
  *                         one rounding per FMA, so their results are identical.
+ *   GEMM_OPT_WIDE_TILE    two-CTA MMA pairs with 256 x 512 tiles (two N = 256 MMAs per
+ *                         K step, one accumulator): 0 (default) when the plan model
+ *                         prefers them, 1 never, 2 whenever pair MMA runs with 256-wide
+ *                         tiles and N >= 512.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
@@ -320,7 +324,8 @@ typedef enum {
     GEMM_OPT_L2_HINTS = 7,
     GEMM_OPT_STREAM_K = 8,
     GEMM_OPT_FAST_EPILOGUE = 9,
-    GEMM_OPT_SGEMM_KERNEL = 10
+    GEMM_OPT_SGEMM_KERNEL = 10,
+    GEMM_OPT_WIDE_TILE = 11
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -536,3 +536,43 @@ def test_inkernel_split_unaligned_c():
     c = run_close(Case("bf16", 1024, 641, 4096, c_dtype="f32", bias=True, act="relu",
                        row_bias=True, seed=503))
     assert c.plan["stream_k"] == 2
+
+
+# ---------------------------------------------------------------- 256 x 512 pair tiles
+
+@pytest.fixture
+def wide_tile():
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.WIDE_TILE, 2)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 3)
+    yield
+    dg.gemm_set_option(dg.Option.WIDE_TILE, 0)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
+
+
+# N = 700 leaves the second 512-wide tile mostly past the edge; M = 600 a
+# partial 256-row block; K = 1000 a ragged last K block
+@pytest.mark.parametrize("la", ["row", "col"])
+@pytest.mark.parametrize("lb", ["row", "col"])
+def test_exact_wide_tile_layouts(wide_tile, la, lb):
+    c = run_exact(Case("bf16", 600, 700, 1000, la=la, lb=lb, values="ints", seed=601))
+    assert c.plan["block_n"] == 512 and c.plan["cta_pair"] == 2, c.plan
+
+
+def test_exact_wide_tile_batched_broadcast(wide_tile):
+    c = run_exact(Case("bf16", 300, 1100, 320, batch=3, broadcast_b=True, values="ints",
+                       seed=602))
+    assert c.plan["block_n"] == 512
+
+
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_wide_tile_epilogue(wide_tile, beta):
+    c = run_close(Case("bf16", 520, 1536, 640, c_dtype="bf16", alpha=0.5, beta=beta, bias=True,
+                       act="gelu_tanh", seed=603))
+    assert c.plan["block_n"] == 512 and c.plan["fast_epilogue"] == (1 if beta == 0.0 else 0)
+
+
+def test_wide_tile_f16_fp32_out_unaligned_c(wide_tile):
+    c = run_close(Case("f16", 512, 1030, 512, c_dtype="f32", bias=True, row_bias=True,
+                       act="relu", seed=604))
+    assert c.plan["block_n"] == 512
