@@ -686,15 +686,17 @@ def fp32_peak_tflops(device):
 
 def measure_rows(names, device, reps=20):
     """Times each named path with its roofline fraction: `reps` launches after
-    3 warm-ups, each preceded by a write of a buffer larger than L2 (so every
-    launch starts with a cold L2) and bracketed by CUDA events on the
+    3 warm-ups, each preceded by a read of a buffer twice the size of L2 (so
+    every launch starts with a cold L2 that holds only clean lines: after a
+    write instead, a memory-bound launch would also pay for writing the
+    flush's dirty lines back to HBM) and bracketed by CUDA events on the
     launching stream.  All launches are queued before the first is waited
     for, so the host's time to issue a call (about 6 us) stays outside the
     events; the median per-launch time is reported."""
     import torch
     import dense_gemm_bf16_gb300 as dg
     peaks, _ = measured_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=device)  # 256 MiB
     out = []
     for name in names:
         saved = {k: dg.gemm_get_option(dg.Option[k]) for k in ROW_OPTIONS.get(name, {})}
@@ -706,7 +708,7 @@ def measure_rows(names, device, reps=20):
         torch.cuda.synchronize()
         evs = []
         for _ in range(reps):
-            flush.zero_()
+            flush.sum()
             s_ = torch.cuda.Event(enable_timing=True)
             e_ = torch.cuda.Event(enable_timing=True)
             s_.record()

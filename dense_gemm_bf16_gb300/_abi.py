@@ -64,6 +64,8 @@ class Option(enum.IntEnum):
     FAST_EPILOGUE = 9
     SGEMM_KERNEL = 10
     WIDE_TILE = 11
+    SPLIT_REDUCE = 12
+    BLOCK_N = 13
 
 
 class Plan(ctypes.Structure):

@@ -98,4 +98,64 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int64_t b, int
     store_elem(c, e.c_dtype, x);
 }
 
+// Four outputs C(b, i, j .. j + 3), j a multiple of 4: one vector access of C
+// (16 bytes for fp32, 8 for 16-bit types) when C is row-major with 16-byte
+// aligned rows and all four columns are inside N; otherwise one element at a
+// time, skipping the columns at or past N.
+__device__ __forceinline__ void epilogue_store4(const Epilogue& e, int64_t b, int64_t i,
+                                                int64_t j, int64_t N, float4 acc) {
+    float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (!(e.c_row_major && e.c_vec_ok && j + 3 < N)) {
+        for (int c = 0; c < 4; ++c)
+            if (j + c < N) epilogue_store(e, b, i, j + c, v[c]);
+        return;
+    }
+    char* c = c_addr(e, b, i, j);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] *= e.alpha;
+    if (e.beta != 0.0f) {
+        float o[4];
+        if (e.c_dtype == DT_F32) {
+            const float4 t = *reinterpret_cast<const float4*>(c);
+            o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+        } else {
+            const uint2 t = *reinterpret_cast<const uint2*>(c);
+            const uint32_t w[2] = {t.x, t.y};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (e.c_dtype == DT_BF16) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+                    o[2 * k] = f.x; o[2 * k + 1] = f.y;
+                } else {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+                    o[2 * k] = f.x; o[2 * k + 1] = f.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = fmaf(e.beta, o[k], v[k]);
+    }
+    if (e.bias) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] += e.bias_on_rows ? e.bias[i] : e.bias[j + k];
+    }
+    act_inplace<4>(v, e.act);
+    if (e.c_dtype == DT_F32) {
+        *reinterpret_cast<float4*>(c) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        uint32_t w[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (e.c_dtype == DT_BF16) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+                w[k] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+                const __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+                w[k] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+        }
+        *reinterpret_cast<uint2*>(c) = make_uint2(w[0], w[1]);
+    }
+}
+
 }  // namespace dg

@@ -32,6 +32,8 @@ std::atomic<int64_t> g_opt_stream_k{0};
 std::atomic<int64_t> g_opt_fast_epilogue{0};
 std::atomic<int64_t> g_opt_sgemm_kernel{0};
 std::atomic<int64_t> g_opt_wide_tile{0};
+std::atomic<int64_t> g_opt_split_reduce{0};
+std::atomic<int64_t> g_opt_block_n{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -172,6 +174,7 @@ struct Plan {
     bool fast_epi = false;  // TMA-store-only epilogue form
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
     int inkernel_split = 0;  // automatic split-K done in one kernel by the split form
+    bool spread = false;     // ... with every piece reducing a share of its tile
     int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
     int64_t dp_units = 0, sk_iters = 0;
     size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0;
@@ -291,6 +294,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.bn = 64;
     else
         pl.bn = (c.batch * tiles_m * cdiv(pl.Nc, 256) >= ctas) ? 256 : 128;
+    if (g_opt_block_n.load() > 0) pl.bn = static_cast<int>(g_opt_block_n.load());
     if (pl.b.mn && pl.bn < 64) pl.bn = 64;  // MN-major B tiles come in 64-wide swizzle atoms
     pl.stages = tc_stages_for(pl.bn, 0);
 
@@ -316,22 +320,30 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.splits = static_cast<int>(c.split_k < pl.kblocks ? c.split_k : pl.kblocks);
     } else {
         const int s_auto = auto_splits(pl.units, pl.kblocks, ctas, c.batch, pl.Mc, pl.Nc, pl.bn);
-        // A small automatic split runs in one kernel, as the split form of
-        // stream-K below: the S K pieces of each unit go to S CTAs that start
-        // together, and piece 0 adds the others' fp32 partials in tensor memory
-        // before writing the output, so there is no reduction pass and no
-        // second launch.  It needs a CTA per piece and at most kMaxInKernel
-        // pieces (piece 0 adds the others one by one).
+        // The automatic split runs in one kernel, as the split form of stream-K
+        // below: the S K pieces of each unit go to S CTAs that start together,
+        // so there is no reduction pass and no second launch.  It needs a CTA
+        // per piece.  Up to kMaxInKernel pieces, piece 0 adds the others' fp32
+        // partials in tensor memory one by one before writing the output; with
+        // more (or GEMM_OPT_SPLIT_REDUCE = 2) every piece publishes its partial
+        // and then reduces one S-th of the tile (GEMM_OPT_SPLIT_REDUCE = 1 keeps
+        // the two-pass form there instead).
         constexpr int kMaxInKernel = 4;
         int s_in = s_auto;
         if (pl.units > 0 && s_in > ctas / pl.units) s_in = static_cast<int>(ctas / pl.units);
         if (s_in > pl.kblocks / 4) s_in = static_cast<int>(pl.kblocks / 4);
-        if (g_opt_stream_k.load() != 1 && s_auto >= 2 && s_auto <= kMaxInKernel && s_in >= 2) {
-            const size_t nslots = static_cast<size_t>(pl.units) * (s_in - 1);
+        const int64_t want_spread = g_opt_split_reduce.load();
+        const bool spread = want_spread == 2 || (want_spread == 0 && s_auto > kMaxInKernel);
+        if (g_opt_stream_k.load() != 1 && s_auto >= 2 && s_in >= 2 &&
+            (spread || s_auto <= kMaxInKernel)) {
+            const size_t nslots = static_cast<size_t>(pl.units) * (spread ? s_in : s_in - 1);
             const size_t need = static_cast<size_t>(round_up(
                                     static_cast<int64_t>(nslots * TC_BLOCK_M * pl.bn * 4), 256)) +
                                 static_cast<size_t>(round_up(static_cast<int64_t>(nslots * 4 * 8), 256));
-            if (c.ws != nullptr && off + need <= c.ws_bytes) pl.inkernel_split = s_in;
+            if (c.ws != nullptr && off + need <= c.ws_bytes) {
+                pl.inkernel_split = s_in;
+                pl.spread = spread;
+            }
         }
         if (pl.inkernel_split > 0) {
             pl.splits = 1;
@@ -411,7 +423,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         // the automatic split-K above, in one kernel: no whole units first, every
         // unit cut into inkernel_split pieces, one CTA each
         const int64_t S = pl.inkernel_split, r = pl.units;
-        const size_t nslots = static_cast<size_t>(r * (S - 1));
+        const size_t nslots = static_cast<size_t>(r * (pl.spread ? S : S - 1));
         const size_t slots = nslots * TC_BLOCK_M * pl.bn * 4;
         const size_t flags = nslots * 4 * 8;
         pl.sk = 2;
@@ -693,7 +705,7 @@ gemm_status_t run(const Call& c) {
     }
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
-    p.test_stall = g_opt_test_stall.exchange(0) ? 1 : 0;
+    p.test_stall = static_cast<int32_t>(g_opt_test_stall.exchange(0));
     p.l2_hints = static_cast<int32_t>(g_opt_l2_hints.load());
     if (pl.sk) {
         p.dp_per_cluster = pl.dp_per_cluster;
@@ -701,6 +713,7 @@ gemm_status_t run(const Call& c) {
         p.sk_iters = pl.sk_iters;
         p.sk_split = pl.sk_split;
         p.sk_tiles = pl.sk_tiles;
+        p.sk_spread = pl.spread ? 1 : 0;
         p.sk_partials = reinterpret_cast<float*>(ws + pl.sk_off);
         p.sk_flags = reinterpret_cast<unsigned long long*>(ws + pl.sk_flags_off);
         p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
@@ -907,7 +920,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
     plan->cta_pair = pl.mode;
     plan->fast_epilogue = pl.fast_epi ? 1 : 0;
-    plan->stream_k = pl.sk;
+    plan->stream_k = pl.spread ? 3 : pl.sk;
     return st;
 }
 
@@ -926,7 +939,7 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             g_opt_timeout_us.store(value);
             return GEMM_OK;
         case GEMM_OPT_TEST_STALL:
-            if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_opt_test_stall.store(value);
             return GEMM_OK;
         case GEMM_OPT_CTA_PAIR:
@@ -957,6 +970,16 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_opt_wide_tile.store(value);
             return GEMM_OK;
+        case GEMM_OPT_SPLIT_REDUCE:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_split_reduce.store(value);
+            return GEMM_OK;
+        case GEMM_OPT_BLOCK_N:
+            if (value != 0 && value != 16 && value != 32 && value != 64 && value != 128 &&
+                value != 256)
+                return GEMM_ERR_INVALID_ARG;
+            g_opt_block_n.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -974,6 +997,8 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_FAST_EPILOGUE: return g_opt_fast_epilogue.load();
         case GEMM_OPT_SGEMM_KERNEL: return g_opt_sgemm_kernel.load();
         case GEMM_OPT_WIDE_TILE: return g_opt_wide_tile.load();
+        case GEMM_OPT_SPLIT_REDUCE: return g_opt_split_reduce.load();
+        case GEMM_OPT_BLOCK_N: return g_opt_block_n.load();
     }
     return -1;
 }

@@ -52,7 +52,7 @@ struct TcParams {
     float* partials;         // split-K: fp32 partial tiles [split][batch][M][N] in C's layout; else null
     int* status;             // device error word
     uint64_t timeout_ns;     // bound on every wait
-    int32_t test_stall;      // test only: leave one stage unfilled
+    int32_t test_stall;      // test only: 1 leave one stage unfilled; 2 CTA 0 publishes no partial flags
     int32_t l2_hints;        // operand L2 policy: 0 normal; 1 A evict-first, B evict-last; 2 the reverse
     // Stream-K.  Every cluster first takes dp_per_cluster whole units round
     // robin; the units from dp_units on are then cut along K, in one of two forms.
@@ -63,11 +63,16 @@ struct TcParams {
     // Split (sk_split > 0): each of the sk_tiles last units is cut into sk_split
     // equal K pieces, one per cluster, so that all pieces start together; piece 0
     // finishes the tile after the other sk_split - 1 have left their partials.
+    // With sk_spread every piece leaves its partial, and once all have, piece j
+    // sums the j-th of sk_split equal shares of the tile over all partials and
+    // writes that share of the output (the launch is cooperative: every piece
+    // waits for every other one).
     int32_t dp_per_cluster;
     int32_t dp_units;
     int64_t sk_iters;        // K blocks of the contiguous form (0: off)
     int32_t sk_split;        // pieces per unit of the split form (0: off)
     int32_t sk_tiles;        // units cut in the split form
+    int32_t sk_spread;       // split form: 1 every piece reduces a share of the tile
     float* sk_partials;      // [slot][cta rank][128][BN] fp32, lane-interleaved per warp
     unsigned long long* sk_flags;  // [slot][cta rank][epilogue warp]: epoch when published
     unsigned long long sk_epoch;   // this launch's flag value

@@ -84,7 +84,7 @@ struct Cfg {
     static constexpr int CHUNK = BN < 32 ? BN : 32;
     static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert((2 * STAGES + 6) * 8 + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
@@ -94,13 +94,16 @@ struct Cfg {
 
 struct Unit {
     int b, split, pid_m, pid_n, kb0, kb1;
-    int kind;  // UNIT_FULL, or a stream-K piece: UNIT_HEAD (finishes the tile) / UNIT_TAIL
-    // stream-K partial slots: a TAIL publishes into slot `slot`; a HEAD adds the
-    // `nslots` partials in slots slot .. slot + nslots - 1
-    int slot, nslots;
+    // UNIT_FULL, or a stream-K piece: UNIT_HEAD (finishes the tile) / UNIT_TAIL /
+    // UNIT_SPREAD (publishes, then reduces share `piece` of the tile)
+    int kind;
+    // stream-K partial slots: a TAIL or SPREAD piece publishes into slot `slot`;
+    // a HEAD adds the `nslots` partials in slots slot .. slot + nslots - 1; a
+    // SPREAD piece reads slots slot - piece .. slot - piece + nslots - 1
+    int slot, nslots, piece;
 };
 
-enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
+enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2, UNIT_SPREAD = 3 };
 
 // Work unit u -> (batch, K slice, tile).  With clusters of CM CTAs along M the
 // unit is a CM-tile-high slab and CTA `rank` of the cluster takes tile-row
@@ -117,6 +120,8 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u, uint32_t r
     w.pid_m = w.pid_m * CM + static_cast<int>(rank);
     w.kb0 = static_cast<int>(static_cast<int64_t>(w.split) * p.kblocks / p.splits);
     w.kb1 = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.kblocks / p.splits);
+    w.kind = UNIT_FULL;
+    w.slot = w.nslots = w.piece = 0;
     return w;
 }
 
@@ -167,9 +172,16 @@ __device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int nc
         w = decode_unit<CM>(p, p.dp_units + t, rank);
         w.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kblocks / S);
         w.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kblocks / S);
-        w.kind = j == 0 ? UNIT_HEAD : UNIT_TAIL;
-        w.slot = t * (S - 1) + (j > 0 ? j - 1 : 0);
-        w.nslots = S - 1;
+        if (p.sk_spread) {
+            w.kind = UNIT_SPREAD;
+            w.slot = t * S + j;
+            w.nslots = S;
+        } else {
+            w.kind = j == 0 ? UNIT_HEAD : UNIT_TAIL;
+            w.slot = t * (S - 1) + (j > 0 ? j - 1 : 0);
+            w.nslots = S - 1;
+        }
+        w.piece = j;
         s.piece = -1;
         return true;
     }
@@ -192,6 +204,13 @@ __device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int nc
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* ptr, unsigned long long v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+
+// Fence with acquire and release semantics at GPU scope: after relaxed loads
+// that observed released values, it makes the releasing threads' earlier
+// writes visible to this thread.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* ptr) {
@@ -467,6 +486,107 @@ __device__ __forceinline__ void add_partial_to_tmem(uint32_t tmem_row, const flo
         for (int j = 0; j < NV; ++j) cur[j] = nxt[j];
     }
     tmem_st_wait();
+}
+
+// Split form with a spread reduction: every piece of the tile has published
+// its fp32 partial (lane-interleaved per warp, as above); piece j now sums
+// share j of the tile's TILE4 float4 positions over the S partials and writes
+// those outputs through the element-wise epilogue.  The share is one
+// contiguous range of every partial, so:
+//  1. one epilogue warp polls the flags of the publishing warps whose rows the
+//     share covers (relaxed loads, each lane a set of flags, all in flight),
+//     then fences (the acquire half of the publishers' release stores) and
+//     issues one bulk copy per partial, each bringing that partial's share
+//     into the stage memory the main loop has finished with;
+//  2. the four epilogue warps wait for the copies on the gather barrier and
+//     sum position by position in piece order (deterministic), then store
+//     four outputs at a time.
+// Returns false on a timeout (the status word is set).  The warp that issued
+// the copies does not return before they have landed (a second bounded wait).
+template <int BN, int CM>
+__device__ __forceinline__ bool spread_reduce(const TcParams& p, int b, int pid_m, int pid_n,
+                                           int slot0, int piece, int S, uint32_t rank, int q,
+                                           int lane, volatile int* abort_flag, uint32_t gather,
+                                           const float4* gather_ptr, uint32_t gather_cap,
+                                           uint32_t gather_bar) {
+    constexpr int QUARTER4 = 32 * BN / 4;  // float4 positions of one warp's 32 rows
+    constexpr int TILE4 = 4 * QUARTER4;
+    const int e0 = static_cast<int>(static_cast<int64_t>(piece) * TILE4 / S);
+    const int e1 = static_cast<int>(static_cast<int64_t>(piece + 1) * TILE4 / S);
+    const int npos = e1 - e0;
+    if (npos <= 0) return true;
+    const uint32_t bytes = static_cast<uint32_t>(npos) * 16u;
+    if (static_cast<uint64_t>(bytes) * S > gather_cap) {
+        // (cannot happen: every tile width's stage memory holds a whole tile
+        // plus one float4 per piece)
+        if (lane == 0 && p.status) atomicExch(p.status, 1);
+        return false;
+    }
+    bool issued = false;
+    if (q == 0) {
+        const int q0 = e0 / QUARTER4;
+        const int nq = (e1 - 1) / QUARTER4 - q0 + 1;
+        const unsigned long long* flags = p.sk_flags + (static_cast<int64_t>(slot0) * CM + rank) * 4;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            bool mine = true;
+            for (int f = lane; f < S * nq; f += 32) {
+                const int s = f / nq;
+                const int qq = q0 + (f - s * nq);
+                if (ld_relaxed_u64(flags + static_cast<int64_t>(s) * CM * 4 + qq) != p.sk_epoch)
+                    mine = false;
+            }
+            if (__all_sync(0xffffffffu, mine)) break;
+            int give_up = 0;
+            if (lane == 0 && (it & 15u) == 0 &&
+                (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns)) {
+                *abort_flag = 1;
+                if (p.status) atomicExch(p.status, 1);
+                give_up = 1;
+            }
+            if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+        }
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(gather_bar, bytes * static_cast<uint32_t>(S));
+        __syncwarp();
+        const float4* src = reinterpret_cast<const float4*>(p.sk_partials) +
+                            (static_cast<int64_t>(slot0) * CM + rank) * TILE4 + e0;
+        const int64_t sstride = static_cast<int64_t>(CM) * TILE4;  // float4 from one piece's slot to the next
+        for (int s = lane; s < S; s += 32)
+            bulk_load(gather + static_cast<uint32_t>(s) * bytes, src + s * sstride, bytes, gather_bar);
+        issued = true;
+    }
+    bool ok = mbar_wait(gather_bar, 0u, abort_flag, p.status, p.timeout_ns);
+    if (issued && !ok) {
+        // the copies read valid memory and finish on their own: wait (bounded
+        // again) until they have landed before this CTA may leave
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(gather_bar, 0u) && globaltimer_ns() - t0 < p.timeout_ns) {
+        }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return false;
+#pragma unroll 1
+    for (int k = q * 32 + lane; k < npos; k += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int s = 0; s < S; ++s) {
+            const float4 v = gather_ptr[s * npos + k];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        // position e: row (e / QUARTER4) * 32 + e % 32, columns 4 * ((e % QUARTER4) / 32) + 0..3
+        const int e = e0 + k;
+        const int qq = e / QUARTER4;
+        const int f = e - qq * QUARTER4;
+        const int64_t i = static_cast<int64_t>(pid_m) * TC_BLOCK_M + qq * 32 + (f & 31);
+        const int64_t j = static_cast<int64_t>(pid_n) * BN + 4 * (f >> 5);
+        if (i < p.M && j < p.N) epilogue_store4(p.epi, b, i, j, p.N, acc);
+    }
+    return true;
 }
 
 // TMA-store epilogue of one tile for this warp's 32 rows.  The tile is cut
@@ -756,13 +876,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint8_t* epi_smem = smem + C::STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + EPI_BYTES);
     const uint32_t bar0 = smem_u32(bars);
-    // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
+    // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain,
+    // gather (the spread reduction's copies)
     const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8u * C::STAGES;
     const uint32_t tfull0 = bar0 + 16u * C::STAGES;
     const uint32_t tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    const uint32_t gather_bar = drain_bar + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -784,6 +906,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             mbar_init(tempty0 + 8u * b, tempty_count);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(gather_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tmap_a);
@@ -824,7 +947,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    if (p.test_stall && armed == 0) {
+                    if (p.test_stall == 1 && armed == 0) {
                         // test only: leave this stage unfilled; the MMA warp's bounded
                         // wait on it must expire and report the timeout.
                         ok = false;
@@ -1041,9 +1164,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
             const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
-            if (w.kind == UNIT_TAIL) {
-                // stream-K tail: publish this CTA's raw fp32 partial for the cluster
-                // that finishes the tile
+            if (w.kind == UNIT_TAIL || w.kind == UNIT_SPREAD) {
+                // stream-K tail or spread piece: publish this CTA's raw fp32 partial
+                // for the cluster(s) that finish the tile
                 const int64_t slot = static_cast<int64_t>(w.slot) * CM + rank;
                 float4* dst = reinterpret_cast<float4*>(p.sk_partials + (slot * BM + q * 32) * BN) + lane;
 #pragma unroll 1
@@ -1062,9 +1185,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                            __uint_as_float(r[4 * i + 2]),
                                            __uint_as_float(r[4 * i + 3])));
                 }
-                __threadfence();
+                // the warp sync orders every lane's stores before lane 0's release
+                // store of the flag, which makes them visible (cumulatively) to a
+                // reader that acquires the flag
                 __syncwarp();
-                if (lane == 0) st_release_u64(p.sk_flags + slot * 4 + q, p.sk_epoch);
+                // (test only: with test_stall 2 the first CTA never publishes, so
+                // the waits for its partial must expire and report a timeout)
+                if (lane == 0 && !(p.test_stall == 2 && blockIdx.x == 0))
+                    st_release_u64(p.sk_flags + slot * 4 + q, p.sk_epoch);
             } else {
                 // stream-K head: wait (bounded) for each other piece's partial of
                 // this tile and add it to the accumulator
@@ -1136,6 +1264,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 aphase ^= 1u;
             }
         }
+        // a spread piece is its cluster's last work item: once it has been
+        // published and the accumulator released, the share is reduced (the
+        // piece is found again from the cluster index, so nothing stays live
+        // across the loop).  The plan runs the spread form with single-CTA
+        // tiles only.
+        if constexpr (MODE == 0) {
+            if (p.sk_spread && !*abort_flag) {
+                WorkIter sw = work_begin(p, cta0, ncta);
+                sw.rr_left = 0;
+                Unit u;
+                if (sw.piece >= 0 && work_next<CM>(p, sw, ncta, rank, u))
+                    spread_reduce<BN, CM>(p, u.b, u.pid_m, u.pid_n, u.slot - u.piece, u.piece,
+                                          u.nslots, rank, q, lane, abort_flag, sA0,
+                                          reinterpret_cast<const float4*>(smem),
+                                          C::STAGES * C::STAGE_BYTES, gather_bar);
+            }
+        }
         // the TMA stores must finish before the CTA exits
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -1151,27 +1296,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     }
 }
 
+// A launch whose pieces all wait for one another (the spread split form) is
+// cooperative: the CUDA runtime then runs every CTA of the grid at once, or
+// refuses the launch, instead of leaving a waiting CTA without its peers.
 template <int BN, int MODE, int EPI>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     constexpr int CM = Cfg<BN, MODE>::CM;
-    if constexpr (CM == 1) {
+    if (CM == 1 && !p.sk_spread) {
         tc_gemm_kernel<BN, MODE, EPI><<<grid, TC_THREADS, Cfg<BN, MODE>::SMEM, stream>>>(p);
         return cudaGetLastError();
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CM;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, MODE, EPI>, p);
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (CM > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = CM;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (p.sk_spread) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BN, MODE, EPI>, p);
 }
 
 template <int BN, int MODE, int EPI>

@@ -257,7 +257,9 @@ typedef struct {
     int32_t stream_k;        /* stream-K: 0 off; 1 the K blocks of the last one-to-two
                                 waves split evenly over all CTAs in contiguous ranges;
                                 2 each unit of the last partial wave cut into equal
-                                K pieces that run side by side                     */
+                                K pieces that run side by side (also the automatic
+                                split-K in one kernel); 3 the same with every piece
+                                reducing an equal share of its tile               */
     int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue (GEMM_OPT_FAST_EPILOGUE) */
 } gemm_plan_t;
 
@@ -306,13 +308,28 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         kernel.  Both add each output's products in ascending k with
  *                         one rounding per FMA, so their results are identical.
  *   GEMM_OPT_WIDE_TILE    two-CTA MMA pairs with 256 x 512 tiles (two N = 256 MMAs per
- *                         K step, one accumulator): 0 (default) when the plan model
- *                         prefers them, 1 never, 2 whenever pair MMA runs with 256-wide
- *                         tiles and N >= 512.
+ *                         K step, one accumulator): 0 (default) and 1 never (they
+ *                         measured slower than 256 x 256 on bf16 8192^3); 2 whenever
+ *                         pair MMA runs with 256-wide tiles and N >= 512.
+ *   GEMM_OPT_SPLIT_REDUCE how an automatic split-K (split_k = 0, no whole wave of
+ *                         tiles) runs in one kernel: 0 (default) up to 4 K pieces per
+ *                         tile, piece 0 adds the others' fp32 partials (plan stream_k
+ *                         2); more pieces each publish a partial and, once all have,
+ *                         reduce one equal share of the tile (plan stream_k 3, a
+ *                         cooperative launch); 1 the serial form up to 4 pieces and
+ *                         the two-pass form (split_k > 1, a second launch) beyond;
+ *                         2 the spread form for any number of pieces.  Both
+ *                         one-kernel forms need the workspace of gemm_workspace_size.
+ *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
+ *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes
+ *                         at least 64).
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
- *                         expires and the kernel reports GEMM_ERR_TIMEOUT; the
- *                         knob resets itself after that launch.
+ *                         expires and the kernel reports GEMM_ERR_TIMEOUT; 2 makes
+ *                         the first CTA of the next launch with stream-K pieces
+ *                         leave its partial unpublished, so the waits of the
+ *                         pieces that need it expire instead.  The knob resets
+ *                         itself after that launch.
  */
 typedef enum {
     GEMM_OPT_GROUP_M = 1,
@@ -325,7 +342,9 @@ typedef enum {
     GEMM_OPT_STREAM_K = 8,
     GEMM_OPT_FAST_EPILOGUE = 9,
     GEMM_OPT_SGEMM_KERNEL = 10,
-    GEMM_OPT_WIDE_TILE = 11
+    GEMM_OPT_WIDE_TILE = 11,
+    GEMM_OPT_SPLIT_REDUCE = 12,
+    GEMM_OPT_BLOCK_N = 13
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

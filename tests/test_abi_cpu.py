@@ -113,9 +113,26 @@ def test_options(lib):
     assert dg.gemm_get_option(Option.GROUP_M) == 3
     assert dg.gemm_set_option(Option.GROUP_M, 8) == Status.OK
     assert dg.gemm_set_option(Option.TIMEOUT_US, 0) == Status.ERR_INVALID_ARG
-    assert dg.gemm_set_option(Option.TEST_STALL, 2) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.TEST_STALL, 3) == Status.ERR_INVALID_ARG
     assert dg.gemm_set_option(99, 1) == Status.ERR_INVALID_ARG
     assert dg.gemm_get_option(99) == -1
+
+
+def test_split_reduce_and_block_n_options(lib):
+    assert dg.gemm_get_option(Option.SPLIT_REDUCE) == 0
+    assert dg.gemm_get_option(Option.BLOCK_N) == 0
+    for v in (0, 1, 2):
+        assert dg.gemm_set_option(Option.SPLIT_REDUCE, v) == Status.OK
+        assert dg.gemm_get_option(Option.SPLIT_REDUCE) == v
+    assert dg.gemm_set_option(Option.SPLIT_REDUCE, 3) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.SPLIT_REDUCE, -1) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.SPLIT_REDUCE, 0) == Status.OK
+    for v in (16, 32, 64, 128, 256, 0):
+        assert dg.gemm_set_option(Option.BLOCK_N, v) == Status.OK
+        assert dg.gemm_get_option(Option.BLOCK_N) == v
+    for v in (8, 48, 96, 512, -16):
+        assert dg.gemm_set_option(Option.BLOCK_N, v) == Status.ERR_INVALID_ARG
+    assert dg.gemm_get_option(Option.BLOCK_N) == 0
 
 
 @pytest.mark.parametrize("group_m", [1, 2, 3, 5, 8, 64])

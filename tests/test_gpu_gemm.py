@@ -493,7 +493,7 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
     args = [0, 1, M, N, K, 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0, 2, 1.0, 0.0,
             None, 0, 0]
     st, big = dg.gemm_plan_query(*args, 1 << 40)
-    assert st == 0 and (big.split_k > 1 or big.stream_k == 2)
+    assert st == 0 and (big.split_k > 1 or big.stream_k in (2, 3))
     st, exact = dg.gemm_plan_query(*args, int(big.workspace_bytes))
     assert st == 0
     assert (exact.split_k, exact.stream_k, exact.grid) == (big.split_k, big.stream_k, big.grid)
@@ -536,6 +536,108 @@ def test_inkernel_split_unaligned_c():
     c = run_close(Case("bf16", 1024, 641, 4096, c_dtype="f32", bias=True, act="relu",
                        row_bias=True, seed=503))
     assert c.plan["stream_k"] == 2
+
+
+# ---------------------------------------------------------------- spread split-K in one kernel
+
+# More than 4 automatic pieces per tile: every piece publishes its fp32 partial
+# and then reduces one equal share of the tile (plan stream_k 3, one launch).
+# Shares end at arbitrary positions of a tile (S does not divide it), tiles run
+# past the matrix edges, and the swapped skinny case has 16-wide tiles.
+SPREAD_CASES = {
+    "square_long_k": dict(M=256, N=256, K=16384),
+    "ragged": dict(M=200, N=312, K=20000),
+    "skinny_swap": dict(M=16, N=1008, K=32768),
+    "batched": dict(M=130, N=200, K=8192, batch=3),
+}
+
+
+def _spread_case(name, **extra):
+    kw = dict(SPREAD_CASES[name])
+    M, N, K = kw.pop("M"), kw.pop("N"), kw.pop("K")
+    return Case("bf16", M, N, K, **kw, **extra)
+
+
+@pytest.mark.parametrize("name", sorted(SPREAD_CASES))
+def test_exact_spread_split(name):
+    c = run_exact(_spread_case(name, values="ints", seed=701))
+    assert c.plan["stream_k"] == 3 and c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
+
+
+@pytest.mark.parametrize("name", ["square_long_k", "ragged"])
+def test_spread_matches_two_pass(name):
+    # GEMM_OPT_SPLIT_REDUCE = 1 keeps the two-pass form; exact inputs, so both
+    # forms give the oracle's result bit for bit
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 1)
+    try:
+        c = run_exact(_spread_case(name, values="ints", seed=702))
+    finally:
+        dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+    assert c.plan["stream_k"] == 0 and c.plan["split_k"] > 1 and c.plan["launches"] == 2, c.plan
+
+
+@pytest.mark.parametrize("name", sorted(INKERNEL_CASES))
+def test_exact_spread_forced_for_few_pieces(name):
+    import dense_gemm_bf16_gb300 as dg
+    kw = INKERNEL_CASES[name]
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 2)
+    try:
+        c = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=703))
+    finally:
+        dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+    assert c.plan["stream_k"] == 3 and c.plan["launches"] == 1, c.plan
+
+
+@pytest.mark.parametrize("lc", ["row", "col"])
+def test_spread_epilogue_and_beta(lc):
+    c = run_close(Case("bf16", 256, 256, 16384, lc=lc, c_dtype="bf16", alpha=0.5, beta=0.75,
+                       bias=True, act="gelu_tanh", seed=704))
+    assert c.plan["stream_k"] == 3
+
+
+def test_spread_fp32_unaligned_c_row_bias():
+    c = run_close(Case("bf16", 200, 301, 20000, c_dtype="f32", bias=True, row_bias=True,
+                       act="relu", seed=705))
+    assert c.plan["stream_k"] == 3
+
+
+def test_spread_f16_swap_with_bias():
+    c = run_close(Case("f16", 16, 1000, 32768, c_dtype="f16", bias=True, act="gelu_erf",
+                       seed=706))
+    assert c.plan["stream_k"] == 3 and c.plan["swap_ab"] == 1
+
+
+@pytest.mark.parametrize("bn", [64, 256])
+def test_exact_spread_other_tile_widths(bn):
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.BLOCK_N, bn)
+    try:
+        c = run_exact(Case("bf16", 256, 512, 16384, values="ints", seed=707))
+    finally:
+        dg.gemm_set_option(dg.Option.BLOCK_N, 0)
+    assert c.plan["block_n"] == bn and c.plan["stream_k"] == 3, c.plan
+
+
+def test_spread_unpublished_partial_reports_timeout_and_recovers():
+    # the first CTA leaves its partial unpublished: the pieces of its tile give
+    # up after the wait bound, the call reports a timeout, and the context stays
+    # usable
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.TIMEOUT_US, 20000)
+    try:
+        dg.gemm_set_option(dg.Option.TEST_STALL, 2)
+        c = Case("bf16", 256, 256, 16384, values="ints", seed=708)
+        st, _ = c.run_gpu()
+        assert st == 0 and c.plan["stream_k"] == 3
+        stream = torch.cuda.current_stream().cuda_stream
+        assert dg.gemm_check_device_status(stream) == dg.Status.ERR_TIMEOUT
+        assert dg.gemm_check_device_status(stream) == dg.Status.OK
+    finally:
+        dg.gemm_set_option(dg.Option.TEST_STALL, 0)
+        dg.gemm_set_option(dg.Option.TIMEOUT_US, 1000000)
+    run_exact(_spread_case("square_long_k", values="ints", seed=709))
+    assert dg.gemm_check_device_status(torch.cuda.current_stream().cuda_stream) == 0
 
 
 # ---------------------------------------------------------------- 256 x 512 pair tiles
