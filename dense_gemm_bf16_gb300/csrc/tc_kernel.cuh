@@ -299,6 +299,37 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
     const float bias_col = (has_bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
     T* const c0 =
         static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c + row_base * ldc + col;
+    if constexpr (CH == 32) {
+        // an interior block (32 rows inside M, 32 columns inside N) with no
+        // beta * C: no per-row tests, each half's values read from the staging
+        // tile before any is stored (the same arithmetic as finish_run)
+        if (nrows == 32 && col0 + 32 <= N && !has_c) {
+            T* o = c0;
+#pragma unroll 1
+            for (int h = 0; h < 32; h += H) {
+                float v[H];
+#pragma unroll
+                for (int i = 0; i < H; ++i) v[i] = stage[(h + i) * STAGE_LD + lane];
+                if (e.alpha != 1.0f) {
+#pragma unroll
+                    for (int i = 0; i < H; ++i) v[i] *= e.alpha;
+                }
+                if (has_bias) {
+                    if (e.bias_on_rows) {
+#pragma unroll
+                        for (int i = 0; i < H; ++i) v[i] += e.bias[row_base + h + i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < H; ++i) v[i] += bias_col;
+                    }
+                }
+                act_inplace<H>(v, e.act);
+#pragma unroll
+                for (int i = 0; i < H; ++i, o += ldc) st_f(o, v[i]);
+            }
+            return;
+        }
+    }
 #pragma unroll 1
     for (int h = 0; h < 32; h += H) {
         float v[H], cv[H], bv[H];
@@ -529,12 +560,22 @@ __device__ __forceinline__ bool spread_reduce(const TcParams& p, int b, int pid_
         const unsigned long long* flags = p.sk_flags + (static_cast<int64_t>(slot0) * CM + rank) * 4;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
+            // up to eight flags per lane are loaded before any is compared, so
+            // that their loads are in flight together
             bool mine = true;
-            for (int f = lane; f < S * nq; f += 32) {
-                const int s = f / nq;
-                const int qq = q0 + (f - s * nq);
-                if (ld_relaxed_u64(flags + static_cast<int64_t>(s) * CM * 4 + qq) != p.sk_epoch)
-                    mine = false;
+            for (int f0 = 0; f0 < S * nq; f0 += 256) {
+                unsigned long long v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int f = f0 + 32 * u + lane;
+                    const int s = f / nq;
+                    const int qq = q0 + (f - s * nq);
+                    v[u] = f < S * nq
+                               ? ld_relaxed_u64(flags + static_cast<int64_t>(s) * CM * 4 + qq)
+                               : p.sk_epoch;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mine = mine && v[u] == p.sk_epoch;
             }
             if (__all_sync(0xffffffffu, mine)) break;
             int give_up = 0;
