@@ -172,6 +172,7 @@ struct Plan {
     int64_t Mc = 0, Nc = 0;
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
     bool fast_epi = false;  // TMA-store-only epilogue form
+    bool beta_epi = false;  // TMA-store epilogue that reads beta * C by TMA loads
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
     int inkernel_split = 0;  // automatic split-K done in one kernel by the split form
     bool spread = false;     // ... with every piece reducing a share of its tile
@@ -504,6 +505,11 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
             const int64_t es = dt_bytes(c.cdt);
             pl.fast_epi = aligned(c.C, 16) && (c.ldc * es) % 16 == 0 &&
                           (c.batch == 1 || (c.sc * es) % 16 == 0);
+        } else if (c.cdt != DT_F32 && tc_has_beta_form(pl.bn, pl.mode)) {
+            // beta * C read by TMA loads through the output's tensor map
+            pl.beta_epi = aligned(c.C, 16) && (c.ldc * 2) % 16 == 0 &&
+                          (c.batch == 1 || (c.sc * 2) % 16 == 0);
+            if (pl.beta_epi) pl.stages = tc_stages_beta(pl.bn, pl.mode);
         }
     }
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
@@ -687,7 +693,7 @@ gemm_status_t run(const Call& c) {
                              sub_n);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
-    const bool want_fast = pl.fast_epi;
+    const bool want_fast = pl.fast_epi || pl.beta_epi;  // 128-byte boxes
     int epi_form = 0;
     if (pl.c_row_major_c && pl.bn >= 32) {
         bool c3 = false;
@@ -701,7 +707,7 @@ gemm_status_t run(const Call& c) {
                                    want_fast, &c3);
         p.c_tma = ok ? 1 : 0;
         p.c_tma_3d = c3 ? 1 : 0;
-        epi_form = ok && want_fast ? 1 : 0;
+        epi_form = ok && pl.beta_epi ? 2 : (ok && pl.fast_epi ? 1 : 0);
     }
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
@@ -919,7 +925,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
     plan->cta_pair = pl.mode;
-    plan->fast_epilogue = pl.fast_epi ? 1 : 0;
+    plan->fast_epilogue = pl.beta_epi ? 2 : (pl.fast_epi ? 1 : 0);
     plan->stream_k = pl.spread ? 3 : pl.sk;
     return st;
 }

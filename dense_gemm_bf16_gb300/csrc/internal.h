@@ -83,10 +83,14 @@ struct TcParams {
 // sharing B through TMA multicast; 2 CTA pair computing a 256 x BN tile with
 // cta_group::2 MMAs.  Epilogue forms: 0 general; 1 TMA store only, for
 // beta == 0 or split-K partials, with tmap_c boxes of 128-byte rows
-// (tc_has_fast tells the tile widths that have it).
+// (tc_has_fast tells the tile widths that have it); 2 the same with beta * C
+// read by TMA loads through tmap_c, for a 16-bit C (tc_has_beta_form tells the
+// tile widths and modes, tc_stages_beta its pipeline depth).
 int tc_stages_for(int block_n, int mode);
 bool tc_has_mode(int block_n, int mode);
 bool tc_has_fast(int block_n);
+bool tc_has_beta_form(int block_n, int mode);
+int tc_stages_beta(int block_n, int mode);
 cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
 cudaError_t tc_launch(int block_n, int mode, int epi, const TcParams& p, int grid,
                       cudaStream_t stream);

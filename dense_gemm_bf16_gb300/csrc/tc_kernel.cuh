@@ -48,11 +48,13 @@ constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
 // bytes, 128-byte swizzled) for the TMA-store epilogue, or one staging tile
 // of 32 rows x 32 fp32 columns (rows padded to 33 words so that row-wise
 // writes and column-wise reads each touch 32 distinct banks) for the
-// st.global fallback.
+// st.global fallback.  The epilogue form that reads beta * C (EPI 2) adds a
+// ring of two more boxes per warp that TMA loads fill with C.
 constexpr int STAGE_LD = 33;
 constexpr uint32_t EPI_WARP_BYTES = 8192;
 constexpr uint32_t EPI_BOX_BYTES = 4096;
 constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;  // four epilogue warps
+constexpr uint32_t C_RING_BYTES = 4 * 2 * EPI_BOX_BYTES;
 static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 
 // MODE 0: one CTA per 128 x BN tile.
@@ -63,10 +65,10 @@ static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 //         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.  With
 //         BN = 512 the tile is two N = 256 MMAs per K step into the two halves
 //         of tensor memory (one accumulator, no double buffering): every CTA
-//         takes in 48 KB per 64-deep K block for twice the work of BN = 256,
-//         which matters because an SM's TMA intake, not the tensor pipe, bounds
-//         the BN = 256 main loop.
-template <int BN, int MODE>
+//         takes in 48 KB per 64-deep K block for twice the work of BN = 256
+//         (an option: it measured slower than BN = 256).
+// EPI: the epilogue form (only its shared memory matters here).
+template <int BN, int MODE, int EPI = 0>
 struct Cfg {
     static constexpr int CM = MODE == 0 ? 1 : 2;        // CTAs per cluster
     static constexpr int CG = MODE == 2 ? 2 : 1;        // tcgen05 cta_group
@@ -77,14 +79,15 @@ struct Cfg {
     static constexpr uint32_t A_BYTES = BM * BK * 2;
     static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t BAR_BYTES = 256;
-    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+    static constexpr uint32_t BAR_BYTES = 512;
+    static constexpr uint32_t EPI_SMEM = EPI_BYTES + (EPI == 2 ? C_RING_BYTES : 0);
+    static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_SMEM) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr uint32_t TMEM_COLS = ACC_BUFS * BN < 32 ? 32 : ACC_BUFS * BN;
     static constexpr int CHUNK = BN < 32 ? BN : 32;
-    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_BYTES;
+    static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_SMEM;
     static_assert(STAGES >= 2, "pipeline needs two stages");
-    static_assert((2 * STAGES + 6) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert((2 * STAGES + 14) * 8 + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
@@ -777,17 +780,78 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
     }
 }
 
+// The C ring of one epilogue warp (epilogue form 2): two 4 KB boxes that TMA
+// loads fill with 32 rows x 64 columns of a 16-bit C (the output's own tensor
+// map and swizzle), each completing on its own mbarrier.  Every lane keeps the
+// counts of boxes requested and consumed; lane 0 issues the loads.  A tile's
+// first two boxes are requested before its accumulator is waited for, each
+// later one when the box two steps before it has been read.
+struct CRing {
+    uint8_t* box;     // this warp's first box
+    uint32_t bar;     // this warp's first barrier
+    uint32_t issued;  // boxes requested
+    uint32_t used;    // boxes consumed
+};
+
+// Requests the C box of 64-column step c of unit w, for this warp's 32 rows.
+template <int BN>
+__device__ __forceinline__ void c_ring_issue(const TcParams& p, const Unit& w, int q, int lane,
+                                             CRing& cr, int c) {
+    const uint32_t slot = cr.issued & 1u;
+    if (lane == 0) {
+        const uint32_t dst = smem_u32(cr.box + slot * EPI_BOX_BYTES);
+        const uint32_t bar = cr.bar + 8u * slot;
+        const int x = w.pid_n * BN + c * 64;
+        const int y = w.pid_m * BM + q * 32;
+        // the box's previous contents were read by this warp (generic proxy)
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, EPI_BOX_BYTES);
+        if (p.c_tma_3d)
+            tma_load_3d(dst, &p.tmap_c, bar, x, y, w.b, l2_policy_evict_first());
+        else
+            tma_load_2d(dst, &p.tmap_c, bar, x, y, l2_policy_evict_first());
+    }
+    ++cr.issued;
+}
+
+// 64-column steps of unit w that lie (at least partly) inside N.
+template <int BN>
+__device__ __forceinline__ int fast_steps(const TcParams& p, const Unit& w) {
+    const int left = p.N - w.pid_n * BN;
+    const int n = (left + 63) / 64;
+    return n < BN / 64 ? n : BN / 64;
+}
+
+// Waits (bounded, ignoring an abort) until every requested C box has landed,
+// so that no TMA load is still writing this CTA's shared memory when it exits.
+__device__ __forceinline__ void c_ring_drain(CRing& cr, int lane, uint64_t timeout_ns) {
+    if (lane == 0) {
+        for (; cr.used < cr.issued; ++cr.used) {
+            const uint32_t slot = cr.used & 1u;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(cr.bar + 8u * slot, (cr.used >> 1) & 1u) &&
+                   globaltimer_ns() - t0 < timeout_ns) {
+            }
+        }
+    }
+    __syncwarp();
+}
+
 // Output of one warp's 32 rows for the common case (C written by TMA store,
 // beta == 0 or a split-K partial): 64 columns per step, two tcgen05.ld in
 // flight, one fence / warp sync / store issue per step.  Each step fills 128
 // bytes of every row: one 64-column box for a 16-bit C, two 32-column boxes
 // for fp32, 128-byte swizzled like the operand tiles (16-byte piece j of row
-// r at j ^ (r % 8); the boxes are 1024-byte aligned).
-template <int BN, int ES>
-__device__ __forceinline__ void tile_out_fast(const TcParams& p, const Unit& w, int q, int lane,
+// r at j ^ (r % 8); the boxes are 1024-byte aligned).  With BETA (epilogue
+// form 2, 16-bit C) each step also adds beta * C from the warp's C ring, whose
+// boxes have the same swizzle.  Returns false when a C box never arrived.
+template <int BN, int ES, bool BETA = false>
+__device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, int q, int lane,
                                               uint32_t tmem_row, uint8_t* wbuf, uint32_t& nbox,
-                                              uint64_t pol) {
+                                              uint64_t pol, CRing* cr = nullptr,
+                                              volatile int* abort_flag = nullptr) {
     static_assert(BN % 64 == 0, "64-column steps");
+    static_assert(!BETA || ES == 2, "beta * C by TMA loads for 16-bit outputs");
     constexpr int NB = ES == 4 ? 2 : 1;  // boxes per step
     constexpr int BOXC = 128 / ES;       // columns per box
     const Epilogue& e = p.epi;
@@ -798,6 +862,8 @@ __device__ __forceinline__ void tile_out_fast(const TcParams& p, const Unit& w, 
     const bool row_ok = row < p.M;
     const int zc = partial ? w.split * p.batch + w.b : w.b;
     const int swz = lane & 7;
+    const bool need_c = BETA && !partial && e.beta != 0.0f;
+    const int nsteps = fast_steps<BN>(p, w);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
         const int col0 = w.pid_n * BN + c * 64;
@@ -817,6 +883,35 @@ __device__ __forceinline__ void tile_out_fast(const TcParams& p, const Unit& w, 
             if (e.alpha != 1.0f) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) v[i] *= e.alpha;
+            }
+            if constexpr (BETA) {
+                if (need_c) {
+                    // this step's C box, requested two steps (or a tile) earlier
+                    const uint32_t slot = cr->used & 1u;
+                    int ok = 1;
+                    if (lane == 0)
+                        ok = mbar_wait(cr->bar + 8u * slot, (cr->used >> 1) & 1u, abort_flag,
+                                       p.status, p.timeout_ns)
+                                 ? 1
+                                 : 0;
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+                    __syncwarp();
+                    const uint8_t* cl = cr->box + slot * EPI_BOX_BYTES + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 t = *reinterpret_cast<const uint4*>(cl + ((j ^ swz) << 4));
+                        const uint32_t wd[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = unpack2_in(dt, wd[k]);
+                            v[8 * j + 2 * k] = fmaf(e.beta, f.x, v[8 * j + 2 * k]);
+                            v[8 * j + 2 * k + 1] = fmaf(e.beta, f.y, v[8 * j + 2 * k + 1]);
+                        }
+                    }
+                    ++cr->used;
+                    __syncwarp();  // every lane has read the box before it is refilled
+                    if (c + 2 < nsteps) c_ring_issue<BN>(p, w, q, lane, *cr, c + 2);
+                }
             }
             if (e.bias) {
                 if (e.bias_on_rows) {
@@ -881,6 +976,7 @@ __device__ __forceinline__ void tile_out_fast(const TcParams& p, const Unit& w, 
         }
         ++nbox;
     }
+    return true;
 }
 
 // Pull this warp's rows of the C tile into L2 before the accumulator is ready
@@ -900,7 +996,7 @@ __device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w
 
 template <int BN, int MODE, int EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<BN, MODE>;
+    using C = Cfg<BN, MODE, EPI>;
     constexpr int CM = C::CM;
     constexpr int CG = C::CG;
     const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
@@ -913,19 +1009,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
-    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][barriers]
+    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][C ring (EPI 2)][barriers]
     uint8_t* epi_smem = smem + C::STAGES * C::STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + EPI_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + C::EPI_SMEM);
     const uint32_t bar0 = smem_u32(bars);
     // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain,
-    // gather (the spread reduction's copies)
+    // gather (the spread reduction's copies), C boxes [4 epilogue warps][2]
     const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8u * C::STAGES;
     const uint32_t tfull0 = bar0 + 16u * C::STAGES;
     const uint32_t tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
     const uint32_t gather_bar = drain_bar + 8u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 6);
+    const uint32_t cbar0 = gather_bar + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 14);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -948,6 +1045,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         }
         mbar_init(drain_bar, 1);
         mbar_init(gather_bar, 1);
+        for (int b = 0; b < 8; ++b) mbar_init(cbar0 + 8u * b, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tmap_a);
@@ -1181,10 +1279,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const uint64_t store_pol = p.partials ? l2_policy_evict_last() : l2_policy_evict_first();
         int abuf = 0;
         uint32_t aphase = 0;
+        // epilogue form 2: this warp's ring of C boxes and their barriers
+        CRing cring{epi_smem + EPI_BYTES + (warp - 2) * 2 * EPI_BOX_BYTES,
+                    cbar0 + 16u * static_cast<uint32_t>(warp - 2), 0u, 0u};
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
         bool first = true;
         while (work_next<CM>(p, wi, ncta, rank, w)) {
+            if constexpr (EPI == 2) {
+                // the first two C boxes of a tile this warp will write, requested
+                // before its accumulator is waited for
+                if (p.epi.beta != 0.0f && (w.kind == UNIT_FULL || w.kind == UNIT_HEAD)) {
+                    const int n = fast_steps<BN>(p, w);
+                    for (int c = 0; c < 2 && c < n; ++c) c_ring_issue<BN>(p, w, q, lane, cring, c);
+                }
+            }
             if constexpr (EPI == 0) {
                 // C tile of the next item into L2 (and of this one, the first time)
                 if (first)
@@ -1269,6 +1378,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
                     else
                         tile_out_fast<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                } else if constexpr (EPI == 2) {
+                    // the plan takes this form for a 16-bit C only
+                    if (!tile_out_fast<BN, 2, true>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol,
+                                                    &cring, abort_flag))
+                        break;
                 } else if (p.c_tma) {
                     if constexpr (BN >= 32) {
                         if (p.partials != nullptr || p.epi.c_dtype == DT_F32)
@@ -1322,7 +1436,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                           C::STAGES * C::STAGE_BYTES, gather_bar);
             }
         }
-        // the TMA stores must finish before the CTA exits
+        // the TMA stores must finish, and no C box may still be loading, before
+        // the CTA exits
+        if constexpr (EPI == 2) c_ring_drain(cring, lane, p.timeout_ns);
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
     }
@@ -1342,15 +1458,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 // refuses the launch, instead of leaving a waiting CTA without its peers.
 template <int BN, int MODE, int EPI>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
-    constexpr int CM = Cfg<BN, MODE>::CM;
+    constexpr int CM = Cfg<BN, MODE, EPI>::CM;
     if (CM == 1 && !p.sk_spread) {
-        tc_gemm_kernel<BN, MODE, EPI><<<grid, TC_THREADS, Cfg<BN, MODE>::SMEM, stream>>>(p);
+        tc_gemm_kernel<BN, MODE, EPI><<<grid, TC_THREADS, Cfg<BN, MODE, EPI>::SMEM, stream>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, MODE, EPI>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned n = 0;
@@ -1375,7 +1491,7 @@ template <int BN, int MODE, int EPI>
 cudaError_t prepare_bn() {
     return cudaFuncSetAttribute(tc_gemm_kernel<BN, MODE, EPI>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(Cfg<BN, MODE>::SMEM));
+                                static_cast<int>(Cfg<BN, MODE, EPI>::SMEM));
 }
 
 // Two-CTA clusters that can be resident at once (0 on error).
@@ -1385,7 +1501,7 @@ int max_clusters_bn() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CM * 64);
     cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = Cfg<BN, MODE>::SMEM;
+    cfg.dynamicSmemBytes = Cfg<BN, MODE, EPI>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CM;

@@ -260,7 +260,8 @@ typedef struct {
                                 K pieces that run side by side (also the automatic
                                 split-K in one kernel); 3 the same with every piece
                                 reducing an equal share of its tile               */
-    int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue (GEMM_OPT_FAST_EPILOGUE) */
+    int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue; 2: the TMA-store epilogue
+                                that reads beta * C by TMA loads (GEMM_OPT_FAST_EPILOGUE) */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
@@ -298,8 +299,11 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         3: force the split form (plan stream_k 2) when S >= 2.
  *   GEMM_OPT_FAST_EPILOGUE 0 (default): when no beta * C is read (beta == 0, or split-K
  *                         partials) and C takes TMA stores, use the epilogue built for
- *                         that case alone (64-column steps, fewer registers); 1: always
- *                         the general epilogue.
+ *                         that case alone (64-column steps, fewer registers); when a
+ *                         16-bit C that takes TMA stores is read (beta != 0), use the
+ *                         same epilogue with beta * C brought in by TMA loads (two
+ *                         64-column boxes ahead per epilogue warp); 1: always the
+ *                         general epilogue.
  *   GEMM_OPT_SGEMM_KERNEL 0 (default): the fp32 CUDA-core path with row-major A and B
  *                         whose rows are 16-byte aligned uses the kernel that copies
  *                         tiles with cp.async and issues packed fp32 FMAs (128 x 64

@@ -418,9 +418,62 @@ def test_fast_epilogue_matches_general(name):
     assert np.array_equal(out_fast.view(np.uint8), out_gen.view(np.uint8))
 
 
-def test_beta_uses_general_epilogue():
+def test_beta_epilogue_forms():
+    # a 16-bit C that takes TMA stores reads beta * C by TMA loads (form 2); an
+    # fp32 C keeps the general form
     c = run_close(Case("bf16", 300, 520, 200, c_dtype="bf16", beta=0.5, seed=311))
+    assert c.plan["fast_epilogue"] == 2
+    c = run_close(Case("bf16", 300, 520, 200, c_dtype="f32", beta=0.5, seed=312))
     assert c.plan["fast_epilogue"] == 0
+
+
+# beta * C by TMA loads: tile widths, pair tiles, ragged edges (N = 712 ends 8
+# columns into a 64-column step; M = 333 inside a 32-row box), a row bias, a
+# batch (3-D maps) and the finishing piece of an in-kernel split
+BETA_FORM_CASES = {
+    "bn64": dict(ab="bf16", M=333, N=712, K=300, opts={"BLOCK_N": 64}),
+    "bn128": dict(ab="bf16", M=333, N=712, K=300, bias=True, act="gelu_tanh"),
+    "bn256": dict(ab="bf16", M=333, N=712, K=300, opts={"BLOCK_N": 256}),
+    "pair128": dict(ab="bf16", M=1100, N=1304, K=320, opts={"CTA_PAIR": 3, "BLOCK_N": 128}),
+    "pair256": dict(ab="bf16", M=1100, N=1304, K=320, bias=True,
+                    opts={"CTA_PAIR": 3, "BLOCK_N": 256}),
+    "f16_row_bias_relu": dict(ab="f16", M=300, N=520, K=200, bias=True, row_bias=True,
+                              act="relu"),
+    "batched": dict(ab="bf16", M=200, N=264, K=130, batch=3, bias=True, act="gelu_erf"),
+    "inkernel_split_head": dict(ab="bf16", M=1024, N=640, K=4096, bias=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BETA_FORM_CASES))
+def test_beta_epilogue_matches_general(name):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(BETA_FORM_CASES[name])
+    opts = kw.pop("opts", {})
+
+    def run(extra):
+        for k, v in {**opts, **extra}.items():
+            dg.gemm_set_option(dg.Option[k], v)
+        try:
+            c = Case(c_dtype=kw["ab"], alpha=0.5, beta=-0.75, seed=331, **kw)
+            st, out = c.run_gpu()
+        finally:
+            for k in {**opts, **extra}:
+                dg.gemm_set_option(dg.Option[k], 0)
+        assert st == 0, f"status {st}"
+        return c, out
+    c, out = run({})
+    assert c.plan["fast_epilogue"] == 2, c.plan
+    if "CTA_PAIR" in opts:
+        assert c.plan["cta_pair"] == 2, c.plan
+    if "BLOCK_N" in opts:
+        assert c.plan["block_n"] == opts["BLOCK_N"], c.plan
+    if name == "inkernel_split_head":
+        assert c.plan["stream_k"] == 2, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+    assert c.untouched_padding(out)
+    g, out_g = run({"FAST_EPILOGUE": 1})
+    assert g.plan["fast_epilogue"] == 0
+    assert np.array_equal(out.view(np.uint8), out_g.view(np.uint8))
 
 
 @pytest.mark.parametrize("shape", [(700, 600, 333), (4097, 700, 64)])
@@ -438,8 +491,10 @@ def test_exact_general_epilogue_forced(general_epilogue, shape):
 EPI_ROUTES = {
     "tc_fast": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", alpha=0.5), {},
                 {"fast_epilogue": 1}),
-    "tc_general_beta": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", beta=0.75), {},
-                        {"fast_epilogue": 0}),
+    "tc_general_beta": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", beta=0.75),
+                        {"FAST_EPILOGUE": 1}, {"fast_epilogue": 0}),
+    "tc_beta_tma": (dict(ab="bf16", M=333, N=712, K=300, c_dtype="bf16", beta=0.75), {},
+                    {"fast_epilogue": 2}),
     "tc_unaligned_ldc": (dict(ab="bf16", M=260, N=701, K=200, c_dtype="f32"), {},
                          {"fast_epilogue": 0}),
     "tc_col_major_c": (dict(ab="f16", M=200, N=300, K=160, lc="col", c_dtype="f32",
