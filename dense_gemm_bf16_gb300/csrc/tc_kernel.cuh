@@ -1294,7 +1294,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     for (int c = 0; c < 2 && c < n; ++c) c_ring_issue<BN>(p, w, q, lane, cring, c);
                 }
             }
-            if constexpr (EPI == 0) {
+            if constexpr (EPI == 0 || EPI == 2) {
                 // C tile of the next item into L2 (and of this one, the first time)
                 if (first)
                     prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
