@@ -1028,6 +1028,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // The launch parameters outside the tensor maps lie in four 64-byte lines.
+    // A role's first reads of them miss the constant cache one after another
+    // along its dependent chain of decisions; one read per line, from four warps
+    // at once during the prologue, takes those misses together instead.
+    if (lane == 0) {
+        if (warp == 2) asm volatile("" ::"r"(p.M));
+        if (warp == 3) asm volatile("" ::"f"(p.epi.alpha));
+        if (warp == 4) asm volatile("" ::"r"(p.c_tma));
+        if (warp == 5) asm volatile("" ::"l"(p.sk_epoch));
+    }
+
     if (threadIdx.x == 0) {
         // MODE 2: the leader's stage barrier collects the bytes of both CTAs'
         // loads; its accumulator-release barrier counts the epilogue warps of
