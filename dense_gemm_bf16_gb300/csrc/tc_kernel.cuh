@@ -1061,6 +1061,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         fence_mbar_init();
         prefetch_tmap(&p.tmap_a);
         prefetch_tmap(&p.tmap_b);
+        if (p.c_tma) prefetch_tmap(&p.tmap_c);
     }
     if (warp == 1) {
         tmem_alloc_cg<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
