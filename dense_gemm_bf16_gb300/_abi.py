@@ -66,6 +66,7 @@ class Option(enum.IntEnum):
     WIDE_TILE = 11
     SPLIT_REDUCE = 12
     BLOCK_N = 13
+    DOUBLE_K = 14
 
 
 class Plan(ctypes.Structure):

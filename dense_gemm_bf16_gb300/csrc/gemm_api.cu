@@ -34,6 +34,7 @@ std::atomic<int64_t> g_opt_sgemm_kernel{0};
 std::atomic<int64_t> g_opt_wide_tile{0};
 std::atomic<int64_t> g_opt_split_reduce{0};
 std::atomic<int64_t> g_opt_block_n{0};
+std::atomic<int64_t> g_opt_double_k{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -173,6 +174,7 @@ struct Plan {
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
     bool fast_epi = false;  // TMA-store-only epilogue form
     bool beta_epi = false;  // TMA-store epilogue that reads beta * C by TMA loads
+    int ks = 1;             // 64-deep K blocks per stage and per operand load
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
     int inkernel_split = 0;  // automatic split-K done in one kernel by the split form
     bool spread = false;     // ... with every piece reducing a share of its tile
@@ -512,6 +514,17 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
             if (pl.beta_epi) pl.stages = tc_stages_beta(pl.bn, pl.mode);
         }
     }
+    // Two K blocks per TMA load (KS = 2) for K-major operands of a CTA-pair
+    // plan with the TMA-store-only epilogue: the operands are seen as
+    // (64 K, rows, K blocks), so K must be a whole number of 64-deep blocks
+    // (an odd count reads its last block's partner past the end: zeros); whole
+    // units only (no stream-K or split pieces), one batch entry.
+    if (g_opt_double_k.load() == 0 && pl.kernel == 1 && pl.fast_epi && pl.splits == 1 &&
+        pl.sk == 0 && tc_has_ks2(pl.bn, pl.mode, 1) && !pl.a.mn && !pl.b.mn && c.batch == 1 &&
+        c.K % TC_BLOCK_K == 0) {
+        pl.ks = 2;
+        pl.stages = tc_stages_ks2(pl.bn);
+    }
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
     if (pl.ws_need > 0 && !aligned(c.ws, 256)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
@@ -541,9 +554,26 @@ Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
 
 gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const void* ptr,
                              int64_t ld, int64_t stride, int64_t batch, uint32_t box_k_major_rows,
-                             bool* is3d) {
+                             bool two_k_blocks, bool* is3d) {
     auto fn = encode_fn();
     if (!fn) return GEMM_ERR_CUDA;
+    const CUtensorMapDataType type =
+        ab == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (two_k_blocks) {
+        // K-major, K a multiple of 64: (64 K, rows, K blocks), two K blocks a box
+        if (o.mn || o.k_ext % 64 != 0) return GEMM_ERR_UNSUPPORTED;
+        cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(o.outer()),
+                              static_cast<cuuint64_t>(o.k_ext / 64)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), 128u};
+        cuuint32_t box[3] = {64u, box_k_major_rows, 2u};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        const CUresult r = fn(map, type, 3u, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+        *is3d = true;
+        return GEMM_OK;
+    }
     const bool three = batch > 1 && stride != 0;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(o.inner()), static_cast<cuuint64_t>(o.outer()),
                           static_cast<cuuint64_t>(batch)};
@@ -551,10 +581,7 @@ gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const v
     // K-major: box = 64 K x rows-of-tile; MN-major: box = 64 MN x 64 K (one swizzle atom column)
     cuuint32_t box[3] = {64u, o.mn ? 64u : box_k_major_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = fn(map,
-                          ab == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                          three ? 3u : 2u, const_cast<void*>(ptr), dims, strides, box, estr,
+    const CUresult r = fn(map, type, three ? 3u : 2u, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
@@ -667,12 +694,13 @@ gemm_status_t run(const Call& c) {
     TcParams p;
     std::memset(&p, 0, sizeof(p));
     bool a3 = false, b3 = false;
-    st = encode_operand(&p.tmap_a, c.ab, pl.a, a_ptr, a_ld, a_stride, c.batch, TC_BLOCK_M, &a3);
+    st = encode_operand(&p.tmap_a, c.ab, pl.a, a_ptr, a_ld, a_stride, c.batch, TC_BLOCK_M,
+                        pl.ks == 2, &a3);
     if (st != GEMM_OK) return st;
     // B box: the rows (N) one load brings, half of an N <= 256 MMA per CTA of a pair
     const int sub_n = pl.bn < 256 ? pl.bn : 256;
     st = encode_operand(&p.tmap_b, c.ab, pl.b, b_ptr, b_ld, b_stride, c.batch,
-                        static_cast<uint32_t>(pl.cm == 2 ? sub_n / 2 : pl.bn), &b3);
+                        static_cast<uint32_t>(pl.cm == 2 ? sub_n / 2 : pl.bn), pl.ks == 2, &b3);
     if (st != GEMM_OK) return st;
     p.M = static_cast<int32_t>(pl.Mc);
     p.N = static_cast<int32_t>(pl.Nc);
@@ -724,7 +752,7 @@ gemm_status_t run(const Call& c) {
         p.sk_flags = reinterpret_cast<unsigned long long*>(ws + pl.sk_flags_off);
         p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
     }
-    if (tc_launch(pl.bn, pl.mode, epi_form, p, pl.grid, c.stream) != cudaSuccess)
+    if (tc_launch(pl.bn, pl.mode, epi_form, pl.ks, p, pl.grid, c.stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
         if (splitk_epilogue_launch(p.partials, pl.splits, c.batch, pl.Mc, pl.Nc, p.epi,
@@ -914,7 +942,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->kernel = pl.kernel;
     plan->block_m = pl.kernel == 1 ? TC_BLOCK_M : (pl.kernel == 2 ? 128 : 0);
     plan->block_n = pl.bn;
-    plan->block_k = pl.kernel == 1 ? TC_BLOCK_K : (pl.kernel == 2 ? 8 : 0);
+    plan->block_k = pl.kernel == 1 ? TC_BLOCK_K * pl.ks : (pl.kernel == 2 ? 8 : 0);
     plan->stages = pl.stages;
     plan->split_k = pl.splits;
     plan->swap_ab = pl.swap ? 1 : 0;
@@ -986,6 +1014,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
                 return GEMM_ERR_INVALID_ARG;
             g_opt_block_n.store(value);
             return GEMM_OK;
+        case GEMM_OPT_DOUBLE_K:
+            if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+            g_opt_double_k.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -1005,6 +1037,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_WIDE_TILE: return g_opt_wide_tile.load();
         case GEMM_OPT_SPLIT_REDUCE: return g_opt_split_reduce.load();
         case GEMM_OPT_BLOCK_N: return g_opt_block_n.load();
+        case GEMM_OPT_DOUBLE_K: return g_opt_double_k.load();
     }
     return -1;
 }

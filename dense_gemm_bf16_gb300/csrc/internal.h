@@ -85,15 +85,20 @@ struct TcParams {
 // beta == 0 or split-K partials, with tmap_c boxes of 128-byte rows
 // (tc_has_fast tells the tile widths that have it); 2 the same with beta * C
 // read by TMA loads through tmap_c, for a 16-bit C (tc_has_beta_form tells the
-// tile widths and modes, tc_stages_beta its pipeline depth).
+// tile widths and modes, tc_stages_beta its pipeline depth).  ks: 64-deep K
+// blocks per stage and per TMA load of a K-major operand, 1 or 2 (tc_has_ks2
+// tells where 2 exists; its operand maps are the three-dimensional views
+// 64 K x rows x K blocks).
 int tc_stages_for(int block_n, int mode);
 bool tc_has_mode(int block_n, int mode);
 bool tc_has_fast(int block_n);
 bool tc_has_beta_form(int block_n, int mode);
 int tc_stages_beta(int block_n, int mode);
 cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribute (per device)
-cudaError_t tc_launch(int block_n, int mode, int epi, const TcParams& p, int grid,
+cudaError_t tc_launch(int block_n, int mode, int epi, int ks, const TcParams& p, int grid,
                       cudaStream_t stream);
+bool tc_has_ks2(int block_n, int mode, int epi);
+int tc_stages_ks2(int block_n);
 int tc_max_pairs(int block_n, int mode);  // two-CTA clusters resident at once on this device
 
 struct SgemmParams {

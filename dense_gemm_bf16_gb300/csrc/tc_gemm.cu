@@ -11,6 +11,8 @@ int tc_max_pairs_general(int bn, int mode);
 cudaError_t tc_launch_general(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t tc_launch_fast(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t tc_prepare_beta(int bn);
+cudaError_t tc_prepare_ks2(int bn);
+cudaError_t tc_launch_ks2(int bn, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t tc_launch_beta(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 
 int tc_stages_for(int bn, int mode) {
@@ -34,6 +36,7 @@ cudaError_t tc_prepare(int bn) {
     cudaError_t e = tc_prepare_general(bn);
     if (e == cudaSuccess) e = tc_prepare_fast(bn);
     if (e == cudaSuccess) e = tc_prepare_beta(bn);
+    if (e == cudaSuccess) e = tc_prepare_ks2(bn);
     return e;
 }
 
@@ -48,7 +51,12 @@ int tc_max_pairs(int bn, int mode) { return tc_max_pairs_general(bn, mode); }
 
 bool tc_has_fast(int bn) { return bn == 64 || bn == 128 || bn == 256 || bn == 512; }
 
-cudaError_t tc_launch(int bn, int mode, int epi, const TcParams& p, int grid, cudaStream_t stream) {
+cudaError_t tc_launch(int bn, int mode, int epi, int ks, const TcParams& p, int grid,
+                      cudaStream_t stream) {
+    if (ks == 2) {
+        if (!tc_has_ks2(bn, mode, epi)) return cudaErrorInvalidValue;
+        return tc_launch_ks2(bn, p, grid, stream);
+    }
     if (epi == 1 && tc_has_fast(bn)) return tc_launch_fast(bn, mode, p, grid, stream);
     if (epi == 2 && tc_has_beta_form(bn, mode)) return tc_launch_beta(bn, mode, p, grid, stream);
     return tc_launch_general(bn, mode, p, grid, stream);

@@ -327,6 +327,10 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
  *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes
  *                         at least 64).
+ *   GEMM_OPT_DOUBLE_K     0 (default): CTA-pair plans with K-major A and B, K a multiple
+ *                         of 64, one batch entry, whole tiles and the TMA-store-only
+ *                         epilogue bring two 64-deep K blocks of each operand per TMA
+ *                         load (plan block_k 128); 1: one K block per load always.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; 2 makes
@@ -348,7 +352,8 @@ typedef enum {
     GEMM_OPT_SGEMM_KERNEL = 10,
     GEMM_OPT_WIDE_TILE = 11,
     GEMM_OPT_SPLIT_REDUCE = 12,
-    GEMM_OPT_BLOCK_N = 13
+    GEMM_OPT_BLOCK_N = 13,
+    GEMM_OPT_DOUBLE_K = 14
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -133,6 +133,11 @@ def test_split_reduce_and_block_n_options(lib):
     for v in (8, 48, 96, 512, -16):
         assert dg.gemm_set_option(Option.BLOCK_N, v) == Status.ERR_INVALID_ARG
     assert dg.gemm_get_option(Option.BLOCK_N) == 0
+    assert dg.gemm_get_option(Option.DOUBLE_K) == 0
+    assert dg.gemm_set_option(Option.DOUBLE_K, 1) == Status.OK
+    assert dg.gemm_get_option(Option.DOUBLE_K) == 1
+    assert dg.gemm_set_option(Option.DOUBLE_K, 2) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.DOUBLE_K, 0) == Status.OK
 
 
 @pytest.mark.parametrize("group_m", [1, 2, 3, 5, 8, 64])

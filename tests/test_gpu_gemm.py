@@ -695,6 +695,69 @@ def test_spread_unpublished_partial_reports_timeout_and_recovers():
     assert dg.gemm_check_device_status(torch.cuda.current_stream().cuda_stream) == 0
 
 
+# ---------------------------------------------------------------- two K blocks per TMA load
+
+# CTA-pair plans with K-major A and B bring two 64-deep K blocks per load (plan
+# block_k 128); an odd count of K blocks reads its last block's partner past
+# the end of K (zeros).  The K order is the same, so the bits match the
+# one-block form exactly.
+DOUBLE_K_CASES = {
+    "even_bn128": dict(M=600, N=700, K=640, opts={"CTA_PAIR": 3, "BLOCK_N": 128}),
+    "odd_bn256": dict(M=600, N=700, K=320, opts={"CTA_PAIR": 3, "BLOCK_N": 256}),
+    "odd_many_tiles": dict(M=1100, N=1304, K=1088, opts={"CTA_PAIR": 3}),
+    "packed_a": dict(M=520, N=600, K=704, pads=(8, 0, 0), offsets=(1, 0, 0),
+                     opts={"CTA_PAIR": 3}),
+}
+
+
+def _double_k_run(kw, extra, **case_kw):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(kw)
+    opts = {**kw.pop("opts"), **extra}
+    for k, v in opts.items():
+        dg.gemm_set_option(dg.Option[k], v)
+    try:
+        c = Case("bf16", la="row", lb="col", **kw, **case_kw)
+        st, out = c.run_gpu()
+    finally:
+        for k in opts:
+            dg.gemm_set_option(dg.Option[k], 0)
+    assert st == 0, f"status {st}"
+    return c, out
+
+
+@pytest.mark.parametrize("name", sorted(DOUBLE_K_CASES))
+def test_exact_double_k(name):
+    c, out = _double_k_run(DOUBLE_K_CASES[name], {}, values="ints", seed=901)
+    assert c.plan["block_k"] == 128 and c.plan["cta_pair"] == 2, c.plan
+    assert np.array_equal(c.result(out), c.oracle_full())
+    assert c.untouched_padding(out)
+    one, out1 = _double_k_run(DOUBLE_K_CASES[name], {"DOUBLE_K": 1}, values="ints", seed=901)
+    assert one.plan["block_k"] == 64
+    assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
+
+
+def test_double_k_bias_gelu_matches_one_block():
+    kw = dict(M=1100, N=1304, K=1024, opts={"CTA_PAIR": 3})
+    c, out = _double_k_run(kw, {}, c_dtype="bf16", bias=True, act="gelu_tanh", seed=902)
+    assert c.plan["block_k"] == 128, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+    _, out1 = _double_k_run(kw, {"DOUBLE_K": 1}, c_dtype="bf16", bias=True, act="gelu_tanh",
+                            seed=902)
+    assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
+
+
+@pytest.mark.parametrize("la,lb", [("col", "col"), ("row", "row")])
+def test_double_k_needs_k_major_operands(la, lb):
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 3)
+    try:
+        c = run_exact(Case("bf16", 600, 700, 640, la=la, lb=lb, values="ints", seed=903))
+    finally:
+        dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
+    assert c.plan["block_k"] == 64 and c.plan["cta_pair"] == 2, c.plan
+
+
 # ---------------------------------------------------------------- 256 x 512 pair tiles
 
 @pytest.fixture
