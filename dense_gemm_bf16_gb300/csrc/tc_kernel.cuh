@@ -5,12 +5,12 @@
 // fp32 accumulator, cast after the loop) mapped onto GB300:
 //
 //   warp 0 (one lane)  TMA producer: fills a ring of STAGES shared-memory
-//                      stages with the A tile [128 x 64] and the B tile
-//                      [BN x 64], 128-byte swizzled, out-of-range elements
+//                      stages with the A tile [128 x 64 KS] and the B tile
+//                      [BN x 64 KS], 128-byte swizzled, out-of-range elements
 //                      zero-filled by the TMA unit (the K / M / N masks of
 //                      "Skill: Write a Triton GEMM Kernel", step 5).
 //   warp 1 (one lane)  MMA issuer: tcgen05.mma kind::f16, M=128, N=BN, K=16,
-//                      four per stage, into one of two TMEM accumulators;
+//                      4 KS per stage, into one of two TMEM accumulators;
 //                      tcgen05.commit frees the stage / publishes the tile.
 //   warps 2-5          epilogue: tcgen05.ld of the accumulator (one TMEM lane =
 //                      one output row per thread), alpha/beta/bias/GELU in fp32,
@@ -26,9 +26,12 @@
 // EPI selects the epilogue's output code: 0 handles every case (beta * C
 // read with loads one chunk ahead, TMA store or an st.global fallback for a C
 // that TMA cannot address); 1 only the TMA store with beta == 0 or a split-K
-// partial, in 64-column steps, and so needs far fewer registers.  The two are
-// instantiated in separate translation units (tc_gemm_general.cu,
-// tc_gemm_fast.cu) that compile in parallel.
+// partial, in 64-column steps, and so needs far fewer registers; 2 the same
+// TMA store with beta * C of a 16-bit C brought in by TMA loads.  KS is the
+// number of 64-deep K blocks per stage (2: one TMA load brings two K blocks of
+// a K-major operand).  The forms are instantiated in separate translation
+// units (tc_gemm_general.cu, tc_gemm_fast.cu, tc_gemm_beta.cu, tc_gemm_ks2.cu)
+// that compile in parallel.
 #pragma once
 #include <stdint.h>
 
