@@ -505,6 +505,7 @@ ABLATION = [  # (label, GEMM options)
     ("single-CTA tiles (no CTA pairs)", {"CTA_PAIR": 1}),
     ("CTA pairs sharing B by multicast", {"CTA_PAIR": 2}),
     ("256 x 512 pair tiles (one accumulator)", {"WIDE_TILE": 2}),
+    ("one K block per TMA load", {"DOUBLE_K": 1}),
 ]
 
 
