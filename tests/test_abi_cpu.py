@@ -162,3 +162,50 @@ def test_tile_order_groups_walk_columns_of_tile_rows(lib):
     assert pm[:8] == list(range(8)) and pn[:8] == [0] * 8
     assert pm[8:16] == list(range(8)) and pn[8:16] == [1] * 8
     assert pm[32:40] == list(range(8, 16)) and pn[32:40] == [0] * 8
+
+
+# ---------------------------------------------------------------- header <-> binding
+
+def _header_source():
+    src = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    return re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+
+
+def _header_enum(type_name):
+    m = re.search(r"typedef enum\s*\{([^{}]*)\}\s*" + type_name + r"\s*;", _header_source())
+    assert m, type_name
+    values = {}
+    for item in m.group(1).split(","):
+        item = item.strip()
+        if item:
+            name, value = (x.strip() for x in item.split("="))
+            values[name] = int(value)
+    return values
+
+
+@pytest.mark.parametrize("type_name,prefix,enum_cls", [
+    ("gemm_status_t", "GEMM_", Status),
+    ("gemm_layout_t", "GEMM_", Layout),
+    ("gemm_dtype_t", "GEMM_DT_", DType),
+    ("gemm_epilogue_t", "GEMM_EPI_", Epi),
+    ("gemm_option_t", "GEMM_OPT_", Option),
+])
+def test_header_enums_match_the_binding(type_name, prefix, enum_cls):
+    header = {name[len(prefix):]: value for name, value in _header_enum(type_name).items()}
+    binding = {member.name: int(member) for member in enum_cls}
+    assert header == binding
+
+
+def test_plan_struct_matches_the_header():
+    import ctypes
+    m = re.search(r"typedef struct\s*\{([^{}]*)\}\s*gemm_plan_t\s*;", _header_source())
+    assert m
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        ctype, names = decl.split(None, 1)
+        for name in names.split(","):
+            fields.append((name.strip(), {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}[ctype]))
+    assert [(n, t) for n, t in dg.Plan._fields_] == fields
