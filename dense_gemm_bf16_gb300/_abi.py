@@ -67,6 +67,7 @@ class Option(enum.IntEnum):
     SPLIT_REDUCE = 12
     BLOCK_N = 13
     DOUBLE_K = 14
+    TEST_SIM_SMS = 15
 
 
 class Plan(ctypes.Structure):

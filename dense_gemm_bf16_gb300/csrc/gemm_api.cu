@@ -35,6 +35,7 @@ std::atomic<int64_t> g_opt_wide_tile{0};
 std::atomic<int64_t> g_opt_split_reduce{0};
 std::atomic<int64_t> g_opt_block_n{0};
 std::atomic<int64_t> g_opt_double_k{0};
+std::atomic<int64_t> g_opt_test_sim_sms{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -53,6 +54,22 @@ struct DevState {
     int max_pairs[3][3] = {};  // co-resident two-CTA clusters [mode][BN 128, 256, 512]
 };
 DevState g_dev[kMaxDevices];
+
+gemm_status_t device_state(DevState** out);
+
+// The device a planning query plans for: the current one, or, with the
+// test-only GEMM_OPT_TEST_SIM_SMS = n, an sm_103 device of n SMs whose CTA
+// pairs of every tile width fit n / 2 at once (nothing is launched).
+gemm_status_t planning_device(DevState& sim, DevState** out) {
+    const int64_t n = g_opt_test_sim_sms.load();
+    if (n <= 0) return device_state(out);
+    sim.sm_count = static_cast<int>(n);
+    sim.cc = 103;
+    for (auto& mode : sim.max_pairs)
+        for (int& v : mode) v = static_cast<int>(n / 2);
+    *out = &sim;
+    return GEMM_OK;
+}
 
 gemm_status_t device_state(DevState** out) {
     int dev = -1;
@@ -849,8 +866,9 @@ size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int6
     if (ab_dtype != GEMM_DT_BF16 && ab_dtype != GEMM_DT_F16) return 0;
     if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || split_k < 0) return 0;
     if (batch > 0x7FFFFFFF || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return 0;
+    DevState sim;
     DevState* d = nullptr;
-    if (device_state(&d) != GEMM_OK) return 0;
+    if (planning_device(sim, &d) != GEMM_OK) return 0;
     const int64_t pa = batch * (M * round_up(K, 8) > K * round_up(M, 8) ? M * round_up(K, 8)
                                                                          : K * round_up(M, 8));
     const int64_t pb = batch * (N * round_up(K, 8) > K * round_up(N, 8) ? N * round_up(K, 8)
@@ -934,8 +952,9 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
                              const_cast<char*>(probe), workspace_bytes, nullptr);
     gemm_status_t st = validate(c);
     if (st != GEMM_OK) return st;
+    DevState sim;
     DevState* d = nullptr;
-    st = device_state(&d);
+    st = planning_device(sim, &d);
     if (st != GEMM_OK) return st;
     Plan pl;
     st = make_plan(c, *d, pl);
@@ -1018,6 +1037,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
             g_opt_double_k.store(value);
             return GEMM_OK;
+        case GEMM_OPT_TEST_SIM_SMS:
+            if (value < 0 || value > 4096) return GEMM_ERR_INVALID_ARG;
+            g_opt_test_sim_sms.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -1038,6 +1061,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_SPLIT_REDUCE: return g_opt_split_reduce.load();
         case GEMM_OPT_BLOCK_N: return g_opt_block_n.load();
         case GEMM_OPT_DOUBLE_K: return g_opt_double_k.load();
+        case GEMM_OPT_TEST_SIM_SMS: return g_opt_test_sim_sms.load();
     }
     return -1;
 }

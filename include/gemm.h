@@ -331,6 +331,12 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         of 64, one batch entry, whole tiles and the TMA-store-only
  *                         epilogue bring two 64-deep K blocks of each operand per TMA
  *                         load (plan block_k 128); 1: one K block per load always.
+ *   GEMM_OPT_TEST_SIM_SMS test only: n > 0 makes gemm_plan_query and
+ *                         gemm_workspace_size plan for a simulated sm_103 device of n
+ *                         SMs whose CTA pairs of every tile width fit n / 2 at once,
+ *                         instead of the current device, so that plans can be
+ *                         checked without a GPU (calls that run GEMMs still need
+ *                         one); 0 (default) off.
  *   GEMM_OPT_TEST_STALL   test only: 1 makes the next tensor-core launch leave one
  *                         pipeline stage unfilled, so its consumer's bounded wait
  *                         expires and the kernel reports GEMM_ERR_TIMEOUT; 2 makes
@@ -353,7 +359,8 @@ typedef enum {
     GEMM_OPT_WIDE_TILE = 11,
     GEMM_OPT_SPLIT_REDUCE = 12,
     GEMM_OPT_BLOCK_N = 13,
-    GEMM_OPT_DOUBLE_K = 14
+    GEMM_OPT_DOUBLE_K = 14,
+    GEMM_OPT_TEST_SIM_SMS = 15
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -1,0 +1,156 @@
+"""The planner without a GPU: with the test-only GEMM_OPT_TEST_SIM_SMS the plan
+queries plan for a simulated sm_103 device of 152 SMs (76 co-resident CTA
+pairs), and these tests pin the plan of every workload the bench times, the
+options that change it, and the workspace rules.  Pointers are stand-in
+addresses that planning only checks for alignment."""
+import pytest
+
+import dense_gemm_bf16_gb300 as dg
+from dense_gemm_bf16_gb300 import Option, Status
+
+BASE = 1 << 24      # 256-byte aligned stand-in address (never dereferenced)
+UNLIMITED = 1 << 40
+
+
+@pytest.fixture(scope="module", autouse=True)
+def simulated_device():
+    dg.build()
+    dg.lib()
+    assert dg.gemm_set_option(Option.TEST_SIM_SMS, 152) == Status.OK
+    yield
+    dg.gemm_set_option(Option.TEST_SIM_SMS, 0)
+
+
+@pytest.fixture
+def options():
+    """Sets options for one test and restores the defaults afterwards."""
+    touched = []
+
+    def set_(**kw):
+        for k, v in kw.items():
+            assert dg.gemm_set_option(Option[k], v) == Status.OK
+            touched.append(k)
+    yield set_
+    for k in touched:
+        dg.gemm_set_option(Option[k], 0 if k != "GROUP_M" else 8)
+
+
+def plan(M, N, K, *, ab=0, batch=1, la=0, lb=0, lc=0, lda=None, ldb=None, ldc=None, cdt=None,
+         alpha=1.0, beta=0.0, epi=0, split_k=0, ws=0, sa=0, sb=0, sc=0, a=BASE, b=BASE, c=BASE):
+    lda = lda or (K if la == 0 else M)
+    ldb = ldb or (N if lb == 0 else K)
+    ldc = ldc or (N if lc == 0 else M)
+    cdt = ab if cdt is None else cdt
+    bias = BASE if epi & 1 else None
+    st, p = dg.gemm_plan_query(ab, batch, M, N, K, a, lda, la, sa, b, ldb, lb, sb, c, ldc, lc, sc,
+                               cdt, alpha, beta, bias, epi, split_k, ws)
+    assert st == Status.OK, Status(st)
+    return p.as_dict()
+
+
+def headline(**kw):
+    # bf16 8192^3, A row-major, B column-major, bias + GELU(tanh), bf16 out, no workspace
+    return plan(8192, 8192, 8192, lb=1, epi=3, **kw)
+
+
+def test_headline_plan():
+    p = headline()
+    assert p["kernel"] == 1 and p["cta_pair"] == 2 and p["block_n"] == 256
+    assert p["block_k"] == 128 and p["stages"] == 3          # two K blocks per load
+    assert p["grid"] == 152 and p["group_m"] == 8 and p["launches"] == 1
+    assert p["fast_epilogue"] == 1 and p["stream_k"] == 0 and p["workspace_bytes"] == 0
+    assert p["swap_ab"] == 0 and p["pack_a"] == 0 and p["pack_b"] == 0
+
+
+def test_one_k_block_per_load_when_asked_or_when_an_operand_is_mn_major(options):
+    assert plan(8192, 8192, 8192, epi=3)["block_k"] == 64          # row-major B
+    assert plan(8192, 8192, 8192, la=1, lb=1, epi=3)["block_k"] == 64  # column-major A
+    options(DOUBLE_K=1)
+    p = headline()
+    assert p["block_k"] == 64 and p["stages"] == 6
+
+
+def test_headline_options_change_the_plan(options):
+    options(CTA_PAIR=1, GROUP_M=4)
+    p = headline()
+    assert p["cta_pair"] == 0 and p["group_m"] == 4 and p["block_k"] == 64
+
+
+def test_split_k_row_runs_the_spread_form(options):
+    p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
+    assert p["stream_k"] == 3 and p["split_k"] == 1 and p["launches"] == 1
+    assert p["grid"] == 152 and p["block_n"] == 128 and p["cta_pair"] == 0
+    options(SPLIT_REDUCE=1)
+    p2 = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
+    assert p2["stream_k"] == 0 and p2["split_k"] > 4 and p2["launches"] == 2
+
+
+def test_split_k_without_workspace_runs_whole_tiles():
+    p = plan(256, 256, 65536, cdt=2)
+    assert p["split_k"] == 1 and p["stream_k"] == 0 and p["workspace_bytes"] == 0
+
+
+def test_skinny_row_swaps_and_splits_in_one_kernel():
+    p = plan(16, 8192, 8192, cdt=2, ws=UNLIMITED)
+    assert p["swap_ab"] == 1 and p["block_n"] == 16
+    assert p["stream_k"] == 2 and p["split_k"] == 1 and p["grid"] == 128 and p["launches"] == 1
+
+
+def test_batched_beta_rows_read_c_by_tma_loads():
+    s = 1024
+    for sb in (s * s, 0):
+        p = plan(s, s, s, batch=64, alpha=0.5, beta=1.0, sa=s * s, sb=sb, sc=s * s)
+        assert p["fast_epilogue"] == 2 and p["cta_pair"] == 2 and p["block_k"] == 64
+
+
+def test_ragged_row_copies_b_and_stores_with_st_global():
+    p = plan(4097, 3001, 1000, cdt=2, ws=UNLIMITED)
+    assert p["pack_b"] == 1 and p["pack_a"] == 0 and p["launches"] == 2
+    assert p["fast_epilogue"] == 0 and p["workspace_bytes"] > 0
+    # B's rows of 3001 bf16 are not 16-byte aligned: TMA cannot read it in place
+    st, _ = dg.gemm_plan_query(0, 1, 4097, 3001, 1000, BASE, 1000, 0, 0, BASE, 3001, 0, 0,
+                               BASE, 3001, 0, 0, 2, 1.0, 0.0, None, 0, 0, 0)
+    assert st == Status.ERR_WORKSPACE
+
+
+def test_flat_row_keeps_single_cta_tiles():
+    p = plan(4096, 4096, 16)
+    assert p["cta_pair"] == 0 and p["block_n"] == 256 and p["fast_epilogue"] == 1
+
+
+def test_stream_k_needs_a_workspace_and_then_loads_one_k_block():
+    p = plan(2560, 2560, 16384, lb=1, ws=UNLIMITED)
+    assert p["stream_k"] == 2 and p["block_k"] == 64
+    p0 = plan(2560, 2560, 16384, lb=1)
+    assert p0["stream_k"] == 0 and p0["block_k"] == 128
+
+
+def test_sgemm_and_epilogue_only_plans():
+    assert plan(4096, 4096, 4096, ab=2, cdt=2, alpha=1.5, beta=0.5)["kernel"] == 2
+    assert plan(70, 90, 0, cdt=2, beta=0.5)["kernel"] == 3
+    assert plan(70, 90, 64, cdt=2, alpha=0.0, beta=0.5)["kernel"] == 3
+
+
+@pytest.mark.parametrize("shape", [(16, 8192, 8192), (256, 256, 65536), (128, 256, 8192),
+                                   (2560, 2560, 16384), (4097, 3001, 1000)])
+def test_exact_reported_workspace_gives_the_same_plan(shape):
+    M, N, K = shape
+    big = plan(M, N, K, cdt=2, ws=UNLIMITED)
+    exact = plan(M, N, K, cdt=2, ws=big["workspace_bytes"])
+    assert exact == big
+
+
+@pytest.mark.parametrize("shape", [(16, 8192, 8192), (256, 256, 65536), (2560, 2560, 16384),
+                                   (4097, 3001, 1000), (333, 712, 300)])
+@pytest.mark.parametrize("layouts", [(0, 0, 0), (1, 1, 1), (0, 1, 0)])
+def test_workspace_size_covers_every_plan(shape, layouts):
+    M, N, K = shape
+    la, lb, lc = layouts
+    need = plan(M, N, K, la=la, lb=lb, lc=lc, cdt=2, ws=UNLIMITED)["workspace_bytes"]
+    assert dg.gemm_workspace_size(0, 1, M, N, K, 0) >= need
+
+
+def test_simulated_device_changes_with_the_sm_count(options):
+    options(TEST_SIM_SMS=64)
+    p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
+    assert p["grid"] <= 64 and p["stream_k"] == 3
