@@ -74,3 +74,33 @@ def test_bf16_rounding_matches_ml_dtypes():
 def test_seed_convention():
     assert datagen.seed_for(3, datagen.ROLE_A) == 3001
     assert datagen.seed_for(3, datagen.ROLE_BIAS) == 3004
+
+
+def test_operand_streams_match_their_recorded_digests():
+    """The first 4096 stored values of every operand stream the bench and the
+    tests draw are unchanged (tests/golden/datagen_digests.txt)."""
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "make_datagen_digests", os.path.join(GOLDEN, "make_datagen_digests.py"))
+    mk = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mk)
+    import hashlib
+
+    n_u = n_n = 0
+    with open(os.path.join(GOLDEN, "datagen_digests.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kind, seed, payload = line.rstrip("\n").split("|")[:3]
+            if kind == "U":
+                recipe, digest = payload, line.split("|")[3]
+                got = hashlib.sha256(mk.uniform_bits(int(seed), recipe)).hexdigest()
+                assert got == digest, line
+                n_u += 1
+            else:
+                want = np.array([float(v) for v in payload.split()])
+                got = datagen.normal(int(seed), (len(want),))
+                np.testing.assert_allclose(got, want, rtol=1e-13, atol=0)
+                n_n += 1
+    assert n_u == len(mk.UNIFORM_STREAMS) and n_n == len(mk.NORMAL_STREAMS)
