@@ -24,6 +24,9 @@ __all__ = [
 def __getattr__(name):
     # the tensor-level API imports torch; load it on first use only
     if name in ("gemm", "plan", "api"):
-        from . import api
+        # import_module, not "from . import api": the latter looks the name up
+        # on this package first, which would land here again
+        import importlib
+        api = importlib.import_module(".api", __name__)
         return api if name == "api" else getattr(api, name)
     raise AttributeError(name)

@@ -11,8 +11,8 @@ from . import _abi
 from ._abi import DType, Epi, GemmError, Layout, Status
 
 _DT = {torch.bfloat16: DType.BF16, torch.float16: DType.F16, torch.float32: DType.F32}
-_EPI = {"none": Epi.NONE, "bias": Epi.BIAS, "gelu_tanh": Epi.GELU_TANH,
-        "bias_gelu_tanh": Epi.BIAS_GELU_TANH}
+# "none", "bias", "gelu_tanh", "bias_gelu_tanh", ..., "row_bias_gelu_erf"
+_EPI = {e.name.lower(): e for e in Epi}
 
 
 def matrix_desc(t: torch.Tensor):
@@ -28,11 +28,17 @@ def matrix_desc(t: torch.Tensor):
         raise ValueError("expected a 2-D or 3-D tensor")
     rows, cols = t3.shape[1], t3.shape[2]
     s_r, s_c = t3.stride(1), t3.stride(2)
-    if s_c == 1 or cols == 1 and s_r != 1:
-        return t.data_ptr(), max(s_r, cols, 1), Layout.ROW_MAJOR, batch, bstride
-    if s_r == 1:
-        return t.data_ptr(), max(s_c, rows, 1), Layout.COL_MAJOR, batch, bstride
-    raise ValueError("the innermost stride must be 1 (row- or column-major matrix)")
+    # a dimension of extent 1 may carry any stride; otherwise the rows (or the
+    # columns) must not overlap, as an expanded dimension of stride 0 would
+    if (s_c == 1 or cols == 1) and (rows == 1 or s_r >= cols):
+        return t.data_ptr(), max(s_r if rows > 1 else cols, cols, 1), Layout.ROW_MAJOR, \
+            batch, bstride
+    if (s_r == 1 or rows == 1) and (cols == 1 or s_c >= rows):
+        return t.data_ptr(), max(s_c if cols > 1 else rows, rows, 1), Layout.COL_MAJOR, \
+            batch, bstride
+    raise ValueError("expected a row- or column-major matrix with unit inner stride and "
+                     f"non-overlapping lines (shape {tuple(t.shape)}, strides {tuple(t.stride())});"
+                     " use .contiguous() or the gemm_strided entry point")
 
 
 def check(status: int) -> None:
@@ -41,8 +47,10 @@ def check(status: int) -> None:
 
 
 def plan(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, alpha=1.0, beta=0.0, bias=None,
-         epilogue="none", split_k=0, workspace_bytes=None):
+         epilogue=None, split_k=0, workspace_bytes=None):
     """The kernel plan gemm() would use (a dict), without launching anything."""
+    if epilogue is None:
+        epilogue = "bias" if bias is not None else "none"
     args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
     ws = (1 << 62) if workspace_bytes is None else int(workspace_bytes)
     st, p = _abi.gemm_plan_query(*args, ws)
@@ -61,14 +69,27 @@ def _args(A, B, C, alpha, beta, bias, epilogue, split_k):
     N = B.shape[-1]
     if B.shape[-2] != K or C.shape[-2] != M or C.shape[-1] != N:
         raise ValueError(f"shape mismatch: A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    if ba not in (1, batch) or bb not in (1, batch):
+        raise ValueError(f"batch sizes {ba} (A) and {bb} (B) do not broadcast to {batch}")
     if bc != batch:
         raise ValueError("C must carry the full batch")
-    bias_ptr = 0 if bias is None else bias.data_ptr()
-    if bias is not None and (bias.dtype != torch.float32 or bias.numel() != N):
-        raise ValueError("bias must be an fp32 vector of length N")
+    epi = epilogue if isinstance(epilogue, Epi) else _EPI.get(str(epilogue).lower())
+    if epi is None:
+        raise ValueError(f"unknown epilogue {epilogue!r}; one of {sorted(_EPI)}")
+    has_bias = bool(epi & Epi.BIAS)
+    if has_bias != (bias is not None):
+        raise ValueError(f"epilogue {epi.name.lower()} " +
+                         ("needs a bias" if has_bias else "takes no bias"))
+    bias_ptr = 0
+    if bias is not None:
+        n_bias = M if epi & 8 else N
+        if bias.dtype != torch.float32 or bias.numel() != n_bias or \
+                (bias.numel() > 1 and bias.stride(-1) != 1):
+            raise ValueError(f"bias must be a contiguous fp32 vector of length {n_bias}")
+        bias_ptr = bias.data_ptr()
     return [int(_DT[A.dtype]), batch, M, N, K, pa, lda, int(la), sa, pb, ldb, int(lb), sb,
             pc, ldc, int(lc), sc, int(_DT[C.dtype]), float(alpha), float(beta), bias_ptr,
-            int(_EPI[epilogue]), int(split_k)]
+            int(epi), int(split_k)]
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alpha=1.0,
@@ -78,8 +99,9 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alp
 
     A: [M,K] or [batch,M,K]; B: [K,N] or [batch,K,N] (a batch stride of 0,
     e.g. from ``expand``, broadcasts); C: output (allocated when None, in
-    ``out_dtype`` or A's dtype).  ``epilogue`` defaults to "bias" when a bias
-    is given.  A workspace is allocated with torch when the plan needs one
+    ``out_dtype`` or A's dtype).  ``epilogue`` is a ``gemm_epilogue_t`` name
+    in lower case ("bias_gelu_tanh", "row_bias_relu", ...) or an ``Epi``; it
+    defaults to "bias" when a bias is given.  A workspace is allocated with torch when the plan needs one
     and none is given.
     """
     if epilogue is None:

@@ -1,0 +1,130 @@
+"""The tensor-level binding (``api.plan`` / ``api.gemm``'s argument reading)
+without a GPU: matrix descriptors read off torch tensors, argument checks, and
+plans for CPU tensors on the simulated 152-SM device (planning only reads the
+pointers' alignment)."""
+import pytest
+import torch
+
+import dense_gemm_bf16_gb300 as dg
+from dense_gemm_bf16_gb300 import Epi, Layout, Option, Status
+from dense_gemm_bf16_gb300 import api
+
+
+@pytest.fixture(scope="module", autouse=True)
+def simulated_device():
+    dg.build()
+    dg.lib()
+    assert dg.gemm_set_option(Option.TEST_SIM_SMS, 152) == Status.OK
+    yield
+    dg.gemm_set_option(Option.TEST_SIM_SMS, 0)
+
+
+def test_matrix_desc_layouts():
+    a = torch.empty(300, 200, dtype=torch.bfloat16)
+    assert api.matrix_desc(a)[1:] == (200, Layout.ROW_MAJOR, 1, 0)
+    assert api.matrix_desc(a.t())[1:] == (200, Layout.COL_MAJOR, 1, 0)
+    padded = torch.empty(300, 256, dtype=torch.bfloat16)[:, :200]
+    assert api.matrix_desc(padded)[1:] == (256, Layout.ROW_MAJOR, 1, 0)
+    assert api.matrix_desc(padded.t())[1:] == (256, Layout.COL_MAJOR, 1, 0)
+    b3 = torch.empty(4, 300, 200, dtype=torch.float16)
+    assert api.matrix_desc(b3)[1:] == (200, Layout.ROW_MAJOR, 4, 60000)
+    assert api.matrix_desc(b3.transpose(1, 2))[1:] == (200, Layout.COL_MAJOR, 4, 60000)
+    # a broadcast batch (stride 0) and a batch of one both give batch stride 0
+    assert api.matrix_desc(a.expand(4, 300, 200))[3:] == (4, 0)
+    assert api.matrix_desc(a.unsqueeze(0))[3:] == (1, 0)
+
+
+def test_matrix_desc_vectors_take_any_stride_on_their_unit_dimension():
+    col = torch.empty(300, 8, dtype=torch.bfloat16)[:, 3:4]       # [300, 1], strides (8, 1)
+    assert api.matrix_desc(col)[1:3] == (8, Layout.ROW_MAJOR)
+    row = torch.empty(8, 300, dtype=torch.bfloat16)[3:4, :]       # [1, 300], strides (300, 1)
+    assert api.matrix_desc(row)[1:3] == (300, Layout.ROW_MAJOR)
+    row_t = torch.empty(300, 8, dtype=torch.bfloat16).t()[3:4]    # [1, 300], strides (1, 8)
+    assert api.matrix_desc(row_t)[1:3] == (8, Layout.COL_MAJOR)    # column c at c * 8
+
+
+@pytest.mark.parametrize("make", [
+    lambda: torch.empty(1, 200, dtype=torch.bfloat16).expand(300, 200),   # rows of stride 0
+    lambda: torch.empty(300, 1, dtype=torch.bfloat16).expand(300, 200).t(),
+    lambda: torch.empty(300, 400, dtype=torch.bfloat16)[:, ::2],          # inner stride 2
+    lambda: torch.empty(300, dtype=torch.bfloat16),                       # not a matrix
+    lambda: torch.empty(2, 2, 30, 20, dtype=torch.bfloat16),
+])
+def test_matrix_desc_rejects_what_the_abi_cannot_address(make):
+    with pytest.raises(ValueError):
+        api.matrix_desc(make())
+
+
+def bf(*shape):
+    return torch.empty(*shape, dtype=torch.bfloat16)
+
+
+def test_plan_of_the_headline_workload_through_tensors():
+    M = N = K = 8192
+    A, B = bf(M, K), bf(N, K).t()         # B column-major
+    C, bias = bf(M, N), torch.empty(N, dtype=torch.float32)
+    p = api.plan(A, B, C, bias=bias, epilogue="bias_gelu_tanh", workspace_bytes=0)
+    assert p["kernel"] == 1 and p["cta_pair"] == 2 and p["block_n"] == 256
+    assert p["block_k"] == 128 and p["grid"] == 152 and p["fast_epilogue"] == 1
+    assert api.plan(A, B, C, bias=bias, epilogue=Epi.BIAS_GELU_TANH, workspace_bytes=0) == p
+
+
+def test_plan_defaults_to_a_bias_epilogue_when_given_a_bias():
+    A, B, C = bf(256, 512), bf(512, 384), bf(256, 384)
+    bias = torch.empty(384, dtype=torch.float32)
+    assert api.plan(A, B, C, bias=bias) == api.plan(A, B, C, bias=bias, epilogue="bias")
+
+
+def test_every_epilogue_name_is_accepted_with_the_right_bias():
+    M, N, K = 256, 384, 512
+    A, B, C = bf(M, K), bf(K, N), bf(M, N)
+    for e in Epi:
+        bias = None
+        if e & Epi.BIAS:
+            bias = torch.empty(M if e & 8 else N, dtype=torch.float32)
+        p = api.plan(A, B, C, bias=bias, epilogue=e.name.lower())
+        assert p["kernel"] == 1
+
+
+def test_argument_errors():
+    M, N, K = 256, 384, 512
+    A, B, C = bf(M, K), bf(K, N), bf(M, N)
+    col_bias = torch.empty(N, dtype=torch.float32)
+    with pytest.raises(ValueError, match="length 256"):
+        api.plan(A, B, C, bias=col_bias, epilogue="row_bias")
+    with pytest.raises(ValueError, match="takes no bias"):
+        api.plan(A, B, C, bias=col_bias, epilogue="relu")
+    with pytest.raises(ValueError, match="needs a bias"):
+        api.plan(A, B, C, epilogue="bias_relu")
+    with pytest.raises(ValueError, match="unknown epilogue"):
+        api.plan(A, B, C, epilogue="swish")
+    with pytest.raises(ValueError, match="fp32 vector"):
+        api.plan(A, B, C, bias=torch.empty(N, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="fp32 vector"):
+        api.plan(A, B, C, bias=torch.empty(2 * N, dtype=torch.float32)[::2])
+    with pytest.raises(TypeError):
+        api.plan(A, B.half(), C)
+    with pytest.raises(ValueError, match="shape mismatch"):
+        api.plan(A, bf(K + 1, N), C)
+    with pytest.raises(ValueError, match="do not broadcast"):
+        api.plan(bf(3, M, K), bf(4, K, N), bf(4, M, N))
+    with pytest.raises(ValueError, match="full batch"):
+        api.plan(bf(4, M, K), B, C)
+
+
+def test_batched_plans_through_tensors():
+    s = 1024
+    A, B, C = bf(64, s, s), bf(64, s, s), bf(64, s, s)
+    p = api.plan(A, B, C, alpha=0.5, beta=1.0)
+    assert p["fast_epilogue"] == 2 and p["cta_pair"] == 2
+    pb = api.plan(A, bf(s, s).expand(64, s, s), C, alpha=0.5, beta=1.0)
+    assert pb["fast_epilogue"] == 2
+
+
+def test_workspace_defaults_to_what_the_plan_needs():
+    A, B = bf(256, 65536), bf(65536, 256)
+    C = torch.empty(256, 256, dtype=torch.float32)
+    p = api.plan(A, B, C)
+    assert p["stream_k"] == 3 and p["workspace_bytes"] > 0
+    assert api.plan(A, B, C, workspace_bytes=p["workspace_bytes"]) == p
+    assert api.plan(A, B, C, workspace_bytes=0)["stream_k"] == 0
