@@ -23,16 +23,16 @@ def simulated_device():
 
 @pytest.fixture
 def options():
-    """Sets options for one test and restores the defaults afterwards."""
-    touched = []
+    """Sets options for one test and restores their previous values afterwards."""
+    saved = []
 
     def set_(**kw):
         for k, v in kw.items():
+            saved.append((Option[k], dg.gemm_get_option(Option[k])))
             assert dg.gemm_set_option(Option[k], v) == Status.OK
-            touched.append(k)
     yield set_
-    for k in touched:
-        dg.gemm_set_option(Option[k], 0 if k != "GROUP_M" else 8)
+    for opt, v in reversed(saved):
+        assert dg.gemm_set_option(opt, v) == Status.OK
 
 
 def plan(M, N, K, *, ab=0, batch=1, la=0, lb=0, lc=0, lda=None, ldb=None, ldc=None, cdt=None,
@@ -154,3 +154,14 @@ def test_simulated_device_changes_with_the_sm_count(options):
     options(TEST_SIM_SMS=64)
     p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
     assert p["grid"] <= 64 and p["stream_k"] == 3
+
+
+@pytest.mark.parametrize("ab,cdt", [(0, 0), (1, 1), (1, 2)])
+@pytest.mark.parametrize("shape", [(4, 16, 4096, 4096), (64, 1024, 1024, 1024),
+                                   (3, 4097, 3001, 1000), (8, 256, 256, 65536)])
+def test_workspace_size_covers_batched_plans(ab, cdt, shape):
+    bt, M, N, K = shape
+    for sb in (K * N, 0):
+        need = plan(M, N, K, ab=ab, cdt=cdt, batch=bt, sa=M * K, sb=sb, sc=M * N,
+                    ws=UNLIMITED)["workspace_bytes"]
+        assert dg.gemm_workspace_size(ab, bt, M, N, K, 0) >= need
