@@ -175,11 +175,11 @@ struct Operand {
     bool mn;          // stored MN-contiguous
     int64_t mn_ext;   // extent along M (A role) or N (B role)
     int64_t k_ext;
-    bool pack;
-    int64_t pack_ld;
-    int64_t pack_batch;
-    size_t pack_off;
-    size_t pack_bytes;
+    bool pack = false;
+    int64_t pack_ld = 0;
+    int64_t pack_batch = 0;
+    size_t pack_off = 0;
+    size_t pack_bytes = 0;
     int64_t inner() const { return mn ? mn_ext : k_ext; }
     int64_t outer() const { return mn ? k_ext : mn_ext; }
 };
