@@ -165,3 +165,103 @@ def test_workspace_size_covers_batched_plans(ab, cdt, shape):
         need = plan(M, N, K, ab=ab, cdt=cdt, batch=bt, sa=M * K, sb=sb, sc=M * N,
                     ws=UNLIMITED)["workspace_bytes"]
         assert dg.gemm_workspace_size(ab, bt, M, N, K, 0) >= need
+
+
+# kernel instantiations compiled into the library: (tile width, CTA mode) per epilogue form,
+# and the two-K-blocks-per-load form (pairs, TMA-store-only epilogue)
+INSTANTIATED = {
+    0: {(16, 0), (32, 0), (64, 0), (128, 0), (256, 0), (128, 1), (256, 1), (128, 2), (256, 2),
+        (512, 2)},
+    1: {(64, 0), (128, 0), (256, 0), (128, 1), (256, 1), (128, 2), (256, 2), (512, 2)},
+    2: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2)},
+}
+TWO_K_BLOCKS = {(128, 2), (256, 2)}
+
+
+def _random_calls(n, seed=20261202):
+    import random
+    rng = random.Random(seed)
+    dims_m = [1, 15, 16, 64, 65, 128, 200, 257, 1000, 2560, 4097, 8192]
+    dims_n = [1, 8, 16, 100, 128, 256, 384, 1000, 3001, 8192]
+    dims_k = [0, 1, 16, 64, 100, 256, 768, 1000, 4096, 8192, 65536]
+    dts = [(0, 0), (0, 2), (1, 1), (1, 2), (2, 2)]
+    for _ in range(n):
+        M, N, K = rng.choice(dims_m), rng.choice(dims_n), rng.choice(dims_k)
+        ab, cdt = rng.choice(dts)
+        la, lb, lc = rng.randrange(2), rng.randrange(2), rng.randrange(2)
+        batch = rng.choice([1, 1, 1, 3, 64])
+        sb_bcast = rng.random() < 0.3
+        beta = rng.choice([0.0, 0.0, 1.0])
+        alpha = rng.choice([1.0, 1.0, 0.5, 0.0])
+        epi = rng.choice([0, 1, 3, 5, 7, 9, 11])
+        ws = rng.choice([0, UNLIMITED])
+        yield dict(M=M, N=N, K=K, ab=ab, cdt=cdt, la=la, lb=lb, lc=lc, batch=batch,
+                   sa=M * K, sb=0 if sb_bcast else K * N, sc=M * N, alpha=alpha, beta=beta,
+                   epi=epi, ws=ws)
+
+
+OPTION_SETS = [
+    {}, {"CTA_PAIR": 1}, {"CTA_PAIR": 2}, {"CTA_PAIR": 3}, {"WIDE_TILE": 2},
+    {"CTA_PAIR": 3, "WIDE_TILE": 2}, {"SWAP_AB": 1}, {"SWAP_AB": 2}, {"STREAM_K": 1},
+    {"STREAM_K": 2}, {"STREAM_K": 3}, {"FAST_EPILOGUE": 1}, {"SPLIT_REDUCE": 1},
+    {"SPLIT_REDUCE": 2}, {"BLOCK_N": 16}, {"BLOCK_N": 64}, {"BLOCK_N": 128}, {"DOUBLE_K": 1},
+    {"MAX_CTAS": 37}, {"GROUP_M": 1},
+]
+
+
+def _opts_id(o):
+    return ",".join(f"{k}={v}" for k, v in o.items()) or "defaults"
+
+
+@pytest.mark.parametrize("opts", OPTION_SETS, ids=_opts_id)
+def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, opts):
+    options(**opts)
+    n_ctas = opts.get("MAX_CTAS", 152)
+    checked = 0
+    for kw in _random_calls(1500):
+        ws = kw.pop("ws")
+        M, N, K = kw.pop("M"), kw.pop("N"), kw.pop("K")
+        lda = K if kw["la"] == 0 else M
+        ldb = N if kw["lb"] == 0 else K
+        ldc = N if kw["lc"] == 0 else M
+        bias = BASE if kw["epi"] & 1 else None
+        st, p = dg.gemm_plan_query(kw["ab"], kw["batch"], M, N, K, BASE, max(lda, 1), kw["la"],
+                                   kw["sa"], BASE, max(ldb, 1), kw["lb"], kw["sb"], BASE,
+                                   max(ldc, 1), kw["lc"], kw["sc"], kw["cdt"], kw["alpha"],
+                                   kw["beta"], bias, kw["epi"], 0, ws)
+        ctx = (M, N, K, kw, ws)
+        if st == Status.ERR_WORKSPACE:
+            assert ws == 0, ctx      # only an operand copy or split-K needs one
+            continue
+        assert st == Status.OK, (Status(st), ctx)
+        p = p.as_dict()
+        assert 0 <= p["workspace_bytes"] <= ws, ctx
+        if kw["ab"] == 2:
+            assert p["kernel"] in (2, 3), ctx
+        if K == 0 or kw["alpha"] == 0.0:
+            assert p["kernel"] == 3, ctx
+        if p["kernel"] != 1:
+            continue
+        checked += 1
+        bn, mode, form = p["block_n"], p["cta_pair"], p["fast_epilogue"]
+        assert (bn, mode) in INSTANTIATED[form], (p, ctx)
+        assert 1 <= p["grid"] <= n_ctas and p["stages"] >= 2, (p, ctx)
+        if mode:
+            assert p["grid"] % 2 == 0, (p, ctx)
+        if p["block_k"] == 128:
+            assert (bn, mode) in TWO_K_BLOCKS and form == 1, (p, ctx)
+            assert kw["batch"] == 1 and K % 64 == 0 and p["split_k"] == 1, (p, ctx)
+            assert p["stream_k"] == 0, (p, ctx)
+        else:
+            assert p["block_k"] == 64, (p, ctx)
+        if form == 2:
+            assert kw["beta"] != 0.0 and kw["cdt"] in (0, 1), (p, ctx)
+        if p["stream_k"] == 3:       # the spread reduction runs on single CTAs only
+            assert mode == 0 and p["workspace_bytes"] > 0, (p, ctx)
+            assert p["launches"] == 1 + p["pack_a"] + p["pack_b"], (p, ctx)   # no reduction pass
+        if p["stream_k"]:
+            assert p["split_k"] == 1 and p["workspace_bytes"] > 0, (p, ctx)
+        if p["split_k"] > 1:
+            assert p["launches"] >= 2 and p["workspace_bytes"] > 0, (p, ctx)
+        assert p["launches"] >= 1 + p["pack_a"] + p["pack_b"], (p, ctx)
+    assert checked > 500
