@@ -458,8 +458,10 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
                static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
         pl.ws_need = off;
         pl.grid = static_cast<int>(S * r);
-    } else if (want_sk != 1 && pl.splits == 1 && P > 0 && pl.units > P && pl.units % P != 0 &&
-               pl.kblocks >= 2 && pl.bn <= 256) {
+    } else if (want_sk != 1 && c.split_k != 1 && pl.splits == 1 && P > 0 && pl.units > P &&
+               pl.units % P != 0 && pl.kblocks >= 2 && pl.bn <= 256) {
+        // (split_k == 1 asks for no split of K at all: every tile is summed over
+        // the whole K in one accumulator, so no stream-K pieces either)
         const int64_t W = pl.units / P, r = pl.units % P;
         // split form: each of the r last units becomes S pieces of at least
         // kMinPiece K blocks, one per cluster, all starting together so that

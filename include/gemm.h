@@ -107,7 +107,9 @@ typedef enum {
  *   bias         fp32 device vector of length N (length M for a row bias), 4-byte
  *                aligned; required iff epi uses a bias, else ignored.
  *   epi          epilogue (gemm_epilogue_t).
- *   split_k      0 = choose automatically, 1 = no split, s > 1 = split K into s
+ *   split_k      0 = choose automatically (split-K or stream-K pieces when they
+ *                pay), 1 = no split (every tile summed over the whole K in one
+ *                accumulator, no stream-K pieces either), s > 1 = split K into s
  *                slices whose fp32 partial tiles are summed in a fixed order by a
  *                second kernel ("Skill: Write a Triton GEMM Kernel", Kernel
  *                design rules, split-K; "2 . La GEMM, de zero a cuBLAS", section 2.10).
@@ -297,6 +299,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         partial-tile traffic and the workspace holds the partials;
  *                         1: never; 2: force the contiguous form (plan stream_k 1);
  *                         3: force the split form (plan stream_k 2) when S >= 2.
+ *                         A call with split_k == 1 never takes stream-K pieces.
  *   GEMM_OPT_FAST_EPILOGUE 0 (default): when no beta * C is read (beta == 0, or split-K
  *                         partials) and C takes TMA stores, use the epilogue built for
  *                         that case alone (64-column steps, fewer registers); when a

@@ -195,9 +195,10 @@ def _random_calls(n, seed=20261202):
         alpha = rng.choice([1.0, 1.0, 0.5, 0.0])
         epi = rng.choice([0, 1, 3, 5, 7, 9, 11])
         ws = rng.choice([0, UNLIMITED])
+        split_k = rng.choice([0, 0, 0, 1, 2, 7])
         yield dict(M=M, N=N, K=K, ab=ab, cdt=cdt, la=la, lb=lb, lc=lc, batch=batch,
                    sa=M * K, sb=0 if sb_bcast else K * N, sc=M * N, alpha=alpha, beta=beta,
-                   epi=epi, ws=ws)
+                   epi=epi, ws=ws, split_k=split_k)
 
 
 OPTION_SETS = [
@@ -228,7 +229,7 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
         st, p = dg.gemm_plan_query(kw["ab"], kw["batch"], M, N, K, BASE, max(lda, 1), kw["la"],
                                    kw["sa"], BASE, max(ldb, 1), kw["lb"], kw["sb"], BASE,
                                    max(ldc, 1), kw["lc"], kw["sc"], kw["cdt"], kw["alpha"],
-                                   kw["beta"], bias, kw["epi"], 0, ws)
+                                   kw["beta"], bias, kw["epi"], kw["split_k"], ws)
         ctx = (M, N, K, kw, ws)
         if st == Status.ERR_WORKSPACE:
             assert ws == 0, ctx      # only an operand copy or split-K needs one
@@ -236,6 +237,11 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
         assert st == Status.OK, (Status(st), ctx)
         p = p.as_dict()
         assert 0 <= p["workspace_bytes"] <= ws, ctx
+        # gemm_workspace_size bounds the scratch of any call with these sizes
+        assert dg.gemm_workspace_size(kw["ab"], kw["batch"], M, N, K, kw["split_k"]) >= \
+            p["workspace_bytes"], (p, ctx)
+        if kw["split_k"] == 1:
+            assert p["split_k"] == 1 and p["stream_k"] == 0, (p, ctx)
         if kw["ab"] == 2:
             assert p["kernel"] in (2, 3), ctx
         if K == 0 or kw["alpha"] == 0.0:
