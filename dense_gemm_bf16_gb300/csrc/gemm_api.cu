@@ -197,7 +197,7 @@ struct Plan {
     bool spread = false;     // ... with every piece reducing a share of its tile
     int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
     int64_t dp_units = 0, sk_iters = 0;
-    size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0;
+    size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0, sk_flags_bytes = 0;
     int64_t kblocks = 0, tiles = 0, units = 0;
     Operand a{}, b{};
     bool c_row_major_c = true;
@@ -454,6 +454,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.sk_off = off;
         pl.sk_bytes = slots;
         pl.sk_flags_off = off + static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256));
+        pl.sk_flags_bytes = flags;
         off += static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256)) +
                static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
         pl.ws_need = off;
@@ -511,6 +512,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
                 pl.sk_off = off;
                 pl.sk_bytes = slots;
                 pl.sk_flags_off = off + static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256));
+                pl.sk_flags_bytes = flags;
                 off += need;
                 pl.ws_need = off;
             }
@@ -769,7 +771,21 @@ gemm_status_t run(const Call& c) {
         p.sk_spread = pl.spread ? 1 : 0;
         p.sk_partials = reinterpret_cast<float*>(ws + pl.sk_off);
         p.sk_flags = reinterpret_cast<unsigned long long*>(ws + pl.sk_flags_off);
-        p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
+        do {
+            p.sk_epoch = g_sk_epoch.fetch_add(1) + 1;
+        } while (p.sk_epoch == 0);  // cleared flags (0) must never read as published
+        // A launch captured into a CUDA graph is replayed with this same epoch,
+        // so the flags an earlier replay published would already read as
+        // published to the next one.  When capturing, clear them in the graph,
+        // right before the kernel, so that every replay starts from zero.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(c.stream, &cap) != cudaSuccess) {
+            cudaGetLastError();
+            cap = cudaStreamCaptureStatusNone;
+        }
+        if (cap == cudaStreamCaptureStatusActive &&
+            cudaMemsetAsync(p.sk_flags, 0, pl.sk_flags_bytes, c.stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
     }
     if (tc_launch(pl.bn, pl.mode, epi_form, pl.ks, p, pl.grid, c.stream) != cudaSuccess)
         return GEMM_ERR_CUDA;

@@ -42,6 +42,14 @@
  *     caller's workspace (see gemm_workspace_size).
  *   - Calls are thread-safe.  The first call on a device queries device
  *     attributes and may set kernel attributes (no allocation).
+ *   - A call may be captured into a CUDA graph once the device has seen one
+ *     uncaptured call (which does the one-time setup above).  The plan,
+ *     pointers and scalars are fixed at capture.  Plans that hand fp32
+ *     partials between the pieces of a tile (stream-K, the one-kernel
+ *     split-K) synchronise through flags in the workspace.  Those flags hold
+ *     a per-launch value that a replay repeats, so a captured call also
+ *     records a clearing of the flags ahead of its kernel.  Replays of one
+ *     graph, like calls that share one workspace, must not overlap.
  */
 #ifndef DGEMM_GB300_GEMM_H
 #define DGEMM_GB300_GEMM_H
