@@ -12,6 +12,7 @@
 #include "gemm.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "span_check.h"
 #include "tile_order.h"
 
 namespace dg {
@@ -221,6 +222,9 @@ gemm_status_t validate(const Call& c) {
     const int64_t c_inner = c.lc == GEMM_ROW_MAJOR ? c.N : c.M;
     const int64_t c_outer = c.lc == GEMM_ROW_MAJOR ? c.M : c.N;
     if (c.ldc < c_inner) return GEMM_ERR_INVALID_ARG;
+    if (!strided_span_ok(c_outer, c_inner, c.ldc, 1, c.batch, c.batch > 1 ? c.sc : 0) ||
+        !count_ok(c.batch, c.M, c.N))
+        return GEMM_ERR_INVALID_ARG;
     if (c.batch > 1) {
         // C[b] must not overlap
         if (c.sc < (c_outer - 1) * c.ldc + c_inner) return GEMM_ERR_INVALID_ARG;
@@ -234,6 +238,12 @@ gemm_status_t validate(const Call& c) {
         const int64_t b_inner = c.lb == GEMM_ROW_MAJOR ? c.N : c.K;
         if (c.lda < a_inner || c.ldb < b_inner) return GEMM_ERR_INVALID_ARG;
         if (c.sa < 0 || c.sb < 0) return GEMM_ERR_INVALID_ARG;
+        const int64_t a_outer = c.la == GEMM_ROW_MAJOR ? c.M : c.K;
+        const int64_t b_outer = c.lb == GEMM_ROW_MAJOR ? c.K : c.N;
+        if (!strided_span_ok(a_outer, a_inner, c.lda, 1, c.batch, c.batch > 1 ? c.sa : 0) ||
+            !strided_span_ok(b_outer, b_inner, c.ldb, 1, c.batch, c.batch > 1 ? c.sb : 0) ||
+            !count_ok(c.batch, c.M, c.K) || !count_ok(c.batch, c.K, c.N))
+            return GEMM_ERR_INVALID_ARG;
     }
     return GEMM_OK;
 }
@@ -884,6 +894,9 @@ size_t gemm_workspace_size(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int6
     if (ab_dtype != GEMM_DT_BF16 && ab_dtype != GEMM_DT_F16) return 0;
     if (batch <= 0 || M <= 0 || N <= 0 || K <= 0 || split_k < 0) return 0;
     if (batch > 0x7FFFFFFF || M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return 0;
+    // the counts every call with these sizes must pass (padding rows to 8 included)
+    if (!count_ok(batch, M, N) || !count_ok(batch, M + 8, K + 8) || !count_ok(batch, K + 8, N + 8))
+        return 0;
     DevState sim;
     DevState* d = nullptr;
     if (planning_device(sim, &d) != GEMM_OK) return 0;

@@ -15,6 +15,7 @@
 
 #include "gemm.h"
 #include "internal.h"
+#include "span_check.h"
 
 namespace dg {
 namespace {
@@ -138,6 +139,16 @@ gemm_status_t make_strided_plan(gemm_dtype_t ab, gemm_dtype_t cdt, int64_t batch
     // distinct output elements need distinct addresses along each extent
     if ((M > 1 && c_rs == 0) || (N > 1 && c_cs == 0) || (batch > 1 && sc == 0))
         return GEMM_ERR_INVALID_ARG;
+    const int64_t lim = 0x7FFFFFFF;
+    if (batch > lim || M > lim || N > lim || K > lim) return GEMM_ERR_INVALID_ARG;
+    if (batch > 0 && M > 0 && N > 0) {
+        if (!strided_span_ok(M, N, c_rs, c_cs, batch, sc) || !count_ok(batch, M, N))
+            return GEMM_ERR_INVALID_ARG;
+        if (K > 0 && (!strided_span_ok(M, K, a_rs, a_cs, batch, sa) ||
+                      !strided_span_ok(K, N, b_rs, b_cs, batch, sb) ||
+                      !count_ok(batch, M, K) || !count_ok(batch, K, N)))
+            return GEMM_ERR_INVALID_ARG;
+    }
     const int es_ab = ab == GEMM_DT_F32 ? 4 : 2;
     const int es_c = cdt == GEMM_DT_F32 ? 4 : 2;
     sp.a = plan_matrix(M, K, a_rs, a_cs, sa, batch, es_ab);

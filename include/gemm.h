@@ -35,7 +35,11 @@
  *     alpha == 0 or K == 0 means A and B are not read:
  *     C <- act(beta*C + bias).  M == 0, N == 0 or batch == 0 is a no-op.
  *   - Argument errors are detected before anything is enqueued and are
- *     reported by the return code; nothing aborts, prints or throws.
+ *     reported by the return code; nothing aborts, prints or throws.  Among
+ *     them: an extent above 2^31 - 1, a matrix whose elements (with its
+ *     leading dimension or strides, over the batch) would span more than
+ *     2^48 elements of memory, and a matrix of more than 2^56 elements over
+ *     the batch.
  *   - Any pointer alignment that the element type allows is accepted.  Fast
  *     TMA paths need 16-byte aligned bases and leading dimensions that are a
  *     multiple of 16 bytes; other operands are first copied into the

@@ -73,6 +73,9 @@ def _bf16(M, N, K, **kw):
     dict(M=4, N=4, K=4, A=17),                         # A not 2-byte aligned
     dict(M=4, N=4, K=4, split_k=-2),
     dict(M=1 << 31, N=4, K=4),
+    dict(M=4, N=4, K=4, lda=1 << 60),                  # span beyond 2^48 elements
+    dict(M=4, N=4, K=4, ldb=(1 << 47) + 1),            # 3 * ldb + 4 > 2^48
+    dict(M=4, N=4, K=4, ldc=(1 << 62) + 5),            # (M - 1) * ldc overflows int64
 ])
 def test_invalid_arguments_rejected_without_gpu(lib, kw):
     assert _bf16(**kw) == Status.ERR_INVALID_ARG
@@ -209,3 +212,44 @@ def test_plan_struct_matches_the_header():
         for name in names.split(","):
             fields.append((name.strip(), {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}[ctype]))
     assert [(n, t) for n, t in dg.Plan._fields_] == fields
+
+
+def _batched(batch, M, N, K, sa, sb, sc, lda=None, ldb=None, ldc=None):
+    return dg.gemm_batched(DType.BF16, batch, M, N, K, 16, lda or K, 0, sa, 16, ldb or N, 0, sb,
+                           16, ldc or N, 0, sc, DType.F32, 1.0, 0.0, None, 0, 0, None, 0, None)
+
+
+def test_oversized_spans_and_counts_rejected(lib):
+    ok = Status.ERR_NO_DEVICE   # the same call with sane sizes gets as far as the device query
+    assert _batched(2, 4, 4, 4, 16, 16, 16) == ok
+    assert _batched(2, 4, 4, 4, 16, 16, 1 << 62) == Status.ERR_INVALID_ARG   # C batch stride
+    assert _batched(3, 4, 4, 4, 1 << 62, 16, 16) == Status.ERR_INVALID_ARG   # A batch stride
+    assert _batched(1 << 20, 4, 4, 4, 16, 16, 1 << 28) == ok     # C spans just under 2^48
+    assert _batched(1 << 20, 4, 4, 4, 16, 16, 1 << 29) == Status.ERR_INVALID_ARG  # about 2^49
+    # batches of A overlapping (stride 1) leave the span small but not the count:
+    # 2^30 x 2^14 x 2^14 = 2^58 elements, which no dense copy could hold
+    assert _batched(1 << 30, 1 << 14, 1, 1 << 14, 1, 0, 1 << 14) == Status.ERR_INVALID_ARG
+    # whereas a broadcast B of the same product is fine
+    assert _batched(1 << 10, 1 << 14, 1, 1 << 14, 1 << 28, 0, 1 << 14) == ok
+
+
+def test_strided_oversized_spans_and_counts_rejected(lib):
+    def strided(batch, M, N, K, a, b, c):
+        return dg.gemm_strided(DType.BF16, batch, M, N, K, 16, *a, 16, *b, 16, *c, DType.F32,
+                               1.0, 0.0, None, 0, 0, None, 0, None)
+    ok = Status.ERR_NO_DEVICE
+    assert strided(1, 4, 4, 4, (4, 1, 0), (4, 1, 0), (4, 1, 0)) == ok
+    assert strided(1, 4, 4, 4, (1 << 60, 1, 0), (4, 1, 0), (4, 1, 0)) == Status.ERR_INVALID_ARG
+    assert strided(2, 4, 4, 4, (4, 1, 0), (4, 1, 0), (4, 1, 1 << 62)) == Status.ERR_INVALID_ARG
+    assert strided(1, 1 << 31, 4, 4, (4, 1, 0), (4, 1, 0), (4, 1, 0)) == Status.ERR_INVALID_ARG
+    # an overlapping C (row and column stride 1) of 2^60 elements spans little memory
+    big = (1 << 30)
+    assert strided(1, big, big, 4, (4, 1, 0), (big, 1, 0), (1, 1, 0)) == Status.ERR_INVALID_ARG
+    assert dg.gemm_strided_workspace_size(0, 2, 1, big, big, 4, 4, 1, 0, big, 1, 0, 1, 1, 0,
+                                          0) == 0
+
+
+def test_workspace_size_of_oversized_problems_is_zero(lib):
+    big = (1 << 31) - 1
+    assert dg.gemm_workspace_size(DType.BF16, big, big, big, big, 0) == 0
+    assert dg.gemm_workspace_size(DType.BF16, 1 << 20, 1 << 20, 1 << 20, 8, 0) == 0
