@@ -556,6 +556,10 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.ks = 2;
         pl.stages = tc_stages_ks2(pl.bn);
     }
+    // the tensor-core kernel counts work units and tiles in 32-bit integers
+    if (pl.kernel == 1 && (pl.units > 0x7FFFFFFF / (pl.splits > 0 ? pl.splits : 1) ||
+                           pl.tiles > 0x7FFFFFFF))
+        return GEMM_ERR_UNSUPPORTED;
     if (pl.ws_need > 0 && (c.ws == nullptr || c.ws_bytes < pl.ws_need)) return GEMM_ERR_WORKSPACE;
     if (pl.ws_need > 0 && !aligned(c.ws, 256)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;

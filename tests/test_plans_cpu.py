@@ -271,3 +271,14 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
             assert p["launches"] >= 2 and p["workspace_bytes"] > 0, (p, ctx)
         assert p["launches"] >= 1 + p["pack_a"] + p["pack_b"], (p, ctx)
     assert checked > 500
+
+
+def test_more_work_units_than_32_bits_count_is_unsupported():
+    # 2^30 batch entries of 256 x 16: two tiles each, 2^31 units in all
+    bt = 1 << 30
+    st, _ = dg.gemm_plan_query(0, bt, 256, 16, 16, BASE, 16, 0, 256 * 16, BASE, 16, 0, 0,
+                               BASE, 16, 0, 256 * 16, 2, 1.0, 0.0, None, 0, 0, 0)
+    assert st == Status.ERR_UNSUPPORTED
+    st, p = dg.gemm_plan_query(0, bt // 2, 256, 16, 16, BASE, 16, 0, 256 * 16, BASE, 16, 0, 0,
+                               BASE, 16, 0, 256 * 16, 2, 1.0, 0.0, None, 0, 0, 0)
+    assert st == Status.OK and p.kernel == 1
