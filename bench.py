@@ -20,6 +20,7 @@ Multi-GPU runs (torchrun) run one independent replica per GPU (weak scaling).
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -237,10 +238,12 @@ def e2e_pipelined(hA, hB, hbias, hC, device, steps, warmup, barrier=None):
         torch.cuda.synchronize(device)
         return start.elapsed_time(stop)
 
-    run(warmup)
+    with nvtx("e2e warmup"):
+        run(warmup)
     if barrier:
         barrier()
-    ms = run(steps)
+    with nvtx("e2e timed"):
+        ms = run(steps)
     if barrier:
         barrier()
     return ms / steps
@@ -303,19 +306,38 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- timing
 
+@contextlib.contextmanager
+def nvtx(name):
+    """An NVTX range around a phase (warm-up, timed, e2e, one row), so that a
+    profiler can select it (ncu --nvtx --nvtx-include "timed/")."""
+    import torch
+    try:
+        torch.cuda.nvtx.range_push(name)
+        pushed = True
+    except Exception:
+        pushed = False
+    try:
+        yield
+    finally:
+        if pushed:
+            torch.cuda.nvtx.range_pop()
+
+
 def time_steps(fn, steps, warmup, barrier=None):
     import torch
-    for _ in range(warmup):
-        fn()
+    with nvtx("warmup"):
+        for _ in range(warmup):
+            fn()
     torch.cuda.synchronize()
     if barrier:
         barrier()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        fn()
-    stop.record()
+    with nvtx("timed"):
+        start.record()
+        for _ in range(steps):
+            fn()
+        stop.record()
     torch.cuda.synchronize()
     if barrier:
         barrier()
@@ -708,14 +730,15 @@ def measure_rows(names, device, reps=20):
             fn()
         torch.cuda.synchronize()
         evs = []
-        for _ in range(reps):
-            flush.sum()
-            s_ = torch.cuda.Event(enable_timing=True)
-            e_ = torch.cuda.Event(enable_timing=True)
-            s_.record()
-            fn()
-            e_.record()
-            evs.append((s_, e_))
+        with nvtx(f"row {name}"):
+            for _ in range(reps):
+                flush.sum()
+                s_ = torch.cuda.Event(enable_timing=True)
+                e_ = torch.cuda.Event(enable_timing=True)
+                s_.record()
+                fn()
+                e_.record()
+                evs.append((s_, e_))
         torch.cuda.synchronize()
         ts = [s_.elapsed_time(e_) for s_, e_ in evs]
         med, mn = statistics.median(ts), min(ts)
