@@ -78,17 +78,22 @@ class Replicas:
     independent).  Barriers bracket the timed regions, a time is the maximum
     over ranks, and whole-job throughput counts every rank's work."""
 
-    def __init__(self, backend, device=None):
+    def __init__(self, backend, device=None, timeout_s=900.0):
         rank, world, local = env_rank()
         self.rank, self.world, self.local = rank, world, local
         self.dist = None
         self.device = device
         if world > 1:
+            import datetime
+
             import torch.distributed as dist
+            # a rank that dies makes the others' next barrier or reduction fail
+            # after timeout_s instead of the backend's default half hour
+            timeout = datetime.timedelta(seconds=timeout_s)
             if backend == "nccl":
-                dist.init_process_group(backend, device_id=device)
+                dist.init_process_group(backend, device_id=device, timeout=timeout)
             else:
-                dist.init_process_group(backend)
+                dist.init_process_group(backend, timeout=timeout)
             self.dist = dist
 
     def barrier(self):
