@@ -1,5 +1,6 @@
 """Tensor-level convenience over the C ABI: reads pointers, leading dimensions,
-layouts and batch strides off torch tensors and calls ``gemm_batched``.
+layouts and batch strides off torch tensors and calls ``gemm_batched``, or
+``gemm_strided`` for views that are not row- or column-major matrices.
 PyTorch only provides device memory and the current stream; every step of the
 GEMM runs in the library's CUDA kernels.
 """
@@ -37,8 +38,17 @@ def matrix_desc(t: torch.Tensor):
         return t.data_ptr(), max(s_c if cols > 1 else rows, rows, 1), Layout.COL_MAJOR, \
             batch, bstride
     raise ValueError("expected a row- or column-major matrix with unit inner stride and "
-                     f"non-overlapping lines (shape {tuple(t.shape)}, strides {tuple(t.stride())});"
-                     " use .contiguous() or the gemm_strided entry point")
+                     f"non-overlapping lines (shape {tuple(t.shape)}, strides {tuple(t.stride())})")
+
+
+def strided_desc(t: torch.Tensor):
+    """(ptr, row stride, column stride, batch stride) in elements of a 2-D or
+    3-D tensor, as ``gemm_strided`` takes them (batch stride 0 for one matrix)."""
+    if t.dim() == 2:
+        return t.data_ptr(), t.stride(0), t.stride(1), 0
+    if t.dim() == 3:
+        return t.data_ptr(), t.stride(1), t.stride(2), (t.stride(0) if t.shape[0] > 1 else 0)
+    raise ValueError("expected a 2-D or 3-D tensor")
 
 
 def check(status: int) -> None:
@@ -46,29 +56,21 @@ def check(status: int) -> None:
         raise GemmError(status)
 
 
-def plan(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, alpha=1.0, beta=0.0, bias=None,
-         epilogue=None, split_k=0, workspace_bytes=None):
-    """The kernel plan gemm() would use (a dict), without launching anything."""
-    if epilogue is None:
-        epilogue = "bias" if bias is not None else "none"
-    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
-    ws = (1 << 62) if workspace_bytes is None else int(workspace_bytes)
-    st, p = _abi.gemm_plan_query(*args, ws)
-    check(st)
-    return p.as_dict()
-
-
-def _args(A, B, C, alpha, beta, bias, epilogue, split_k):
+def _common(A, B, C, bias, epilogue):
+    """Checks shared by both routes: (M, N, K, batch, epilogue, bias pointer)."""
     if A.dtype != B.dtype or A.dtype not in _DT:
         raise TypeError("A and B must share one dtype among bfloat16, float16, float32")
-    pa, lda, la, ba, sa = matrix_desc(A)
-    pb, ldb, lb, bb, sb = matrix_desc(B)
-    pc, ldc, lc, bc, sc = matrix_desc(C)
-    batch = max(ba, bb, bc)
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.dim() not in (2, 3):
+            raise ValueError(f"{name} must be a 2-D or 3-D tensor")
+    if C.dtype not in _DT:
+        raise TypeError("C must be bfloat16, float16 or float32")
     M, K = A.shape[-2], A.shape[-1]
     N = B.shape[-1]
     if B.shape[-2] != K or C.shape[-2] != M or C.shape[-1] != N:
         raise ValueError(f"shape mismatch: A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    ba, bb, bc = (t.shape[0] if t.dim() == 3 else 1 for t in (A, B, C))
+    batch = max(ba, bb, bc)
     if ba not in (1, batch) or bb not in (1, batch):
         raise ValueError(f"batch sizes {ba} (A) and {bb} (B) do not broadcast to {batch}")
     if bc != batch:
@@ -87,9 +89,51 @@ def _args(A, B, C, alpha, beta, bias, epilogue, split_k):
                 (bias.numel() > 1 and bias.stride(-1) != 1):
             raise ValueError(f"bias must be a contiguous fp32 vector of length {n_bias}")
         bias_ptr = bias.data_ptr()
+    return M, N, K, batch, epi, bias_ptr
+
+
+def _args(A, B, C, alpha, beta, bias, epilogue, split_k):
+    """Arguments of gemm_batched / gemm_plan_query (without the workspace and
+    stream); raises ValueError for a view that is not row- or column-major."""
+    M, N, K, batch, epi, bias_ptr = _common(A, B, C, bias, epilogue)
+    pa, lda, la, _, sa = matrix_desc(A)
+    pb, ldb, lb, _, sb = matrix_desc(B)
+    pc, ldc, lc, _, sc = matrix_desc(C)
     return [int(_DT[A.dtype]), batch, M, N, K, pa, lda, int(la), sa, pb, ldb, int(lb), sb,
             pc, ldc, int(lc), sc, int(_DT[C.dtype]), float(alpha), float(beta), bias_ptr,
             int(epi), int(split_k)]
+
+
+def _strided_args(A, B, C, alpha, beta, bias, epilogue, split_k):
+    """Arguments of gemm_strided (without the workspace and stream)."""
+    M, N, K, batch, epi, bias_ptr = _common(A, B, C, bias, epilogue)
+    pa, ars, acs, sa = strided_desc(A)
+    pb, brs, bcs, sb = strided_desc(B)
+    pc, crs, ccs, sc = strided_desc(C)
+    return [int(_DT[A.dtype]), batch, M, N, K, pa, ars, acs, sa, pb, brs, bcs, sb,
+            pc, crs, ccs, sc, int(_DT[C.dtype]), float(alpha), float(beta), bias_ptr,
+            int(epi), int(split_k)]
+
+
+def _is_matrix(t):
+    try:
+        matrix_desc(t)
+        return True
+    except ValueError:
+        return False
+
+
+def plan(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, alpha=1.0, beta=0.0, bias=None,
+         epilogue=None, split_k=0, workspace_bytes=None):
+    """The kernel plan gemm() would use (a dict), without launching anything.
+    Only for row- or column-major views (others are copied by gemm_strided)."""
+    if epilogue is None:
+        epilogue = "bias" if bias is not None else "none"
+    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
+    ws = (1 << 62) if workspace_bytes is None else int(workspace_bytes)
+    st, p = _abi.gemm_plan_query(*args, ws)
+    check(st)
+    return p.as_dict()
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alpha=1.0,
@@ -99,10 +143,13 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alp
 
     A: [M,K] or [batch,M,K]; B: [K,N] or [batch,K,N] (a batch stride of 0,
     e.g. from ``expand``, broadcasts); C: output (allocated when None, in
-    ``out_dtype`` or A's dtype).  ``epilogue`` is a ``gemm_epilogue_t`` name
-    in lower case ("bias_gelu_tanh", "row_bias_relu", ...) or an ``Epi``; it
-    defaults to "bias" when a bias is given.  A workspace is allocated with torch when the plan needs one
-    and none is given.
+    ``out_dtype`` or A's dtype).  Row- and column-major views run in place
+    through ``gemm_batched``; any other strides (a step along the inner
+    dimension, repeated rows) go through ``gemm_strided``, which copies those
+    matrices into the workspace.  ``epilogue`` is a ``gemm_epilogue_t`` name in
+    lower case ("bias_gelu_tanh", "row_bias_relu", ...) or an ``Epi``; it
+    defaults to "bias" when a bias is given.  A workspace is allocated with
+    torch when the call needs one and none is given.
     """
     if epilogue is None:
         epilogue = "bias" if bias is not None else "none"
@@ -113,15 +160,25 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alp
         shape = (A.shape[-2], B.shape[-1]) if A.dim() == 2 and B.dim() == 2 else \
             (batch, A.shape[-2], B.shape[-1])
         C = torch.empty(shape, dtype=out_dtype or A.dtype, device=A.device)
-    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
+    strided = not all(_is_matrix(t) for t in (A, B, C))
+    if strided:
+        args = _strided_args(A, B, C, alpha, beta, bias, epilogue, split_k)
+    else:
+        args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
     if workspace is None:
-        st, p = _abi.gemm_plan_query(*args, 1 << 62)
-        check(st)
-        need = int(p.workspace_bytes)
+        if strided:
+            ab, batch, M, N, K = args[:5]
+            need = int(_abi.gemm_strided_workspace_size(ab, args[17], batch, M, N, K, *args[6:9],
+                                                        *args[10:13], *args[14:17], args[22]))
+        else:
+            st, p = _abi.gemm_plan_query(*args, 1 << 62)
+            check(st)
+            need = int(p.workspace_bytes)
         workspace = torch.empty(need, dtype=torch.uint8, device=A.device) if need > 0 else None
     ws_ptr = 0 if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
-    check(_abi.gemm_batched(*args, ws_ptr, ws_bytes, stream))
+    call = _abi.gemm_strided if strided else _abi.gemm_batched
+    check(call(*args, ws_ptr, ws_bytes, stream))
     return C

@@ -128,3 +128,68 @@ def test_workspace_defaults_to_what_the_plan_needs():
     assert p["stream_k"] == 3 and p["workspace_bytes"] > 0
     assert api.plan(A, B, C, workspace_bytes=p["workspace_bytes"]) == p
     assert api.plan(A, B, C, workspace_bytes=0)["stream_k"] == 0
+
+
+def _capture(monkeypatch, name, status=0):
+    seen = []
+
+    def fake(*args):
+        seen.append(args)
+        return status
+    monkeypatch.setattr(api._abi, name, fake)
+    return seen
+
+
+def test_views_that_are_not_matrices_go_through_gemm_strided(monkeypatch):
+    M, N, K = 64, 48, 32
+    base_a = bf(M, 2 * K)
+    A = base_a[:, ::2]                                   # a step of 2 along K
+    row = bf(1, N)
+    B = row.expand(K, N)                                 # every row the same
+    C = torch.empty(M, N, dtype=torch.float32)
+    sizes = _capture(monkeypatch, "gemm_strided_workspace_size", 4096)
+    calls = _capture(monkeypatch, "gemm_strided")
+    batched = _capture(monkeypatch, "gemm_batched")
+    out = api.gemm(A, B, C, alpha=0.5, stream=0)
+    assert out is C and batched == [] and len(calls) == 1
+    args = calls[0]
+    assert args[:5] == (0, 1, M, N, K)
+    assert args[5:9] == (A.data_ptr(), 2 * K, 2, 0)      # A: row stride, column stride, batch
+    assert args[9:13] == (B.data_ptr(), 0, 1, 0)          # B: rows of stride 0
+    assert args[13:17] == (C.data_ptr(), N, 1, 0)
+    assert args[17:23] == (2, 0.5, 0.0, 0, 0, 0)
+    assert args[24] >= 4096                              # the workspace it was told to need
+    assert sizes[0] == (0, 2, 1, M, N, K, 2 * K, 2, 0, 0, 1, 0, N, 1, 0, 0)
+
+
+def test_batched_views_pass_their_batch_strides(monkeypatch):
+    bt, M, N, K = 3, 32, 40, 24
+    A = bf(bt, M, 3 * K)[:, :, ::3]
+    B = bf(K, N)                                         # broadcast over the batch
+    C = torch.empty(bt, M, N, dtype=torch.bfloat16)
+    _capture(monkeypatch, "gemm_strided_workspace_size", 0)
+    calls = _capture(monkeypatch, "gemm_strided")
+    api.gemm(A, B, C, stream=0)
+    args = calls[0]
+    assert args[1] == bt and args[5:9] == (A.data_ptr(), 3 * K, 3, M * 3 * K)
+    assert args[9:13] == (B.data_ptr(), N, 1, 0) and args[13:17] == (C.data_ptr(), N, 1, M * N)
+    assert args[23] == 0 and args[24] == 0               # no workspace needed, none passed
+
+
+def test_matrix_views_stay_on_gemm_batched(monkeypatch):
+    A, B = bf(64, 32), bf(48, 32).t()
+    C = torch.empty(64, 48, dtype=torch.float32)
+    calls = _capture(monkeypatch, "gemm_batched")
+    strided = _capture(monkeypatch, "gemm_strided")
+    api.gemm(A, B, C, stream=0)
+    assert strided == [] and len(calls) == 1
+    assert calls[0][5:9] == (A.data_ptr(), 32, int(Layout.ROW_MAJOR), 0)
+    assert calls[0][9:13] == (B.data_ptr(), 32, int(Layout.COL_MAJOR), 0)
+
+
+def test_an_output_with_repeated_rows_is_rejected_by_the_library():
+    A, B = bf(64, 32), bf(32, 48)
+    C = torch.empty(1, 48, dtype=torch.float32).expand(64, 48)
+    with pytest.raises(dg.GemmError) as e:
+        api.gemm(A, B, C, stream=0)
+    assert e.value.status == Status.ERR_INVALID_ARG

@@ -104,3 +104,18 @@ def test_fp32_inputs_run_the_cuda_core_sgemm():
     p = oracle.Problem(ab_dtype="f32", c_dtype="f32", M=M, N=N, K=K, A=bits(A), B=bits(B),
                        alpha=1.5, strides=((K, 1), (N, 1), (N, 1)))
     assert np.array_equal(out.numpy().astype(np.float64), oracle.gemm(p)[0])
+
+
+@pytest.mark.skip(reason="written without a GPU run: enable after its first one")
+def test_strided_views_run_through_gemm_strided():
+    M, N, K = 96, 80, 72
+    base_a = ints(96001, (M, 2 * K))
+    row = ints(96002, (1, N))
+    base_b = row.expand(K, N)                     # every row of B the same
+    dev = torch.device("cuda:0")
+    out = dg.gemm(base_a.to(dev)[:, ::2], row.to(dev).expand(K, N),
+                  out_dtype=torch.float32).cpu()
+    A = base_a[:, ::2].contiguous()
+    p = oracle.Problem(ab_dtype="bf16", c_dtype="f32", M=M, N=N, K=K, A=bits(A),
+                       B=bits(base_b.contiguous()), strides=((K, 1), (N, 1), (N, 1)))
+    assert np.array_equal(out.numpy().astype(np.float64), oracle.gemm(p)[0])
