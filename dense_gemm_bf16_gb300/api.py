@@ -115,6 +115,16 @@ def _strided_args(A, B, C, alpha, beta, bias, epilogue, split_k):
             int(epi), int(split_k)]
 
 
+def _require_cuda(**tensors):
+    """The kernels read every buffer through device pointers: a host tensor,
+    or one on another GPU than A, would be an illegal address there."""
+    dev = tensors["A"].device
+    for name, t in tensors.items():
+        if t is not None and (not t.is_cuda or t.device != dev):
+            where = dev if dev.type == "cuda" else "one CUDA device"
+            raise ValueError(f"{name} must be a CUDA tensor on {where} (it is on {t.device})")
+
+
 def _is_matrix(t):
     try:
         matrix_desc(t)
@@ -153,6 +163,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *, alp
     """
     if epilogue is None:
         epilogue = "bias" if bias is not None else "none"
+    _require_cuda(A=A, B=B, C=C, bias=bias, workspace=workspace)
     if C is None:
         if beta != 0.0:
             raise ValueError("beta != 0 needs an input C")

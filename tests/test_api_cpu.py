@@ -131,6 +131,8 @@ def test_workspace_defaults_to_what_the_plan_needs():
 
 
 def _capture(monkeypatch, name, status=0):
+    # these tests read the arguments a call would pass, with host tensors
+    monkeypatch.setattr(api, "_require_cuda", lambda **kw: None)
     seen = []
 
     def fake(*args):
@@ -187,7 +189,14 @@ def test_matrix_views_stay_on_gemm_batched(monkeypatch):
     assert calls[0][9:13] == (B.data_ptr(), 32, int(Layout.COL_MAJOR), 0)
 
 
-def test_an_output_with_repeated_rows_is_rejected_by_the_library():
+def test_host_tensors_are_refused_before_any_call():
+    A, B = bf(64, 32), bf(32, 48)
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        api.gemm(A, B, stream=0)
+
+
+def test_an_output_with_repeated_rows_is_rejected_by_the_library(monkeypatch):
+    monkeypatch.setattr(api, "_require_cuda", lambda **kw: None)
     A, B = bf(64, 32), bf(32, 48)
     C = torch.empty(1, 48, dtype=torch.float32).expand(64, 48)
     with pytest.raises(dg.GemmError) as e:
