@@ -34,6 +34,8 @@ MUTANTS = {
     "relu_passes_negatives": ("return x > 0.0 ? x : 0.0;", "return x > 0.0 ? x : -x;"),
     "gelu_erf_scale": ("erf(x / sqrt(2.0))", "erf(x / 2.0)"),
     "bias_orientation_swapped": ("bias[bias_rows ? i : j]", "bias[bias_rows ? j : i]"),
+    "sampled_last_k_dropped": ("for (int64_t k = 0; k < K; ++k)\n            acc +=",
+                               "for (int64_t k = 0; k + 1 < K; ++k)\n            acc +="),
     "strided_column_stride_dropped": ("int64_t idx = b * stride + r * rs + c * cs;", "int64_t idx = b * stride + r * rs + c;"),
 }
 

@@ -558,3 +558,31 @@ def test_strided_storage(oracle_mod, dt):
     pid = oracle_mod.Problem(ab_dtype=dt, M=M, N=K, K=K, A=fa, B=fi, c_dtype="f32",
                              alpha=2.0, strides=[(3, 17), (1, K + 2), (K, 1)])
     assert np.array_equal(oracle_mod.gemm(pid)[0], 2.0 * A)
+
+
+def test_strided_sampled_equals_strided_full(oracle_mod):
+    # the one-by-one form of the strided oracle against its full form, with a
+    # batch, batch strides, a broadcast B, a bias along rows and an activation
+    nb, M, N, K = 2, 5, 6, 7
+    A = representable(datagen.uniform(181, (nb, M, K)), "bf16")
+    B = representable(datagen.uniform(182, (K, N)), "bf16")
+    C0 = representable(datagen.normal(183, (nb, M, N)), "f32")
+    bias = datagen.to_f32(datagen.normal(184, (M,)))
+    sa = 3 * M + 17 * K
+    fa = np.concatenate([_store_strided(A[b], 3, 17, "bf16", sa) for b in range(nb)])
+    fb = _store_strided(B, 2, 2 * K + 3, "bf16", 2 * K + (2 * K + 3) * N)
+    sc = (2 * N + 1) * M + 2 * N
+    fc = np.concatenate([_store_strided(C0[b], 2 * N + 1, 2, "f32", sc) for b in range(nb)])
+    p = oracle_mod.Problem(ab_dtype="bf16", M=M, N=N, K=K, batch=nb, A=fa, B=fb, c_dtype="f32",
+                           C0=fc, stride_a=sa, stride_b=0, stride_c=sc, alpha=0.75, beta=0.5,
+                           bias=bias, bias_rows=True, act="gelu_tanh",
+                           strides=[(3, 17), (2, 2 * K + 3), (2 * N + 1, 2)])
+    full = oracle_mod.gemm(p)
+    bs, is_, js = np.meshgrid(np.arange(nb), np.arange(M), np.arange(N), indexing="ij")
+    s = oracle_mod.gemm_sampled(p, bs.ravel(), is_.ravel(), js.ravel())
+    assert np.array_equal(s, full.ravel())
+    # and the full form against the dense definition, batch by batch
+    for b in range(nb):
+        dense = make_problem(oracle_mod, A[b], B, "bf16", "row", "row", C0=C0[b], alpha=0.75,
+                             beta=0.5, bias=bias, bias_rows=True, act="gelu_tanh")
+        assert np.array_equal(full[b], oracle_mod.gemm(dense)[0])
