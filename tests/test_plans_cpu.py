@@ -282,3 +282,25 @@ def test_more_work_units_than_32_bits_count_is_unsupported():
     st, p = dg.gemm_plan_query(0, bt // 2, 256, 16, 16, BASE, 16, 0, 256 * 16, BASE, 16, 0, 0,
                                BASE, 16, 0, 256 * 16, 2, 1.0, 0.0, None, 0, 0, 0)
     assert st == Status.OK and p.kernel == 1
+
+
+# The automatic stream-K choice against the shapes it was measured on (bf16,
+# A row-major, B column-major, a workspace given): the split form where it ran
+# faster than whole tiles, whole tiles where it ran slower.
+STREAM_K_MEASURED = [
+    ((2560, 2560, 16384), 2),   # +25 %
+    ((4096, 4096, 8192), 2),    # +6 %
+    ((4096, 4096, 4096), 2),    # +3 %
+    ((5120, 5120, 4096), 2),    # +2 %
+    ((4096, 4096, 2048), 0),    # -3 % when forced
+    ((6144, 4096, 4096), 0),    # -18 % when forced
+]
+
+
+@pytest.mark.parametrize("shape,form", STREAM_K_MEASURED)
+def test_auto_stream_k_follows_the_measurements(shape, form):
+    M, N, K = shape
+    p = plan(M, N, K, lb=1, ws=UNLIMITED)
+    assert p["stream_k"] == form and p["cta_pair"] == 2, p
+    if form == 0:
+        assert plan(M, N, K, lb=1)["stream_k"] == 0
