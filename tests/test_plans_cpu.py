@@ -304,3 +304,12 @@ def test_auto_stream_k_follows_the_measurements(shape, form):
     assert p["stream_k"] == form and p["cta_pair"] == 2, p
     if form == 0:
         assert plan(M, N, K, lb=1)["stream_k"] == 0
+
+
+@pytest.mark.parametrize("K,pair", [(128, 0), (256, 0), (512, 0), (704, 0), (768, 2), (1024, 2),
+                                    (2048, 2)])
+def test_cta_pairs_start_at_twelve_k_blocks(K, pair):
+    # measured on 4096 x 4096 x K: paired tiles ran 10-25 % slower for K <= 256,
+    # even at 512 and 5-20 % faster from 1024; the threshold is 12 K blocks
+    p = plan(4096, 4096, K, lb=1)
+    assert p["cta_pair"] == pair and p["block_n"] == 256, p
