@@ -114,6 +114,9 @@ _SIGNATURES = {
     "gemm_plan_query": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp, _i64, _i32,
                          _i64, _vp, _i64, _i32, _i64, _i32, _f32, _f32, _vp, _i32, _i32, _sz,
                          ctypes.POINTER(Plan)], _i32),
+    "gemm_strided_plan_query": ([_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _vp, _i64,
+                                 _i64, _i64, _vp, _i64, _i64, _i64, _i32, _f32, _f32, _vp, _i32,
+                                 _i32, _sz, ctypes.POINTER(Plan)], _i32),
     "gemm_set_option": ([_i32, _i64], _i32),
     "gemm_get_option": ([_i32], _i64),
     "gemm_tile_order": ([_i32, _i32, _i32, ctypes.POINTER(ctypes.c_int),
@@ -223,6 +226,18 @@ def gemm_plan_query(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb, 
     st = lib().gemm_plan_query(ab_dtype, batch, M, N, K, A, lda, la, stride_a, B, ldb, lb,
                                stride_b, C, ldc, lc, stride_c, c_dtype, alpha, beta, bias, epi,
                                split_k, workspace_bytes, ctypes.byref(plan))
+    return st, plan
+
+
+def gemm_strided_plan_query(ab_dtype, batch, M, N, K, A, a_rs, a_cs, stride_a, B, b_rs, b_cs,
+                            stride_b, C, c_rs, c_cs, stride_c, c_dtype, alpha, beta, bias, epi,
+                            split_k, workspace_bytes):
+    """Returns (status, Plan) of the gemm_strided call with these arguments."""
+    plan = Plan()
+    st = lib().gemm_strided_plan_query(ab_dtype, batch, M, N, K, A, a_rs, a_cs, stride_a, B, b_rs,
+                                       b_cs, stride_b, C, c_rs, c_cs, stride_c, c_dtype, alpha,
+                                       beta, bias, epi, split_k, workspace_bytes,
+                                       ctypes.byref(plan))
     return st, plan
 
 

@@ -135,13 +135,17 @@ def _is_matrix(t):
 
 def plan(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, alpha=1.0, beta=0.0, bias=None,
          epilogue=None, split_k=0, workspace_bytes=None):
-    """The kernel plan gemm() would use (a dict), without launching anything.
-    Only for row- or column-major views (others are copied by gemm_strided)."""
+    """The kernel plan gemm() would use (a dict), without launching anything;
+    for views that go through gemm_strided, the plan of that call (its copies
+    counted in pack_a / pack_b, launches and workspace_bytes)."""
     if epilogue is None:
         epilogue = "bias" if bias is not None else "none"
-    args = _args(A, B, C, alpha, beta, bias, epilogue, split_k)
     ws = (1 << 62) if workspace_bytes is None else int(workspace_bytes)
-    st, p = _abi.gemm_plan_query(*args, ws)
+    if all(_is_matrix(t) for t in (A, B, C)):
+        st, p = _abi.gemm_plan_query(*_args(A, B, C, alpha, beta, bias, epilogue, split_k), ws)
+    else:
+        st, p = _abi.gemm_strided_plan_query(
+            *_strided_args(A, B, C, alpha, beta, bias, epilogue, split_k), ws)
     check(st)
     return p.as_dict()
 

@@ -246,4 +246,43 @@ gemm_status_t gemm_strided(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int6
     return GEMM_OK;
 }
 
+gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N,
+                                      int64_t K, const void* A, int64_t a_rs, int64_t a_cs,
+                                      int64_t stride_a, const void* B, int64_t b_rs, int64_t b_cs,
+                                      int64_t stride_b, void* C, int64_t c_rs, int64_t c_cs,
+                                      int64_t stride_c, gemm_dtype_t c_dtype, float alpha,
+                                      float beta, const float* bias, gemm_epilogue_t epi,
+                                      int split_k, size_t workspace_bytes, gemm_plan_t* plan) {
+    using namespace dg;
+    if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+    StridedPlan sp;
+    gemm_status_t st = make_strided_plan(ab_dtype, c_dtype, batch, M, N, K, a_rs, a_cs, stride_a,
+                                         b_rs, b_cs, stride_b, c_rs, c_cs, stride_c, split_k, sp);
+    if (st != GEMM_OK) return st;
+    const bool any_copy = sp.a.copy || sp.b.copy || sp.c.copy;
+    const size_t copies = any_copy ? sp.total - sp.inner_bytes : 0;
+    if (any_copy && workspace_bytes < copies) return GEMM_ERR_WORKSPACE;
+    // the copies sit in the workspace, which is 256-byte aligned: planning reads
+    // only the alignment of their addresses, so an aligned stand-in serves
+    alignas(256) static const char copy_standin[256] = {0};
+    const bool need_ab = K > 0 && alpha != 0.0f;
+    const void* a = sp.a.copy ? static_cast<const void*>(copy_standin) : A;
+    const void* b = sp.b.copy ? static_cast<const void*>(copy_standin) : B;
+    void* c = sp.c.copy ? const_cast<char*>(copy_standin) : C;
+    const int64_t sa = sp.a.copy ? (sp.a.batches > 1 ? M * sp.a.pitch : 0) : stride_a;
+    const int64_t sb = sp.b.copy ? (sp.b.batches > 1 ? K * sp.b.pitch : 0) : stride_b;
+    const int64_t sc = sp.c.copy ? M * sp.c.pitch : stride_c;
+    st = gemm_plan_query(ab_dtype, batch, M, N, K, a, sp.a.ld, sp.a.layout, sa, b, sp.b.ld,
+                         sp.b.layout, sb, c, sp.c.ld, sp.c.layout, sc, c_dtype, alpha, beta, bias,
+                         epi, split_k, workspace_bytes - copies, plan);
+    if (st != GEMM_OK) return st;
+    if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
+    plan->pack_a = plan->pack_a || sp.a.copy;
+    plan->pack_b = plan->pack_b || sp.b.copy;
+    plan->launches += (sp.a.copy && need_ab) + (sp.b.copy && need_ab) +
+                      (sp.c.copy ? 1 + (beta != 0.0f) : 0);
+    plan->workspace_bytes += static_cast<int64_t>(copies);
+    return GEMM_OK;
+}
+
 }  // extern "C"

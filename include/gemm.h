@@ -288,6 +288,26 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
                               int split_k, size_t workspace_bytes, gemm_plan_t* plan);
 
 /*
+ * gemm_strided_plan_query -- the plan gemm_strided would follow for these
+ * arguments, without enqueuing anything (host only; nothing is read through
+ * the pointers, whose alignment alone is used).  The plan is that of the
+ * gemm_batched call on the dense layouts, with pack_a / pack_b also set for an
+ * A or B gathered into a copy, launches counting the gathers and the scatter,
+ * and workspace_bytes including the copies.  Returns what gemm_strided would
+ * return before enqueuing (GEMM_ERR_WORKSPACE when workspace_bytes cannot hold
+ * the copies and the inner plan).  The copies' placement assumes a 256-byte
+ * aligned workspace, as gemm_strided requires.
+ */
+gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
+                                      int64_t M, int64_t N, int64_t K,
+                                      const void* A, int64_t a_rs, int64_t a_cs, int64_t stride_a,
+                                      const void* B, int64_t b_rs, int64_t b_cs, int64_t stride_b,
+                                      void* C, int64_t c_rs, int64_t c_cs, int64_t stride_c,
+                                      gemm_dtype_t c_dtype, float alpha, float beta,
+                                      const float* bias, gemm_epilogue_t epi, int split_k,
+                                      size_t workspace_bytes, gemm_plan_t* plan);
+
+/*
  * Process-wide tuning knobs (for measurements and tests; defaults are what the
  * library ships with).  Returns GEMM_ERR_INVALID_ARG for an unknown option or
  * value out of range.

@@ -202,3 +202,12 @@ def test_an_output_with_repeated_rows_is_rejected_by_the_library(monkeypatch):
     with pytest.raises(dg.GemmError) as e:
         api.gemm(A, B, C, stream=0)
     assert e.value.status == Status.ERR_INVALID_ARG
+
+
+def test_plan_of_a_strided_view_counts_its_copy():
+    A = bf(300, 400)[:, ::2]                     # a step of 2 along K = 200
+    B, C = bf(200, 256), torch.empty(300, 256, dtype=torch.float32)
+    p = api.plan(A, B, C)
+    dense = api.plan(A.contiguous(), B, C)
+    assert p["pack_a"] == 1 and dense["pack_a"] == 0
+    assert p["launches"] == dense["launches"] + 1

@@ -315,3 +315,63 @@ def test_cta_pairs_start_at_twelve_k_blocks(K, pair):
     # even at 512 and 5-20 % faster from 1024; the threshold is 12 K blocks
     p = plan(4096, 4096, K, lb=1)
     assert p["cta_pair"] == pair and p["block_n"] == 256, p
+
+
+def splan(M, N, K, a, b, c, *, ab=0, cdt=2, batch=1, alpha=1.0, beta=0.0, ws=UNLIMITED,
+          split_k=0):
+    """gemm_strided_plan_query with (row stride, column stride, batch stride) per matrix."""
+    st, p = dg.gemm_strided_plan_query(ab, batch, M, N, K, BASE, *a, BASE, *b, BASE, *c, cdt,
+                                       alpha, beta, None, 0, split_k, ws)
+    return st, p.as_dict()
+
+
+def test_strided_plan_of_dense_strides_is_the_batched_plan():
+    M, N, K = 2560, 2560, 16384
+    st, sp = splan(M, N, K, (K, 1, 0), (1, K, 0), (N, 1, 0))     # B column-major
+    assert st == Status.OK
+    assert sp == plan(M, N, K, lb=1, ws=UNLIMITED)
+
+
+def test_strided_plan_counts_the_copies():
+    M, N, K = 300, 256, 200     # dense rows of 400 and 512 bytes: TMA reads them in place
+    st, dense = splan(M, N, K, (K, 1, 0), (N, 1, 0), (N, 1, 0))
+    assert st == Status.OK and dense["pack_a"] == 0 and dense["pack_b"] == 0
+    # A with a step of 2 along K: gathered into a copy, one more launch
+    st, p = splan(M, N, K, (2 * K, 2, 0), (N, 1, 0), (N, 1, 0))
+    assert st == Status.OK and p["pack_a"] == 1 and p["pack_b"] == 0
+    assert p["launches"] == dense["launches"] + 1
+    assert p["workspace_bytes"] > dense["workspace_bytes"]
+    # C interleaved (column stride 2): computed densely, then scattered; with
+    # beta != 0 also gathered first
+    st, pc = splan(M, N, K, (K, 1, 0), (N, 1, 0), (2 * N, 2, 0))
+    assert st == Status.OK and pc["launches"] == dense["launches"] + 1
+    st, pcb = splan(M, N, K, (K, 1, 0), (N, 1, 0), (2 * N, 2, 0), beta=1.0)
+    assert st == Status.OK and pcb["launches"] >= dense["launches"] + 2
+    # with alpha == 0 A and B are never read, so they are not gathered either
+    st, p0 = splan(M, N, K, (2 * K, 2, 0), (N, 1, 0), (N, 1, 0), alpha=0.0, beta=1.0)
+    assert st == Status.OK and p0["kernel"] == 3
+
+
+def test_strided_plan_workspace_rules():
+    M, N, K = 300, 260, 200
+    a, b, c = (2 * K, 2, 0), (N, 1, 0), (N, 1, 0)
+    st, p = splan(M, N, K, a, b, c)
+    assert st == Status.OK
+    need = p["workspace_bytes"]
+    assert dg.gemm_strided_workspace_size(0, 2, 1, M, N, K, *a, *b, *c, 0) >= need
+    st, exact = splan(M, N, K, a, b, c, ws=need)
+    assert st == Status.OK and exact == p
+    st, _ = splan(M, N, K, a, b, c, ws=need - 256)
+    assert st == Status.ERR_WORKSPACE
+    st, _ = splan(M, N, K, a, b, c, ws=0)
+    assert st == Status.ERR_WORKSPACE
+
+
+def test_strided_plan_rejects_what_gemm_strided_rejects():
+    M, N, K = 64, 64, 64
+    st, _ = splan(M, N, K, (K, 1, 0), (N, 1, 0), (0, 1, 0))          # rows of C repeated
+    assert st == Status.ERR_INVALID_ARG
+    st, _ = splan(M, N, K, (-K, 1, 0), (N, 1, 0), (N, 1, 0))         # negative stride
+    assert st == Status.ERR_INVALID_ARG
+    st, _ = splan(M, N, K, (1 << 60, 1, 0), (N, 1, 0), (N, 1, 0))    # span too large
+    assert st == Status.ERR_INVALID_ARG
