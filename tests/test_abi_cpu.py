@@ -253,3 +253,21 @@ def test_workspace_size_of_oversized_problems_is_zero(lib):
     big = (1 << 31) - 1
     assert dg.gemm_workspace_size(DType.BF16, big, big, big, big, 0) == 0
     assert dg.gemm_workspace_size(DType.BF16, 1 << 20, 1 << 20, 1 << 20, 8, 0) == 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host has a GPU")
+def test_every_compute_entry_reports_no_device_without_a_gpu(lib):
+    nd = Status.ERR_NO_DEVICE
+    assert dg.gemm_f16(4, 4, 4, 16, 4, 0, 16, 4, 0, 16, 4, 0, DType.F32, 1.0, 0.0, None, 0, 0,
+                       None, 0, None) == nd
+    assert dg.sgemm_f32(4, 4, 4, 16, 4, 0, 16, 4, 0, 16, 4, 0, 1.0, 0.0, None, 0, None) == nd
+    assert dg.gemm_batched(DType.BF16, 2, 4, 4, 4, 16, 4, 0, 16, 16, 4, 0, 16, 16, 4, 0, 16,
+                           DType.F32, 1.0, 0.0, None, 0, 0, None, 0, None) == nd
+    assert dg.gemm_strided(DType.BF16, 1, 4, 4, 4, 16, 4, 1, 0, 16, 4, 1, 0, 16, 4, 1, 0,
+                           DType.F32, 1.0, 0.0, None, 0, 0, None, 0, None) == nd
+    assert dg.gemm_bf16_static_workspace(4, 4, 4, 16, 4, 0, 16, 4, 0, 16, 4, 0, DType.F32, 1.0,
+                                         0.0, None, 0, 0, None) == nd
+    assert dg.gemm_check_device_status(None) == nd
+    st, _ = dg.gemm_plan_query(DType.BF16, 1, 4, 4, 4, 16, 4, 0, 0, 16, 4, 0, 0, 16, 4, 0, 0,
+                               DType.F32, 1.0, 0.0, None, 0, 0, 0)
+    assert st == nd
