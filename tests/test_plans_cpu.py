@@ -375,3 +375,11 @@ def test_strided_plan_rejects_what_gemm_strided_rejects():
     assert st == Status.ERR_INVALID_ARG
     st, _ = splan(M, N, K, (1 << 60, 1, 0), (N, 1, 0), (N, 1, 0))    # span too large
     assert st == Status.ERR_INVALID_ARG
+
+
+def test_wide_tiles_on_request(options):
+    options(WIDE_TILE=2)
+    p = headline()
+    assert p["block_n"] == 512 and p["cta_pair"] == 2 and p["block_k"] == 64   # one K block
+    q = plan(4096, 256, 4096, lb=1)                # N < 512: the 256-wide pair tile stays
+    assert q["block_n"] != 512
