@@ -530,7 +530,6 @@ ABLATION = [  # (label, GEMM options)
     ("L2 hints: A evict-first, B evict-last", {"L2_HINTS": 1}),
     ("L2 hints: A evict-last, B evict-first", {"L2_HINTS": 2}),
     ("single-CTA tiles (no CTA pairs)", {"CTA_PAIR": 1}),
-    ("CTA pairs sharing B by multicast", {"CTA_PAIR": 2}),
     ("256 x 512 pair tiles (one accumulator)", {"WIDE_TILE": 2}),
     ("one K block per TMA load", {"DOUBLE_K": 1}),
 ]

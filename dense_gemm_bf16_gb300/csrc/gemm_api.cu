@@ -52,7 +52,7 @@ struct DevState {
     int sm_count = 0;
     int cc = 0;
     int* status = nullptr;
-    int max_pairs[3][3] = {};  // co-resident two-CTA clusters [mode][BN 128, 256, 512]
+    int max_pairs[3][3] = {};  // co-resident two-CTA clusters [mode][BN 128, 256, 512] (mode 2)
 };
 DevState g_dev[kMaxDevices];
 
@@ -93,11 +93,9 @@ gemm_status_t device_state(DevState** out) {
                 if (e == cudaSuccess) e = tc_prepare(bn);
             if (e == cudaSuccess) e = sgemm_prepare();
             if (e == cudaSuccess) {
-                for (int mode = 1; mode <= 2; ++mode) {
-                    d.max_pairs[mode][0] = tc_max_pairs(128, mode);
-                    d.max_pairs[mode][1] = tc_max_pairs(256, mode);
-                    d.max_pairs[mode][2] = tc_max_pairs(512, mode);
-                }
+                d.max_pairs[2][0] = tc_max_pairs(128, 2);
+                d.max_pairs[2][1] = tc_max_pairs(256, 2);
+                d.max_pairs[2][2] = tc_max_pairs(512, 2);
             }
         }
         d.sm_count = sms;
@@ -396,8 +394,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.launches += 1;
     }
     pl.ws_need = off;
-    // CTA pairs along M (GEMM_OPT_CTA_PAIR: 0 auto, 1 never, 2 B-multicast pair,
-    // 3 pair MMA) for problems with at least a full wave of tile pairs and a
+    // CTA pairs along M (GEMM_OPT_CTA_PAIR: 0 auto, 1 never, 3 pair MMA) for problems with at least a full wave of tile pairs and a
     // main loop of at least kPairMinKBlocks K blocks: with shorter ones the
     // pair's shared epilogue hand-off costs more than the halved B traffic
     // saves (measured: K <= 256 ran 10-25 % slower paired, K = 512 even,
@@ -405,16 +402,13 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     constexpr int64_t kPairMinKBlocks = 12;
     const int64_t want = g_opt_cta_pair.load();
     int mode = 0;
-    if (want == 2 || want == 3)
-        mode = static_cast<int>(want) - 1;
-    else if (want == 0)
-        mode = 2;
+    if (want == 3 || want == 0) mode = 2;
     const int bn_idx = pl.bn == 256 ? 1 : 0;
     int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
     if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
         pl.inkernel_split == 0 &&
-        (want >= 2 || (pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
+        (want == 3 || (pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
         pl.mode = mode;
         pl.cm = 2;
         pl.stages = tc_stages_for(pl.bn, mode);
@@ -1031,7 +1025,9 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             g_opt_test_stall.store(value);
             return GEMM_OK;
         case GEMM_OPT_CTA_PAIR:
-            if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
+            // (2 named pairs that shared B through multicast loads; that form
+            // is gone and the value is refused)
+            if (value < 0 || value > 3 || value == 2) return GEMM_ERR_INVALID_ARG;
             g_opt_cta_pair.store(value);
             return GEMM_OK;
         case GEMM_OPT_SWAP_AB:

@@ -79,9 +79,9 @@ struct TcParams {
 };
 
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).
-// Tensor-core kernel modes: 0 one CTA per 128 x BN tile; 1 CTA pair along M
-// sharing B through TMA multicast; 2 CTA pair computing a 256 x BN tile with
-// cta_group::2 MMAs.  Epilogue forms: 0 general; 1 TMA store only, for
+// Tensor-core kernel modes: 0 one CTA per 128 x BN tile; 2 CTA pair computing
+// a 256 x BN tile with cta_group::2 MMAs (each CTA loads its own half of A and
+// B; no operand load is multicast).  Epilogue forms: 0 general; 1 TMA store only, for
 // beta == 0 or split-K partials, with tmap_c boxes of 128-byte rows
 // (tc_has_fast tells the tile widths that have it); 2 the same with beta * C
 // read by TMA loads through tmap_c, for a 16-bit C (tc_has_beta_form tells the

@@ -116,31 +116,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Multicast variants: the box lands at the same shared-memory offset in every
-// CTA of the cluster named in `mask`, and completes bytes on the mbarrier at
-// the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t mask,
-                                               uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask),
-          "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t x, int32_t y, int32_t z, uint16_t mask,
-                                               uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar),
-          "h"(mask), "l"(policy)
-        : "memory");
-}
-
 // CTA-pair variants: the box lands in this CTA's shared memory at `dst`, and
 // its bytes complete on `bar`, which may be the peer CTA's mbarrier (a
 // shared::cluster address from mapa).

@@ -42,7 +42,6 @@ cudaError_t tc_prepare(int bn) {
 
 bool tc_has_mode(int bn, int mode) {
     if (mode == 0) return bn == 16 || bn == 32 || bn == 64 || bn == 128 || bn == 256;
-    if (mode == 1) return bn == 128 || bn == 256;
     if (mode == 2) return bn == 128 || bn == 256 || bn == 512;
     return false;
 }

@@ -9,13 +9,11 @@ cudaError_t tc_prepare_fast(int bn) {
         case 64: return prepare_bn<64, 0, 1>();
         case 128: {
             cudaError_t e = prepare_bn<128, 0, 1>();
-            if (e == cudaSuccess) e = prepare_bn<128, 1, 1>();
             if (e == cudaSuccess) e = prepare_bn<128, 2, 1>();
             return e;
         }
         case 256: {
             cudaError_t e = prepare_bn<256, 0, 1>();
-            if (e == cudaSuccess) e = prepare_bn<256, 1, 1>();
             if (e == cudaSuccess) e = prepare_bn<256, 2, 1>();
             return e;
         }
@@ -29,11 +27,6 @@ cudaError_t tc_launch_fast(int bn, int mode, const TcParams& p, int grid, cudaSt
         if (bn == 128) return launch_bn<128, 2, 1>(p, grid, stream);
         if (bn == 256) return launch_bn<256, 2, 1>(p, grid, stream);
         if (bn == 512) return launch_bn<512, 2, 1>(p, grid, stream);
-        return cudaErrorInvalidValue;
-    }
-    if (mode == 1) {
-        if (bn == 128) return launch_bn<128, 1, 1>(p, grid, stream);
-        if (bn == 256) return launch_bn<256, 1, 1>(p, grid, stream);
         return cudaErrorInvalidValue;
     }
     switch (bn) {

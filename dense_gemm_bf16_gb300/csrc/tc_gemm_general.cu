@@ -10,13 +10,11 @@ cudaError_t tc_prepare_general(int bn) {
         case 64: return prepare_bn<64, 0, 0>();
         case 128: {
             cudaError_t e = prepare_bn<128, 0, 0>();
-            if (e == cudaSuccess) e = prepare_bn<128, 1, 0>();
             if (e == cudaSuccess) e = prepare_bn<128, 2, 0>();
             return e;
         }
         case 256: {
             cudaError_t e = prepare_bn<256, 0, 0>();
-            if (e == cudaSuccess) e = prepare_bn<256, 1, 0>();
             if (e == cudaSuccess) e = prepare_bn<256, 2, 0>();
             return e;
         }
@@ -26,8 +24,6 @@ cudaError_t tc_prepare_general(int bn) {
 }
 
 int tc_max_pairs_general(int bn, int mode) {
-    if (mode == 1 && bn == 128) return max_clusters_bn<128, 1, 0>();
-    if (mode == 1 && bn == 256) return max_clusters_bn<256, 1, 0>();
     if (mode == 2 && bn == 128) return max_clusters_bn<128, 2, 0>();
     if (mode == 2 && bn == 256) return max_clusters_bn<256, 2, 0>();
     if (mode == 2 && bn == 512) return max_clusters_bn<512, 2, 0>();
@@ -39,11 +35,6 @@ cudaError_t tc_launch_general(int bn, int mode, const TcParams& p, int grid, cud
         if (bn == 128) return launch_bn<128, 2, 0>(p, grid, stream);
         if (bn == 256) return launch_bn<256, 2, 0>(p, grid, stream);
         if (bn == 512) return launch_bn<512, 2, 0>(p, grid, stream);
-        return cudaErrorInvalidValue;
-    }
-    if (mode == 1) {
-        if (bn == 128) return launch_bn<128, 1, 0>(p, grid, stream);
-        if (bn == 256) return launch_bn<256, 1, 0>(p, grid, stream);
         return cudaErrorInvalidValue;
     }
     switch (bn) {

@@ -61,8 +61,6 @@ constexpr uint32_t C_RING_BYTES = 4 * 2 * EPI_BOX_BYTES;
 static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 
 // MODE 0: one CTA per 128 x BN tile.
-// MODE 1: two CTAs of a cluster stacked along M; each loads its own A rows and
-//         one half of the shared B tile, multicast into both CTAs.
 // MODE 2: two CTAs of a cluster compute one 256 x BN tile with cta_group::2
 //         MMAs issued by the even CTA; each CTA holds its own 128 A rows and
 //         BN/2 B columns, so a stage is 16 KB + BN*64 bytes per CTA.  With
@@ -78,6 +76,7 @@ static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 // bounded number of loads outstanding; measured 3 % faster on 8192^3).
 template <int BN, int MODE, int EPI = 0, int KS = 1>
 struct Cfg {
+    static_assert(MODE == 0 || MODE == 2, "one CTA per tile, or a two-CTA MMA pair");
     static constexpr int CM = MODE == 0 ? 1 : 2;        // CTAs per cluster
     static constexpr int CG = MODE == 2 ? 2 : 1;        // tcgen05 cta_group
     static constexpr int B_ROWS = MODE == 2 ? BN / 2 : BN;  // B rows (N) held per CTA
@@ -1061,7 +1060,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // loads; its accumulator-release barrier counts the epilogue warps of
         // both CTAs.  Accumulator releases are one arrival per epilogue warp.
         const uint32_t full_count = 1u;
-        const uint32_t empty_count = MODE == 1 ? 2u : 1u;
+        const uint32_t empty_count = 1u;
         const uint32_t tempty_count = MODE == 2 ? 2u * (TC_EPI_THREADS / 32) : TC_EPI_THREADS / 32;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8u * s, full_count);
@@ -1122,8 +1121,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     const uint32_t fb = full0 + 8u * stage;
-                    // MODE 1: own A + both B halves.  MODE 2: the leader's barrier
-                    // takes the bytes of both CTAs; the peer's barrier is unused.
+                    // MODE 2: the leader's barrier takes the bytes of both CTAs;
+                    // the peer's barrier is unused.
                     if (MODE != 2 || leader)
                         mbar_arrive_expect_tx(fb, MODE == 2 ? 2u * C::STAGE_BYTES : C::STAGE_BYTES);
                     const uint32_t a_dst = sA0 + stage * C::A_BYTES;
@@ -1177,28 +1176,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                 for (int h = 0; h < BN / 64; ++h)
                                     load_tile(&p.tmap_b, b_dst + h * 8192u, fb,
                                               w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol_b);
-                            }
-                        }
-                    } else if constexpr (MODE == 1) {
-                        // this CTA's half of the B tile, multicast to the pair
-                        constexpr int HALF = BN / 2;
-                        if (!p.b_mn) {
-                            const uint32_t dst = b_dst + rank * (HALF * 128u);
-                            const int y = w.pid_n * BN + static_cast<int>(rank) * HALF;
-                            if (p.b_3d)
-                                tma_load_3d_mc(dst, &p.tmap_b, fb, k0, y, w.b, kPair, pol_b);
-                            else
-                                tma_load_2d_mc(dst, &p.tmap_b, fb, k0, y, kPair, pol_b);
-                        } else {
-#pragma unroll
-                            for (int hh = 0; hh < HALF / 64; ++hh) {
-                                const int h = static_cast<int>(rank) * (HALF / 64) + hh;
-                                const uint32_t dst = b_dst + h * 8192u;
-                                const int x = w.pid_n * BN + 64 * h;
-                                if (p.b_3d)
-                                    tma_load_3d_mc(dst, &p.tmap_b, fb, x, k0, w.b, kPair, pol_b);
-                                else
-                                    tma_load_2d_mc(dst, &p.tmap_b, fb, x, k0, kPair, pol_b);
                             }
                         }
                     }

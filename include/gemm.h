@@ -265,9 +265,9 @@ typedef struct {
     int32_t group_m;         /* tile-order grouping                                */
     int32_t launches;        /* kernels enqueued by the call                       */
     int64_t workspace_bytes; /* workspace the plan uses                            */
-    int32_t cta_pair;        /* 0 one CTA per tile; 1 CTA pair along M sharing B by
-                                TMA multicast; 2 CTA pair computing 256-row tiles
-                                with two-CTA (cta_group::2) MMAs                   */
+    int32_t cta_pair;        /* 0 one CTA per tile; 2 CTA pair computing 256-row tiles
+                                with two-CTA (cta_group::2) MMAs, each CTA loading
+                                its own half of A and B (1 is not used)            */
     int32_t stream_k;        /* stream-K: 0 off; 1 the K blocks of the last one-to-two
                                 waves split evenly over all CTAs in contiguous ranges;
                                 2 each unit of the last partial wave cut into equal
@@ -316,9 +316,9 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *   GEMM_OPT_MAX_CTAS     cap on persistent CTAs (0 = one per SM).
  *   GEMM_OPT_TIMEOUT_US   bound on any single in-kernel wait, microseconds (>= 1).
  *   GEMM_OPT_CTA_PAIR     0 (default): two-CTA MMA pairs along M when a problem has a
- *                         full wave of tile pairs and K >= 768; 1: never; 2: B-multicast
- *                         pairs whenever the tile width allows; 3: two-CTA MMA pairs
- *                         likewise.
+ *                         full wave of tile pairs and K >= 768; 1: never; 3: two-CTA
+ *                         MMA pairs whenever the tile width allows.  2 is refused
+ *                         (GEMM_ERR_INVALID_ARG).
  *   GEMM_OPT_SWAP_AB      0 (default): compute C^T = B^T A^T when M <= 64 < N;
  *                         1: never; 2: always.
  *   GEMM_OPT_L2_HINTS     L2 policy of the tensor-core operand loads: 0 (default) normal;

@@ -260,7 +260,7 @@ def test_stalled_pipeline_reports_timeout_and_recovers():
 
 # ---------------------------------------------------------------- two-CTA clusters
 
-@pytest.fixture(params=[2, 3], ids=["multicast_pair", "pair_mma"])
+@pytest.fixture(params=[3], ids=["pair_mma"])
 def pairs(request):
     import dense_gemm_bf16_gb300 as dg
     dg.gemm_set_option(dg.Option.CTA_PAIR, request.param)
@@ -380,7 +380,6 @@ FORM_CASES = {
     "swap_row_bias": dict(ab="bf16", M=40, N=900, K=256, lc="col", c_dtype="f32", bias=True),
     "pair_mma": dict(ab="bf16", M=1100, N=1304, K=320, c_dtype="bf16", alpha=0.25, bias=True,
                      opts={"CTA_PAIR": 3}),
-    "pair_multicast": dict(ab="bf16", M=700, N=600, K=200, c_dtype="f32", opts={"CTA_PAIR": 2}),
 }
 
 

@@ -170,9 +170,8 @@ def test_workspace_size_covers_batched_plans(ab, cdt, shape):
 # kernel instantiations compiled into the library: (tile width, CTA mode) per epilogue form,
 # and the two-K-blocks-per-load form (pairs, TMA-store-only epilogue)
 INSTANTIATED = {
-    0: {(16, 0), (32, 0), (64, 0), (128, 0), (256, 0), (128, 1), (256, 1), (128, 2), (256, 2),
-        (512, 2)},
-    1: {(64, 0), (128, 0), (256, 0), (128, 1), (256, 1), (128, 2), (256, 2), (512, 2)},
+    0: {(16, 0), (32, 0), (64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
+    1: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
     2: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2)},
 }
 TWO_K_BLOCKS = {(128, 2), (256, 2)}
@@ -202,7 +201,7 @@ def _random_calls(n, seed=20261202):
 
 
 OPTION_SETS = [
-    {}, {"CTA_PAIR": 1}, {"CTA_PAIR": 2}, {"CTA_PAIR": 3}, {"WIDE_TILE": 2},
+    {}, {"CTA_PAIR": 1}, {"CTA_PAIR": 3}, {"WIDE_TILE": 2},
     {"CTA_PAIR": 3, "WIDE_TILE": 2}, {"SWAP_AB": 1}, {"SWAP_AB": 2}, {"STREAM_K": 1},
     {"STREAM_K": 2}, {"STREAM_K": 3}, {"FAST_EPILOGUE": 1}, {"SPLIT_REDUCE": 1},
     {"SPLIT_REDUCE": 2}, {"BLOCK_N": 16}, {"BLOCK_N": 64}, {"BLOCK_N": 128}, {"DOUBLE_K": 1},
@@ -383,3 +382,28 @@ def test_wide_tiles_on_request(options):
     assert p["block_n"] == 512 and p["cta_pair"] == 2 and p["block_k"] == 64   # one K block
     q = plan(4096, 256, 4096, lb=1)                # N < 512: the 256-wide pair tile stays
     assert q["block_n"] != 512
+
+
+def test_the_multicast_pair_value_is_refused():
+    """GEMM_OPT_CTA_PAIR = 2 named CTA pairs that shared B through multicast TMA
+    loads; the library has no such load any more, and the value is refused
+    without changing the option."""
+    before = dg.gemm_get_option(Option.CTA_PAIR)
+    assert dg.gemm_set_option(Option.CTA_PAIR, 2) == Status.ERR_INVALID_ARG
+    assert dg.gemm_get_option(Option.CTA_PAIR) == before
+    for v in (0, 1, 3):
+        assert dg.gemm_set_option(Option.CTA_PAIR, v) == Status.OK
+    assert dg.gemm_set_option(Option.CTA_PAIR, before) == Status.OK
+
+
+def test_no_source_names_a_multicast_load():
+    """No TMA load in the library's sources is multicast (the commit arrive
+    that signals both CTAs of a pair is an mbarrier signal, not a load)."""
+    import pathlib
+    csrc = pathlib.Path(dg.__file__).parent / "csrc"
+    for f in sorted(csrc.iterdir()):
+        if f.suffix not in (".cu", ".cuh", ".h"):
+            continue
+        for n, line in enumerate(f.read_text().splitlines(), 1):
+            if "multicast::cluster" in line:
+                assert "cp.async" not in line and "tcgen05.commit" in line, (f.name, n, line)
