@@ -433,10 +433,15 @@ void gemm_tile_order(int num_pid_m, int num_pid_n, int group_m, int* pid_m, int*
  *     (with that device current); make that first call before any stream
  *     capture begins.
  *   - All calls share the one array, and it keeps the last call's contents.
- *     Nothing in it needs to start at zero: every call writes each scratch
- *     byte before reading it.  Calls whose work overlaps on the GPU (on
- *     different streams, or from different host threads without ordering)
- *     race on the array and may produce wrong results: order them.
+ *     Nothing in it needs to start at zero.  Split-K partial tiles and
+ *     operand copies are written before they are read.  The stream-K flags
+ *     that K pieces poll are read before their publisher writes them, so
+ *     they may still hold an earlier call's values; a piece takes a partial
+ *     only once its flag equals the launch's epoch, a fresh non-zero value
+ *     for every call (and a call made during a stream capture clears the
+ *     flags inside the graph first).  Calls whose work overlaps on the GPU
+ *     (on different streams, or from different host threads without
+ *     ordering) race on the array and may produce wrong results: order them.
  */
 #define GEMM_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 

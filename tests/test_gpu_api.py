@@ -106,7 +106,6 @@ def test_fp32_inputs_run_the_cuda_core_sgemm():
     assert np.array_equal(out.numpy().astype(np.float64), oracle.gemm(p)[0])
 
 
-@pytest.mark.skip(reason="written without a GPU run: enable after its first one")
 def test_strided_views_run_through_gemm_strided():
     M, N, K = 96, 80, 72
     base_a = ints(96001, (M, 2 * K))

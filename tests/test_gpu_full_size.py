@@ -79,6 +79,96 @@ def test_c3_bf16_8192_bias_gelu_full_size():
     check_16bit(vals[i, j], ref)
 
 
+def _c3_layout_call(dA, dB_cm, dC, c_dtype, dbias, epi):
+    """One 8192^3 call in the headline's layout (A row-major, B column-major,
+    C row-major, no workspace) with the given output type and epilogue;
+    returns the plan it ran under."""
+    import torch
+
+    import bench
+    import dense_gemm_bf16_gb300 as dg
+    M, N, K = bench.M, bench.N, bench.K
+    args = [0, 1, M, N, K, dA.data_ptr(), K, 0, 0, dB_cm.data_ptr(), K, 1, 0, dC.data_ptr(), N,
+            0, 0, c_dtype, 1.0, 0.0, dbias.data_ptr() if dbias is not None else None, epi, 0]
+    st, plan = dg.gemm_plan_query(*args, 0)
+    assert st == 0
+    st = dg.gemm_batched(*args, None, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == 0, dg.gemm_status_string(st)
+    return plan.as_dict()
+
+
+def _planted_zero_gemm_fails(check, got, p):
+    """The same check against the oracle run with A = 0 (the GEMM term
+    dropped) must fail: the test can see the product."""
+    import copy
+    zero = copy.copy(p)
+    zero.A = np.zeros_like(p.A)
+    _, i, j = sample_positions(p.M, p.N, 256, seed=9011)
+    ref0 = oracle.gemm_sampled(zero, None, i, j)
+    with pytest.raises(AssertionError):
+        check(got[i, j], ref0)
+
+
+def test_c3_layout_scaled_inputs_fp32_out_no_epilogue():
+    """The headline's inputs (U(-1,1)/sqrt(K) on both operands) and layout,
+    without bias or GELU and with an fp32 output, at the sqrt(K)-normalised
+    1e-4 bound.  The product's std is about 1/(3 sqrt(K)) and the bound
+    allows 1e-4 of sqrt(K) max|A| max|B| = 1/sqrt(K), so a missing or wrong
+    GEMM term fails here where the bias + GELU check cannot see it."""
+    import torch
+
+    import bench
+    a, b_cm, _ = bench.c3_host_inputs()
+    M, N, K = bench.M, bench.N, bench.K
+    dA = torch.from_numpy(a.view(np.int16)).cuda()
+    dB = torch.from_numpy(b_cm.view(np.int16)).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    plan = _c3_layout_call(dA, dB, dC, 2, None, 0)
+    # the bench's kernel form: CTA pairs, two K blocks per load, TMA-store epilogue
+    assert plan["cta_pair"] == 2 and plan["block_k"] == 128 and plan["fast_epilogue"] == 1, plan
+    got = dC.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    _, i, j = sample_positions(M, N, 2048, seed=9005)
+    p = oracle.Problem(ab_dtype="bf16", M=M, N=N, K=K, A=a.ravel(), lda=K, la="row",
+                       B=b_cm.ravel(), ldb=K, lb="col", c_dtype="f32")
+    scale = math.sqrt(K) * bf16_to_f64(a).__abs__().max() * bf16_to_f64(b_cm).__abs__().max()
+    check = lambda g, r: check_f32(g, r, scale)   # noqa: E731
+    check(got[i, j], oracle.gemm_sampled(p, None, i, j))
+    _planted_zero_gemm_fails(check, got, p)
+
+
+def test_c3_layout_unscaled_inputs_bias_gelu():
+    """The headline's call (bias + GELU(tanh), bf16 out, the bench's plan) on
+    unscaled U(-1,1) inputs, so that the product (std about sqrt(K/9) = 30)
+    dominates the N(0,1) bias: element-wise 1e-2 + 1e-2 |ref|."""
+    import torch
+
+    import bench
+    M, N, K = bench.M, bench.N, bench.K
+    a = datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(3, datagen.ROLE_A) + 100, (M, K)))
+    b = datagen.to_bf16_bits(datagen.uniform(datagen.seed_for(3, datagen.ROLE_B) + 100, (K, N)))
+    b_cm = np.ascontiguousarray(b.T)
+    del b
+    bias = datagen.to_f32(datagen.normal(datagen.seed_for(3, datagen.ROLE_BIAS), (N,)))
+    dA = torch.from_numpy(a.view(np.int16)).cuda()
+    dB = torch.from_numpy(b_cm.view(np.int16)).cuda()
+    dbias = torch.from_numpy(bias).cuda()
+    dC = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    gemm = bench.Gemm(dA, dB, dbias, dC, torch.cuda.current_stream().cuda_stream)
+    assert gemm.plan["cta_pair"] == 2 and gemm.plan["block_k"] == 128, gemm.plan
+    gemm()
+    torch.cuda.synchronize()
+    got = bf16_to_f64(dC.cpu().numpy().view(np.uint16))
+    assert np.isfinite(got).all() and got.min() >= -0.1701
+    _, i, j = sample_positions(M, N, 2048, seed=9006)
+    p = oracle.Problem(ab_dtype="bf16", M=M, N=N, K=K, A=a.ravel(), lda=K, la="row",
+                       B=b_cm.ravel(), ldb=K, lb="col", c_dtype="bf16", bias=bias,
+                       act="gelu_tanh")
+    check_16bit(got[i, j], oracle.gemm_sampled(p, None, i, j))
+    _planted_zero_gemm_fails(check_16bit, got, p)
+
+
 # ----------------------------------------------------------------------------- bench.py rows
 
 def _row(name):

@@ -15,8 +15,7 @@ import pytest
 
 from gemm_case import Case, check_close
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="written without a GPU run: enable after its first one")]
+pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 

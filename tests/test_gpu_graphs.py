@@ -14,8 +14,7 @@ import dense_gemm_bf16_gb300 as dg
 import oracle
 from dense_gemm_bf16_gb300 import Option
 
-pytestmark = [pytest.mark.gpu,
-              pytest.mark.skip(reason="written without a GPU run: enable after its first one")]
+pytestmark = pytest.mark.gpu
 
 # name: (M, N, K), options during planning and capture, expected plan stream_k
 CASES = {
