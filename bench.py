@@ -9,12 +9,16 @@ fp32 N(0,1), fp32 accumulation, bf16 output; one call of the library's C ABI
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                     [--rows FILE] [--row NAME]
 
---impl reference times the CPU oracle (plain fp64 C, one host core) on a
-bounded slice of the same workload: the deliberately slow baseline.
---rows FILE additionally measures the other library paths (SGEMM 4096^3,
-ragged 4097x3001x1000, split-K 256x256x65536, skinny 16x8192x8192, batched
-64x1024^3) and writes one JSON object per path to FILE; --row NAME runs only
-that path (--steps launches) and prints its JSON object.
+The line also carries ``rows``: the other workloads (bf16 256^3, SGEMM
+4096^3, ragged 4097x3001x1000, split-K 256x256x65536, skinny 16x8192x8192,
+batched 64x1024^3 with per-entry and broadcast B), each timed over cold-L2
+launches with its roofline fraction and a clock sample (--no-rows skips them).
+--impl reference times the CPU oracle (plain fp64 C, unchanged) on a bounded
+slice of the same workload, split into row slices over one process per host
+core: the deliberately slow baseline.  The line's cpu_baseline is the same
+harness.  --rows FILE measures every library path (the rows above plus
+stream-K and flat-K shapes) into FILE; --row NAME runs only that path
+(--steps launches) and prints its JSON object.
 Multi-GPU runs (torchrun) run one independent replica per GPU (weak scaling).
 """
 from __future__ import annotations
@@ -59,6 +63,7 @@ def parse_args():
                          "into this file (JSON)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="leave the other workloads out")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -351,58 +356,169 @@ def time_steps(fn, steps, warmup, barrier=None):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_tflops(a, b_cm, bias, rows, cols):
+def _oracle_problem(a_rows, b_cm_cols, bias_cols):
+    """The workload restricted to some rows of A and columns of B (full K)."""
+    import oracle
+    return oracle.Problem(ab_dtype="bf16", M=a_rows.shape[0], N=b_cm_cols.shape[0], K=K,
+                          A=a_rows.ravel(), lda=K, la="row", B=b_cm_cols.ravel(), ldb=K,
+                          lb="col", c_dtype="bf16", bias=bias_cols, act="gelu_tanh")
+
+
+def oracle_sample_seconds(a, b_cm, bias, rows, cols):
     """The oracle, as it stands, on the first `rows` x `cols` outputs of the
-    workload (full K).  Returns (seconds, flops)."""
+    workload (full K), in this process.  Returns (seconds, flops)."""
     import numpy as np
 
     import oracle
-    b_sub = np.ascontiguousarray(b_cm[:cols])  # first `cols` columns of the column-major B
-    p = oracle.Problem(ab_dtype="bf16", M=rows, N=cols, K=K, A=a[:rows].ravel(), lda=K,
-                       la="row", B=b_sub.ravel(), ldb=K, lb="col", c_dtype="bf16",
-                       bias=bias[:cols], act="gelu_tanh")
+    p = _oracle_problem(a[:rows], np.ascontiguousarray(b_cm[:cols]), bias[:cols])
     t0 = time.perf_counter()
     oracle.gemm(p)
-    dt = time.perf_counter() - t0
-    return dt, 2.0 * rows * cols * K
+    return time.perf_counter() - t0, 2.0 * rows * cols * K
 
 
-def cpu_baseline(a, b_cm, bias, target_s=12.0):
-    # calibrate on 1 x 512 outputs, then size the sample for ~target_s of CPU work
-    dt, fl = oracle_sample_tflops(a, b_cm, bias, 1, 512)
-    per_out = dt / 512
-    n_out = max(512, min(int(target_s / max(per_out, 1e-9)), 64 * N))
-    rows = max(1, n_out // N)
-    cols = N if n_out >= N else n_out
-    dt, fl = oracle_sample_tflops(a, b_cm, bias, rows, cols)
-    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {rows} row(s) x {cols} column(s) of C (full K = {K}), "
-                      f"{dt:.1f} s, fp64 oracle, one thread"}
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+# worker side of OracleCores (a spawned process: module-level state only)
+_W = {}
+
+
+def _oracle_worker_init(names, shapes):
+    import numpy as np
+    from multiprocessing import shared_memory
+
+    import oracle
+    oracle.build()
+    for key in ("a", "b", "bias"):
+        shm = shared_memory.SharedMemory(name=names[key])
+        dt = np.float32 if key == "bias" else np.uint16
+        _W[key + "_shm"] = shm
+        _W[key] = np.ndarray(shapes[key], dtype=dt, buffer=shm.buf)
+
+
+def _oracle_worker_ready(_):
+    return os.getpid()
+
+
+def _oracle_worker_run(job):
+    """Rows r0 .. r1 (of the first rows of A) x the first `cols` columns."""
+    import numpy as np
+
+    import oracle
+    r0, r1, cols = job
+    if r1 <= r0:
+        return 0.0
+    p = _oracle_problem(np.ascontiguousarray(_W["a"][r0:r1]),
+                        np.ascontiguousarray(_W["b"][:cols]), _W["bias"][:cols])
+    t0 = time.perf_counter()
+    oracle.gemm(p)
+    return time.perf_counter() - t0
+
+
+class OracleCores:
+    """The oracle (unchanged, single-threaded C) on every host core: one
+    spawned process per core, each computing a slice of rows of the same
+    sample from A and B in shared memory.  A sample's time is the wall time
+    from handing out the slices to the last one's return."""
+
+    def __init__(self, a, b_cm, bias, max_rows):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        self.cores = _host_cores()
+        arrays = {"a": a[:max_rows], "b": b_cm, "bias": bias}
+        self.shm, names, shapes = {}, {}, {}
+        for key, arr in arrays.items():
+            shm = shared_memory.SharedMemory(create=True, size=max(arr.nbytes, 1))
+            import numpy as np
+            np.ndarray(arr.shape, dtype=arr.dtype, buffer=shm.buf)[...] = arr
+            self.shm[key], names[key], shapes[key] = shm, shm.name, arr.shape
+        self.max_rows = max_rows
+        # spawn: the parent holds a CUDA context, which a forked child must not inherit
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init,
+                                                 initargs=(names, shapes))
+        # every worker started and initialised before anything is timed (a
+        # worker that cannot start would be replaced forever: bounded wait)
+        self._map(_oracle_worker_ready, range(4 * self.cores), 300)
+
+    def _map(self, fn, jobs, timeout_s):
+        try:
+            return self.pool.map_async(fn, jobs, chunksize=1).get(timeout_s)
+        except BaseException:
+            self.pool.terminate()
+            raise
+
+    def run(self, rows, cols):
+        """Wall seconds for rows x cols outputs split over the cores."""
+        rows = min(rows, self.max_rows)
+        bounds = [rows * i // self.cores for i in range(self.cores + 1)]
+        jobs = [(bounds[i], bounds[i + 1], cols) for i in range(self.cores)]
+        t0 = time.perf_counter()
+        self._map(_oracle_worker_run, jobs, 1800)
+        return time.perf_counter() - t0, 2.0 * rows * cols * K
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        for shm in self.shm.values():
+            shm.close()
+            shm.unlink()
+
+
+def _rows_for(seconds, per_out, cores):
+    """Rows of the full-width sample that take about `seconds` on `cores`."""
+    return max(cores, int(seconds * cores / max(per_out, 1e-9)) // N)
+
+
+def cpu_baseline(a, b_cm, bias, target_s=8.0):
+    """The oracle on every host core, on a sample of whole rows of the
+    workload sized for about target_s seconds (calibrated on one core)."""
+    dt, _ = oracle_sample_seconds(a, b_cm, bias, 1, 512)
+    cores = _host_cores()
+    rows = min(_rows_for(target_s, dt / 512, cores), M)
+    pool = OracleCores(a, b_cm, bias, rows)
+    try:
+        t, fl = pool.run(rows, N)
+    finally:
+        pool.close()
+    return {"value": fl / t / 1e12, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+            "sample": f"first {rows} rows x {N} columns of C (full K = {K}), split into row "
+                      f"slices over {pool.cores} processes (one per host core), {t:.1f} s "
+                      "wall; fp64 oracle, unchanged, one thread per process"}
 
 
 def reference_arm(args):
-    """Times the oracle on this host's cores: one bounded slice per step."""
+    """Times the oracle on this host's cores: one bounded sample of whole rows
+    per step, split over one process per core."""
     a, b_cm, bias = c3_host_inputs()
-    dt, _ = oracle_sample_tflops(a, b_cm, bias, 1, 256)
-    per_out = dt / 256
+    dt, _ = oracle_sample_seconds(a, b_cm, bias, 1, 256)
+    cores = _host_cores()
     budget = 150.0 / (args.steps + args.warmup)  # whole run within a few minutes
-    cols = int(max(16, min(N, budget / max(per_out, 1e-9))))
-    for _ in range(args.warmup):
-        oracle_sample_tflops(a, b_cm, bias, 1, cols)
-    tot_t, tot_f = 0.0, 0.0
-    for _ in range(args.steps):
-        t, f = oracle_sample_tflops(a, b_cm, bias, 1, cols)
-        tot_t += t
-        tot_f += f
+    rows = min(_rows_for(budget, dt / 256, cores), M)
+    pool = OracleCores(a, b_cm, bias, rows)
+    try:
+        for _ in range(args.warmup):
+            pool.run(rows, N)
+        tot_t, tot_f = 0.0, 0.0
+        for _ in range(args.steps):
+            t, f = pool.run(rows, N)
+            tot_t += t
+            tot_f += f
+    finally:
+        pool.close()
     value = tot_f / tot_t / 1e12
-    sample = (f"per step: 1 row x {cols} columns of C (full K = {K}), fp64 oracle, one thread; "
-              f"{args.steps} steps")
+    sample = (f"per step: the first {rows} rows x {N} columns of C (full K = {K}), split into "
+              f"row slices over {pool.cores} processes (one per host core); fp64 oracle, "
+              f"unchanged, one thread per process; {args.steps} steps")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -498,6 +614,11 @@ def main():
         with open(args.rows, "w") as f:
             json.dump(measure_rows(ROW_NAMES, device), f, indent=1)
 
+    # the other workloads, one GPU at a time (a single-GPU run only)
+    rows = None
+    if not args.no_rows and world == 1:
+        rows = line_rows(device)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(a, b_cm, bias)
@@ -514,7 +635,7 @@ def main():
                            "plan": gemm.plan},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps * gemm.plan["launches"],
-                "clocks": clocks}
+                "clocks": clocks, "rows": rows}
         print(json.dumps(line), flush=True)
     reps.close()
 
@@ -692,6 +813,35 @@ def build_row(name, device):
         nbytes = (m_ * k_ + k_ * n_) * 2 + m_ * n_ * (4 if f32 else 2)
         return fn, 2.0 * m_ * n_ * k_, nbytes, "hbm", plan, (A, B, C, wst)
     raise ValueError(f"unknown row {name!r}")
+
+
+# the workloads besides the headline that the default line reports
+LINE_ROWS = ("small_256", "sgemm_4096", "ragged_4097x3001x1000", "splitk_256x256x65536",
+             "skinny_16x8192x8192", "batched_64x1024", "batched_64x1024_bcast")
+PLAN_KEYS = ("block_n", "block_k", "cta_pair", "split_k", "stream_k", "fast_epilogue",
+             "swap_ab", "pack_a", "pack_b", "grid", "launches")
+
+
+def line_rows(device, reps=20):
+    """The other workloads for the default line: per row the median time of
+    `reps` cold-L2 launches, throughput, roofline fraction and plan, plus one
+    clock sample over all of them."""
+    sampler = ClockSampler(device.index)
+    out = measure_rows(LINE_ROWS, device, reps=reps)
+    clocks = sampler.stop()
+    rows = {}
+    for r in out:
+        plan = r["plan"]
+        rows[r["path"]] = {
+            "us_median": r["ms_median"] * 1e3, "us_min": r["ms_min"] * 1e3,
+            "tflops": r["tflops"], "gbs": r["gbs"], "bound": r["bound"], "peak": r["peak"],
+            "frac": r["frac"], "flops": r["flops"], "algorithmic_bytes": r["algorithmic_bytes"],
+            "plan": {k: plan[k] for k in PLAN_KEYS if k in plan} if "block_n" in plan else plan}
+        if "peak_source" in r:
+            rows[r["path"]]["peak_source"] = r["peak_source"]
+    return {"timing": f"median of {reps} launches, each after a read of a 256 MiB buffer "
+                      "(cold L2), CUDA events on the launching stream",
+            "clocks": clocks, "results": rows}
 
 
 def fp32_peak_tflops(device):

@@ -539,14 +539,18 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
             if (pl.beta_epi) pl.stages = tc_stages_beta(pl.bn, pl.mode);
         }
     }
-    // Two K blocks per TMA load (KS = 2) for K-major operands of a CTA-pair
-    // plan with the TMA-store-only epilogue: the operands are seen as
-    // (64 K, rows, K blocks), so K must be a whole number of 64-deep blocks
-    // (an odd count reads its last block's partner past the end: zeros); whole
-    // units only (no stream-K or split pieces), one batch entry.
+    // Two K blocks per TMA load (KS = 2) for a CTA-pair plan with the
+    // TMA-store-only epilogue, whole units only (no stream-K or split pieces).
+    // A K-major operand is seen as (64 K, rows, K blocks), so K must be a whole
+    // number of 64-deep blocks (an odd count reads its last block's partner
+    // past the end: zeros) and the operand one matrix (one batch entry, or a
+    // broadcast).  An MN-major operand keeps its own map with boxes of 128 K
+    // rows instead of 64 (rows past K: zeros), batched or not.
+    auto ks2_ok = [&](const Operand& o) {
+        return o.mn || (c.K % TC_BLOCK_K == 0 && (c.batch == 1 || o.stride == 0));
+    };
     if (g_opt_double_k.load() == 0 && pl.kernel == 1 && pl.fast_epi && pl.splits == 1 &&
-        pl.sk == 0 && tc_has_ks2(pl.bn, pl.mode, 1) && !pl.a.mn && !pl.b.mn && c.batch == 1 &&
-        c.K % TC_BLOCK_K == 0) {
+        pl.sk == 0 && tc_has_ks2(pl.bn, pl.mode, 1) && ks2_ok(pl.a) && ks2_ok(pl.b)) {
         pl.ks = 2;
         pl.stages = tc_stages_ks2(pl.bn);
     }
@@ -588,9 +592,9 @@ gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const v
     if (!fn) return GEMM_ERR_CUDA;
     const CUtensorMapDataType type =
         ab == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (two_k_blocks) {
+    if (two_k_blocks && !o.mn) {
         // K-major, K a multiple of 64: (64 K, rows, K blocks), two K blocks a box
-        if (o.mn || o.k_ext % 64 != 0) return GEMM_ERR_UNSUPPORTED;
+        if (o.k_ext % 64 != 0) return GEMM_ERR_UNSUPPORTED;
         cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(o.outer()),
                               static_cast<cuuint64_t>(o.k_ext / 64)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), 128u};
@@ -607,8 +611,9 @@ gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const v
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(o.inner()), static_cast<cuuint64_t>(o.outer()),
                           static_cast<cuuint64_t>(batch)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(stride * 2)};
-    // K-major: box = 64 K x rows-of-tile; MN-major: box = 64 MN x 64 K (one swizzle atom column)
-    cuuint32_t box[3] = {64u, o.mn ? 64u : box_k_major_rows, 1u};
+    // K-major: box = 64 K x rows-of-tile; MN-major: box = 64 MN x 64 K (one swizzle atom
+    // column), or 64 MN x 128 K when one load brings two K blocks (rows past K: zeros)
+    cuuint32_t box[3] = {64u, o.mn ? (two_k_blocks ? 128u : 64u) : box_k_major_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = fn(map, type, three ? 3u : 2u, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

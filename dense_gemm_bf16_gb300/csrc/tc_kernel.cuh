@@ -1034,15 +1034,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    if constexpr (KS == 2) {
-        // two K blocks per load exist for K-major operands only (the plan
-        // never asks otherwise); report instead of computing garbage
-        if (p.a_mn || p.b_mn) {
-            if (threadIdx.x == 0 && p.status) atomicExch(p.status, 1);
-            return;
-        }
-    }
+    // An MN-contiguous operand arrives in 64-wide atom columns of 64 * KS K
+    // rows (128 bytes each, 128-byte swizzled): one column takes 8 KB * KS.
+    constexpr uint32_t kAtomCol = 8192u * KS;
 
     // The launch parameters outside the tensor maps lie in four 64-byte lines.
     // A role's first reads of them miss the constant cache one after another
@@ -1131,32 +1125,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     if constexpr (MODE == 2) {
                         // own A rows and own BN/2 B columns; bytes complete on the leader
                         const uint32_t lb = leader ? fb : mapa_shared(fb, 0u);
-                        if constexpr (KS == 2) {
-                            // K blocks kb and kb + 1 (past the end: zeros) in one load
-                            tma_load_3d_pair(a_dst, &p.tmap_a, lb, 0, w.pid_m * BM, kb, pol_a);
-                        } else if (!p.a_mn) {
-                            load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
+                        if (!p.a_mn) {
+                            if constexpr (KS == 2)  // K blocks kb and kb + 1 (past the end: zeros)
+                                tma_load_3d_pair(a_dst, &p.tmap_a, lb, 0, w.pid_m * BM, kb, pol_a);
+                            else
+                                load_pair(&p.tmap_a, a_dst, lb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
                         } else {
+                            // 64-wide atom columns of 64 * KS K rows (rows past K: zeros)
 #pragma unroll
                             for (int h = 0; h < BM / 64; ++h)
-                                load_pair(&p.tmap_a, a_dst + h * 8192u, lb, w.pid_m * BM + 64 * h,
+                                load_pair(&p.tmap_a, a_dst + h * kAtomCol, lb, w.pid_m * BM + 64 * h,
                                           k0, w.b, p.a_3d, pol_a);
                         }
                         // per N = SUB_N MMA, this CTA's half of its columns
                         constexpr int HALF = C::SUB_N / 2;
+                        static_assert(KS == 1 || C::NSUB == 1, "two K blocks per load: one sub-MMA");
 #pragma unroll
                         for (int sn = 0; sn < C::NSUB; ++sn) {
                             const uint32_t bs = b_dst + sn * (HALF * 128u);
                             const int n0 = w.pid_n * BN + sn * C::SUB_N + static_cast<int>(rank) * HALF;
-                            if constexpr (KS == 2) {
-                                tma_load_3d_pair(bs, &p.tmap_b, lb, 0, n0, kb, pol_b);
-                            } else if (!p.b_mn) {
-                                load_pair(&p.tmap_b, bs, lb, k0, n0, w.b, p.b_3d, pol_b);
+                            if (!p.b_mn) {
+                                if constexpr (KS == 2)
+                                    tma_load_3d_pair(bs, &p.tmap_b, lb, 0, n0, kb, pol_b);
+                                else
+                                    load_pair(&p.tmap_b, bs, lb, k0, n0, w.b, p.b_3d, pol_b);
                             } else {
 #pragma unroll
                                 for (int hh = 0; hh < HALF / 64; ++hh)
-                                    load_pair(&p.tmap_b, bs + hh * 8192u, lb, n0 + 64 * hh, k0, w.b,
-                                              p.b_3d, pol_b);
+                                    load_pair(&p.tmap_b, bs + hh * kAtomCol, lb, n0 + 64 * hh, k0,
+                                              w.b, p.b_3d, pol_b);
                             }
                         }
                     } else if (!p.a_mn) {
@@ -1164,7 +1161,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     } else {
 #pragma unroll
                         for (int h = 0; h < BM / 64; ++h)
-                            load_tile(&p.tmap_a, a_dst + h * 8192u, fb, w.pid_m * BM + 64 * h, k0,
+                            load_tile(&p.tmap_a, a_dst + h * kAtomCol, fb, w.pid_m * BM + 64 * h, k0,
                                       w.b, p.a_3d, pol_a);
                     }
                     if constexpr (MODE == 0) {
@@ -1174,7 +1171,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             if constexpr (BN >= 64) {
 #pragma unroll
                                 for (int h = 0; h < BN / 64; ++h)
-                                    load_tile(&p.tmap_b, b_dst + h * 8192u, fb,
+                                    load_tile(&p.tmap_b, b_dst + h * kAtomCol, fb,
                                               w.pid_n * BN + 64 * h, k0, w.b, p.b_3d, pol_b);
                             }
                         }
@@ -1214,12 +1211,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             uint32_t aphase = 0;
             bool issued = false;
             bool ok = true;
-            // K-major operands advance 32 bytes per K=16 step inside the 128-byte
-            // swizzle row; MN-major ones advance two 8-row (1024-byte) groups.
-            const uint32_t a_kstep = p.a_mn ? 2048u : 32u;
-            const uint32_t b_kstep = p.b_mn ? 2048u : 32u;
-            const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
-            const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+            // K step k (16 deep) of a stage.  K-major: 32 bytes per step inside
+            // the 128-byte swizzle row, and with KS = 2 the second K block BM
+            // (or B_ROWS) rows of 128 bytes after the first.  MN-major: two
+            // 8-row (1024-byte) groups per step down one atom column of 64 * KS
+            // K rows; the descriptor's leading byte offset is the distance
+            // between atom columns.
+            auto k_off = [](bool mn, int k, uint32_t rows) -> uint32_t {
+                return mn ? static_cast<uint32_t>(k) * 2048u
+                          : static_cast<uint32_t>(k / 4) * (rows * 128u) + static_cast<uint32_t>(k % 4) * 32u;
+            };
+            const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
+            const uint32_t a_lbo = a_mn ? kAtomCol : 16u;
+            const uint32_t b_lbo = b_mn ? kAtomCol : 16u;
             WorkIter wi = work_begin(p, cta0, ncta);
             Unit w;
             while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
@@ -1240,19 +1244,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     const uint32_t a_base = sA0 + stage * C::A_BYTES;
                     const uint32_t b_base = sB0 + stage * C::B_BYTES;
 #pragma unroll
-                    // K step k: K block k / 4 of the stage (KS = 2: the second one
-                    // BM or B_ROWS rows of 128 bytes after the first), 16 deep
                     for (int k = 0; k < KS * BK / 16; ++k) {
-                        const uint64_t ad = smem_desc_sw128(
-                            a_base + (k / 4) * (BM * 128u) + (k % 4) * a_kstep, a_lbo, 1024u);
+                        const uint64_t ad =
+                            smem_desc_sw128(a_base + k_off(a_mn, k, BM), a_lbo, 1024u);
 #pragma unroll
                         for (int sn = 0; sn < C::NSUB; ++sn) {
                             // sub-tile sn: its B rows from (SUB_N / 2) * 128 bytes on, its
                             // accumulator SUB_N columns on (one 64-wide atom column is 8 KB
                             // for MN-major B, the same offset)
                             const uint32_t bsub = b_base + sn * (C::SUB_N / 2) * 128u;
-                            const uint64_t bd = smem_desc_sw128(
-                                bsub + (k / 4) * (C::B_ROWS * 128u) + (k % 4) * b_kstep, b_lbo, 1024u);
+                            const uint64_t bd =
+                                smem_desc_sw128(bsub + k_off(b_mn, k, C::B_ROWS), b_lbo, 1024u);
                             umma_f16_cg<CG>(d_tmem + sn * C::SUB_N, ad, bd, p.idesc,
                                             (kb > w.kb0 || k > 0) ? 1u : 0u);
                         }

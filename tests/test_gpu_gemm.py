@@ -696,10 +696,12 @@ def test_spread_unpublished_partial_reports_timeout_and_recovers():
 
 # ---------------------------------------------------------------- two K blocks per TMA load
 
-# CTA-pair plans with K-major A and B bring two 64-deep K blocks per load (plan
-# block_k 128); an odd count of K blocks reads its last block's partner past
-# the end of K (zeros).  The K order is the same, so the bits match the
-# one-block form exactly.
+# CTA-pair plans bring two 64-deep K blocks per load (plan block_k 128): a
+# K-major operand through a (64 K, rows, K blocks) view, where an odd count of
+# K blocks reads its last block's partner past the end of K (zeros); an
+# MN-major operand in atom columns of 128 K rows, where rows past K read
+# zeros.  The K order is the same, so the bits match the one-block form
+# exactly.
 DOUBLE_K_CASES = {
     "even_bn128": dict(M=600, N=700, K=640, opts={"CTA_PAIR": 3, "BLOCK_N": 128}),
     "odd_bn256": dict(M=600, N=700, K=320, opts={"CTA_PAIR": 3, "BLOCK_N": 256}),
@@ -711,12 +713,12 @@ DOUBLE_K_CASES = {
 
 def _double_k_run(kw, extra, **case_kw):
     import dense_gemm_bf16_gb300 as dg
-    kw = dict(kw)
+    kw = {"la": "row", "lb": "col", **kw}
     opts = {**kw.pop("opts"), **extra}
     for k, v in opts.items():
         dg.gemm_set_option(dg.Option[k], v)
     try:
-        c = Case("bf16", la="row", lb="col", **kw, **case_kw)
+        c = Case("bf16", **kw, **case_kw)
         st, out = c.run_gpu()
     finally:
         for k in opts:
@@ -746,15 +748,54 @@ def test_double_k_bias_gelu_matches_one_block():
     assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
-@pytest.mark.parametrize("la,lb", [("col", "col"), ("row", "row")])
-def test_double_k_needs_k_major_operands(la, lb):
-    import dense_gemm_bf16_gb300 as dg
-    dg.gemm_set_option(dg.Option.CTA_PAIR, 3)
-    try:
-        c = run_exact(Case("bf16", 600, 700, 640, la=la, lb=lb, values="ints", seed=903))
-    finally:
-        dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
-    assert c.plan["block_k"] == 64 and c.plan["cta_pair"] == 2, c.plan
+# MN-major operands (row-major B, column-major A): every layout pair, even and
+# odd K-block counts, K ragged inside its last block (MN-major only), batches
+# with per-entry operands, an operand copied for alignment, 128-wide tiles
+MN_DOUBLE_K_CASES = {
+    "rr_even": dict(M=600, N=700, K=640, la="row", lb="row"),
+    "rr_odd_bn128": dict(M=600, N=700, K=320, la="row", lb="row", opts={"BLOCK_N": 128}),
+    "cc_odd": dict(M=600, N=700, K=1088, la="col", lb="col"),
+    "cr_ragged_k": dict(M=600, N=700, K=1000, la="col", lb="row"),
+    "cr_ragged_k_bn128": dict(M=520, N=332, K=777, la="col", lb="row", opts={"BLOCK_N": 128}),
+    "rr_many_tiles": dict(M=1100, N=1304, K=1088, la="row", lb="row"),
+    "cr_batched": dict(M=300, N=400, K=520, batch=3, la="col", lb="row"),
+    "cc_broadcast_b": dict(M=300, N=400, K=512, batch=2, la="col", lb="col", broadcast_b=True),
+    "rr_packed_b": dict(M=520, N=600, K=704, la="row", lb="row", pads=(0, 1, 0)),
+    "rr_bn256": dict(M=600, N=704, K=640, la="row", lb="row", opts={"BLOCK_N": 256}),
+    "cr_bn256_ragged_k": dict(M=520, N=768, K=1000, la="col", lb="row", opts={"BLOCK_N": 256}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MN_DOUBLE_K_CASES))
+def test_exact_double_k_mn_major(name):
+    # CTA pairs forced, and split_k = 1 so that no split or stream-K pieces
+    # take the plan off whole units
+    kw = dict(MN_DOUBLE_K_CASES[name], split_k=1)
+    kw["opts"] = {"CTA_PAIR": 3, **kw.get("opts", {})}
+    c, out = _double_k_run(kw, {}, values="ints", seed=903)
+    a_mn, b_mn = kw["la"] == "col", kw["lb"] == "row"
+    k_major_ok = kw["K"] % 64 == 0 and (kw.get("batch", 1) == 1)
+    expect = 128 if (a_mn or k_major_ok) and (b_mn or k_major_ok or kw.get("broadcast_b")) \
+        else 64
+    assert c.plan["block_k"] == expect and c.plan["cta_pair"] == 2, c.plan
+    assert np.array_equal(c.result(out), c.oracle_full())
+    assert c.untouched_padding(out)
+    one, out1 = _double_k_run(kw, {"DOUBLE_K": 1}, values="ints", seed=903)
+    assert one.plan["block_k"] == 64
+    assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
+
+
+def test_double_k_mn_major_bias_gelu_bf16_matches_one_block():
+    kw = dict(M=1100, N=1304, K=1000, la="row", lb="row", opts={"CTA_PAIR": 3})
+    c, out = _double_k_run(kw, {}, c_dtype="bf16", bias=True, act="gelu_tanh", seed=904)
+    assert c.plan["block_k"] == 64, c.plan        # K-major A with a ragged K: one block
+    kw = dict(kw, K=1024)
+    c, out = _double_k_run(kw, {}, c_dtype="bf16", bias=True, act="gelu_tanh", seed=904)
+    assert c.plan["block_k"] == 128, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+    _, out1 = _double_k_run(kw, {"DOUBLE_K": 1}, c_dtype="bf16", bias=True, act="gelu_tanh",
+                            seed=904)
+    assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
 # ---------------------------------------------------------------- 256 x 512 pair tiles

@@ -62,9 +62,20 @@ def test_headline_plan():
     assert p["swap_ab"] == 0 and p["pack_a"] == 0 and p["pack_b"] == 0
 
 
-def test_one_k_block_per_load_when_asked_or_when_an_operand_is_mn_major(options):
-    assert plan(8192, 8192, 8192, epi=3)["block_k"] == 64          # row-major B
-    assert plan(8192, 8192, 8192, la=1, lb=1, epi=3)["block_k"] == 64  # column-major A
+def test_two_k_blocks_per_load_for_mn_major_operands_too(options):
+    assert plan(8192, 8192, 8192, epi=3)["block_k"] == 128           # row-major B
+    assert plan(8192, 8192, 8192, la=1, lb=1, epi=3)["block_k"] == 128  # column-major A
+    assert plan(8192, 8192, 8192, la=1, epi=3)["block_k"] == 128     # both MN-major
+    # an MN-major operand needs no whole number of K blocks (rows past K read zeros)
+    assert plan(8192, 8192, 8120, la=1, epi=3)["block_k"] == 128
+    # a K-major one does: the two-block view is (64 K, rows, K blocks)
+    assert plan(8192, 8192, 8120, epi=3)["block_k"] == 64            # A row-major
+    # batched: MN-major operands keep their batch dimension; a K-major A must be
+    # broadcast (one matrix) to take the two-block view
+    n = 2048
+    assert plan(n, n, n, la=1, batch=4, sa=n * n, sb=n * n, sc=n * n)["block_k"] == 128
+    assert plan(n, n, n, batch=4, sa=n * n, sb=n * n, sc=n * n)["block_k"] == 64
+    assert plan(n, n, n, batch=4, sa=0, sb=n * n, sc=n * n)["block_k"] == 128
     options(DOUBLE_K=1)
     p = headline()
     assert p["block_k"] == 64 and p["stages"] == 6
@@ -257,7 +268,10 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
             assert p["grid"] % 2 == 0, (p, ctx)
         if p["block_k"] == 128:
             assert (bn, mode) in TWO_K_BLOCKS and form == 1, (p, ctx)
-            assert kw["batch"] == 1 and K % 64 == 0 and p["split_k"] == 1, (p, ctx)
+            # each operand MN-major, or K-major with whole K blocks and one matrix
+            for mn, stride in ((kw["la"] == 1, kw["sa"]), (kw["lb"] == 0, kw["sb"])):
+                assert mn or (K % 64 == 0 and (kw["batch"] == 1 or stride == 0)), (p, ctx)
+            assert p["split_k"] == 1, (p, ctx)
             assert p["stream_k"] == 0, (p, ctx)
         else:
             assert p["block_k"] == 64, (p, ctx)
