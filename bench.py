@@ -46,7 +46,7 @@ WORKLOAD = ("bf16 GEMM M=N=K=8192, A row-major, B column-major, fused bias + GEL
 WORKLOAD_ID = 3  # seeds 3001 (A), 3002 (B), 3004 (bias)
 L2_NOTE = "inputs larger than L2: A + B = 256 MiB and C = 128 MiB vs a 126.5 MiB L2; no flush"
 TC_SOURCES = ["tc_kernel.cuh", "tc_gemm.cu", "tc_gemm_fast.cu", "tc_gemm_general.cu", "ptx.cuh",
-              "epilogue.cuh", "tile_order.h", "internal.h", "tc_gemm_ks2.cu"]
+              "epilogue.cuh", "tile_order.h", "internal.h", "tc_gemm_ks2.cu", "debug_check.cuh"]
 
 
 def parse_args():

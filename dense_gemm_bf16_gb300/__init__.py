@@ -7,16 +7,17 @@ general-stride entry point.  This package is its binding: ``_abi`` mirrors the C
 one to one; ``api.gemm`` is the tensor-level convenience.
 """
 from ._abi import (EXPORTED, STATIC_WORKSPACE_BYTES, DType, Epi, GemmError, Layout, Option, Plan,
-                   Status, build, gemm_batched, gemm_bf16, gemm_bf16_static_workspace,
-                   gemm_check_device_status, gemm_f16, gemm_get_option, gemm_plan_query,
+                   Status, build, debug_lib, gemm_batched, gemm_bf16, gemm_bf16_static_workspace,
+                   gemm_build_flags, gemm_check_device_status, gemm_debug_count_writes,
+                   gemm_f16, gemm_get_option, gemm_plan_query,
                    gemm_set_option, gemm_status_string, gemm_strided, gemm_strided_plan_query,
                    gemm_strided_workspace_size, gemm_tile_order, gemm_workspace_size, lib,
                    library_path, sgemm_f32)
 
 __all__ = [
     "EXPORTED", "STATIC_WORKSPACE_BYTES", "DType", "Epi", "GemmError", "Layout", "Option", "Plan",
-    "Status", "build", "gemm_batched", "gemm_bf16", "gemm_bf16_static_workspace",
-    "gemm_check_device_status", "gemm_f16", "gemm_get_option", "gemm_plan_query",
+    "Status", "build", "debug_lib", "gemm_batched", "gemm_bf16", "gemm_bf16_static_workspace",
+    "gemm_build_flags", "gemm_check_device_status", "gemm_debug_count_writes", "gemm_f16", "gemm_get_option", "gemm_plan_query",
     "gemm_set_option", "gemm_status_string", "gemm_strided", "gemm_strided_plan_query",
     "gemm_strided_workspace_size", "gemm_tile_order", "gemm_workspace_size", "lib", "library_path", "sgemm_f32", "gemm", "plan",
 ]

@@ -14,6 +14,7 @@ from . import _build
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
 
 
 class Status(enum.IntEnum):
@@ -24,6 +25,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = 4
     ERR_TIMEOUT = 5
     ERR_NO_DEVICE = 6
+    ERR_DEVICE_CHECK = 7
 
 
 class Layout(enum.IntEnum):
@@ -68,6 +70,7 @@ class Option(enum.IntEnum):
     BLOCK_N = 13
     DOUBLE_K = 14
     TEST_SIM_SMS = 15
+    TEST_DEBUG_BOUND = 16
 
 
 class Plan(ctypes.Structure):
@@ -123,6 +126,8 @@ _SIGNATURES = {
                          ctypes.POINTER(ctypes.c_int)], None),
     "gemm_bf16_static_workspace": ([_i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp,
                                     _i64, _i32, _i32, _f32, _f32, _vp, _i32, _i32, _vp], _i32),
+    "gemm_build_flags": ([], _i32),
+    "gemm_debug_count_writes": ([_vp, _i64], _i32),
 }
 # size of the library-owned scratch array used by gemm_bf16_static_workspace
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -138,24 +143,39 @@ def build(force: bool = False) -> str:
     return _build.build(force=force)
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(dense_gemm_bf16_gb300.build() or __graft_entry__.build())")
+    L = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
 def lib():
     """The loaded library.  Raises if it has not been built: there is no
     fallback implementation."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB_PATH
-            if not os.path.exists(path):
-                raise RuntimeError(
-                    f"{path} is missing: build the CUDA library first "
-                    "(dense_gemm_bf16_gb300.build() or __graft_entry__.build())")
-            L = ctypes.CDLL(path)
-            for name, (args, res) in _SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.argtypes = args
-                fn.restype = res
-            _lib = L
+            _lib = _load(_build.LIB_PATH)
     return _lib
+
+
+def debug_lib():
+    """The debug build (libdgemm_gb300_debug.so: the same entry points, with
+    device-side checks and the count-writes mode), as a ctypes library whose
+    functions take the C arguments directly.  It keeps its own device state
+    (status word, options) apart from lib()'s."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _load(_build.DEBUG_LIB_PATH)
+    return _debug_lib
 
 
 def gemm_bf16(M, N, K, A, lda, la, B, ldb, lb, C, ldc, lc, c_dtype, alpha, beta, bias, epi,
@@ -239,6 +259,14 @@ def gemm_strided_plan_query(ab_dtype, batch, M, N, K, A, a_rs, a_cs, stride_a, B
                                        beta, bias, epi, split_k, workspace_bytes,
                                        ctypes.byref(plan))
     return st, plan
+
+
+def gemm_build_flags() -> int:
+    return lib().gemm_build_flags()
+
+
+def gemm_debug_count_writes(counts, count_elems) -> int:
+    return lib().gemm_debug_count_writes(counts, count_elems)
 
 
 def gemm_set_option(option, value) -> int:

@@ -81,21 +81,63 @@ __device__ __forceinline__ void store_elem(void* p, int dt, float x) {
 
 __device__ __forceinline__ int dt_size(int dt) { return dt == DT_F32 ? 4 : 2; }
 
+// Element offset of C(b, i, j) from C.
+__device__ __forceinline__ int64_t c_off(const Epilogue& e, int64_t b, int64_t i, int64_t j) {
+    return b * e.stride_c + (e.c_row_major ? i * e.ldc + j : j * e.ldc + i);
+}
+
 // Address of C(b, i, j).
 __device__ __forceinline__ char* c_addr(const Epilogue& e, int64_t b, int64_t i, int64_t j) {
-    const int64_t off = b * e.stride_c + (e.c_row_major ? i * e.ldc + j : j * e.ldc + i);
-    return reinterpret_cast<char*>(e.C) + off * dt_size(e.c_dtype);
+    return reinterpret_cast<char*>(e.C) + c_off(e, b, i, j) * dt_size(e.c_dtype);
+}
+
+// Debug build: elements [off, off + n) of C lie inside the span the call may
+// touch (always true in the product build).
+__device__ __forceinline__ bool c_span_ok(const Epilogue& e, int64_t off, int64_t n = 1) {
+#if DG_DEBUG
+    return DG_CHECK(off >= 0 && off + n <= e.dbg_c_elems, e.dbg_status, STATUS_CHECK_BOUNDS);
+#else
+    (void)e, (void)off, (void)n;
+    return true;
+#endif
+}
+
+// Debug build: entry k of the bias exists.
+__device__ __forceinline__ bool bias_ok(const Epilogue& e, int64_t k) {
+#if DG_DEBUG
+    return DG_CHECK(k >= 0 && k < e.dbg_bias_len, e.dbg_status, STATUS_CHECK_BOUNDS);
+#else
+    (void)e, (void)k;
+    return true;
+#endif
+}
+
+// Debug build, count-writes mode: one more write of the final value of
+// C(b, i, j) (computed-problem coordinates; transposed back for swap-AB).
+__device__ __forceinline__ void count_write(const Epilogue& e, int64_t b, int64_t i, int64_t j) {
+#if DG_DEBUG
+    if (e.dbg_counts) {
+        const int64_t ci = e.dbg_swap ? j : i, cj = e.dbg_swap ? i : j;
+        if (DG_CHECK(ci >= 0 && ci < e.dbg_m && cj >= 0 && cj < e.dbg_n, e.dbg_status,
+                     STATUS_CHECK_BOUNDS))
+            atomicAdd(e.dbg_counts + (b * e.dbg_m + ci) * e.dbg_n + cj, 1u);
+    }
+#else
+    (void)e, (void)b, (void)i, (void)j;
+#endif
 }
 
 // One element: acc is the fp32 accumulator value of C(b, i, j).
 __device__ __forceinline__ void epilogue_store(const Epilogue& e, int64_t b, int64_t i, int64_t j,
                                                float acc) {
+    if (!c_span_ok(e, c_off(e, b, i, j))) return;
     char* c = c_addr(e, b, i, j);
     float x = e.alpha * acc;
     if (e.beta != 0.0f) x = fmaf(e.beta, load_elem(c, e.c_dtype), x);
-    if (e.bias) x += e.bias_on_rows ? e.bias[i] : e.bias[j];
+    if (e.bias && bias_ok(e, e.bias_on_rows ? i : j)) x += e.bias_on_rows ? e.bias[i] : e.bias[j];
     x = apply_act(x, e.act);
     store_elem(c, e.c_dtype, x);
+    count_write(e, b, i, j);
 }
 
 // Four outputs C(b, i, j .. j + 3), j a multiple of 4: one vector access of C
@@ -110,7 +152,11 @@ __device__ __forceinline__ void epilogue_store4(const Epilogue& e, int64_t b, in
             if (j + c < N) epilogue_store(e, b, i, j + c, v[c]);
         return;
     }
+    if (!c_span_ok(e, c_off(e, b, i, j), 4)) return;
     char* c = c_addr(e, b, i, j);
+    if (!DG_CHECK(reinterpret_cast<uintptr_t>(c) % (4 * dt_size(e.c_dtype)) == 0, e.dbg_status,
+                  STATUS_CHECK_ALIGN))
+        return;
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] *= e.alpha;
     if (e.beta != 0.0f) {
@@ -135,7 +181,7 @@ __device__ __forceinline__ void epilogue_store4(const Epilogue& e, int64_t b, in
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[k] = fmaf(e.beta, o[k], v[k]);
     }
-    if (e.bias) {
+    if (e.bias && bias_ok(e, e.bias_on_rows ? i : j + 3)) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[k] += e.bias_on_rows ? e.bias[i] : e.bias[j + k];
     }
@@ -156,6 +202,8 @@ __device__ __forceinline__ void epilogue_store4(const Epilogue& e, int64_t b, in
         }
         *reinterpret_cast<uint2*>(c) = make_uint2(w[0], w[1]);
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) count_write(e, b, i, j + k);
 }
 
 }  // namespace dg

@@ -37,6 +37,10 @@ std::atomic<int64_t> g_opt_split_reduce{0};
 std::atomic<int64_t> g_opt_block_n{0};
 std::atomic<int64_t> g_opt_double_k{0};
 std::atomic<int64_t> g_opt_test_sim_sms{0};
+std::atomic<int64_t> g_opt_test_debug_bound{0};
+// count-writes mode of the debug build: counter array and its length
+std::atomic<uint32_t*> g_dbg_counts{nullptr};
+std::atomic<int64_t> g_dbg_count_elems{0};
 // stream-K flag values: one fresh 64-bit value per launch (stale or garbage
 // workspace contents never equal it)
 std::atomic<unsigned long long> g_sk_epoch{0x9E3779B97F4A7C15ull ^
@@ -540,7 +544,9 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         }
     }
     // Two K blocks per TMA load (KS = 2) for a CTA-pair plan with the
-    // TMA-store-only epilogue, whole units only (no stream-K or split pieces).
+    // TMA-store-only epilogue: whole units, or the split form of stream-K
+    // (its pieces then start and end on whole two-block steps; the contiguous
+    // form's ranges do not, and explicit split-K slices are not cut that way).
     // A K-major operand is seen as (64 K, rows, K blocks), so K must be a whole
     // number of 64-deep blocks (an odd count reads its last block's partner
     // past the end: zeros) and the operand one matrix (one batch entry, or a
@@ -550,7 +556,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         return o.mn || (c.K % TC_BLOCK_K == 0 && (c.batch == 1 || o.stride == 0));
     };
     if (g_opt_double_k.load() == 0 && pl.kernel == 1 && pl.fast_epi && pl.splits == 1 &&
-        pl.sk == 0 && tc_has_ks2(pl.bn, pl.mode, 1) && ks2_ok(pl.a) && ks2_ok(pl.b)) {
+        pl.sk != 1 && tc_has_ks2(pl.bn, pl.mode, 1) && ks2_ok(pl.a) && ks2_ok(pl.b)) {
         pl.ks = 2;
         pl.stages = tc_stages_ks2(pl.bn);
     }
@@ -583,6 +589,28 @@ Epilogue make_epilogue(const Call& c, bool row_major, bool bias_on_rows) {
     e.bias_on_rows = (bias_on_rows != epi_row_bias(c.epi)) ? 1 : 0;
     e.act = epi_act(c.epi);
     return e;
+}
+
+// Debug build: the bounds the device-side checks use for the output side of
+// a call (C's span, the bias length, the count-writes array), and whether the
+// count array is large enough.  A no-op returning GEMM_OK in the product build.
+gemm_status_t debug_epilogue(Epilogue& e, const Call& c, bool swap, int* status) {
+#if DG_DEBUG
+    const int64_t inner = c.lc == GEMM_ROW_MAJOR ? c.N : c.M;
+    const int64_t outer = c.lc == GEMM_ROW_MAJOR ? c.M : c.N;
+    e.dbg_status = status;
+    e.dbg_c_elems = (c.batch > 1 ? (c.batch - 1) * c.sc : 0) + (outer - 1) * c.ldc + inner;
+    e.dbg_bias_len = epi_bias(c.epi) ? (epi_row_bias(c.epi) ? c.M : c.N) : 0;
+    e.dbg_counts = g_dbg_counts.load();
+    e.dbg_m = c.M;
+    e.dbg_n = c.N;
+    e.dbg_swap = swap ? 1 : 0;
+    if (e.dbg_counts && c.batch * c.M * c.N > g_dbg_count_elems.load())
+        return GEMM_ERR_INVALID_ARG;
+#else
+    (void)e, (void)c, (void)swap, (void)status;
+#endif
+    return GEMM_OK;
 }
 
 gemm_status_t encode_operand(CUtensorMap* map, int ab, const Operand& o, const void* ptr,
@@ -668,7 +696,9 @@ gemm_status_t run(const Call& c) {
     if (st != GEMM_OK) return st;
 
     if (pl.kernel == 3) {
-        const Epilogue e = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
+        Epilogue e = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
+        st = debug_epilogue(e, c, false, d->status);
+        if (st != GEMM_OK) return st;
         return splitk_epilogue_launch(nullptr, 0, c.batch, c.M, c.N, e, c.stream) == cudaSuccess
                    ? GEMM_OK
                    : GEMM_ERR_CUDA;
@@ -699,6 +729,8 @@ gemm_status_t run(const Call& c) {
         p.num_pid_n = static_cast<int32_t>(cdiv(c.N, p.kernel == 0 ? 64 : 128));
         p.group_m = pl.group_m;
         p.epi = make_epilogue(c, c.lc == GEMM_ROW_MAJOR, false);
+        st = debug_epilogue(p.epi, c, false, d->status);
+        if (st != GEMM_OK) return st;
         return sgemm_launch(p, c.stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
@@ -754,6 +786,8 @@ gemm_status_t run(const Call& c) {
     p.idesc = make_idesc_f16(c.ab == DT_BF16, pl.a.mn, pl.b.mn, pl.mode == 2 ? 2 * TC_BLOCK_M : TC_BLOCK_M,
                              sub_n);
     p.epi = make_epilogue(c, pl.c_row_major_c, pl.swap);
+    st = debug_epilogue(p.epi, c, pl.swap, d->status);
+    if (st != GEMM_OK) return st;
     p.partials = pl.splits > 1 ? reinterpret_cast<float*>(ws + pl.part_off) : nullptr;
     const bool want_fast = pl.fast_epi || pl.beta_epi;  // 128-byte boxes
     int epi_form = 0;
@@ -800,6 +834,15 @@ gemm_status_t run(const Call& c) {
             cudaMemsetAsync(p.sk_flags, 0, pl.sk_flags_bytes, c.stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
     }
+#if DG_DEBUG
+    p.dbg_sk_slots = pl.sk ? static_cast<int64_t>(pl.sk_bytes / (TC_BLOCK_M * pl.bn * 4)) : 0;
+    p.dbg_partials_elems = pl.splits > 1 ? static_cast<int64_t>(pl.part_bytes / 4) : 0;
+    p.dbg_num_pid_n = p.num_pid_n;
+    // test only: one bound set too small, so that a check fails (buffers untouched)
+    const int64_t plant = g_opt_test_debug_bound.exchange(0);
+    if (plant == 1) p.epi.dbg_c_elems /= 2;
+    if (plant == 2) p.dbg_num_pid_n -= 1;
+#endif
     if (tc_launch(pl.bn, pl.mode, epi_form, pl.ks, p, pl.grid, c.stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (pl.splits > 1) {
@@ -946,6 +989,7 @@ const char* gemm_status_string(gemm_status_t s) {
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
         case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE";
+        case GEMM_ERR_DEVICE_CHECK: return "GEMM_ERR_DEVICE_CHECK";
     }
     return "GEMM_ERR_UNKNOWN";
 }
@@ -965,9 +1009,24 @@ gemm_status_t gemm_check_device_status(gemm_stream_t stream) {
         const int zero = 0;
         if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        return GEMM_ERR_TIMEOUT;
+        // bits 8 and up: a failed device-side check (debug build); bit 0: a wait expired
+        return (v & ~0xFF) ? GEMM_ERR_DEVICE_CHECK : GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;
+}
+
+int32_t gemm_build_flags(void) { return DG_DEBUG ? 1 : 0; }
+
+gemm_status_t gemm_debug_count_writes(uint32_t* counts, int64_t count_elems) {
+#if DG_DEBUG
+    if (counts != nullptr && count_elems <= 0) return GEMM_ERR_INVALID_ARG;
+    g_dbg_count_elems.store(counts ? count_elems : 0);
+    g_dbg_counts.store(counts);
+    return GEMM_OK;
+#else
+    (void)counts, (void)count_elems;
+    return GEMM_ERR_UNSUPPORTED;
+#endif
 }
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, int64_t N,
@@ -1077,6 +1136,11 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 4096) return GEMM_ERR_INVALID_ARG;
             g_opt_test_sim_sms.store(value);
             return GEMM_OK;
+        case GEMM_OPT_TEST_DEBUG_BOUND:
+            if (!DG_DEBUG) return GEMM_ERR_UNSUPPORTED;
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            g_opt_test_debug_bound.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -1098,6 +1162,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_BLOCK_N: return g_opt_block_n.load();
         case GEMM_OPT_DOUBLE_K: return g_opt_double_k.load();
         case GEMM_OPT_TEST_SIM_SMS: return g_opt_test_sim_sms.load();
+        case GEMM_OPT_TEST_DEBUG_BOUND: return g_opt_test_debug_bound.load();
     }
     return -1;
 }

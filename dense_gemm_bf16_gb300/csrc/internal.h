@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "debug_check.cuh"
+
 namespace dg {
 
 enum : int { DT_BF16 = 0, DT_F16 = 1, DT_F32 = 2 };
@@ -29,6 +31,15 @@ struct Epilogue {
     const float* bias;       // may be null
     int32_t bias_on_rows;    // 1: bias indexed by row i (swapped problem), 0: by column j
     int32_t act;             // ACT_NONE / ACT_GELU_TANH / ACT_RELU / ACT_GELU_ERF
+#if DG_DEBUG
+    // debug build only: the bounds the device-side checks hold accesses to
+    int* dbg_status;         // device status word
+    int64_t dbg_c_elems;     // C element offsets [0, dbg_c_elems) from C may be touched
+    int64_t dbg_bias_len;    // entries of bias
+    uint32_t* dbg_counts;    // count-writes mode: [batch][M][N] of the caller's C, or null
+    int64_t dbg_m, dbg_n;    // the caller's M and N
+    int32_t dbg_swap;        // 1: the computed problem is the caller's transposed
+#endif
 };
 
 // Parameters of the persistent tcgen05 kernel (passed as a __grid_constant__).
@@ -76,6 +87,12 @@ struct TcParams {
     float* sk_partials;      // [slot][cta rank][128][BN] fp32, lane-interleaved per warp
     unsigned long long* sk_flags;  // [slot][cta rank][epilogue warp]: epoch when published
     unsigned long long sk_epoch;   // this launch's flag value
+#if DG_DEBUG
+    // debug build only: the bounds of the workspace areas and of the tile grid
+    int64_t dbg_sk_slots;        // stream-K partial slots the workspace holds (x CTAs per cluster)
+    int64_t dbg_partials_elems;  // fp32 elements of the split-K partials
+    int32_t dbg_num_pid_n;       // tile columns a work unit may name
+#endif
 };
 
 // Host-side launchers (defined in tc_gemm.cu / sgemm.cu / aux_kernels.cu).

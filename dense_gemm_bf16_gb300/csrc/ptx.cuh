@@ -8,6 +8,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "debug_check.cuh"
+
 namespace dg {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,7 +67,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
-                if (status) atomicExch(status, 1);
+                if (status) DG_SET_TIMEOUT(status);
                 return false;
             }
         }

@@ -122,6 +122,7 @@ __device__ __forceinline__ void sgemm_store(const SgemmParams& p, int b, int m0,
         for (int h = 0; h < 2; ++h) {
             const int n = n0 + h * 64 + tx * 4;
             if (e.c_row_major && e.c_vec_ok && n + 3 < p.N) {
+                if (!c_span_ok(e, c_off(e, b, m, n), 4)) continue;
                 float v[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = e.alpha * acc[i][4 * h + j];
@@ -133,7 +134,7 @@ __device__ __forceinline__ void sgemm_store(const SgemmParams& p, int b, int m0,
                     v[2] = fmaf(e.beta, o.z, v[2]);
                     v[3] = fmaf(e.beta, o.w, v[3]);
                 }
-                if (e.bias) {
+                if (e.bias && bias_ok(e, e.bias_on_rows ? m : n + 3)) {
                     if (e.bias_on_rows) {
                         const float br = e.bias[m];
 #pragma unroll
@@ -145,6 +146,8 @@ __device__ __forceinline__ void sgemm_store(const SgemmParams& p, int b, int m0,
                 }
                 act_inplace<4>(v, e.act);
                 *c = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) count_write(e, b, m, n + j);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -448,6 +451,7 @@ __global__ void __launch_bounds__(NT, (RrCfg<NT, BK, STAGES>::MIN_BLOCKS))
             const int n = n0 + 4 * NTX * g + tx * 4;
             const float* ag = acc[i] + 4 * g;
             if (e.c_row_major && e.c_vec_ok && n + 3 < p.N) {
+                if (!c_span_ok(e, c_off(e, b, m, n), 4)) continue;
                 float v[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = e.alpha * ag[j];
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(NT, (RrCfg<NT, BK, STAGES>::MIN_BLOCKS))
                     v[2] = fmaf(e.beta, o4.z, v[2]);
                     v[3] = fmaf(e.beta, o4.w, v[3]);
                 }
-                if (e.bias) {
+                if (e.bias && bias_ok(e, e.bias_on_rows ? m : n + 3)) {
                     if (e.bias_on_rows) {
                         const float br = e.bias[m];
 #pragma unroll
@@ -471,6 +475,8 @@ __global__ void __launch_bounds__(NT, (RrCfg<NT, BK, STAGES>::MIN_BLOCKS))
                 }
                 act_inplace<4>(v, e.act);
                 *c = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) count_write(e, b, m, n + j);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)

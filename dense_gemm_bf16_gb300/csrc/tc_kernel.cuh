@@ -163,9 +163,12 @@ __device__ __forceinline__ WorkIter work_begin(const TcParams& p, int cta0, int 
     return s;
 }
 
-template <int CM>
-__device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int ncta, uint32_t rank,
-                                          Unit& w) {
+// KS: K blocks per pipeline step; the split form's pieces start and end on
+// whole steps (the last may end at an odd kblocks: its last step reads a
+// partner block past the end of K, which loads zeros).
+template <int CM, int KS = 1>
+__device__ __forceinline__ bool work_next_raw(const TcParams& p, WorkIter& s, int ncta,
+                                              uint32_t rank, Unit& w) {
     if (s.rr_left > 0) {
         w = decode_unit<CM>(p, s.unit_rr, rank);
         w.kind = UNIT_FULL;
@@ -174,14 +177,16 @@ __device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int nc
         return true;
     }
     if (s.piece >= 0) {
-        // split form: piece j of last-wave tile t covers K blocks
-        // [j * kblocks / S, (j + 1) * kblocks / S); piece 0 finishes the tile
+        // split form: piece j of last-wave tile t covers the steps of KS K
+        // blocks [j * steps / S, (j + 1) * steps / S); piece 0 finishes the tile
         const int S = p.sk_split;
         const int j = s.piece / p.sk_tiles;
         const int t = s.piece - j * p.sk_tiles;
+        const int64_t steps = (p.kblocks + KS - 1) / KS;
         w = decode_unit<CM>(p, p.dp_units + t, rank);
-        w.kb0 = static_cast<int>(static_cast<int64_t>(j) * p.kblocks / S);
-        w.kb1 = static_cast<int>(static_cast<int64_t>(j + 1) * p.kblocks / S);
+        w.kb0 = KS * static_cast<int>(static_cast<int64_t>(j) * steps / S);
+        const int kb1 = KS * static_cast<int>(static_cast<int64_t>(j + 1) * steps / S);
+        w.kb1 = kb1 < p.kblocks ? kb1 : p.kblocks;
         if (p.sk_spread) {
             w.kind = UNIT_SPREAD;
             w.slot = t * S + j;
@@ -210,6 +215,42 @@ __device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int nc
     w.nslots = 1;
     s.it = lim;
     return true;
+}
+
+// Debug build: the decoded unit lies inside the problem (batch entry, K
+// slice, tile row and column, K blocks) and the stream-K slots it publishes
+// into or reads from inside the workspace's slots.
+template <int CM>
+__device__ __forceinline__ bool unit_ok(const TcParams& p, const Unit& w) {
+#if DG_DEBUG
+    bool ok = w.b >= 0 && w.b < p.batch && w.split >= 0 && w.split < p.splits && w.pid_m >= 0 &&
+              w.pid_m < p.num_pid_m * CM && w.pid_n >= 0 && w.pid_n < p.dbg_num_pid_n &&
+              w.kb0 >= 0 && w.kb0 < w.kb1 && w.kb1 <= p.kblocks;
+    if (w.kind != UNIT_FULL) {
+        const int64_t lo = w.kind == UNIT_SPREAD ? w.slot - w.piece : w.slot;
+        const int64_t hi = w.kind == UNIT_TAIL ? w.slot + 1 : lo + w.nslots;
+        ok = ok && lo >= 0 && hi * CM <= p.dbg_sk_slots;
+    }
+    return DG_CHECK(ok, p.status, STATUS_CHECK_UNIT);
+#else
+    (void)p, (void)w;
+    return true;
+#endif
+}
+
+// The next work item of this cluster.  The debug build skips (and reports)
+// a unit that fails unit_ok; every role of the CTA decodes the same units, so
+// all of them skip it together.
+template <int CM, int KS = 1>
+__device__ __forceinline__ bool work_next(const TcParams& p, WorkIter& s, int ncta, uint32_t rank,
+                                          Unit& w) {
+#if DG_DEBUG
+    while (work_next_raw<CM, KS>(p, s, ncta, rank, w))
+        if (unit_ok<CM>(p, w)) return true;
+    return false;
+#else
+    return work_next_raw<CM, KS>(p, s, ncta, rank, w);
+#endif
 }
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* ptr, unsigned long long v) {
@@ -290,6 +331,12 @@ __device__ __forceinline__ void finish_run(const Epilogue& e, float (&v)[H], con
     act_inplace<H>(v, e.act);
 }
 
+// Debug build: the element at ptr lies inside C's span.
+template <typename T>
+__device__ __forceinline__ bool c_ptr_ok(const Epilogue& e, const T* ptr) {
+    return c_span_ok(e, ptr - static_cast<const T*>(e.C));
+}
+
 // Row-major C: lane t owns column col0 + t of the warp's 32 rows, read from
 // the staging tile.  All beta*C loads of a half-chunk are issued before any
 // store (C is read and written in place, so the compiler may not reorder a
@@ -306,7 +353,8 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
     const int64_t ldc = e.ldc;
     const bool has_c = e.beta != 0.0f;
     const bool has_bias = e.bias != nullptr;
-    const float bias_col = (has_bias && !e.bias_on_rows && col_ok) ? e.bias[col] : 0.0f;
+    const float bias_col =
+        (has_bias && !e.bias_on_rows && col_ok && bias_ok(e, col)) ? e.bias[col] : 0.0f;
     T* const c0 =
         static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c + row_base * ldc + col;
     if constexpr (CH == 32) {
@@ -327,7 +375,8 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
                 if (has_bias) {
                     if (e.bias_on_rows) {
 #pragma unroll
-                        for (int i = 0; i < H; ++i) v[i] += e.bias[row_base + h + i];
+                        for (int i = 0; i < H; ++i)
+                            if (bias_ok(e, row_base + h + i)) v[i] += e.bias[row_base + h + i];
                     } else {
 #pragma unroll
                         for (int i = 0; i < H; ++i) v[i] += bias_col;
@@ -335,7 +384,11 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
                 }
                 act_inplace<H>(v, e.act);
 #pragma unroll
-                for (int i = 0; i < H; ++i, o += ldc) st_f(o, v[i]);
+                for (int i = 0; i < H; ++i, o += ldc) {
+                    if (!c_ptr_ok(e, o)) continue;
+                    st_f(o, v[i]);
+                    count_write(e, w.b, row_base + h + i, col);
+                }
             }
             return;
         }
@@ -347,20 +400,24 @@ __device__ __forceinline__ void rows_out(const Epilogue& e, const Unit& w, int M
 #pragma unroll
         for (int i = 0; i < H; ++i, q += ldc) {
             const bool ok = h + i < nrows && col_ok;
-            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
+            cv[i] = (has_c && ok && c_ptr_ok(e, q)) ? ld_f(q) : 0.0f;
             v[i] = stage[(h + i) * STAGE_LD + lane];
             bv[i] = bias_col;
         }
         if (has_bias && e.bias_on_rows) {
 #pragma unroll
             for (int i = 0; i < H; ++i)
-                bv[i] = h + i < nrows ? e.bias[row_base + h + i] : 0.0f;
+                bv[i] = h + i < nrows && bias_ok(e, row_base + h + i) ? e.bias[row_base + h + i]
+                                                                       : 0.0f;
         }
         finish_run<H>(e, v, cv, bv, has_c, has_bias);
         T* o = c0 + h * ldc;
 #pragma unroll
         for (int i = 0; i < H; ++i, o += ldc)
-            if (h + i < nrows && col_ok) st_f(o, v[i]);
+            if (h + i < nrows && col_ok && c_ptr_ok(e, o)) {
+                st_f(o, v[i]);
+                count_write(e, w.b, row_base + h + i, col);
+            }
     }
 }
 
@@ -378,7 +435,7 @@ __device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M
     const int64_t ldc = e.ldc;
     const bool has_c = e.beta != 0.0f;
     const bool has_bias = e.bias != nullptr;
-    const float bias_row = (has_bias && e.bias_on_rows) ? e.bias[row] : 0.0f;
+    const float bias_row = (has_bias && e.bias_on_rows && bias_ok(e, row)) ? e.bias[row] : 0.0f;
     T* const c0 = static_cast<T*>(e.C) + static_cast<int64_t>(w.b) * e.stride_c +
                   static_cast<int64_t>(col0) * ldc + row;
 #pragma unroll
@@ -388,19 +445,23 @@ __device__ __forceinline__ void cols_out(const Epilogue& e, const Unit& w, int M
 #pragma unroll
         for (int i = 0; i < H; ++i, q += ldc) {
             const bool ok = h + i < ncols;
-            cv[i] = (has_c && ok) ? ld_f(q) : 0.0f;
+            cv[i] = (has_c && ok && c_ptr_ok(e, q)) ? ld_f(q) : 0.0f;
             v[i] = __uint_as_float(r[h + i]);
             bv[i] = bias_row;
         }
         if (has_bias && !e.bias_on_rows) {
 #pragma unroll
-            for (int i = 0; i < H; ++i) bv[i] = h + i < ncols ? e.bias[col0 + h + i] : 0.0f;
+            for (int i = 0; i < H; ++i)
+                bv[i] = h + i < ncols && bias_ok(e, col0 + h + i) ? e.bias[col0 + h + i] : 0.0f;
         }
         finish_run<H>(e, v, cv, bv, has_c, has_bias);
         T* o = c0 + h * ldc;
 #pragma unroll
         for (int i = 0; i < H; ++i, o += ldc)
-            if (h + i < ncols) st_f(o, v[i]);
+            if (h + i < ncols && c_ptr_ok(e, o)) {
+                st_f(o, v[i]);
+                count_write(e, w.b, row, col0 + h + i);
+            }
     }
 }
 
@@ -411,6 +472,17 @@ __device__ __forceinline__ void load_pair(const CUtensorMap* map, uint32_t dst, 
         tma_load_3d_pair(dst, map, bar, x, y, z, pol);
     else
         tma_load_2d_pair(dst, map, bar, x, y, pol);
+}
+
+// Debug build: element `at` of the split-K partials exists.
+__device__ __forceinline__ bool partial_ok(const TcParams& p, const float* at) {
+#if DG_DEBUG
+    const int64_t k = at - p.partials;
+    return DG_CHECK(k >= 0 && k < p.dbg_partials_elems, p.status, STATUS_CHECK_BOUNDS);
+#else
+    (void)p, (void)at;
+    return true;
+#endif
 }
 
 // Epilogue of one CH-column chunk of this warp's 32 rows.  On entry lane t
@@ -429,9 +501,10 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w,
             const int64_t row = row_base + lane;
             if (row >= p.M) return;
 #pragma unroll
-            for (int c = 0; c < CH; ++c)
-                if (col0 + c < p.N)
-                    P[static_cast<int64_t>(col0 + c) * p.M + row] = __uint_as_float(r[c]);
+            for (int c = 0; c < CH; ++c) {
+                float* at = P + static_cast<int64_t>(col0 + c) * p.M + row;
+                if (col0 + c < p.N && partial_ok(p, at)) *at = __uint_as_float(r[c]);
+            }
             return;
         }
 #pragma unroll
@@ -442,7 +515,8 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w,
 #pragma unroll 8
             for (int rr = 0; rr < 32; ++rr) {
                 const int64_t row = row_base + rr;
-                if (row < p.M) P[row * p.N + col] = stage[rr * STAGE_LD + lane];
+                if (row < p.M && partial_ok(p, P + row * p.N + col))
+                    P[row * p.N + col] = stage[rr * STAGE_LD + lane];
             }
         }
         __syncwarp();
@@ -560,7 +634,7 @@ __device__ __forceinline__ bool spread_reduce(const TcParams& p, int b, int pid_
     if (static_cast<uint64_t>(bytes) * S > gather_cap) {
         // (cannot happen: every tile width's stage memory holds a whole tile
         // plus one float4 per piece)
-        if (lane == 0 && p.status) atomicExch(p.status, 1);
+        if (lane == 0 && p.status) DG_SET_TIMEOUT(p.status);
         return false;
     }
     bool issued = false;
@@ -592,7 +666,7 @@ __device__ __forceinline__ bool spread_reduce(const TcParams& p, int b, int pid_
             if (lane == 0 && (it & 15u) == 0 &&
                 (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns)) {
                 *abort_flag = 1;
-                if (p.status) atomicExch(p.status, 1);
+                if (p.status) DG_SET_TIMEOUT(p.status);
                 give_up = 1;
             }
             if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
@@ -640,6 +714,32 @@ __device__ __forceinline__ bool spread_reduce(const TcParams& p, int b, int pid_
     return true;
 }
 
+// Debug build: a TMA box store or load of the output starts at a column, row
+// and depth inside it (the unit clips the far edges, but a store must never
+// start at a negative coordinate).
+__device__ __forceinline__ bool out_box_ok(const TcParams& p, int x, int y, int z) {
+#if DG_DEBUG
+    const int depth = p.partials ? p.splits * p.batch : p.batch;
+    return DG_CHECK(x >= 0 && x < p.N && y >= 0 && z >= 0 && z < depth, p.status,
+                    STATUS_CHECK_BOUNDS);
+#else
+    (void)p, (void)x, (void)y, (void)z;
+    return true;
+#endif
+}
+
+// Debug build, count-writes mode: the final values of row `row`, columns
+// col0 .. col0 + ncols - 1 (those inside the output) were written.
+__device__ __forceinline__ void count_row(const TcParams& p, int b, int64_t row, int col0,
+                                          int ncols) {
+#if DG_DEBUG
+    if (p.epi.dbg_counts && !p.partials && row < p.M)
+        for (int c = 0; c < ncols && col0 + c < p.N; ++c) count_write(p.epi, b, row, col0 + c);
+#else
+    (void)p, (void)b, (void)row, (void)col0, (void)ncols;
+#endif
+}
+
 // TMA-store epilogue of one tile for this warp's 32 rows.  The tile is cut
 // into chunks of 32 columns.  Per chunk, lane t turns row t's accumulators
 // into output values (alpha, beta*C, bias, GELU, one rounding; or raw fp32
@@ -672,6 +772,15 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
                : nullptr;
     // beta*C of this thread's row segment for one chunk, as raw output words
     auto load_c = [&](int col0, uint32_t (&craw)[NW]) {
+        const int64_t off = static_cast<int64_t>(w.b) * e.stride_c + row * e.ldc + col0;
+        const int n = p.N - col0 < EB ? p.N - col0 : EB;
+        if (!c_span_ok(e, off, n) ||
+            !DG_CHECK(col0 + EB > p.N || (reinterpret_cast<uintptr_t>(crow + col0 * ES) & 15) == 0,
+                      e.dbg_status, STATUS_CHECK_ALIGN)) {
+#pragma unroll
+            for (int i = 0; i < NW; ++i) craw[i] = 0u;
+            return;
+        }
         if (col0 + EB <= p.N) {
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
@@ -741,16 +850,18 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
             }
             if (e.bias) {
                 if (e.bias_on_rows) {
-                    const float bias_row = row_ok ? e.bias[row] : 0.0f;
+                    const float bias_row = row_ok && bias_ok(e, row) ? e.bias[row] : 0.0f;
 #pragma unroll
                     for (int i = 0; i < EB; ++i) v[i] += bias_row;
                 } else if (full) {
+                    if (bias_ok(e, col0 + EB - 1)) {
 #pragma unroll
-                    for (int i = 0; i < EB; ++i) v[i] += __ldg(e.bias + col0 + i);
+                        for (int i = 0; i < EB; ++i) v[i] += __ldg(e.bias + col0 + i);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < EB; ++i)
-                        if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
+                        if (col0 + i < p.N && bias_ok(e, col0 + i)) v[i] += __ldg(e.bias + col0 + i);
                 }
             }
             act_inplace<EB>(v, e.act);
@@ -777,12 +888,15 @@ __device__ __forceinline__ void tile_out_tma(const TcParams& p, const Unit& w, i
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (p.c_tma_3d)
-                tma_store_3d(&p.tmap_c, smem_u32(box), col0, row0, zc, pol);
-            else
-                tma_store_2d(&p.tmap_c, smem_u32(box), col0, row0, pol);
+            if (out_box_ok(p, col0, row0, zc)) {
+                if (p.c_tma_3d)
+                    tma_store_3d(&p.tmap_c, smem_u32(box), col0, row0, zc, pol);
+                else
+                    tma_store_2d(&p.tmap_c, smem_u32(box), col0, row0, pol);
+            }
             bulk_commit_group();
         }
+        count_row(p, w.b, row, col0, EB);
         ++nbox;
     }
 }
@@ -922,16 +1036,18 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
             }
             if (e.bias) {
                 if (e.bias_on_rows) {
-                    const float bias_row = row_ok ? e.bias[row] : 0.0f;
+                    const float bias_row = row_ok && bias_ok(e, row) ? e.bias[row] : 0.0f;
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] += bias_row;
                 } else if (full) {
+                    if (bias_ok(e, col0 + 64 - 1)) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] += __ldg(e.bias + col0 + i);
+                        for (int i = 0; i < 64; ++i) v[i] += __ldg(e.bias + col0 + i);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
-                        if (col0 + i < p.N) v[i] += __ldg(e.bias + col0 + i);
+                        if (col0 + i < p.N && bias_ok(e, col0 + i)) v[i] += __ldg(e.bias + col0 + i);
                 }
             }
             act_inplace<64>(v, e.act);
@@ -974,6 +1090,7 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
                 const int bc = col0 + k * BOXC;
                 if (bc >= p.N) break;
                 const uint32_t box = smem_u32(wbuf + (NB == 2 ? k : (nbox & 1u)) * EPI_BOX_BYTES);
+                if (!out_box_ok(p, bc, row0, zc)) continue;
                 if (p.c_tma_3d)
                     tma_store_3d(&p.tmap_c, box, bc, row0, zc, pol);
                 else
@@ -981,6 +1098,7 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
             }
             bulk_commit_group();
         }
+        count_row(p, w.b, row, col0, 64);
         ++nbox;
     }
     return true;
@@ -1049,6 +1167,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         if (warp == 5) asm volatile("" ::"l"(p.sk_epoch));
     }
 
+    // Debug build: the stage ring sits on 1024-byte boundaries (the 128-byte
+    // swizzle atoms) and the barriers on 8-byte ones (recorded only: the
+    // layout is fixed at compile time).
+    if (threadIdx.x == 0)
+        (void)DG_CHECK((sA0 & 1023u) == 0 && (sB0 & 1023u) == 0 && (bar0 & 7u) == 0 &&
+                           (smem_u32(epi_smem) & 1023u) == 0,
+                       p.status, STATUS_CHECK_ALIGN);
+
     if (threadIdx.x == 0) {
         // MODE 2: the leader's stage barrier collects the bytes of both CTAs'
         // loads; its accumulator-release barrier counts the epilogue warps of
@@ -1101,7 +1227,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             bool ok = true;
             WorkIter wi = work_begin(p, cta0, ncta);
             Unit w;
-            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
+            while (ok && work_next<CM, KS>(p, wi, ncta, rank, w)) {
                 for (int kb = w.kb0; kb < w.kb1; kb += KS) {
                     if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.status,
                                    p.timeout_ns)) {
@@ -1226,7 +1352,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const uint32_t b_lbo = b_mn ? kAtomCol : 16u;
             WorkIter wi = work_begin(p, cta0, ncta);
             Unit w;
-            while (ok && work_next<CM>(p, wi, ncta, rank, w)) {
+            while (ok && work_next<CM, KS>(p, wi, ncta, rank, w)) {
                 if (!mbar_wait(tempty0 + 8u * abuf, aphase ^ 1u, abort_flag, p.status,
                                p.timeout_ns)) {
                     ok = false;
@@ -1302,7 +1428,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
         bool first = true;
-        while (work_next<CM>(p, wi, ncta, rank, w)) {
+        while (work_next<CM, KS>(p, wi, ncta, rank, w)) {
             if constexpr (EPI == 2) {
                 // the first two C boxes of a tile this warp will write, requested
                 // before its accumulator is waited for
@@ -1318,7 +1444,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 first = false;
                 WorkIter peek = wi;
                 Unit wn;
-                if (work_next<CM>(p, peek, ncta, rank, wn))
+                if (work_next<CM, KS>(p, peek, ncta, rank, wn))
                     prefetch_c_tile<BN>(p, wn, static_cast<int64_t>(wn.pid_m) * BM + q * 32 + lane);
             }
             int ok = 1;
@@ -1375,7 +1501,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                 if ((it & 15u) == 0) {
                                     if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
                                         *abort_flag = 1;
-                                        if (p.status) atomicExch(p.status, 1);
+                                        if (p.status) DG_SET_TIMEOUT(p.status);
                                         got = 0;
                                         break;
                                     }
@@ -1446,7 +1572,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 WorkIter sw = work_begin(p, cta0, ncta);
                 sw.rr_left = 0;
                 Unit u;
-                if (sw.piece >= 0 && work_next<CM>(p, sw, ncta, rank, u))
+                if (sw.piece >= 0 && work_next<CM, KS>(p, sw, ncta, rank, u))
                     spread_reduce<BN, CM>(p, u.b, u.pid_m, u.pid_n, u.slot - u.piece, u.piece,
                                           u.nslots, rank, q, lane, abort_flag, sA0,
                                           reinterpret_cast<const float4*>(smem),
@@ -1470,13 +1596,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     }
 }
 
-// A launch whose pieces all wait for one another (the spread split form) is
-// cooperative: the CUDA runtime then runs every CTA of the grid at once, or
-// refuses the launch, instead of leaving a waiting CTA without its peers.
+// A launch in which CTAs wait for partials that other CTAs publish (every
+// stream-K form: the finishing piece of a tile waits for the others; in the
+// spread form every piece waits for every other one) is cooperative: the CUDA
+// runtime then starts every CTA of the grid together, or refuses the launch,
+// so a waiting CTA never holds an SM that one of its publishers needs, even
+// when another kernel (a second GEMM on another stream) occupies the rest of
+// the GPU.  The bounded waits remain as a second line of defence.
 template <int BN, int MODE, int EPI, int KS = 1>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     constexpr int CM = Cfg<BN, MODE, EPI, KS>::CM;
-    if (CM == 1 && !p.sk_spread) {
+    const bool waits = p.sk_spread || p.sk_split > 0 || p.sk_iters > 0;
+    if (CM == 1 && !waits) {
         tc_gemm_kernel<BN, MODE, EPI, KS><<<grid, TC_THREADS, Cfg<BN, MODE, EPI, KS>::SMEM, stream>>>(p);
         return cudaGetLastError();
     }
@@ -1494,7 +1625,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
-    if (p.sk_spread) {
+    if (waits) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
         ++n;

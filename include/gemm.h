@@ -106,7 +106,9 @@ typedef enum {
     GEMM_ERR_WORKSPACE = 3,    /* workspace smaller than the plan needs                                   */
     GEMM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, attribute, tensor map)      */
     GEMM_ERR_TIMEOUT = 5,      /* a kernel gave up a bounded wait (reported by gemm_check_device_status) */
-    GEMM_ERR_NO_DEVICE = 6     /* no usable sm_103 device is current                                      */
+    GEMM_ERR_NO_DEVICE = 6,    /* no usable sm_103 device is current                                      */
+    GEMM_ERR_DEVICE_CHECK = 7  /* debug build only: a device-side check failed and its access was skipped
+                                  (reported by gemm_check_device_status)                                  */
 } gemm_status_t;
 
 /*
@@ -244,10 +246,42 @@ const char* gemm_status_string(gemm_status_t status);
 /*
  * gemm_check_device_status -- synchronises `stream`, then reads and clears the
  * current device's error word, which a kernel sets when one of its bounded
- * waits expires.  Returns GEMM_ERR_TIMEOUT if it was set, GEMM_ERR_CUDA if the
- * synchronisation failed, else GEMM_OK.  For tests and debugging; it blocks.
+ * waits expires (or, in the debug build, when a device-side check fails).
+ * Returns GEMM_ERR_DEVICE_CHECK if a check failed, else GEMM_ERR_TIMEOUT if a
+ * wait expired, GEMM_ERR_CUDA if the synchronisation failed, else GEMM_OK.
+ * For tests and debugging; it blocks.
  */
 gemm_status_t gemm_check_device_status(gemm_stream_t stream);
+
+/*
+ * Debug build (libdgemm_gb300_debug.so: the same sources and entry points
+ * compiled with device-side checks; the pages have no counterpart, this is an
+ * interface of this library only).  Its kernels check, before each access,
+ * that global addresses lie inside the buffers the call described (C's span,
+ * the bias, the split-K partials, the stream-K slots and flags), that TMA
+ * store boxes start inside the output, that every decoded work unit lies
+ * inside the problem, and that shared-memory stages are aligned.  A failed
+ * check sets a bit of the device status word and skips the access (no trap,
+ * no assert); gemm_check_device_status then returns GEMM_ERR_DEVICE_CHECK.
+ *
+ * gemm_build_flags -- bit 0 set in the debug build, 0 in the product library.
+ */
+int32_t gemm_build_flags(void);
+
+/*
+ * gemm_debug_count_writes -- count-writes mode of the debug build.  With a
+ * non-NULL `counts` (device memory of count_elems uint32 values, zeroed by
+ * the caller), every later GEMM call of this process adds one to
+ * counts[(b * M + i) * N + j] each time it writes the final value of C(b, i, j)
+ * (the caller's batch entry, row and column, whatever C's layout), so that a
+ * correct call leaves exactly 1 in each of its batch * M * N counters.  Split-K
+ * partials and stream-K partial tiles are not final values and are not
+ * counted; gemm_strided's scatter of a dense result is not counted either.
+ * Calls whose batch * M * N exceeds count_elems return GEMM_ERR_INVALID_ARG
+ * while the mode is on.  NULL turns the mode off.  The caller owns `counts`.
+ * Returns GEMM_ERR_UNSUPPORTED in the product library.
+ */
+gemm_status_t gemm_debug_count_writes(uint32_t* counts, int64_t count_elems);
 
 /*
  * Plan inspection (no launch): fills *plan with the kernel choice that
@@ -362,10 +396,12 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
  *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes
  *                         at least 64).
- *   GEMM_OPT_DOUBLE_K     0 (default): CTA-pair plans with K-major A and B, K a multiple
- *                         of 64, one batch entry, whole tiles and the TMA-store-only
- *                         epilogue bring two 64-deep K blocks of each operand per TMA
- *                         load (plan block_k 128); 1: one K block per load always.
+ *   GEMM_OPT_DOUBLE_K     0 (default): CTA-pair plans with the TMA-store-only epilogue,
+ *                         whole tiles or split-form stream-K pieces, bring two 64-deep
+ *                         K blocks of each operand per TMA load (plan block_k 128); a
+ *                         K-major operand then needs K a multiple of 64 and one matrix
+ *                         (one batch entry or a broadcast), an MN-major one nothing
+ *                         more; 1: one K block per load always.
  *   GEMM_OPT_TEST_SIM_SMS test only: n > 0 makes gemm_plan_query and
  *                         gemm_workspace_size plan for a simulated sm_103 device of n
  *                         SMs whose CTA pairs of every tile width fit n / 2 at once,
@@ -379,6 +415,13 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         leave its partial unpublished, so the waits of the
  *                         pieces that need it expire instead.  The knob resets
  *                         itself after that launch.
+ *   GEMM_OPT_TEST_DEBUG_BOUND  debug build, test only: the next tensor-core launch
+ *                         gets one bound of its device-side checks set too small
+ *                         (the buffers themselves are untouched), so that a check
+ *                         fails and its access is skipped: 1 C's span is halved; 2
+ *                         the last tile column counts as outside the problem.
+ *                         Resets itself after that launch.  The product library
+ *                         refuses it (GEMM_ERR_UNSUPPORTED).
  */
 typedef enum {
     GEMM_OPT_GROUP_M = 1,
@@ -395,7 +438,8 @@ typedef enum {
     GEMM_OPT_SPLIT_REDUCE = 12,
     GEMM_OPT_BLOCK_N = 13,
     GEMM_OPT_DOUBLE_K = 14,
-    GEMM_OPT_TEST_SIM_SMS = 15
+    GEMM_OPT_TEST_SIM_SMS = 15,
+    GEMM_OPT_TEST_DEBUG_BOUND = 16
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -116,10 +116,15 @@ class Case:
         return oracle.gemm_sampled(self.problem(), b, i, j)
 
     # ------------------------------------------------------------------ GPU
-    def run_gpu(self, stream=None, workspace=None):
-        """Runs through the C ABI; returns (status, C storage after the call)."""
+    def run_gpu(self, stream=None, workspace=None, L=None):
+        """Runs through the C ABI; returns (status, C storage after the call).
+        L: a loaded library (ctypes) to call instead of the product one, e.g.
+        the debug build."""
+        import ctypes
+
         import torch
         import dense_gemm_bf16_gb300 as dg
+        L = L or dg.lib()
 
         def up(flat):
             t = torch.from_numpy(flat.copy())
@@ -138,13 +143,14 @@ class Case:
                 DT_CODE[self.c_dtype], self.alpha, self.beta,
                 dbias.data_ptr() if dbias is not None else None, epi, self.split_k]
         if workspace is None:
-            st, plan = dg.gemm_plan_query(*args, 1 << 62)
+            plan = dg.Plan()
+            st = L.gemm_plan_query(*args, 1 << 62, ctypes.byref(plan))
             self.plan = plan.as_dict()
             need = int(plan.workspace_bytes) if st == 0 else 0
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
-        st = dg.gemm_batched(*args, workspace.data_ptr(), workspace.numel(), stream)
+        st = L.gemm_batched(*args, workspace.data_ptr(), workspace.numel(), stream)
         torch.cuda.synchronize()
         out = dC.cpu().numpy()
         return st, out

@@ -271,3 +271,20 @@ def test_every_compute_entry_reports_no_device_without_a_gpu(lib):
     st, _ = dg.gemm_plan_query(DType.BF16, 1, 4, 4, 4, 16, 4, 0, 0, 16, 4, 0, 0, 16, 4, 0, 0,
                                DType.F32, 1.0, 0.0, None, 0, 0, 0)
     assert st == nd
+
+
+def test_debug_build_exports_the_same_entry_points_and_reports_itself():
+    """libdgemm_gb300_debug.so (device-side checks, count-writes mode) has the
+    same C interface; only it takes the debug-only option and count mode."""
+    import dense_gemm_bf16_gb300 as dg
+    D = dg.debug_lib()
+    for name in dg.EXPORTED:
+        assert hasattr(D, name), name
+    assert dg.gemm_build_flags() == 0 and D.gemm_build_flags() == 1
+    assert dg.gemm_set_option(dg.Option.TEST_DEBUG_BOUND, 1) == dg.Status.ERR_UNSUPPORTED
+    assert dg.gemm_debug_count_writes(None, 0) == dg.Status.ERR_UNSUPPORTED
+    assert D.gemm_set_option(int(dg.Option.TEST_DEBUG_BOUND), 3) == dg.Status.ERR_INVALID_ARG
+    assert D.gemm_set_option(int(dg.Option.TEST_DEBUG_BOUND), 0) == dg.Status.OK
+    assert D.gemm_debug_count_writes(1 << 24, 0) == dg.Status.ERR_INVALID_ARG
+    assert D.gemm_debug_count_writes(None, 0) == dg.Status.OK
+    assert D.gemm_status_string(7) == b"GEMM_ERR_DEVICE_CHECK"

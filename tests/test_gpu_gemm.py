@@ -798,6 +798,41 @@ def test_double_k_mn_major_bias_gelu_bf16_matches_one_block():
     assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
+# The split form on CTA pairs with two K blocks per load: pieces start and end
+# on whole two-block steps (an odd count of K blocks ends with a step whose
+# partner block lies past K).  4 CTA pairs, 9 units of 256 x 256: a last wave of
+# one unit cut into 4 pieces.
+SK_TWO_BLOCK_CASES = {
+    "k_major_odd_blocks": dict(la="row", lb="col", K=1088),      # 17 blocks
+    "mn_major_ragged_k": dict(la="col", lb="row", K=1000),       # 16 blocks, last one 40 deep
+    "rr_odd_blocks": dict(la="row", lb="row", K=704),            # 11 blocks
+}
+
+
+@pytest.mark.parametrize("name", sorted(SK_TWO_BLOCK_CASES))
+def test_exact_stream_k_split_pieces_two_k_blocks(name):
+    kw = dict(SK_TWO_BLOCK_CASES[name])
+    K = kw.pop("K")
+    opts = {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}
+    c, out = _double_k_run(dict(M=700, N=600, K=K, opts=opts, **kw), {}, values="ints",
+                           seed=905)
+    assert c.plan["stream_k"] == 2 and c.plan["block_k"] == 128, c.plan
+    assert np.array_equal(c.result(out), c.oracle_full())
+    assert c.untouched_padding(out)
+    one, out1 = _double_k_run(dict(M=700, N=600, K=K, opts=opts, **kw), {"DOUBLE_K": 1},
+                              values="ints", seed=905)
+    assert one.plan["stream_k"] == 2 and one.plan["block_k"] == 64, one.plan
+    assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
+
+
+def test_stream_k_split_two_k_blocks_bias_gelu():
+    opts = {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}
+    c, out = _double_k_run(dict(M=700, N=600, K=1024, opts=opts), {}, c_dtype="bf16",
+                           bias=True, act="gelu_tanh", seed=906)
+    assert c.plan["stream_k"] == 2 and c.plan["block_k"] == 128, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+
+
 # ---------------------------------------------------------------- 256 x 512 pair tiles
 
 @pytest.fixture

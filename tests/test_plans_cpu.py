@@ -129,9 +129,14 @@ def test_flat_row_keeps_single_cta_tiles():
     assert p["cta_pair"] == 0 and p["block_n"] == 256 and p["fast_epilogue"] == 1
 
 
-def test_stream_k_needs_a_workspace_and_then_loads_one_k_block():
+def test_stream_k_needs_a_workspace_and_keeps_two_k_blocks_in_the_split_form(options):
     p = plan(2560, 2560, 16384, lb=1, ws=UNLIMITED)
-    assert p["stream_k"] == 2 and p["block_k"] == 64
+    assert p["stream_k"] == 2 and p["block_k"] == 128
+    # the headline with a workspace: split-form pieces on whole two-block steps
+    assert headline(ws=UNLIMITED)["block_k"] == 128
+    options(STREAM_K=2)           # the contiguous form's ranges: one block per load
+    p = plan(2560, 2560, 16384, lb=1, ws=UNLIMITED)
+    assert p["stream_k"] == 1 and p["block_k"] == 64
     p0 = plan(2560, 2560, 16384, lb=1)
     assert p0["stream_k"] == 0 and p0["block_k"] == 128
 
@@ -272,7 +277,7 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
             for mn, stride in ((kw["la"] == 1, kw["sa"]), (kw["lb"] == 0, kw["sb"])):
                 assert mn or (K % 64 == 0 and (kw["batch"] == 1 or stride == 0)), (p, ctx)
             assert p["split_k"] == 1, (p, ctx)
-            assert p["stream_k"] == 0, (p, ctx)
+            assert p["stream_k"] in (0, 2), (p, ctx)    # never the contiguous form
         else:
             assert p["block_k"] == 64, (p, ctx)
         if form == 2:
