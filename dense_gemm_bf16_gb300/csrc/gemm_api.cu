@@ -200,6 +200,7 @@ struct Plan {
     bool spread = false;     // ... with every piece reducing a share of its tile
     int dp_per_cluster = 0, sk_split = 0, sk_tiles = 0;
     int64_t dp_units = 0, sk_iters = 0;
+    int64_t sk_units = 0;    // contiguous form: units cut along K (sk_iters counts their steps)
     size_t sk_off = 0, sk_bytes = 0, sk_flags_off = 0, sk_flags_bytes = 0;
     int64_t kblocks = 0, tiles = 0, units = 0;
     Operand a{}, b{};
@@ -365,7 +366,8 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         if (pl.units > 0 && s_in > ctas / pl.units) s_in = static_cast<int>(ctas / pl.units);
         if (s_in > pl.kblocks / 4) s_in = static_cast<int>(pl.kblocks / 4);
         const int64_t want_spread = g_opt_split_reduce.load();
-        const bool spread = want_spread == 2 || (want_spread == 0 && s_auto > kMaxInKernel);
+        const bool spread =
+            want_spread == 2 || ((want_spread == 0 || want_spread == 3) && s_auto > kMaxInKernel);
         if (g_opt_stream_k.load() != 1 && s_auto >= 2 && s_in >= 2 &&
             (spread || s_auto <= kMaxInKernel)) {
             const size_t nslots = static_cast<size_t>(pl.units) * (spread ? s_in : s_in - 1);
@@ -447,7 +449,35 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     // (both forced whenever a partial last wave follows at least one full wave).
     const int64_t want_sk = g_opt_stream_k.load();
     const int64_t P = pl.grid / pl.cm;
-    if (pl.inkernel_split > 0) {
+    auto sk_need = [&](size_t nslots) {
+        return static_cast<size_t>(round_up(static_cast<int64_t>(nslots * TC_BLOCK_M * pl.bn * 4), 256)) +
+               static_cast<size_t>(round_up(static_cast<int64_t>(nslots * 4 * 8), 256));
+    };
+    if (pl.inkernel_split > 0 && !pl.spread && g_opt_split_reduce.load() != 3 && pl.units > 0 &&
+        ctas / pl.units <= 4 && ctas > pl.units && off + sk_need(ctas) <= c.ws_bytes) {
+        // the automatic split-K above, in one kernel, balanced over every CTA:
+        // the contiguous form with no whole units first, each CTA taking an
+        // equal range of the units' K steps.  A unit then spans a few CTAs
+        // (at most ceil(ctas / units) + 1); the one holding its first step adds
+        // the others' partials.  (GEMM_OPT_SPLIT_REDUCE = 3 keeps equal
+        // pieces, one CTA each, on inkernel_split * units CTAs instead.)
+        const size_t nslots = static_cast<size_t>(ctas);
+        const size_t slots = nslots * TC_BLOCK_M * pl.bn * 4;
+        const size_t flags = nslots * 4 * 8;
+        pl.sk = 1;
+        pl.inkernel_split = 0;
+        pl.dp_per_cluster = 0;
+        pl.dp_units = 0;
+        pl.sk_units = pl.units;
+        pl.sk_off = off;
+        pl.sk_bytes = slots;
+        pl.sk_flags_off = off + static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256));
+        pl.sk_flags_bytes = flags;
+        off += static_cast<size_t>(round_up(static_cast<int64_t>(slots), 256)) +
+               static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
+        pl.ws_need = off;
+        pl.grid = ctas;
+    } else if (pl.inkernel_split > 0) {
         // the automatic split-K above, in one kernel: no whole units first, every
         // unit cut into inkernel_split pieces, one CTA each
         const int64_t S = pl.inkernel_split, r = pl.units;
@@ -510,7 +540,7 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
                 if (form == 1) {
                     pl.dp_per_cluster = static_cast<int>(W - 1);
                     pl.dp_units = (W - 1) * P;
-                    pl.sk_iters = (pl.units - pl.dp_units) * pl.kblocks;
+                    pl.sk_units = pl.units - pl.dp_units;
                 } else {
                     pl.dp_per_cluster = static_cast<int>(W);
                     pl.dp_units = W * P;
@@ -543,10 +573,11 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
             if (pl.beta_epi) pl.stages = tc_stages_beta(pl.bn, pl.mode);
         }
     }
-    // Two K blocks per TMA load (KS = 2) for a CTA-pair plan with the
-    // TMA-store-only epilogue: whole units, or the split form of stream-K
-    // (its pieces then start and end on whole two-block steps; the contiguous
-    // form's ranges do not, and explicit split-K slices are not cut that way).
+    // Two K blocks per TMA load (KS = 2) wherever the kernel is compiled that
+    // way (tc_has_ks2: CTA pairs with the TMA-store-only epilogue; single CTAs
+    // with it or with the general epilogue, for at least 8 K blocks): whole
+    // units and stream-K pieces alike, whose boundaries then fall on whole
+    // two-block steps; explicit split-K slices are not cut that way.
     // A K-major operand is seen as (64 K, rows, K blocks), so K must be a whole
     // number of 64-deep blocks (an odd count reads its last block's partner
     // past the end: zeros) and the operand one matrix (one batch entry, or a
@@ -555,11 +586,15 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     auto ks2_ok = [&](const Operand& o) {
         return o.mn || (c.K % TC_BLOCK_K == 0 && (c.batch == 1 || o.stride == 0));
     };
-    if (g_opt_double_k.load() == 0 && pl.kernel == 1 && pl.fast_epi && pl.splits == 1 &&
-        pl.sk != 1 && tc_has_ks2(pl.bn, pl.mode, 1) && ks2_ok(pl.a) && ks2_ok(pl.b)) {
+    const int epi_form = pl.beta_epi ? 2 : (pl.fast_epi ? 1 : 0);
+    if (g_opt_double_k.load() == 0 && pl.kernel == 1 && pl.splits == 1 &&
+        tc_has_ks2(pl.bn, pl.mode, epi_form) && (pl.mode == 2 || pl.kblocks >= 8) &&
+        ks2_ok(pl.a) && ks2_ok(pl.b)) {
         pl.ks = 2;
-        pl.stages = tc_stages_ks2(pl.bn);
+        pl.stages = tc_stages_ks2(pl.bn, pl.mode, epi_form);
     }
+    // the contiguous form's iterations are steps of ks K blocks
+    if (pl.sk == 1) pl.sk_iters = pl.sk_units * cdiv(pl.kblocks, pl.ks);
     // the tensor-core kernel counts work units and tiles in 32-bit integers
     if (pl.kernel == 1 && (pl.units > 0x7FFFFFFF / (pl.splits > 0 ? pl.splits : 1) ||
                            pl.tiles > 0x7FFFFFFF))
@@ -1119,7 +1154,7 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             g_opt_wide_tile.store(value);
             return GEMM_OK;
         case GEMM_OPT_SPLIT_REDUCE:
-            if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return GEMM_ERR_INVALID_ARG;
             g_opt_split_reduce.store(value);
             return GEMM_OK;
         case GEMM_OPT_BLOCK_N:

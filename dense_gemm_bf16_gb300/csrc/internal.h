@@ -67,10 +67,11 @@ struct TcParams {
     int32_t l2_hints;        // operand L2 policy: 0 normal; 1 A evict-first, B evict-last; 2 the reverse
     // Stream-K.  Every cluster first takes dp_per_cluster whole units round
     // robin; the units from dp_units on are then cut along K, in one of two forms.
-    // Contiguous (sk_iters > 0): their K blocks are split evenly over the
-    // clusters, each taking one contiguous range; a unit cut at a cluster
-    // boundary is finished by the cluster that holds its first K blocks, after
-    // the next cluster has left its fp32 partial in the slot of that boundary.
+    // Contiguous (sk_iters > 0): their steps (of KS K blocks) are split evenly
+    // over the clusters, each taking one contiguous range; a unit cut at
+    // cluster boundaries is finished by the cluster that holds its first step,
+    // after each later cluster holding part of it has left its fp32 partial in
+    // that cluster's own slot.
     // Split (sk_split > 0): each of the sk_tiles last units is cut into sk_split
     // equal K pieces, one per cluster, so that all pieces start together; piece 0
     // finishes the tile after the other sk_split - 1 have left their partials.
@@ -80,7 +81,7 @@ struct TcParams {
     // waits for every other one).
     int32_t dp_per_cluster;
     int32_t dp_units;
-    int64_t sk_iters;        // K blocks of the contiguous form (0: off)
+    int64_t sk_iters;        // steps (of KS K blocks) of the contiguous form (0: off)
     int32_t sk_split;        // pieces per unit of the split form (0: off)
     int32_t sk_tiles;        // units cut in the split form
     int32_t sk_spread;       // split form: 1 every piece reduces a share of the tile
@@ -103,9 +104,9 @@ struct TcParams {
 // (tc_has_fast tells the tile widths that have it); 2 the same with beta * C
 // read by TMA loads through tmap_c, for a 16-bit C (tc_has_beta_form tells the
 // tile widths and modes, tc_stages_beta its pipeline depth).  ks: 64-deep K
-// blocks per stage and per TMA load of a K-major operand, 1 or 2 (tc_has_ks2
-// tells where 2 exists; its operand maps are the three-dimensional views
-// 64 K x rows x K blocks).
+// blocks per stage and per TMA load of each operand, 1 or 2 (tc_has_ks2
+// tells where 2 exists; a K-major operand's map is then the three-dimensional
+// view 64 K x rows x K blocks, an MN-major one's takes boxes of 128 K rows).
 int tc_stages_for(int block_n, int mode);
 bool tc_has_mode(int block_n, int mode);
 bool tc_has_fast(int block_n);
@@ -115,7 +116,7 @@ cudaError_t tc_prepare(int block_n);   // sets the dynamic shared memory attribu
 cudaError_t tc_launch(int block_n, int mode, int epi, int ks, const TcParams& p, int grid,
                       cudaStream_t stream);
 bool tc_has_ks2(int block_n, int mode, int epi);
-int tc_stages_ks2(int block_n);
+int tc_stages_ks2(int block_n, int mode, int epi);
 int tc_max_pairs(int block_n, int mode);  // two-CTA clusters resident at once on this device
 
 struct SgemmParams {

@@ -12,7 +12,8 @@ cudaError_t tc_launch_general(int bn, int mode, const TcParams& p, int grid, cud
 cudaError_t tc_launch_fast(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t tc_prepare_beta(int bn);
 cudaError_t tc_prepare_ks2(int bn);
-cudaError_t tc_launch_ks2(int bn, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc_launch_ks2(int bn, int mode, int epi, const TcParams& p, int grid,
+                          cudaStream_t stream);
 cudaError_t tc_launch_beta(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
 
 int tc_stages_for(int bn, int mode) {
@@ -54,7 +55,7 @@ cudaError_t tc_launch(int bn, int mode, int epi, int ks, const TcParams& p, int 
                       cudaStream_t stream) {
     if (ks == 2) {
         if (!tc_has_ks2(bn, mode, epi)) return cudaErrorInvalidValue;
-        return tc_launch_ks2(bn, p, grid, stream);
+        return tc_launch_ks2(bn, mode, epi, p, grid, stream);
     }
     if (epi == 1 && tc_has_fast(bn)) return tc_launch_fast(bn, mode, p, grid, stream);
     if (epi == 2 && tc_has_beta_form(bn, mode)) return tc_launch_beta(bn, mode, p, grid, stream);

@@ -201,18 +201,33 @@ __device__ __forceinline__ bool work_next_raw(const TcParams& p, WorkIter& s, in
         return true;
     }
     if (s.it >= s.end) return false;
-    const int64_t kb_unit = p.kblocks;
-    const int64_t u_off = s.it / kb_unit;
-    const int kb0 = static_cast<int>(s.it - u_off * kb_unit);
-    int64_t lim = (u_off + 1) * kb_unit;
+    // contiguous form: the iterations are steps of KS K blocks, steps_u per unit
+    const int64_t steps_u = (p.kblocks + KS - 1) / KS;
+    const int64_t u_off = s.it / steps_u;
+    const int st0 = static_cast<int>(s.it - u_off * steps_u);
+    int64_t lim = (u_off + 1) * steps_u;
     if (lim > s.end) lim = s.end;
     w = decode_unit<CM>(p, static_cast<int>(p.dp_units + u_off), rank);
-    w.kb0 = kb0;
-    w.kb1 = kb0 + static_cast<int>(lim - s.it);
-    w.kind = (kb0 == 0 && w.kb1 == p.kblocks) ? UNIT_FULL : (kb0 == 0 ? UNIT_HEAD : UNIT_TAIL);
-    // contiguous form: the partial crosses the boundary before this cluster
-    w.slot = w.kind == UNIT_TAIL ? s.cluster - 1 : s.cluster;
-    w.nslots = 1;
+    w.kb0 = st0 * KS;
+    const int kb1 = (st0 + static_cast<int>(lim - s.it)) * KS;
+    w.kb1 = kb1 < p.kblocks ? kb1 : p.kblocks;
+    w.kind = (w.kb0 == 0 && w.kb1 == p.kblocks) ? UNIT_FULL : (w.kb0 == 0 ? UNIT_HEAD : UNIT_TAIL);
+    // A cluster's range starts with at most one piece that continues a unit
+    // (a TAIL, published into the cluster's own slot) and ends with at most
+    // one that another cluster continues (a HEAD).  The HEAD adds the
+    // partials of the clusters that hold the rest of its unit, in order: the
+    // next cluster through the one holding the unit's last step.
+    if (w.kind == UNIT_TAIL) {
+        w.slot = s.cluster;
+        w.nslots = 1;
+    } else if (w.kind == UNIT_HEAD) {
+        const int64_t last = (u_off + 1) * steps_u - 1;  // the unit's last step
+        int64_t c = last * ncta / p.sk_iters;             // first guess of its cluster
+        while (c + 1 < ncta && p.sk_iters * (c + 1) / ncta <= last) ++c;
+        while (c > 0 && p.sk_iters * c / ncta > last) --c;
+        w.slot = s.cluster + 1;
+        w.nslots = static_cast<int>(c) - s.cluster;
+    }
     s.it = lim;
     return true;
 }
@@ -229,7 +244,7 @@ __device__ __forceinline__ bool unit_ok(const TcParams& p, const Unit& w) {
     if (w.kind != UNIT_FULL) {
         const int64_t lo = w.kind == UNIT_SPREAD ? w.slot - w.piece : w.slot;
         const int64_t hi = w.kind == UNIT_TAIL ? w.slot + 1 : lo + w.nslots;
-        ok = ok && lo >= 0 && hi * CM <= p.dbg_sk_slots;
+        ok = ok && lo >= 0 && hi * CM <= p.dbg_sk_slots && (w.kind != UNIT_HEAD || w.nslots >= 1);
     }
     return DG_CHECK(ok, p.status, STATUS_CHECK_UNIT);
 #else
@@ -1283,7 +1298,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             }
                         }
                     } else if (!p.a_mn) {
-                        load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
+                        if constexpr (KS == 2)  // K blocks kb and kb + 1 (past the end: zeros)
+                            tma_load_3d(a_dst, &p.tmap_a, fb, 0, w.pid_m * BM, kb, pol_a);
+                        else
+                            load_tile(&p.tmap_a, a_dst, fb, k0, w.pid_m * BM, w.b, p.a_3d, pol_a);
                     } else {
 #pragma unroll
                         for (int h = 0; h < BM / 64; ++h)
@@ -1292,7 +1310,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                     if constexpr (MODE == 0) {
                         if (!p.b_mn) {
-                            load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol_b);
+                            if constexpr (KS == 2)
+                                tma_load_3d(b_dst, &p.tmap_b, fb, 0, w.pid_n * BN, kb, pol_b);
+                            else
+                                load_tile(&p.tmap_b, b_dst, fb, k0, w.pid_n * BN, w.b, p.b_3d, pol_b);
                         } else {
                             if constexpr (BN >= 64) {
 #pragma unroll

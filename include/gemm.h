@@ -385,14 +385,18 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         measured slower than 256 x 256 on bf16 8192^3); 2 whenever
  *                         pair MMA runs with 256-wide tiles and N >= 512.
  *   GEMM_OPT_SPLIT_REDUCE how an automatic split-K (split_k = 0, no whole wave of
- *                         tiles) runs in one kernel: 0 (default) up to 4 K pieces per
- *                         tile, piece 0 adds the others' fp32 partials (plan stream_k
- *                         2); more pieces each publish a partial and, once all have,
- *                         reduce one equal share of the tile (plan stream_k 3, a
- *                         cooperative launch); 1 the serial form up to 4 pieces and
- *                         the two-pass form (split_k > 1, a second launch) beyond;
- *                         2 the spread form for any number of pieces.  Both
- *                         one-kernel forms need the workspace of gemm_workspace_size.
+ *                         tiles) runs in one kernel: 0 (default) with up to 4 K pieces
+ *                         per tile, the K steps of all tiles are dealt to every CTA
+ *                         in equal contiguous ranges and the piece holding a tile's
+ *                         first step adds the others' fp32 partials (plan stream_k 1);
+ *                         with more pieces each publishes a partial and, once all
+ *                         have, reduces one equal share of the tile (plan stream_k 3);
+ *                         1 the serial form up to 4 pieces and the two-pass form
+ *                         (split_k > 1, a second launch) beyond; 2 the spread form for
+ *                         any number of pieces; 3 as 0, but up to 4 pieces as equal K
+ *                         pieces, one CTA each (plan stream_k 2).  The one-kernel
+ *                         forms are cooperative launches and need the workspace of
+ *                         gemm_workspace_size.
  *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
  *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes
  *                         at least 64).

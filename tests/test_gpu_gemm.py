@@ -439,7 +439,9 @@ BETA_FORM_CASES = {
     "f16_row_bias_relu": dict(ab="f16", M=300, N=520, K=200, bias=True, row_bias=True,
                               act="relu"),
     "batched": dict(ab="bf16", M=200, N=264, K=130, batch=3, bias=True, act="gelu_erf"),
-    "inkernel_split_head": dict(ab="bf16", M=1024, N=640, K=4096, bias=True),
+    "inkernel_split_head": dict(ab="bf16", M=1024, N=640, K=4096, bias=True,
+                                opts={"SPLIT_REDUCE": 3}),
+    "balanced_contiguous_head": dict(ab="bf16", M=1024, N=640, K=4096, bias=True),
 }
 
 
@@ -468,6 +470,8 @@ def test_beta_epilogue_matches_general(name):
         assert c.plan["block_n"] == opts["BLOCK_N"], c.plan
     if name == "inkernel_split_head":
         assert c.plan["stream_k"] == 2, c.plan
+    if name == "balanced_contiguous_head":
+        assert c.plan["stream_k"] == 1, c.plan
     check_close(c, c.result(out), c.oracle_full())
     assert c.untouched_padding(out)
     g, out_g = run({"FAST_EPILOGUE": 1})
@@ -547,7 +551,7 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
     args = [0, 1, M, N, K, 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0, 2, 1.0, 0.0,
             None, 0, 0]
     st, big = dg.gemm_plan_query(*args, 1 << 40)
-    assert st == 0 and (big.split_k > 1 or big.stream_k in (2, 3))
+    assert st == 0 and (big.split_k > 1 or big.stream_k in (1, 2, 3))
     st, exact = dg.gemm_plan_query(*args, int(big.workspace_bytes))
     assert st == 0
     assert (exact.split_k, exact.stream_k, exact.grid) == (big.split_k, big.stream_k, big.grid)
@@ -556,21 +560,36 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
 
 # ---------------------------------------------------------------- automatic split-K in one kernel
 
-# An automatic split of 2-4 pieces per unit, with a CTA for every piece, runs
-# as the split form of stream-K (plan: split_k 1, stream_k 2, no reduction
-# launch); GEMM_OPT_STREAM_K = 1 falls back to the two-pass split-K.
+# An automatic split of 2-4 pieces per unit runs in one kernel (plan split_k 1,
+# no reduction launch): by default balanced over every CTA as the contiguous
+# form of stream-K (plan stream_k 1), or with GEMM_OPT_SPLIT_REDUCE = 3 as equal
+# pieces, one CTA each (the split form, stream_k 2); GEMM_OPT_STREAM_K = 1
+# falls back to the two-pass split-K.
 INKERNEL_CASES = {
     "skinny_swap": dict(M=16, N=8192, K=4096),
     "three_pieces": dict(M=1024, N=640, K=4096),
 }
+INKERNEL_FORMS = {"balanced": ({}, 1), "equal_pieces": ({"SPLIT_REDUCE": 3}, 2)}
+
+
+@pytest.fixture(params=sorted(INKERNEL_FORMS))
+def inkernel_form(request):
+    import dense_gemm_bf16_gb300 as dg
+    opts, form = INKERNEL_FORMS[request.param]
+    for k, v in opts.items():
+        dg.gemm_set_option(dg.Option[k], v)
+    yield form
+    for k in opts:
+        dg.gemm_set_option(dg.Option[k], 0)
 
 
 @pytest.mark.parametrize("name", sorted(INKERNEL_CASES))
-def test_exact_inkernel_split(name):
+def test_exact_inkernel_split(name, inkernel_form):
     import dense_gemm_bf16_gb300 as dg
     kw = INKERNEL_CASES[name]
     c = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
-    assert c.plan["stream_k"] == 2 and c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
+    assert c.plan["stream_k"] == inkernel_form and c.plan["split_k"] == 1, c.plan
+    assert c.plan["launches"] == 1, c.plan
     dg.gemm_set_option(dg.Option.STREAM_K, 1)
     try:
         c2 = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
@@ -579,17 +598,17 @@ def test_exact_inkernel_split(name):
     assert c2.plan["stream_k"] == 0 and c2.plan["split_k"] > 1
 
 
-def test_inkernel_split_epilogue_and_beta():
+def test_inkernel_split_epilogue_and_beta(inkernel_form):
     c = run_close(Case("bf16", 1024, 640, 4096, c_dtype="bf16", alpha=0.5, beta=0.75, bias=True,
                        act="gelu_tanh", seed=502))
-    assert c.plan["stream_k"] == 2
+    assert c.plan["stream_k"] == inkernel_form
 
 
-def test_inkernel_split_unaligned_c():
+def test_inkernel_split_unaligned_c(inkernel_form):
     # fp32 C with ldc = 641: the head's output goes through the st.global path
     c = run_close(Case("bf16", 1024, 641, 4096, c_dtype="f32", bias=True, act="relu",
                        row_bias=True, seed=503))
-    assert c.plan["stream_k"] == 2
+    assert c.plan["stream_k"] == inkernel_form
 
 
 # ---------------------------------------------------------------- spread split-K in one kernel
@@ -830,6 +849,43 @@ def test_stream_k_split_two_k_blocks_bias_gelu():
     c, out = _double_k_run(dict(M=700, N=600, K=1024, opts=opts), {}, c_dtype="bf16",
                            bias=True, act="gelu_tanh", seed=906)
     assert c.plan["stream_k"] == 2 and c.plan["block_k"] == 128, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+
+
+# The automatic split-K balanced over every CTA (the contiguous form with no
+# whole units first): on 8 CTAs a few tiles' K steps are dealt in equal ranges,
+# so one tile spans up to four CTAs and its first piece adds the partials of
+# every later one, in order.  Forced contiguous form on CTA pairs likewise.
+BALANCED_CASES = {
+    "3_tiles_8_ctas": dict(M=384, N=128, K=4096, opts={"MAX_CTAS": 8}),
+    "mn_major_ragged_k": dict(M=384, N=100, K=3000, la="col", lb="row", opts={"MAX_CTAS": 8}),
+    "swap_ab_8_tiles_16_ctas": dict(M=16, N=1000, K=4096, opts={"MAX_CTAS": 16}),
+    "pairs_contiguous_long_spans": dict(M=700, N=600, K=2048, lb="col",
+                                        opts={"STREAM_K": 2, "CTA_PAIR": 3, "MAX_CTAS": 8,
+                                              "BLOCK_N": 256}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BALANCED_CASES))
+def test_exact_contiguous_form_spans_several_ctas(name):
+    kw = dict(BALANCED_CASES[name])
+    for dk in (0, 1):   # two K blocks per load where the plan takes them, then one
+        c, out = _double_k_run(kw, {"DOUBLE_K": dk}, values="ints", seed=907)
+        assert c.plan["stream_k"] == 1, c.plan
+        if dk == 1:
+            assert c.plan["block_k"] == 64
+        assert np.array_equal(c.result(out), c.oracle_full()), (c.plan, dk)
+        assert c.untouched_padding(out)
+        if dk == 0:
+            first, out0 = c, out
+    assert np.array_equal(out0.view(np.uint8), out.view(np.uint8))
+
+
+def test_contiguous_form_epilogue():
+    kw = dict(M=384, N=100, K=3000, la="col", lb="row", opts={"MAX_CTAS": 8})
+    c, out = _double_k_run(kw, {}, c_dtype="bf16", beta=0.5, bias=True, act="gelu_tanh",
+                           seed=908)
+    assert c.plan["stream_k"] == 1, c.plan
     check_close(c, c.result(out), c.oracle_full())
 
 

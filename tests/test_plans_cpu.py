@@ -84,7 +84,7 @@ def test_two_k_blocks_per_load_for_mn_major_operands_too(options):
 def test_headline_options_change_the_plan(options):
     options(CTA_PAIR=1, GROUP_M=4)
     p = headline()
-    assert p["cta_pair"] == 0 and p["group_m"] == 4 and p["block_k"] == 64
+    assert p["cta_pair"] == 0 and p["group_m"] == 4 and p["block_k"] == 128
 
 
 def test_split_k_row_runs_the_spread_form(options):
@@ -101,10 +101,15 @@ def test_split_k_without_workspace_runs_whole_tiles():
     assert p["split_k"] == 1 and p["stream_k"] == 0 and p["workspace_bytes"] == 0
 
 
-def test_skinny_row_swaps_and_splits_in_one_kernel():
+def test_skinny_row_swaps_and_spreads_k_over_every_cta(options):
+    # 64 tiles of 128 x 16 on 152 CTAs: the contiguous form, each CTA an equal
+    # range of two-block K steps, no whole units first
     p = plan(16, 8192, 8192, cdt=2, ws=UNLIMITED)
-    assert p["swap_ab"] == 1 and p["block_n"] == 16
-    assert p["stream_k"] == 2 and p["split_k"] == 1 and p["grid"] == 128 and p["launches"] == 1
+    assert p["swap_ab"] == 1 and p["block_n"] == 16 and p["block_k"] == 128
+    assert p["stream_k"] == 1 and p["split_k"] == 1 and p["grid"] == 152 and p["launches"] == 1
+    options(SPLIT_REDUCE=3)   # equal pieces instead: 2 per tile, on 128 CTAs
+    q = plan(16, 8192, 8192, cdt=2, ws=UNLIMITED)
+    assert q["stream_k"] == 2 and q["grid"] == 128 and q["block_k"] == 128
 
 
 def test_batched_beta_rows_read_c_by_tma_loads():
@@ -129,14 +134,14 @@ def test_flat_row_keeps_single_cta_tiles():
     assert p["cta_pair"] == 0 and p["block_n"] == 256 and p["fast_epilogue"] == 1
 
 
-def test_stream_k_needs_a_workspace_and_keeps_two_k_blocks_in_the_split_form(options):
+def test_stream_k_needs_a_workspace_and_keeps_two_k_blocks(options):
     p = plan(2560, 2560, 16384, lb=1, ws=UNLIMITED)
     assert p["stream_k"] == 2 and p["block_k"] == 128
     # the headline with a workspace: split-form pieces on whole two-block steps
     assert headline(ws=UNLIMITED)["block_k"] == 128
-    options(STREAM_K=2)           # the contiguous form's ranges: one block per load
+    options(STREAM_K=2)           # the contiguous form's ranges, in two-block steps too
     p = plan(2560, 2560, 16384, lb=1, ws=UNLIMITED)
-    assert p["stream_k"] == 1 and p["block_k"] == 64
+    assert p["stream_k"] == 1 and p["block_k"] == 128
     p0 = plan(2560, 2560, 16384, lb=1)
     assert p0["stream_k"] == 0 and p0["block_k"] == 128
 
@@ -190,7 +195,9 @@ INSTANTIATED = {
     1: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
     2: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2)},
 }
-TWO_K_BLOCKS = {(128, 2), (256, 2)}
+# (tile width, mode, epilogue form) compiled with two K blocks per load
+TWO_K_BLOCKS = {(128, 2, 1), (256, 2, 1), (16, 0, 0), (32, 0, 0), (64, 0, 0), (64, 0, 1),
+                (128, 0, 1), (256, 0, 1)}
 
 
 def _random_calls(n, seed=20261202):
@@ -272,12 +279,12 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
         if mode:
             assert p["grid"] % 2 == 0, (p, ctx)
         if p["block_k"] == 128:
-            assert (bn, mode) in TWO_K_BLOCKS and form == 1, (p, ctx)
+            assert (bn, mode, form) in TWO_K_BLOCKS, (p, ctx)
             # each operand MN-major, or K-major with whole K blocks and one matrix
             for mn, stride in ((kw["la"] == 1, kw["sa"]), (kw["lb"] == 0, kw["sb"])):
                 assert mn or (K % 64 == 0 and (kw["batch"] == 1 or stride == 0)), (p, ctx)
             assert p["split_k"] == 1, (p, ctx)
-            assert p["stream_k"] in (0, 2), (p, ctx)    # never the contiguous form
+            assert mode == 2 or K > 7 * 64, (p, ctx)    # single CTAs: 8 K blocks at least
         else:
             assert p["block_k"] == 64, (p, ctx)
         if form == 2:
