@@ -85,6 +85,11 @@ struct TcParams {
     int32_t sk_split;        // pieces per unit of the split form (0: off)
     int32_t sk_tiles;        // units cut in the split form
     int32_t sk_spread;       // split form: 1 every piece reduces a share of the tile
+    // 1: no fix-up at all: every K piece adds alpha * its accumulator into C
+    // (fp32, row-major) by TMA reduce-add, after the CTAs have set C to
+    // beta * C + bias, each for its share of rows, and published that share's
+    // flag (sk_flags[cta]) with the epoch
+    int32_t sk_atomic;
     float* sk_partials;      // [slot][cta rank][128][BN] fp32, lane-interleaved per warp
     unsigned long long* sk_flags;  // [slot][cta rank][epilogue warp]: epoch when published
     unsigned long long sk_epoch;   // this launch's flag value

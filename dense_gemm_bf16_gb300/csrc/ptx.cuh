@@ -166,6 +166,27 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
         : "memory");
 }
 
+// Element-wise add of the shared-memory box into the global box at (x, y)
+// (the element type is the tensor map's; performed at L2, atomically per
+// element); completes in the bulk group like a store.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                                  int32_t y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                                  int32_t y, int32_t z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2, %3}], [%4];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y, int32_t z, uint64_t policy) {
     asm volatile(

@@ -241,7 +241,7 @@ __device__ __forceinline__ bool unit_ok(const TcParams& p, const Unit& w) {
     bool ok = w.b >= 0 && w.b < p.batch && w.split >= 0 && w.split < p.splits && w.pid_m >= 0 &&
               w.pid_m < p.num_pid_m * CM && w.pid_n >= 0 && w.pid_n < p.dbg_num_pid_n &&
               w.kb0 >= 0 && w.kb0 < w.kb1 && w.kb1 <= p.kblocks;
-    if (w.kind != UNIT_FULL) {
+    if (w.kind != UNIT_FULL && !p.sk_atomic) {
         const int64_t lo = w.kind == UNIT_SPREAD ? w.slot - w.piece : w.slot;
         const int64_t hi = w.kind == UNIT_TAIL ? w.slot + 1 : lo + w.nslots;
         ok = ok && lo >= 0 && hi * CM <= p.dbg_sk_slots && (w.kind != UNIT_HEAD || w.nslots >= 1);
@@ -973,6 +973,78 @@ __device__ __forceinline__ void c_ring_drain(CRing& cr, int lane, uint64_t timeo
     __syncwarp();
 }
 
+// Atomic split-K: this CTA's share of the rows of C (all batch entries as one
+// row range) set to beta * C + bias by its four epilogue warps (warp q takes
+// every fourth row, lanes 16-byte column groups), then the share's flag is
+// published with the launch's epoch.  In the debug build's count-writes mode
+// this is the one counted write of each element.
+__device__ __forceinline__ void atomic_init_c(const TcParams& p, int cta, int ncta, int q,
+                                              int lane) {
+    const Epilogue& e = p.epi;
+    const int64_t rows = static_cast<int64_t>(p.batch) * p.M;
+    const int64_t r0 = rows * cta / ncta, r1 = rows * (cta + 1) / ncta;
+    const int n4 = p.N / 4;
+    for (int64_t r = r0 + q; r < r1; r += 4) {
+        const int64_t b = r / p.M, i = r - b * p.M;
+        float* row = static_cast<float*>(e.C) + b * e.stride_c + i * e.ldc;
+        const float brow = e.bias && e.bias_on_rows && bias_ok(e, i) ? e.bias[i] : 0.0f;
+        for (int j4 = lane; j4 < n4; j4 += 32) {
+            if (!c_span_ok(e, b * e.stride_c + i * e.ldc + 4 * j4, 4)) continue;
+            float4 v = make_float4(brow, brow, brow, brow);
+            if (e.beta != 0.0f) {
+                const float4 c = reinterpret_cast<const float4*>(row)[j4];
+                v.x = fmaf(e.beta, c.x, v.x), v.y = fmaf(e.beta, c.y, v.y);
+                v.z = fmaf(e.beta, c.z, v.z), v.w = fmaf(e.beta, c.w, v.w);
+            }
+            if (e.bias && !e.bias_on_rows && bias_ok(e, 4 * j4 + 3)) {
+                v.x += e.bias[4 * j4], v.y += e.bias[4 * j4 + 1];
+                v.z += e.bias[4 * j4 + 2], v.w += e.bias[4 * j4 + 3];
+            }
+            reinterpret_cast<float4*>(row)[j4] = v;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) count_write(e, b, i, 4 * j4 + k);
+        }
+        for (int j = 4 * n4 + lane; j < p.N; j += 32) {
+            if (!c_span_ok(e, b * e.stride_c + i * e.ldc + j)) continue;
+            float v = brow;
+            if (e.beta != 0.0f) v = fmaf(e.beta, row[j], v);
+            if (e.bias && !e.bias_on_rows && bias_ok(e, j)) v += e.bias[j];
+            row[j] = v;
+            count_write(e, b, i, j);
+        }
+    }
+    // every epilogue thread's stores, then one release of the share's flag
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(TC_EPI_THREADS) : "memory");
+    if (q == 0 && lane == 0) st_release_u64(p.sk_flags + cta, p.sk_epoch);
+}
+
+// Atomic split-K: waits (bounded) until every CTA has published its share of
+// C's initial values; then TMA reduce-adds of this warp may follow.  Returns
+// false on a timeout (the status word is set).
+__device__ __forceinline__ bool atomic_wait_init(const TcParams& p, int ncta, int lane,
+                                                 volatile int* abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        bool mine = true;
+        for (int c = lane; c < ncta; c += 32) mine = mine && ld_relaxed_u64(p.sk_flags + c) == p.sk_epoch;
+        if (__all_sync(0xffffffffu, mine)) break;
+        int give_up = 0;
+        if (lane == 0 && (it & 15u) == 0 && (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns)) {
+            *abort_flag = 1;
+            if (p.status) DG_SET_TIMEOUT(p.status);
+            give_up = 1;
+        }
+        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+    }
+    // the relaxed loads saw the released flags: acquire, then order the other
+    // CTAs' generic stores before this warp's async-proxy reduce-adds
+    fence_acq_rel_gpu();
+    fence_proxy_async_global();
+    __syncwarp();
+    return true;
+}
+
 // Output of one warp's 32 rows for the common case (C written by TMA store,
 // beta == 0 or a split-K partial): 64 columns per step, two tcgen05.ld in
 // flight, one fence / warp sync / store issue per step.  Each step fills 128
@@ -999,6 +1071,8 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
     const int zc = partial ? w.split * p.batch + w.b : w.b;
     const int swz = lane & 7;
     const bool need_c = BETA && !partial && e.beta != 0.0f;
+    // atomic split-K: add alpha * acc into C (initialised to beta * C + bias)
+    const bool reduce = !BETA && ES == 4 && p.sk_atomic != 0;
     const int nsteps = fast_steps<BN>(p, w);
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
@@ -1015,7 +1089,12 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
             v[i] = __uint_as_float(ra[i]);
             v[32 + i] = __uint_as_float(rb[i]);
         }
-        if (!partial) {
+        if (reduce) {
+            if (e.alpha != 1.0f) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) v[i] *= e.alpha;
+            }
+        } else if (!partial) {
             if (e.alpha != 1.0f) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) v[i] *= e.alpha;
@@ -1106,14 +1185,20 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
                 if (bc >= p.N) break;
                 const uint32_t box = smem_u32(wbuf + (NB == 2 ? k : (nbox & 1u)) * EPI_BOX_BYTES);
                 if (!out_box_ok(p, bc, row0, zc)) continue;
-                if (p.c_tma_3d)
+                if (reduce) {
+                    if (p.c_tma_3d)
+                        tma_reduce_add_3d(&p.tmap_c, box, bc, row0, zc);
+                    else
+                        tma_reduce_add_2d(&p.tmap_c, box, bc, row0);
+                } else if (p.c_tma_3d) {
                     tma_store_3d(&p.tmap_c, box, bc, row0, zc, pol);
-                else
+                } else {
                     tma_store_2d(&p.tmap_c, box, bc, row0, pol);
+                }
             }
             bulk_commit_group();
         }
-        count_row(p, w.b, row, col0, 64);
+        if (!reduce) count_row(p, w.b, row, col0, 64);
         ++nbox;
     }
     return true;
@@ -1170,6 +1255,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     // An MN-contiguous operand arrives in 64-wide atom columns of 64 * KS K
     // rows (128 bytes each, 128-byte swizzled): one column takes 8 KB * KS.
     constexpr uint32_t kAtomCol = 8192u * KS;
+
+    if constexpr (!(EPI == 1 && C::CM == 1)) {
+        // the atomic split-K runs on single CTAs with the TMA-store epilogue
+        // only (the plan never asks otherwise); report instead of skipping work
+        if (p.sk_atomic) {
+            if (threadIdx.x == 0 && p.status) DG_SET_TIMEOUT(p.status);
+            return;
+        }
+    }
 
     // The launch parameters outside the tensor maps lie in four 64-byte lines.
     // A role's first reads of them miss the constant cache one after another
@@ -1449,6 +1543,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
         bool first = true;
+        // atomic split-K: this CTA's share of C's initial values first
+        bool init_seen = false;
+        if constexpr (EPI == 1 && CM == 1) {
+            if (p.sk_atomic) atomic_init_c(p, cta0, ncta, q, lane);
+        }
         while (work_next<CM, KS>(p, wi, ncta, rank, w)) {
             if constexpr (EPI == 2) {
                 // the first two C boxes of a tile this warp will write, requested
@@ -1478,7 +1577,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
             const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
-            if (w.kind == UNIT_TAIL || w.kind == UNIT_SPREAD) {
+            if (p.sk_atomic) {
+                // atomic split-K (fp32 C, TMA-store epilogue): every piece adds
+                // its share, once C's initial values are all in place
+                if constexpr (EPI == 1 && CM == 1) {
+                    if (!init_seen) {
+                        if (!atomic_wait_init(p, ncta, lane, abort_flag)) break;
+                        init_seen = true;
+                    }
+                    tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                }
+            } else if (w.kind == UNIT_TAIL || w.kind == UNIT_SPREAD) {
                 // stream-K tail or spread piece: publish this CTA's raw fp32 partial
                 // for the cluster(s) that finish the tile
                 const int64_t slot = static_cast<int64_t>(w.slot) * CM + rank;
@@ -1627,7 +1736,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 template <int BN, int MODE, int EPI, int KS = 1>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     constexpr int CM = Cfg<BN, MODE, EPI, KS>::CM;
-    const bool waits = p.sk_spread || p.sk_split > 0 || p.sk_iters > 0;
+    const bool waits = p.sk_spread || p.sk_split > 0 || p.sk_iters > 0 || p.sk_atomic;
     if (CM == 1 && !waits) {
         tc_gemm_kernel<BN, MODE, EPI, KS><<<grid, TC_THREADS, Cfg<BN, MODE, EPI, KS>::SMEM, stream>>>(p);
         return cudaGetLastError();

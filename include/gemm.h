@@ -302,12 +302,14 @@ typedef struct {
     int32_t cta_pair;        /* 0 one CTA per tile; 2 CTA pair computing 256-row tiles
                                 with two-CTA (cta_group::2) MMAs, each CTA loading
                                 its own half of A and B (1 is not used)            */
-    int32_t stream_k;        /* stream-K: 0 off; 1 the K blocks of the last one-to-two
-                                waves split evenly over all CTAs in contiguous ranges;
+    int32_t stream_k;        /* stream-K: 0 off; 1 the K steps of the last one-to-two
+                                waves (or, for an automatic split-K, of every tile)
+                                split evenly over all CTAs in contiguous ranges;
                                 2 each unit of the last partial wave cut into equal
-                                K pieces that run side by side (also the automatic
-                                split-K in one kernel); 3 the same with every piece
-                                reducing an equal share of its tile               */
+                                K pieces that run side by side; 3 the same with every
+                                piece reducing an equal share of its tile; 4 K steps
+                                dealt as in 1 with every piece adding its partial
+                                into C (GEMM_OPT_SPLIT_REDUCE = 4)                */
     int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue; 2: the TMA-store epilogue
                                 that reads beta * C by TMA loads (GEMM_OPT_FAST_EPILOGUE) */
 } gemm_plan_t;
@@ -389,13 +391,23 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         per tile, the K steps of all tiles are dealt to every CTA
  *                         in equal contiguous ranges and the piece holding a tile's
  *                         first step adds the others' fp32 partials (plan stream_k 1);
- *                         with more pieces each publishes a partial and, once all
- *                         have, reduces one equal share of the tile (plan stream_k 3);
+ *                         with more pieces, for an fp32 C that takes TMA stores and no
+ *                         activation, the atomic form below (plan stream_k 4), else
+ *                         each piece publishes a partial and, once all have, reduces
+ *                         one equal share of the tile (plan stream_k 3);
  *                         1 the serial form up to 4 pieces and the two-pass form
  *                         (split_k > 1, a second launch) beyond; 2 the spread form for
- *                         any number of pieces; 3 as 0, but up to 4 pieces as equal K
- *                         pieces, one CTA each (plan stream_k 2).  The one-kernel
- *                         forms are cooperative launches and need the workspace of
+ *                         any number of pieces (1 and 2 keep a fixed order of addition,
+ *                         so results repeat bit for bit); 3 as 0, but up to 4 pieces
+ *                         as equal K pieces, one CTA each (plan stream_k 2); 4 the
+ *                         atomic form whenever it applies (an fp32 C that takes TMA
+ *                         stores, no activation; plan stream_k 4): K steps dealt to
+ *                         every CTA as in 0, and every
+ *                         piece adds alpha times its partial into C by TMA reduce-add
+ *                         after the CTAs have set C to beta * C + bias (the order of
+ *                         the additions varies between runs, so the last bits may
+ *                         too); other calls as 0.  The one-kernel forms are
+ *                         cooperative launches and need the workspace of
  *                         gemm_workspace_size.
  *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
  *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes

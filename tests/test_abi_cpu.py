@@ -124,10 +124,10 @@ def test_options(lib):
 def test_split_reduce_and_block_n_options(lib):
     assert dg.gemm_get_option(Option.SPLIT_REDUCE) == 0
     assert dg.gemm_get_option(Option.BLOCK_N) == 0
-    for v in (0, 1, 2, 3):
+    for v in (0, 1, 2, 3, 4):
         assert dg.gemm_set_option(Option.SPLIT_REDUCE, v) == Status.OK
         assert dg.gemm_get_option(Option.SPLIT_REDUCE) == v
-    assert dg.gemm_set_option(Option.SPLIT_REDUCE, 4) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.SPLIT_REDUCE, 5) == Status.ERR_INVALID_ARG
     assert dg.gemm_set_option(Option.SPLIT_REDUCE, -1) == Status.ERR_INVALID_ARG
     assert dg.gemm_set_option(Option.SPLIT_REDUCE, 0) == Status.OK
     for v in (16, 32, 64, 128, 256, 0):

@@ -20,7 +20,8 @@ CASES = {
     "split_pairs": ((2560, 2560, 16384), {}, 2),
     "contiguous_pairs": ((2560, 2560, 16384), {"STREAM_K": 2}, 1),
     "contiguous_single": ((2560, 2560, 8192), {"STREAM_K": 2, "CTA_PAIR": 1}, 1),
-    "spread_split_k": ((256, 256, 65536), {}, 3),
+    "spread_split_k": ((256, 256, 65536), {"SPLIT_REDUCE": 2}, 3),
+    "atomic_split_k": ((256, 256, 65536), {}, 4),
 }
 
 

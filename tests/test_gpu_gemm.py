@@ -551,7 +551,7 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
     args = [0, 1, M, N, K, 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0, 2, 1.0, 0.0,
             None, 0, 0]
     st, big = dg.gemm_plan_query(*args, 1 << 40)
-    assert st == 0 and (big.split_k > 1 or big.stream_k in (1, 2, 3))
+    assert st == 0 and (big.split_k > 1 or big.stream_k in (1, 2, 3, 4))
     st, exact = dg.gemm_plan_query(*args, int(big.workspace_bytes))
     assert st == 0
     assert (exact.split_k, exact.stream_k, exact.grid) == (big.split_k, big.stream_k, big.grid)
@@ -611,6 +611,64 @@ def test_inkernel_split_unaligned_c(inkernel_form):
     assert c.plan["stream_k"] == inkernel_form
 
 
+# ---------------------------------------------------------------- atomic split-K (option)
+
+# GEMM_OPT_SPLIT_REDUCE = 4: every K piece adds alpha * its partial into an fp32
+# C by TMA reduce-add, after the CTAs set C to beta * C + bias (the pages'
+# atomic accumulation; the sum order varies between runs, so only small-integer
+# data is bit-exact).  An activation or a 16-bit C keeps the default forms.
+ATOMIC_CASES = {
+    "square_long_k": dict(M=256, N=256, K=16384),
+    "pieces_per_tile_38": dict(M=256, N=256, K=65536),
+    "one_tile_152_pieces": dict(M=128, N=128, K=32768),
+    "alpha_beta_bias": dict(M=256, N=384, K=8192, alpha=0.5, beta=2.0, bias=True,
+                            c_values="ints"),
+    "row_bias_batched": dict(M=128, N=256, K=8192, batch=2, bias=True, row_bias=True),
+    "ragged_k": dict(M=200, N=264, K=6000),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ATOMIC_CASES))
+def test_exact_atomic_split_k(name):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(ATOMIC_CASES[name])
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 4)
+    try:
+        c = Case("bf16", values="ints", seed=509, **kw)
+        if c.bias is not None:
+            c.bias = np.round(c.bias * 4).astype(np.float32)
+        st, out = c.run_gpu()
+    finally:
+        dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+    assert st == 0, c.plan
+    assert c.plan["stream_k"] == 4 and c.plan["split_k"] == 1 and c.plan["launches"] == 1 + \
+        c.plan["pack_a"] + c.plan["pack_b"], c.plan
+    assert np.array_equal(c.result(out), c.oracle_full()), c.plan
+    assert c.untouched_padding(out)
+    assert dg.gemm_check_device_status(None) == 0
+
+
+def test_atomic_split_k_uniform_values_within_tolerance():
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 4)
+    try:
+        c = run_close(Case("bf16", 256, 256, 65536, alpha=1.5, beta=0.5, bias=True, seed=510))
+    finally:
+        dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+    assert c.plan["stream_k"] == 4, c.plan
+
+
+@pytest.mark.parametrize("kw", [dict(c_dtype="bf16"), dict(act="relu")], ids=["bf16_out", "relu"])
+def test_atomic_split_k_needs_fp32_out_and_no_activation(kw):
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 4)
+    try:
+        c = run_close(Case("bf16", 256, 256, 16384, seed=511, **kw))
+    finally:
+        dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+    assert c.plan["stream_k"] in (1, 3), c.plan     # the default one-kernel forms
+
+
 # ---------------------------------------------------------------- spread split-K in one kernel
 
 # More than 4 automatic pieces per tile: every piece publishes its fp32 partial
@@ -631,10 +689,31 @@ def _spread_case(name, **extra):
     return Case("bf16", M, N, K, **kw, **extra)
 
 
+@pytest.fixture
+def fixed_order():
+    # GEMM_OPT_SPLIT_REDUCE = 2: the spread reduction (fixed order of addition)
+    # also where the default would add the pieces atomically (an fp32 C that
+    # takes TMA stores, no activation)
+    import dense_gemm_bf16_gb300 as dg
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 2)
+    yield
+    dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+
+
 @pytest.mark.parametrize("name", sorted(SPREAD_CASES))
-def test_exact_spread_split(name):
+def test_exact_spread_split(name, fixed_order):
     c = run_exact(_spread_case(name, values="ints", seed=701))
     assert c.plan["stream_k"] == 3 and c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
+
+
+@pytest.mark.parametrize("name", sorted(SPREAD_CASES))
+def test_exact_default_many_pieces(name):
+    # by default an fp32 C that takes TMA stores (without an activation) gets
+    # the atomic form; the swapped skinny case's C^T is column-major, so it
+    # keeps the spread reduction
+    c = run_exact(_spread_case(name, values="ints", seed=710))
+    assert c.plan["stream_k"] == (3 if name == "skinny_swap" else 4), c.plan
+    assert c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
 
 
 @pytest.mark.parametrize("name", ["square_long_k", "ragged"])
@@ -682,7 +761,7 @@ def test_spread_f16_swap_with_bias():
 
 
 @pytest.mark.parametrize("bn", [64, 256])
-def test_exact_spread_other_tile_widths(bn):
+def test_exact_spread_other_tile_widths(bn, fixed_order):
     import dense_gemm_bf16_gb300 as dg
     dg.gemm_set_option(dg.Option.BLOCK_N, bn)
     try:
@@ -692,7 +771,7 @@ def test_exact_spread_other_tile_widths(bn):
     assert c.plan["block_n"] == bn and c.plan["stream_k"] == 3, c.plan
 
 
-def test_spread_unpublished_partial_reports_timeout_and_recovers():
+def test_spread_unpublished_partial_reports_timeout_and_recovers(fixed_order):
     # the first CTA leaves its partial unpublished: the pieces of its tile give
     # up after the wait bound, the call reports a timeout, and the context stays
     # usable

@@ -21,7 +21,8 @@ CASES = {
     "contiguous": ((700, 600, 1000), {"STREAM_K": 2, "MAX_CTAS": 8, "CTA_PAIR": 1}, 1),
     "split": ((700, 600, 1000), {"STREAM_K": 3, "MAX_CTAS": 8, "CTA_PAIR": 1}, 2),
     "split_pair_mma": ((700, 600, 1000), {"STREAM_K": 3, "MAX_CTAS": 8, "CTA_PAIR": 3}, 2),
-    "spread": ((128, 256, 8192), {}, 3),
+    "spread": ((128, 256, 8192), {"SPLIT_REDUCE": 2}, 3),
+    "atomic": ((128, 256, 8192), {}, 4),
 }
 
 

@@ -87,13 +87,30 @@ def test_headline_options_change_the_plan(options):
     assert p["cta_pair"] == 0 and p["group_m"] == 4 and p["block_k"] == 128
 
 
-def test_split_k_row_runs_the_spread_form(options):
+def test_split_k_row_adds_its_pieces_atomically(options):
+    # fp32 C, no activation, 38 pieces per tile: the atomic form, whose scratch
+    # is one flag per CTA
     p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
-    assert p["stream_k"] == 3 and p["split_k"] == 1 and p["launches"] == 1
+    assert p["stream_k"] == 4 and p["split_k"] == 1 and p["launches"] == 1
     assert p["grid"] == 152 and p["block_n"] == 128 and p["cta_pair"] == 0
+    assert p["workspace_bytes"] == 256 * ((152 * 8 + 255) // 256)
+    # an activation, or a 16-bit C: the spread reduction
+    assert plan(256, 256, 65536, cdt=2, epi=4, ws=UNLIMITED)["stream_k"] == 3
+    assert plan(256, 256, 65536, cdt=0, ws=UNLIMITED)["stream_k"] == 3
+    options(SPLIT_REDUCE=2)       # fixed order of addition: the spread reduction
+    assert plan(256, 256, 65536, cdt=2, ws=UNLIMITED)["stream_k"] == 3
     options(SPLIT_REDUCE=1)
     p2 = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
     assert p2["stream_k"] == 0 and p2["split_k"] > 4 and p2["launches"] == 2
+
+
+def test_atomic_split_k_on_request_for_few_pieces(options):
+    # 3 tiles' worth of pieces per CTA stay in the balanced form by default;
+    # GEMM_OPT_SPLIT_REDUCE = 4 adds them atomically instead
+    assert plan(1024, 640, 4096, cdt=2, ws=UNLIMITED)["stream_k"] == 1
+    options(SPLIT_REDUCE=4)
+    assert plan(1024, 640, 4096, cdt=2, ws=UNLIMITED)["stream_k"] == 4
+    assert plan(1024, 640, 4096, cdt=2, epi=4, ws=UNLIMITED)["stream_k"] == 1
 
 
 def test_split_k_without_workspace_runs_whole_tiles():
@@ -174,7 +191,7 @@ def test_workspace_size_covers_every_plan(shape, layouts):
 def test_simulated_device_changes_with_the_sm_count(options):
     options(TEST_SIM_SMS=64)
     p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
-    assert p["grid"] <= 64 and p["stream_k"] == 3
+    assert p["grid"] <= 64 and p["stream_k"] == 4
 
 
 @pytest.mark.parametrize("ab,cdt", [(0, 0), (1, 1), (1, 2)])
