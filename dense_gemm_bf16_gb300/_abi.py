@@ -71,6 +71,7 @@ class Option(enum.IntEnum):
     DOUBLE_K = 14
     TEST_SIM_SMS = 15
     TEST_DEBUG_BOUND = 16
+    OVERLAP_COPY = 17
 
 
 class Plan(ctypes.Structure):

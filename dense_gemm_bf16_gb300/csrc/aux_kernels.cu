@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "epilogue.cuh"
+#include "ptx.cuh"
 #include "internal.h"
 
 namespace dg {
@@ -29,10 +30,14 @@ constexpr int kThreads = 256;
 // aligned; a warp's loads still cover 512 contiguous bytes) and one 16-byte
 // store (the destination pitch is a multiple of 8 elements and its base
 // 256-byte aligned).  Columns past `cols` in the last group are written as 0.
+// The GEMM that reads the copy may be launched as this grid's programmatic
+// dependent: it is let in at once, sets itself up while the copy runs, and
+// waits for the copy's completion before its first operand load.
 __global__ void __launch_bounds__(kThreads) pack16_kernel(const uint16_t* __restrict__ src,
                                                           int64_t ld, int64_t stride, int64_t rows,
                                                           int64_t cols, uint16_t* __restrict__ dst,
                                                           int64_t ld_dst) {
+    griddep_launch_dependents();
     const int64_t b = blockIdx.z;
     const int64_t c0 = 8 * (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x);
     if (c0 >= cols) return;

@@ -29,6 +29,7 @@ std::atomic<int64_t> g_opt_test_stall{0};
 std::atomic<int64_t> g_opt_cta_pair{0};
 std::atomic<int64_t> g_opt_swap_ab{0};
 std::atomic<int64_t> g_opt_l2_hints{0};
+std::atomic<int64_t> g_opt_overlap_copy{0};
 std::atomic<int64_t> g_opt_stream_k{0};
 std::atomic<int64_t> g_opt_fast_epilogue{0};
 std::atomic<int64_t> g_opt_sgemm_kernel{0};
@@ -621,7 +622,10 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     // number of 64-deep blocks (an odd count reads its last block's partner
     // past the end: zeros) and the operand one matrix (one batch entry, or a
     // broadcast).  An MN-major operand keeps its own map with boxes of 128 K
-    // rows instead of 64 (rows past K: zeros), batched or not.
+    // rows instead of 64 (rows past K: zeros), batched or not.  (A K-major
+    // operand with a K that ends inside a block could load its last step
+    // through the ordinary map; measured on K = 1000 that was 1-2 us slower
+    // than one block per load, so such a K keeps one block per load.)
     auto ks2_ok = [&](const Operand& o) {
         return o.mn || (c.K % TC_BLOCK_K == 0 && (c.batch == 1 || o.stride == 0));
     };
@@ -883,6 +887,8 @@ gemm_status_t run(const Call& c) {
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;
     p.test_stall = static_cast<int32_t>(g_opt_test_stall.exchange(0));
     p.l2_hints = static_cast<int32_t>(g_opt_l2_hints.load());
+    // the launch right before this one is an operand copy: let the GEMM in early
+    p.pdl = (pl.a.pack || pl.b.pack) && g_opt_overlap_copy.load() == 0 ? 1 : 0;
     if (pl.sk) {
         p.dp_per_cluster = pl.dp_per_cluster;
         p.dp_units = static_cast<int32_t>(pl.dp_units);
@@ -1216,6 +1222,10 @@ gemm_status_t gemm_set_option(gemm_option_t option, int64_t value) {
             if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
             g_opt_test_debug_bound.store(value);
             return GEMM_OK;
+        case GEMM_OPT_OVERLAP_COPY:
+            if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+            g_opt_overlap_copy.store(value);
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_ARG;
 }
@@ -1238,6 +1248,7 @@ int64_t gemm_get_option(gemm_option_t option) {
         case GEMM_OPT_DOUBLE_K: return g_opt_double_k.load();
         case GEMM_OPT_TEST_SIM_SMS: return g_opt_test_sim_sms.load();
         case GEMM_OPT_TEST_DEBUG_BOUND: return g_opt_test_debug_bound.load();
+        case GEMM_OPT_OVERLAP_COPY: return g_opt_overlap_copy.load();
     }
     return -1;
 }

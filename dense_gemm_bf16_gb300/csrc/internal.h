@@ -65,6 +65,11 @@ struct TcParams {
     uint64_t timeout_ns;     // bound on every wait
     int32_t test_stall;      // test only: 1 leave one stage unfilled; 2 CTA 0 publishes no partial flags
     int32_t l2_hints;        // operand L2 policy: 0 normal; 1 A evict-first, B evict-last; 2 the reverse
+    // 1: launched as the programmatic dependent of the operand copy just before
+    // it on the stream (never with the cooperative forms): the CTAs set up while
+    // the copy runs, and the producer waits for the copy's completion
+    // (griddepcontrol.wait) before its first load
+    int32_t pdl;
     // Stream-K.  Every cluster first takes dp_per_cluster whole units round
     // robin; the units from dp_units on are then cut along K, in one of two forms.
     // Contiguous (sk_iters > 0): their steps (of KS K blocks) are split evenly

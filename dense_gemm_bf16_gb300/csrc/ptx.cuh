@@ -22,6 +22,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// (PTX ISA: "Parallel Synchronization and Communication Instructions:
+// griddepcontrol").  Both are no-ops for a grid launched without the
+// programmatic-serialization attribute, or with no dependent grid.
+
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the dependent grid be scheduled before this one completes (it still
+// waits for this grid's completion in griddep_wait before reading its output).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

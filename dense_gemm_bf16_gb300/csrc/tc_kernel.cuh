@@ -1330,6 +1330,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const uint64_t pol_last = l2_policy_evict_last();
             const uint64_t pol_a = p.l2_hints == 1 ? pol_first : (p.l2_hints == 2 ? pol_last : pol_normal);
             const uint64_t pol_b = p.l2_hints == 1 ? pol_last : (p.l2_hints == 2 ? pol_first : pol_normal);
+            // an operand copied by the launch before this one: every CTA waits
+            // for the copy to complete (so this grid never completes before it)
+            if (p.pdl) griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0;
@@ -1737,7 +1740,8 @@ template <int BN, int MODE, int EPI, int KS = 1>
 cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     constexpr int CM = Cfg<BN, MODE, EPI, KS>::CM;
     const bool waits = p.sk_spread || p.sk_split > 0 || p.sk_iters > 0 || p.sk_atomic;
-    if (CM == 1 && !waits) {
+    const bool pdl = p.pdl && !waits;
+    if (CM == 1 && !waits && !pdl) {
         tc_gemm_kernel<BN, MODE, EPI, KS><<<grid, TC_THREADS, Cfg<BN, MODE, EPI, KS>::SMEM, stream>>>(p);
         return cudaGetLastError();
     }
@@ -1746,7 +1750,7 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = Cfg<BN, MODE, EPI, KS>::SMEM;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     unsigned n = 0;
     if (CM > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
@@ -1758,6 +1762,11 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     if (waits) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
     cfg.attrs = attr;

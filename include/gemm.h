@@ -412,12 +412,22 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *   GEMM_OPT_BLOCK_N      tile width of the tensor-core path: 0 (default) chosen by
  *                         the plan, else 16, 32, 64, 128 or 256 (an MN-major B takes
  *                         at least 64).
- *   GEMM_OPT_DOUBLE_K     0 (default): CTA-pair plans with the TMA-store-only epilogue,
- *                         whole tiles or split-form stream-K pieces, bring two 64-deep
- *                         K blocks of each operand per TMA load (plan block_k 128); a
- *                         K-major operand then needs K a multiple of 64 and one matrix
- *                         (one batch entry or a broadcast), an MN-major one nothing
- *                         more; 1: one K block per load always.
+ *   GEMM_OPT_DOUBLE_K     0 (default): plans whose kernel form has it (CTA pairs with
+ *                         128- or 256-column tiles and the TMA-store-only epilogue;
+ *                         single CTAs of at least 8 K blocks with 16- to 64-column
+ *                         tiles and the general epilogue, or 64- to 256-column tiles
+ *                         and the TMA-store-only one), whole tiles or stream-K
+ *                         pieces, bring two 64-deep K blocks of each operand per TMA
+ *                         load (plan block_k 128); a K-major operand then needs K a
+ *                         multiple of 64 and one matrix (one batch entry or a
+ *                         broadcast), an MN-major one nothing more; 1: one K block
+ *                         per load always.
+ *   GEMM_OPT_OVERLAP_COPY 0 (default): when a call first copies an operand TMA cannot
+ *                         address, the GEMM is launched as that copy's programmatic
+ *                         dependent (not for the cooperative stream-K forms): its
+ *                         CTAs set up while the copy runs and wait for the copy's
+ *                         completion before their first operand load; 1: the GEMM
+ *                         starts after the copy in plain stream order.
  *   GEMM_OPT_TEST_SIM_SMS test only: n > 0 makes gemm_plan_query and
  *                         gemm_workspace_size plan for a simulated sm_103 device of n
  *                         SMs whose CTA pairs of every tile width fit n / 2 at once,
@@ -455,7 +465,8 @@ typedef enum {
     GEMM_OPT_BLOCK_N = 13,
     GEMM_OPT_DOUBLE_K = 14,
     GEMM_OPT_TEST_SIM_SMS = 15,
-    GEMM_OPT_TEST_DEBUG_BOUND = 16
+    GEMM_OPT_TEST_DEBUG_BOUND = 16,
+    GEMM_OPT_OVERLAP_COPY = 17
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -119,6 +119,11 @@ def test_options(lib):
     assert dg.gemm_set_option(Option.TEST_STALL, 3) == Status.ERR_INVALID_ARG
     assert dg.gemm_set_option(99, 1) == Status.ERR_INVALID_ARG
     assert dg.gemm_get_option(99) == -1
+    assert dg.gemm_get_option(Option.OVERLAP_COPY) == 0
+    assert dg.gemm_set_option(Option.OVERLAP_COPY, 2) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.OVERLAP_COPY, 1) == Status.OK
+    assert dg.gemm_get_option(Option.OVERLAP_COPY) == 1
+    assert dg.gemm_set_option(Option.OVERLAP_COPY, 0) == Status.OK
 
 
 def test_split_reduce_and_block_n_options(lib):

@@ -63,6 +63,8 @@ CLEAN = {
     "pair_two_k_blocks": (dict(M=700, N=600, K=640, lb="col"), {"CTA_PAIR": 3}, True),
     "pair_two_k_blocks_mn_major": (dict(M=700, N=600, K=640), {"CTA_PAIR": 3}, True),
     "single_cta_bn64": (dict(M=300, N=100, K=200), {}, True),
+    "pairs_copied_b_overlapped": (dict(M=700, N=601, K=1000, lb="row"),
+                                  {"CTA_PAIR": 3, "BLOCK_N": 256}, True),
     "stream_k_split_pairs": (dict(M=700, N=600, K=1088, lb="col"),
                              {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}, True),
     "stream_k_contiguous": (dict(M=700, N=600, K=1000),
@@ -148,7 +150,8 @@ def test_headline_writes_every_element_once(D):
 
 def test_ragged_workload_writes_every_element_once(D):
     """4097 x 3001 x 1000 with an fp32 output whose rows are not 16-byte
-    aligned (st.global epilogue) and a B copied for alignment."""
+    aligned (st.global epilogue) and a B copied for alignment (the GEMM
+    launched as the copy's programmatic dependent)."""
     import ctypes
 
     import dense_gemm_bf16_gb300 as dg

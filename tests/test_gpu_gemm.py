@@ -923,6 +923,54 @@ def test_exact_stream_k_split_pieces_two_k_blocks(name):
     assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
+def test_copied_operand_calls_back_to_back():
+    # B with 601-element rows is copied into the workspace before each GEMM,
+    # which is launched as the copy's programmatic dependent.  Three calls on
+    # one stream with no host sync between them, each with new B values in the
+    # same workspace: each result must be its own inputs' (a GEMM that read the
+    # copy before it completed would see the previous call's B).  Then the same
+    # with the overlap off, byte for byte.
+    import dense_gemm_bf16_gb300 as dg
+    import datagen
+    import oracle
+    dev = torch.device("cuda:0")
+    M, N, K = 700, 601, 1000
+    args0 = [0, 1, M, N, K, None, K, 0, 0, None, N, 0, 0, None, N, 0, 0, 2, 1.0, 0.0, None, 0, 0]
+    st, plan = dg.gemm_plan_query(*args0[:5], 1 << 20, K, 0, 0, 1 << 20, N, 0, 0, 1 << 20, N, 0, 0,
+                                  2, 1.0, 0.0, None, 0, 0, 1 << 40)
+    assert st == 0 and plan.pack_b == 1 and plan.launches == 2, plan.as_dict()
+    ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    outs = {}
+    for overlap in (0, 1):
+        assert dg.gemm_set_option(dg.Option.OVERLAP_COPY, overlap) == 0
+        try:
+            jobs = []
+            for seed in (98001, 98011, 98021):
+                a = datagen.to_bf16_bits(datagen.small_ints(seed, (M, K), -4, 4))
+                b = datagen.to_bf16_bits(datagen.small_ints(seed + 1, (K, N), -4, 4))
+                dA = torch.from_numpy(a.view(np.int16)).to(dev)
+                dB = torch.from_numpy(b.view(np.int16)).to(dev)
+                dC = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+                jobs.append((a, b, dA, dB, dC))
+            torch.cuda.synchronize()
+            s = torch.cuda.current_stream().cuda_stream
+            for a, b, dA, dB, dC in jobs:
+                args = list(args0)
+                args[5], args[9], args[13] = dA.data_ptr(), dB.data_ptr(), dC.data_ptr()
+                assert dg.gemm_batched(*args, ws.data_ptr(), ws.numel(), s) == 0
+            torch.cuda.synchronize()
+        finally:
+            dg.gemm_set_option(dg.Option.OVERLAP_COPY, 0)
+        assert dg.gemm_check_device_status(None) == 0
+        outs[overlap] = [dC.cpu().numpy() for *_, dC in jobs]
+        for a, b, *_, dC in jobs:
+            ref = oracle.gemm(oracle.Problem(ab_dtype="bf16", c_dtype="f32", M=M, N=N, K=K,
+                                             A=a.reshape(-1), B=b.reshape(-1), lda=K, ldb=N))[0]
+            assert np.array_equal(dC.cpu().numpy().astype(np.float64), ref), overlap
+    for x, y in zip(outs[0], outs[1]):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
 def test_stream_k_split_two_k_blocks_bias_gelu():
     opts = {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}
     c, out = _double_k_run(dict(M=700, N=600, K=1024, opts=opts), {}, c_dtype="bf16",

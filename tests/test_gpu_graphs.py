@@ -1,8 +1,9 @@
 """CUDA-graph capture of calls whose plans cut tiles into K pieces (stream-K in
-its contiguous and split forms, on single CTAs and CTA pairs, and the spread
-split-K).  Those pieces hand partials over through flags that hold the launch's
-epoch; a graph replays the epoch it captured, so the library clears the flags
-inside the graph before each kernel.  Each case captures one call, then replays
+its contiguous and split forms, on single CTAs and CTA pairs, the spread and
+the atomic split-K), and of a call that copies an operand first.  Those pieces
+hand partials over through flags that hold the launch's epoch; a graph replays
+the epoch it captured, so the library clears the flags inside the graph before
+each kernel.  Each case captures one call, then replays
 it with two input sets in turn, and every replay must equal the oracle exactly
 (small-integer inputs, fp32 output)."""
 import numpy as np
@@ -23,6 +24,9 @@ CASES = {
     "split_pair_mma": ((700, 600, 1000), {"STREAM_K": 3, "MAX_CTAS": 8, "CTA_PAIR": 3}, 2),
     "spread": ((128, 256, 8192), {"SPLIT_REDUCE": 2}, 3),
     "atomic": ((128, 256, 8192), {}, 4),
+    # B's 601-element rows are not 16-byte aligned: the call copies B, and the
+    # GEMM is the copy's programmatic dependent (a graph edge of that kind)
+    "copied_operand": ((700, 601, 1000), {}, 0),
 }
 
 
@@ -52,6 +56,7 @@ def test_captured_call_replays_with_fresh_flags(name):
             assert dg.gemm_set_option(Option[k], v) == 0
         st, plan = dg.gemm_plan_query(*args, 1 << 40)
         assert st == 0 and plan.stream_k == form, plan.as_dict()
+        assert plan.pack_b == (1 if name == "copied_operand" else 0), plan.as_dict()
         ws = torch.empty(int(plan.workspace_bytes), dtype=torch.uint8, device=dev)
         A.copy_(sets[0][0])
         B.copy_(sets[0][1])

@@ -70,6 +70,7 @@ def test_two_k_blocks_per_load_for_mn_major_operands_too(options):
     assert plan(8192, 8192, 8120, la=1, epi=3)["block_k"] == 128
     # a K-major one does: the two-block view is (64 K, rows, K blocks)
     assert plan(8192, 8192, 8120, epi=3)["block_k"] == 64            # A row-major
+    assert plan(4097, 3001, 1000, cdt=2, ws=1 << 40)["block_k"] == 64   # the ragged workload
     # batched: MN-major operands keep their batch dimension; a K-major A must be
     # broadcast (one matrix) to take the two-block view
     n = 2048
