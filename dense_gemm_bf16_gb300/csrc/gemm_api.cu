@@ -435,9 +435,14 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     const int bn_idx = pl.bn == 256 ? 1 : 0;
     int max_pairs = mode > 0 && (pl.bn == 128 || pl.bn == 256) ? d.max_pairs[mode][bn_idx] : 0;
     const int64_t pair_units = c.batch * cdiv(pl.Mc, 2 * TC_BLOCK_M) * cdiv(pl.Nc, pl.bn);
+    // The atomic split-K runs paired whenever two tile rows allow it: a pair
+    // loads each operand element once per K piece instead of once per tile
+    // row or column that uses it (measured on 256 x 256 x 65536).
+    const bool pair_atomic = pl.atomic && (pl.bn == 128 || pl.bn == 256);
     if (mode > 0 && tc_has_mode(pl.bn, mode) && max_pairs > 0 && pl.splits == 1 && tiles_m >= 2 &&
-        pl.inkernel_split == 0 && !pl.atomic &&
-        (want == 3 || (pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
+        pl.inkernel_split == 0 &&
+        (want == 3 || pair_atomic ||
+         (!pl.atomic && pair_units >= max_pairs && pl.kblocks >= kPairMinKBlocks))) {
         pl.mode = mode;
         pl.cm = 2;
         pl.stages = tc_stages_for(pl.bn, mode);
@@ -490,7 +495,14 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.sk_flags_bytes = flags;
         off += static_cast<size_t>(round_up(static_cast<int64_t>(flags), 256));
         pl.ws_need = off;
-        pl.grid = ctas;
+        if (pl.cm == 2) {
+            // every cluster that fits takes a piece, whatever the unit count
+            int clusters = max_pairs;
+            if (cap > 0 && cap / 2 < clusters) clusters = static_cast<int>(cap / 2 > 0 ? cap / 2 : 1);
+            pl.grid = 2 * clusters;
+        } else {
+            pl.grid = ctas;
+        }
     } else if (pl.inkernel_split > 0 && !pl.spread && g_opt_split_reduce.load() != 3 && pl.units > 0 &&
         ctas / pl.units <= 4 && ctas > pl.units && off + sk_need(ctas) <= c.ws_bytes) {
         // the automatic split-K above, in one kernel, balanced over every CTA:

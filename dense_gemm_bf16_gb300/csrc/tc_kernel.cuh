@@ -1256,9 +1256,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     // rows (128 bytes each, 128-byte swizzled): one column takes 8 KB * KS.
     constexpr uint32_t kAtomCol = 8192u * KS;
 
-    if constexpr (!(EPI == 1 && C::CM == 1)) {
-        // the atomic split-K runs on single CTAs with the TMA-store epilogue
-        // only (the plan never asks otherwise); report instead of skipping work
+    if constexpr (EPI != 1) {
+        // the atomic split-K runs with the TMA-store epilogue only (the plan
+        // never asks otherwise); report instead of skipping work
         if (p.sk_atomic) {
             if (threadIdx.x == 0 && p.status) DG_SET_TIMEOUT(p.status);
             return;
@@ -1546,10 +1546,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
         bool first = true;
-        // atomic split-K: this CTA's share of C's initial values first
+        // atomic split-K: this CTA's share of C's initial values first (shares
+        // and flags per CTA of the grid, pairs or not)
         bool init_seen = false;
-        if constexpr (EPI == 1 && CM == 1) {
-            if (p.sk_atomic) atomic_init_c(p, cta0, ncta, q, lane);
+        if constexpr (EPI == 1) {
+            if (p.sk_atomic)
+                atomic_init_c(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), q, lane);
         }
         while (work_next<CM, KS>(p, wi, ncta, rank, w)) {
             if constexpr (EPI == 2) {
@@ -1583,9 +1585,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             if (p.sk_atomic) {
                 // atomic split-K (fp32 C, TMA-store epilogue): every piece adds
                 // its share, once C's initial values are all in place
-                if constexpr (EPI == 1 && CM == 1) {
+                if constexpr (EPI == 1) {
                     if (!init_seen) {
-                        if (!atomic_wait_init(p, ncta, lane, abort_flag)) break;
+                        if (!atomic_wait_init(p, static_cast<int>(gridDim.x), lane, abort_flag))
+                            break;
                         init_seen = true;
                     }
                     tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);

@@ -625,14 +625,21 @@ ATOMIC_CASES = {
                             c_values="ints"),
     "row_bias_batched": dict(M=128, N=256, K=8192, batch=2, bias=True, row_bias=True),
     "ragged_k": dict(M=200, N=264, K=6000),
+    "ragged_m": dict(M=384, N=256, K=8192),
+    "batched_pairs": dict(M=256, N=256, K=4096, batch=2),
+    "wide_n": dict(M=256, N=768, K=16384),
 }
 
 
+# each case with the plan's own pairing (CTA pairs wherever there are two tile
+# rows) and with single CTAs forced
+@pytest.mark.parametrize("pairs", [True, False], ids=["auto", "single"])
 @pytest.mark.parametrize("name", sorted(ATOMIC_CASES))
-def test_exact_atomic_split_k(name):
+def test_exact_atomic_split_k(name, pairs):
     import dense_gemm_bf16_gb300 as dg
     kw = dict(ATOMIC_CASES[name])
     dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 4)
+    dg.gemm_set_option(dg.Option.CTA_PAIR, 0 if pairs else 1)
     try:
         c = Case("bf16", values="ints", seed=509, **kw)
         if c.bias is not None:
@@ -640,9 +647,11 @@ def test_exact_atomic_split_k(name):
         st, out = c.run_gpu()
     finally:
         dg.gemm_set_option(dg.Option.SPLIT_REDUCE, 0)
+        dg.gemm_set_option(dg.Option.CTA_PAIR, 0)
     assert st == 0, c.plan
     assert c.plan["stream_k"] == 4 and c.plan["split_k"] == 1 and c.plan["launches"] == 1 + \
         c.plan["pack_a"] + c.plan["pack_b"], c.plan
+    assert c.plan["cta_pair"] == (2 if pairs and kw["M"] > 128 else 0), c.plan
     assert np.array_equal(c.result(out), c.oracle_full()), c.plan
     assert c.untouched_padding(out)
     assert dg.gemm_check_device_status(None) == 0

@@ -90,11 +90,16 @@ def test_headline_options_change_the_plan(options):
 
 def test_split_k_row_adds_its_pieces_atomically(options):
     # fp32 C, no activation, 38 pieces per tile: the atomic form, whose scratch
-    # is one flag per CTA
+    # is one flag per CTA; CTA pairs (each operand element loaded once per piece)
     p = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
     assert p["stream_k"] == 4 and p["split_k"] == 1 and p["launches"] == 1
-    assert p["grid"] == 152 and p["block_n"] == 128 and p["cta_pair"] == 0
+    assert p["grid"] == 152 and p["block_n"] == 128 and p["cta_pair"] == 2
     assert p["workspace_bytes"] == 256 * ((152 * 8 + 255) // 256)
+    assert plan(128, 256, 65536, cdt=2, ws=UNLIMITED)["cta_pair"] == 0   # one tile row
+    options(CTA_PAIR=1)
+    p1 = plan(256, 256, 65536, cdt=2, ws=UNLIMITED)
+    assert p1["stream_k"] == 4 and p1["cta_pair"] == 0 and p1["grid"] == 152
+    options(CTA_PAIR=0)
     # an activation, or a 16-bit C: the spread reduction
     assert plan(256, 256, 65536, cdt=2, epi=4, ws=UNLIMITED)["stream_k"] == 3
     assert plan(256, 256, 65536, cdt=0, ws=UNLIMITED)["stream_k"] == 3
