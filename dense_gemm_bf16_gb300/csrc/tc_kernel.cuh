@@ -1026,8 +1026,9 @@ __device__ __forceinline__ bool atomic_wait_init(const TcParams& p, int ncta, in
                                                  volatile int* abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
+        // every flag load of the lane in flight at once (no short-circuit)
         bool mine = true;
-        for (int c = lane; c < ncta; c += 32) mine = mine && ld_relaxed_u64(p.sk_flags + c) == p.sk_epoch;
+        for (int c = lane; c < ncta; c += 32) mine &= ld_relaxed_u64(p.sk_flags + c) == p.sk_epoch;
         if (__all_sync(0xffffffffu, mine)) break;
         int give_up = 0;
         if (lane == 0 && (it & 15u) == 0 && (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns)) {
@@ -1547,7 +1548,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         Unit w;
         bool first = true;
         // atomic split-K: this CTA's share of C's initial values first (shares
-        // and flags per CTA of the grid, pairs or not)
+        // and flags per CTA of the grid, pairs or not).  The wait for every
+        // other CTA's share comes with the first accumulator: polling the flags
+        // while the main loop runs (every CTA's epilogue warps on the same few
+        // lines) measured 2 us slower on 256 x 256 x 65536.
         bool init_seen = false;
         if constexpr (EPI == 1) {
             if (p.sk_atomic)
