@@ -386,17 +386,24 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         // Kernel design rules), for an fp32 C that takes TMA stores and no
         // activation: every K piece adds alpha * its partial into C, which the
         // CTAs first set to beta * C + bias; no partial slots, no fix-up, no
-        // waiting on pieces.  By default where more than kMaxInKernel pieces
-        // would otherwise need the spread reduction (measured 30.7 -> 24.6 us
-        // on 256 x 256 x 65536); GEMM_OPT_SPLIT_REDUCE = 4 whenever it applies,
-        // 1 and 2 never (their reductions keep a fixed order).
+        // waiting on pieces.  A column-major computed C (a swapped skinny
+        // product, one matrix) takes it too, with tiles up to 64 wide and the
+        // general epilogue's column-major boxes.  By default where more than
+        // kMaxInKernel pieces would otherwise need the spread reduction
+        // (measured 30.7 -> 24.6 us on 256 x 256 x 65536), and for a swapped
+        // skinny product whatever its piece count (16 x 8192 x 8192: 32.8 ->
+        // 30.7 us against the balanced form, whose last pieces wait for the
+        // others' partials); GEMM_OPT_SPLIT_REDUCE = 4 whenever it applies, 1
+        // and 2 never (their reductions keep a fixed order).
         const int64_t es4 = 4;
         const bool want_atomic =
-            want_spread == 4 || (want_spread == 0 && s_auto > kMaxInKernel);
+            want_spread == 4 ||
+            (want_spread == 0 && (s_auto > kMaxInKernel || !pl.c_row_major_c));
         if (want_atomic && g_opt_stream_k.load() != 1 && s_auto >= 2 && c.cdt == DT_F32 &&
-            epi_act(c.epi) == ACT_NONE && pl.c_row_major_c && aligned(c.C, 16) &&
+            epi_act(c.epi) == ACT_NONE && aligned(c.C, 16) &&
             (c.ldc * es4) % 16 == 0 && (c.batch == 1 || (c.sc * es4) % 16 == 0) &&
-            tc_has_fast(pl.bn) && c.ws != nullptr &&
+            (pl.c_row_major_c ? tc_has_fast(pl.bn) : (c.batch == 1 && pl.bn <= 64)) &&
+            c.ws != nullptr &&
             off + static_cast<size_t>(round_up(static_cast<int64_t>(ctas) * 8, 256)) <= c.ws_bytes) {
             pl.atomic = true;
             pl.inkernel_split = 0;
@@ -610,7 +617,9 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
     // epilogue form: the TMA-store-only one when the output (C, or the split-K
     // partials) takes TMA stores and no beta * C has to be read
     if (pl.atomic) {
-        pl.fast_epi = true;   // checked above: fp32 C that takes TMA stores
+        // checked above: fp32 C that takes TMA stores (row-major: the TMA-store
+        // epilogue; column-major: the general one's column boxes)
+        pl.fast_epi = pl.c_row_major_c;
     } else if (g_opt_fast_epilogue.load() == 0 && tc_has_fast(pl.bn) && pl.c_row_major_c) {
         if (pl.splits > 1) {
             pl.fast_epi = (pl.Nc * 4) % 16 == 0;
@@ -774,6 +783,22 @@ bool encode_output_map(CUtensorMap* map, int dt, void* ptr, int64_t N, int64_t M
     return true;
 }
 
+// Output map of a column-major fp32 C (one matrix) for the atomic split-K:
+// rows contiguous, boxes of 32 rows by `cols` columns, no swizzle.
+bool encode_output_cols_map(CUtensorMap* map, void* ptr, int64_t rows, int64_t cols_total,
+                            int64_t ld, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    if (!aligned(ptr, 16) || (ld * 4) % 16 != 0) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols_total)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 4)};
+    cuuint32_t box[2] = {32u, static_cast<cuuint32_t>(cols)};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2u, ptr, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 gemm_status_t run(const Call& c) {
     gemm_status_t st = validate(c);
     if (st != GEMM_OK) return st;
@@ -894,6 +919,11 @@ gemm_status_t run(const Call& c) {
         p.c_tma = ok ? 1 : 0;
         p.c_tma_3d = c3 ? 1 : 0;
         epi_form = ok && pl.beta_epi ? 2 : (ok && pl.fast_epi ? 1 : 0);
+    } else if (pl.atomic) {
+        // column-major computed C, one matrix: boxes of 32 contiguous rows by
+        // the tile's columns, for the TMA reduce-adds
+        if (!encode_output_cols_map(&p.tmap_c, c.C, pl.Mc, pl.Nc, c.ldc, pl.bn))
+            return GEMM_ERR_CUDA;
     }
     p.status = d->status;
     p.timeout_ns = static_cast<uint64_t>(g_opt_timeout_us.load()) * 1000ull;

@@ -973,44 +973,51 @@ __device__ __forceinline__ void c_ring_drain(CRing& cr, int lane, uint64_t timeo
     __syncwarp();
 }
 
-// Atomic split-K: this CTA's share of the rows of C (all batch entries as one
-// row range) set to beta * C + bias by its four epilogue warps (warp q takes
-// every fourth row, lanes 16-byte column groups), then the share's flag is
-// published with the launch's epoch.  In the debug build's count-writes mode
-// this is the one counted write of each element.
+// Atomic split-K: this CTA's share of C's memory rows (rows of a row-major C,
+// columns of a column-major one; all batch entries as one range) set to
+// beta * C + bias by its four epilogue warps (warp q takes every fourth memory
+// row, lanes 16-byte groups along it), then the share's flag is published with
+// the launch's epoch.  In the debug build's count-writes mode this is the one
+// counted write of each element.
 __device__ __forceinline__ void atomic_init_c(const TcParams& p, int cta, int ncta, int q,
                                               int lane) {
     const Epilogue& e = p.epi;
-    const int64_t rows = static_cast<int64_t>(p.batch) * p.M;
+    const bool cm = !e.c_row_major;
+    const int64_t outer = cm ? p.N : p.M;  // memory rows
+    const int inner = cm ? p.M : p.N;      // elements along one
+    // the bias runs along a memory row, or is one value per memory row
+    const bool bias_inner = e.bias && (cm ? e.bias_on_rows : !e.bias_on_rows);
+    const int64_t rows = static_cast<int64_t>(p.batch) * outer;
     const int64_t r0 = rows * cta / ncta, r1 = rows * (cta + 1) / ncta;
-    const int n4 = p.N / 4;
+    const int n4 = inner / 4;
     for (int64_t r = r0 + q; r < r1; r += 4) {
-        const int64_t b = r / p.M, i = r - b * p.M;
-        float* row = static_cast<float*>(e.C) + b * e.stride_c + i * e.ldc;
-        const float brow = e.bias && e.bias_on_rows && bias_ok(e, i) ? e.bias[i] : 0.0f;
+        const int64_t b = r / outer, o = r - b * outer;
+        float* row = static_cast<float*>(e.C) + b * e.stride_c + o * e.ldc;
+        const float brow = e.bias && !bias_inner && bias_ok(e, o) ? e.bias[o] : 0.0f;
         for (int j4 = lane; j4 < n4; j4 += 32) {
-            if (!c_span_ok(e, b * e.stride_c + i * e.ldc + 4 * j4, 4)) continue;
+            if (!c_span_ok(e, b * e.stride_c + o * e.ldc + 4 * j4, 4)) continue;
             float4 v = make_float4(brow, brow, brow, brow);
             if (e.beta != 0.0f) {
                 const float4 c = reinterpret_cast<const float4*>(row)[j4];
                 v.x = fmaf(e.beta, c.x, v.x), v.y = fmaf(e.beta, c.y, v.y);
                 v.z = fmaf(e.beta, c.z, v.z), v.w = fmaf(e.beta, c.w, v.w);
             }
-            if (e.bias && !e.bias_on_rows && bias_ok(e, 4 * j4 + 3)) {
+            if (bias_inner && bias_ok(e, 4 * j4 + 3)) {
                 v.x += e.bias[4 * j4], v.y += e.bias[4 * j4 + 1];
                 v.z += e.bias[4 * j4 + 2], v.w += e.bias[4 * j4 + 3];
             }
             reinterpret_cast<float4*>(row)[j4] = v;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) count_write(e, b, i, 4 * j4 + k);
+            for (int k = 0; k < 4; ++k)
+                count_write(e, b, cm ? 4 * j4 + k : o, cm ? o : 4 * j4 + k);
         }
-        for (int j = 4 * n4 + lane; j < p.N; j += 32) {
-            if (!c_span_ok(e, b * e.stride_c + i * e.ldc + j)) continue;
+        for (int j = 4 * n4 + lane; j < inner; j += 32) {
+            if (!c_span_ok(e, b * e.stride_c + o * e.ldc + j)) continue;
             float v = brow;
             if (e.beta != 0.0f) v = fmaf(e.beta, row[j], v);
-            if (e.bias && !e.bias_on_rows && bias_ok(e, j)) v += e.bias[j];
+            if (bias_inner && bias_ok(e, j)) v += e.bias[j];
             row[j] = v;
-            count_write(e, b, i, j);
+            count_write(e, b, cm ? j : o, cm ? o : j);
         }
     }
     // every epilogue thread's stores, then one release of the share's flag
@@ -1044,6 +1051,41 @@ __device__ __forceinline__ bool atomic_wait_init(const TcParams& p, int ncta, in
     fence_proxy_async_global();
     __syncwarp();
     return true;
+}
+
+// Atomic split-K with a column-major C (a swapped skinny product): the warp's
+// 32 rows x BN columns of alpha * accumulator go into one box laid out as C is
+// (BN columns of 32 contiguous rows, 128 bytes each), which one TMA reduce-add
+// adds into C through the output map (boxes of 32 rows x BN columns; the TMA
+// unit skips rows and columns outside C).
+template <int BN>
+__device__ __forceinline__ void tile_reduce_cols(const TcParams& p, const Unit& w, int q, int lane,
+                                                 uint32_t tmem_row, uint8_t* wbuf) {
+    static_assert(BN <= 64, "a box of 32 x BN floats fits the warp's 8 KB");
+    constexpr int CH = BN < 32 ? BN : 32;
+    const int row0 = w.pid_m * BM + q * 32;
+    float* box = reinterpret_cast<float*>(wbuf);
+    // this warp's previous reduce-add has read the box
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += CH) {
+        uint32_t r[32];
+        if constexpr (CH == 32)
+            tmem_ld_x32(tmem_row + static_cast<uint32_t>(c0), r);
+        else
+            tmem_ld_x16(tmem_row + static_cast<uint32_t>(c0), r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) box[(c0 + c) * 32 + lane] = p.epi.alpha * __uint_as_float(r[c]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < p.M &&
+        DG_CHECK(w.pid_n * BN < p.N && p.batch == 1, p.status, STATUS_CHECK_BOUNDS)) {
+        tma_reduce_add_2d(&p.tmap_c, smem_u32(box), row0, w.pid_n * BN);
+        bulk_commit_group();
+    }
 }
 
 // Output of one warp's 32 rows for the common case (C written by TMA store,
@@ -1257,8 +1299,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     // rows (128 bytes each, 128-byte swizzled): one column takes 8 KB * KS.
     constexpr uint32_t kAtomCol = 8192u * KS;
 
-    if constexpr (EPI != 1) {
-        // the atomic split-K runs with the TMA-store epilogue only (the plan
+    if constexpr (EPI == 2 || (EPI == 0 && BN > 64)) {
+        // the atomic split-K runs with the TMA-store epilogue, or with the
+        // general one for a column-major C and tiles up to 64 wide (the plan
         // never asks otherwise); report instead of skipping work
         if (p.sk_atomic) {
             if (threadIdx.x == 0 && p.status) DG_SET_TIMEOUT(p.status);
@@ -1307,7 +1350,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         fence_mbar_init();
         prefetch_tmap(&p.tmap_a);
         prefetch_tmap(&p.tmap_b);
-        if (p.c_tma) prefetch_tmap(&p.tmap_c);
+        if (p.c_tma || p.sk_atomic) prefetch_tmap(&p.tmap_c);
     }
     if (warp == 1) {
         tmem_alloc_cg<CG>(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -1553,7 +1596,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // while the main loop runs (every CTA's epilogue warps on the same few
         // lines) measured 2 us slower on 256 x 256 x 65536.
         bool init_seen = false;
-        if constexpr (EPI == 1) {
+        if constexpr (EPI == 1 || (EPI == 0 && BN <= 64)) {
             if (p.sk_atomic)
                 atomic_init_c(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), q, lane);
         }
@@ -1587,15 +1630,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int col_base = w.pid_n * BN;
             const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
             if (p.sk_atomic) {
-                // atomic split-K (fp32 C, TMA-store epilogue): every piece adds
+                // atomic split-K (fp32 C, TMA reduce-adds): every piece adds
                 // its share, once C's initial values are all in place
-                if constexpr (EPI == 1) {
+                if constexpr (EPI == 1 || (EPI == 0 && BN <= 64)) {
                     if (!init_seen) {
                         if (!atomic_wait_init(p, static_cast<int>(gridDim.x), lane, abort_flag))
                             break;
                         init_seen = true;
                     }
-                    tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                    if constexpr (EPI == 1)
+                        tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
+                    else
+                        tile_reduce_cols<BN>(p, w, q, lane, tmem_row, wbuf);
                 }
             } else if (w.kind == UNIT_TAIL || w.kind == UNIT_SPREAD) {
                 // stream-K tail or spread piece: publish this CTA's raw fp32 partial

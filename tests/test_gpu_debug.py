@@ -71,6 +71,8 @@ CLEAN = {
                             {"STREAM_K": 2, "MAX_CTAS": 8, "CTA_PAIR": 1}, True),
     "spread_split_k": (dict(M=128, N=256, K=8192), {"SPLIT_REDUCE": 2}, True),
     "atomic_split_k": (dict(M=128, N=256, K=8192, beta=2.0, c_values="ints"), {}, True),
+    "atomic_swapped": (dict(M=16, N=900, K=8192, beta=2.0, c_values="ints"),
+                       {"SPLIT_REDUCE": 4}, True),
     "explicit_split_k": (dict(M=130, N=200, K=2048, split_k=4), {}, True),
     "swap_ab": (dict(M=16, N=900, K=256), {}, True),
     "batched_broadcast": (dict(M=300, N=400, K=150, batch=3, broadcast_b=True), {}, True),

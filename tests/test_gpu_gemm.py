@@ -566,7 +566,9 @@ def test_auto_split_keeps_its_splits_in_the_reported_workspace(shape):
 # pieces, one CTA each (the split form, stream_k 2); GEMM_OPT_STREAM_K = 1
 # falls back to the two-pass split-K.
 INKERNEL_CASES = {
-    "skinny_swap": dict(M=16, N=8192, K=4096),
+    # C rows 4 bytes past a 16-byte multiple: no TMA reduce-adds, so the
+    # swapped product keeps a one-kernel form with partials
+    "skinny_swap": dict(M=16, N=8192, K=4096, pads=(0, 0, 1)),
     "three_pieces": dict(M=1024, N=640, K=4096),
 }
 INKERNEL_FORMS = {"balanced": ({}, 1), "equal_pieces": ({"SPLIT_REDUCE": 3}, 2)}
@@ -586,13 +588,14 @@ def inkernel_form(request):
 @pytest.mark.parametrize("name", sorted(INKERNEL_CASES))
 def test_exact_inkernel_split(name, inkernel_form):
     import dense_gemm_bf16_gb300 as dg
-    kw = INKERNEL_CASES[name]
-    c = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
+    kw = dict(INKERNEL_CASES[name])
+    M, N, K = kw.pop("M"), kw.pop("N"), kw.pop("K")
+    c = run_exact(Case("bf16", M, N, K, values="ints", seed=501, **kw))
     assert c.plan["stream_k"] == inkernel_form and c.plan["split_k"] == 1, c.plan
     assert c.plan["launches"] == 1, c.plan
     dg.gemm_set_option(dg.Option.STREAM_K, 1)
     try:
-        c2 = run_exact(Case("bf16", kw["M"], kw["N"], kw["K"], values="ints", seed=501))
+        c2 = run_exact(Case("bf16", M, N, K, values="ints", seed=501, **kw))
     finally:
         dg.gemm_set_option(dg.Option.STREAM_K, 0)
     assert c2.plan["stream_k"] == 0 and c2.plan["split_k"] > 1
@@ -628,6 +631,12 @@ ATOMIC_CASES = {
     "ragged_m": dict(M=384, N=256, K=8192),
     "batched_pairs": dict(M=256, N=256, K=4096, batch=2),
     "wide_n": dict(M=256, N=768, K=16384),
+    # swapped skinny products (C^T = B^T A^T, column-major computed C): 16-,
+    # 32- and 64-wide tiles reduce-added through column boxes
+    "swapped_bn16": dict(M=16, N=900, K=8192),
+    "swapped_bn32": dict(M=32, N=520, K=8192, alpha=0.5, beta=2.0, bias=True, c_values="ints"),
+    "swapped_bn64_row_bias": dict(M=48, N=640, K=16384, bias=True, row_bias=True),
+    "swapped_ragged_k": dict(M=16, N=1000, K=6000),
 }
 
 
@@ -718,10 +727,9 @@ def test_exact_spread_split(name, fixed_order):
 @pytest.mark.parametrize("name", sorted(SPREAD_CASES))
 def test_exact_default_many_pieces(name):
     # by default an fp32 C that takes TMA stores (without an activation) gets
-    # the atomic form; the swapped skinny case's C^T is column-major, so it
-    # keeps the spread reduction
+    # the atomic form, the swapped skinny case (column-major C^T) included
     c = run_exact(_spread_case(name, values="ints", seed=710))
-    assert c.plan["stream_k"] == (3 if name == "skinny_swap" else 4), c.plan
+    assert c.plan["stream_k"] == 4, c.plan
     assert c.plan["split_k"] == 1 and c.plan["launches"] == 1, c.plan
 
 
@@ -995,7 +1003,7 @@ def test_stream_k_split_two_k_blocks_bias_gelu():
 BALANCED_CASES = {
     "3_tiles_8_ctas": dict(M=384, N=128, K=4096, opts={"MAX_CTAS": 8}),
     "mn_major_ragged_k": dict(M=384, N=100, K=3000, la="col", lb="row", opts={"MAX_CTAS": 8}),
-    "swap_ab_8_tiles_16_ctas": dict(M=16, N=1000, K=4096, opts={"MAX_CTAS": 16}),
+    "swap_ab_8_tiles_16_ctas": dict(M=16, N=1000, K=4096, pads=(0, 0, 1), opts={"MAX_CTAS": 16}),
     "pairs_contiguous_long_spans": dict(M=700, N=600, K=2048, lb="col",
                                         opts={"STREAM_K": 2, "CTA_PAIR": 3, "MAX_CTAS": 8,
                                               "BLOCK_N": 256}),

@@ -125,11 +125,17 @@ def test_split_k_without_workspace_runs_whole_tiles():
 
 
 def test_skinny_row_swaps_and_spreads_k_over_every_cta(options):
-    # 64 tiles of 128 x 16 on 152 CTAs: the contiguous form, each CTA an equal
-    # range of two-block K steps, no whole units first
+    # 64 tiles of 128 x 16 on 152 CTAs, each CTA an equal range of two-block K
+    # steps, no whole units first: every piece adds its partial into the fp32
+    # C^T (column-major) by TMA reduce-add, whose scratch is one flag per CTA
     p = plan(16, 8192, 8192, cdt=2, ws=UNLIMITED)
     assert p["swap_ab"] == 1 and p["block_n"] == 16 and p["block_k"] == 128
-    assert p["stream_k"] == 1 and p["split_k"] == 1 and p["grid"] == 152 and p["launches"] == 1
+    assert p["stream_k"] == 4 and p["split_k"] == 1 and p["grid"] == 152 and p["launches"] == 1
+    assert p["workspace_bytes"] == 256 * ((152 * 8 + 255) // 256)
+    # a 16-bit C, or C rows that are not 16-byte aligned: the partials of the
+    # pieces go to the piece holding each tile's first step (contiguous form)
+    assert plan(16, 8192, 8192, cdt=0, ws=UNLIMITED)["stream_k"] == 1
+    assert plan(16, 8190, 8192, cdt=2, ws=UNLIMITED)["stream_k"] == 1
     options(SPLIT_REDUCE=3)   # equal pieces instead: 2 per tile, on 128 CTAs
     q = plan(16, 8192, 8192, cdt=2, ws=UNLIMITED)
     assert q["stream_k"] == 2 and q["grid"] == 128 and q["block_k"] == 128
