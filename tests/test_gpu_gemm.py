@@ -940,6 +940,39 @@ def test_exact_stream_k_split_pieces_two_k_blocks(name):
     assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
+# Operands copied for alignment before the GEMM (A, B, both, batched per
+# entry, a broadcast B), each GEMM launched as its copy's programmatic
+# dependent: exact against the oracle, and byte-identical to plain stream
+# order (GEMM_OPT_OVERLAP_COPY = 1).
+OVERLAP_CASES = {
+    "copied_a": dict(M=300, N=520, K=200, pads=(3, 0, 0)),
+    "copied_b_row_major": dict(M=700, N=600, K=1000, lb="row", pads=(0, 1, 0)),
+    "copied_both_col_major": dict(M=520, N=300, K=330, la="col", lb="col", pads=(5, 3, 0)),
+    "batched_copied": dict(M=130, N=200, K=90, batch=3, pads=(1, 3, 0)),
+    "broadcast_b_copied": dict(M=260, N=200, K=150, batch=2, broadcast_b=True, pads=(0, 1, 0)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(OVERLAP_CASES))
+def test_exact_overlapped_operand_copy(name):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(OVERLAP_CASES[name])
+    M, N, K = kw.pop("M"), kw.pop("N"), kw.pop("K")
+    outs = []
+    for overlap in (0, 1):
+        dg.gemm_set_option(dg.Option.OVERLAP_COPY, overlap)
+        try:
+            c = Case("bf16", M, N, K, values="ints", seed=1401, **kw)
+            st, out = c.run_gpu()
+        finally:
+            dg.gemm_set_option(dg.Option.OVERLAP_COPY, 0)
+        assert st == 0 and c.plan["pack_a"] + c.plan["pack_b"] >= 1, c.plan
+        assert np.array_equal(c.result(out), c.oracle_full()), (c.plan, overlap)
+        assert c.untouched_padding(out)
+        outs.append(out)
+    assert np.array_equal(outs[0].view(np.uint8), outs[1].view(np.uint8))
+
+
 def test_copied_operand_calls_back_to_back():
     # B with 601-element rows is copied into the workspace before each GEMM,
     # which is launched as the copy's programmatic dependent.  Three calls on
