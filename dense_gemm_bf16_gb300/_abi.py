@@ -72,6 +72,7 @@ class Option(enum.IntEnum):
     TEST_SIM_SMS = 15
     TEST_DEBUG_BOUND = 16
     OVERLAP_COPY = 17
+    EPILOGUE_WARPS = 18
 
 
 class Plan(ctypes.Structure):

@@ -87,7 +87,11 @@ struct Cfg {
     static constexpr uint32_t B_BYTES = B_ROWS * BK * 2 * KS;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t BAR_BYTES = 512;
-    static constexpr uint32_t EPI_SMEM = EPI_BYTES + (EPI == 2 ? C_RING_BYTES : 0);
+    // epilogue warps: four (one per tensor-memory lane quarter), or eight in
+    // form 3 (two per quarter, each taking half of the tile's columns)
+    static constexpr int EPI_WARPS = EPI == 3 ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr uint32_t EPI_SMEM = EPI_WARPS * EPI_WARP_BYTES + (EPI == 2 ? C_RING_BYTES : 0);
     static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_SMEM) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr uint32_t TMEM_COLS = ACC_BUFS * BN < 32 ? 32 : ACC_BUFS * BN;
@@ -99,6 +103,7 @@ struct Cfg {
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
     static_assert(MODE != 2 || BN >= 128, "pair MMA splits B into 64-column atoms");
+    static_assert(EPI != 3 || (BN % 64 == 0 && KS == 1), "form 3: 32-column chunks per half tile");
     static_assert(BN <= 256 || MODE == 2, "N > 256 only as two pair MMAs");
 };
 
@@ -1263,7 +1268,8 @@ __device__ __forceinline__ void prefetch_c_tile(const TcParams& p, const Unit& w
 }
 
 template <int BN, int MODE, int EPI, int KS = 1>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<BN, MODE, EPI, KS>;
     constexpr int CM = C::CM;
     constexpr int CG = C::CG;
@@ -1308,6 +1314,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             return;
         }
     }
+    if constexpr (EPI == 3) {
+        // form 3 takes whole tiles with plain stores only (the plan never asks
+        // otherwise); report instead of skipping work
+        if (p.sk_atomic || p.sk_iters > 0 || p.sk_split > 0 || p.sk_spread || p.partials ||
+            p.c_tma) {
+            if (threadIdx.x == 0 && p.status) DG_SET_TIMEOUT(p.status);
+            return;
+        }
+    }
 
     // The launch parameters outside the tensor maps lie in four 64-byte lines.
     // A role's first reads of them miss the constant cache one after another
@@ -1334,7 +1349,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // both CTAs.  Accumulator releases are one arrival per epilogue warp.
         const uint32_t full_count = 1u;
         const uint32_t empty_count = 1u;
-        const uint32_t tempty_count = MODE == 2 ? 2u * (TC_EPI_THREADS / 32) : TC_EPI_THREADS / 32;
+        const uint32_t tempty_count = MODE == 2 ? 2u * C::EPI_WARPS : C::EPI_WARPS;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full0 + 8u * s, full_count);
             mbar_init(empty0 + 8u * s, empty_count);
@@ -1574,10 +1589,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..5, or 2..9)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
         uint8_t* wbuf = epi_smem + (warp - 2) * EPI_WARP_BYTES;
+        // form 3: the column half of each tile this warp writes
+        const int col_half = (warp - 2) >> 2;
         float* stage = reinterpret_cast<float*>(wbuf);
         uint32_t nbox = 0;
         // outputs leave L2 first; split-K partials stay for the reduction that follows
@@ -1585,7 +1602,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         int abuf = 0;
         uint32_t aphase = 0;
         // epilogue form 2: this warp's ring of C boxes and their barriers
-        CRing cring{epi_smem + EPI_BYTES + (warp - 2) * 2 * EPI_BOX_BYTES,
+        CRing cring{epi_smem + C::EPI_WARPS * EPI_WARP_BYTES + (warp - 2) * 2 * EPI_BOX_BYTES,
                     cbar0 + 16u * static_cast<uint32_t>(warp - 2), 0u, 0u};
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
@@ -1609,7 +1626,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     for (int c = 0; c < 2 && c < n; ++c) c_ring_issue<BN>(p, w, q, lane, cring, c);
                 }
             }
-            if constexpr (EPI == 0 || EPI == 2) {
+            if constexpr (EPI == 0 || EPI == 2 || EPI == 3) {
                 // C tile of the next item into L2 (and of this one, the first time)
                 if (first)
                     prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
@@ -1629,7 +1646,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int64_t row_base = static_cast<int64_t>(w.pid_m) * BM + q * 32;
             const int col_base = w.pid_n * BN;
             const uint32_t tmem_row = tmem_base + lane_field + static_cast<uint32_t>(abuf * BN);
-            if (p.sk_atomic) {
+            if constexpr (EPI == 3) {
+                // form 3: whole tiles, plain stores; this warp's half of the
+                // columns, 32 at a time
+#pragma unroll 1
+                for (int c0 = col_half * (BN / 2); c0 < (col_half + 1) * (BN / 2); c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_x32(tmem_row + static_cast<uint32_t>(c0), r);
+                    tmem_ld_wait(r);
+                    epilogue_chunk<32>(p, w, row_base, lane, col_base + c0, r, stage);
+                }
+            } else if (p.sk_atomic) {
                 // atomic split-K (fp32 C, TMA reduce-adds): every piece adds
                 // its share, once C's initial values are all in place
                 if constexpr (EPI == 1 || (EPI == 0 && BN <= 64)) {
@@ -1753,7 +1780,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // piece is found again from the cluster index, so nothing stays live
         // across the loop).  The plan runs the spread form with single-CTA
         // tiles only.
-        if constexpr (MODE == 0) {
+        if constexpr (MODE == 0 && EPI != 3) {
             if (p.sk_spread && !*abort_flag) {
                 WorkIter sw = work_begin(p, cta0, ncta);
                 sw.rr_left = 0;
@@ -1795,12 +1822,13 @@ cudaError_t launch_bn(const TcParams& p, int grid, cudaStream_t stream) {
     const bool waits = p.sk_spread || p.sk_split > 0 || p.sk_iters > 0 || p.sk_atomic;
     const bool pdl = p.pdl && !waits;
     if (CM == 1 && !waits && !pdl) {
-        tc_gemm_kernel<BN, MODE, EPI, KS><<<grid, TC_THREADS, Cfg<BN, MODE, EPI, KS>::SMEM, stream>>>(p);
+        tc_gemm_kernel<BN, MODE, EPI, KS>
+            <<<grid, Cfg<BN, MODE, EPI, KS>::THREADS, Cfg<BN, MODE, EPI, KS>::SMEM, stream>>>(p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(TC_THREADS);
+    cfg.blockDim = dim3(Cfg<BN, MODE, EPI, KS>::THREADS);
     cfg.dynamicSmemBytes = Cfg<BN, MODE, EPI, KS>::SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[3];
@@ -1840,7 +1868,7 @@ int max_clusters_bn() {
     constexpr int CM = 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CM * 64);
-    cfg.blockDim = dim3(TC_THREADS);
+    cfg.blockDim = dim3(Cfg<BN, MODE, EPI, KS>::THREADS);
     cfg.dynamicSmemBytes = Cfg<BN, MODE, EPI, KS>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -310,8 +310,10 @@ typedef struct {
                                 piece reducing an equal share of its tile; 4 K steps
                                 dealt as in 1 with every piece adding its partial
                                 into C (GEMM_OPT_SPLIT_REDUCE = 4)                */
-    int32_t fast_epilogue;   /* 1: the TMA-store-only epilogue; 2: the TMA-store epilogue
-                                that reads beta * C by TMA loads (GEMM_OPT_FAST_EPILOGUE) */
+    int32_t fast_epilogue;   /* 0: the general epilogue (four warps); 1: the TMA-store-only
+                                epilogue; 2: the TMA-store epilogue that reads beta * C by
+                                TMA loads (GEMM_OPT_FAST_EPILOGUE); 3: the general
+                                epilogue on eight warps (GEMM_OPT_EPILOGUE_WARPS)      */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
@@ -428,6 +430,11 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         CTAs set up while the copy runs and wait for the copy's
  *                         completion before their first operand load; 1: the GEMM
  *                         starts after the copy in plain stream order.
+ *   GEMM_OPT_EPILOGUE_WARPS 0 (default): whole 256-wide CTA-pair tiles whose output the
+ *                         TMA unit cannot store (plain stores: rows, base or batch
+ *                         stride not 16-byte aligned, or a column-major C) run their
+ *                         epilogue on eight warps, each writing half of a lane
+ *                         quarter's columns (plan fast_epilogue 3); 4: four warps.
  *   GEMM_OPT_TEST_SIM_SMS test only: n > 0 makes gemm_plan_query and
  *                         gemm_workspace_size plan for a simulated sm_103 device of n
  *                         SMs whose CTA pairs of every tile width fit n / 2 at once,
@@ -466,7 +473,8 @@ typedef enum {
     GEMM_OPT_DOUBLE_K = 14,
     GEMM_OPT_TEST_SIM_SMS = 15,
     GEMM_OPT_TEST_DEBUG_BOUND = 16,
-    GEMM_OPT_OVERLAP_COPY = 17
+    GEMM_OPT_OVERLAP_COPY = 17,
+    GEMM_OPT_EPILOGUE_WARPS = 18
 } gemm_option_t;
 
 gemm_status_t gemm_set_option(gemm_option_t option, int64_t value);

@@ -124,6 +124,11 @@ def test_options(lib):
     assert dg.gemm_set_option(Option.OVERLAP_COPY, 1) == Status.OK
     assert dg.gemm_get_option(Option.OVERLAP_COPY) == 1
     assert dg.gemm_set_option(Option.OVERLAP_COPY, 0) == Status.OK
+    assert dg.gemm_get_option(Option.EPILOGUE_WARPS) == 0
+    assert dg.gemm_set_option(Option.EPILOGUE_WARPS, 8) == Status.ERR_INVALID_ARG
+    assert dg.gemm_set_option(Option.EPILOGUE_WARPS, 4) == Status.OK
+    assert dg.gemm_get_option(Option.EPILOGUE_WARPS) == 4
+    assert dg.gemm_set_option(Option.EPILOGUE_WARPS, 0) == Status.OK
 
 
 def test_split_reduce_and_block_n_options(lib):

@@ -65,6 +65,8 @@ CLEAN = {
     "single_cta_bn64": (dict(M=300, N=100, K=200), {}, True),
     "pairs_copied_b_overlapped": (dict(M=700, N=601, K=1000, lb="row"),
                                   {"CTA_PAIR": 3, "BLOCK_N": 256}, True),
+    "eight_epilogue_warps_col_major": (dict(M=600, N=520, K=256, lc="col"),
+                                       {"CTA_PAIR": 3, "BLOCK_N": 256}, True),
     "stream_k_split_pairs": (dict(M=700, N=600, K=1088, lb="col"),
                              {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}, True),
     "stream_k_contiguous": (dict(M=700, N=600, K=1000),
@@ -152,8 +154,8 @@ def test_headline_writes_every_element_once(D):
 
 def test_ragged_workload_writes_every_element_once(D):
     """4097 x 3001 x 1000 with an fp32 output whose rows are not 16-byte
-    aligned (st.global epilogue) and a B copied for alignment (the GEMM
-    launched as the copy's programmatic dependent)."""
+    aligned (st.global epilogue on eight warps) and a B copied for alignment
+    (the GEMM launched as the copy's programmatic dependent)."""
     import ctypes
 
     import dense_gemm_bf16_gb300 as dg
@@ -167,7 +169,7 @@ def test_ragged_workload_writes_every_element_once(D):
                 0, 2, 1.0, 0.0, None, 0, 0]
     plan = dg.Plan()
     assert D.gemm_plan_query(*args(), 1 << 40, ctypes.byref(plan)) == 0
-    assert plan.pack_b == 1 and plan.fast_epilogue == 0
+    assert plan.pack_b == 1 and plan.fast_epilogue == 3
     _count_full_size(D, M, N, K, args, int(plan.workspace_bytes))
 
 

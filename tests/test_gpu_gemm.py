@@ -973,6 +973,68 @@ def test_exact_overlapped_operand_copy(name):
     assert np.array_equal(outs[0].view(np.uint8), outs[1].view(np.uint8))
 
 
+# Epilogue form 3: whole 256-wide pair tiles whose output takes plain stores
+# run the epilogue on eight warps, two per tensor-memory lane quarter, each
+# writing half of the columns.  fp32 rows 4, 8 and 12 bytes past a 16-byte
+# multiple, 16-bit outputs, a column-major C, beta * C, ragged M and N, a
+# batch with an unaligned C stride, a copied operand: bit-exact against the
+# oracle and byte-identical to four warps (GEMM_OPT_EPILOGUE_WARPS = 4).
+EPI8_CASES = {
+    "f32_ldc_1_mod_4": dict(M=700, N=601, K=1000),
+    "f32_ldc_2_mod_4": dict(M=520, N=770, K=512),
+    "f32_ldc_3_mod_4": dict(M=600, N=515, K=384),
+    "bf16_odd_ldc": dict(M=520, N=601, K=512, c_dtype="bf16", values="uniform"),
+    "col_major_c": dict(M=600, N=520, K=256, lc="col"),
+    "beta_f32": dict(M=520, N=601, K=512, beta=2.0, c_values="ints"),
+    "ragged_m_n": dict(M=257, N=259, K=200),
+    "batched": dict(M=300, N=257, K=128, batch=2),
+    "copied_b": dict(M=700, N=601, K=1000, lb="row"),
+}
+
+
+def _epi8_run(name, warps, **case_kw):
+    import dense_gemm_bf16_gb300 as dg
+    kw = dict(EPI8_CASES[name])
+    kw.setdefault("values", "ints")
+    M, N, K = kw.pop("M"), kw.pop("N"), kw.pop("K")
+    opts = {"CTA_PAIR": 3, "BLOCK_N": 256, "EPILOGUE_WARPS": warps}
+    for k, v in opts.items():
+        dg.gemm_set_option(dg.Option[k], v)
+    try:
+        # split_k = 1: whole tiles (no automatic split or stream-K pieces)
+        c = Case("bf16", M, N, K, seed=1501, split_k=1, **kw, **case_kw)
+        st, out = c.run_gpu()
+    finally:
+        for k in opts:
+            dg.gemm_set_option(dg.Option[k], 0)
+    assert st == 0, f"status {st}"
+    return c, out
+
+
+@pytest.mark.parametrize("name", sorted(EPI8_CASES))
+def test_exact_eight_epilogue_warps(name):
+    c, out = _epi8_run(name, 0)
+    assert c.plan["fast_epilogue"] == 3 and c.plan["cta_pair"] == 2, c.plan
+    ref = c.oracle_full()
+    if c.c_dtype == "f32":
+        assert np.array_equal(c.result(out), ref), c.plan
+    else:
+        check_close(c, c.result(out), ref)
+    assert c.untouched_padding(out)
+    four, out4 = _epi8_run(name, 4)
+    assert four.plan["fast_epilogue"] == 0, four.plan
+    assert np.array_equal(out.view(np.uint8), out4.view(np.uint8))
+
+
+def test_eight_epilogue_warps_epilogue_terms():
+    c, out = _epi8_run("f32_ldc_1_mod_4", 0, alpha=0.75, bias=True, act="gelu_tanh")
+    assert c.plan["fast_epilogue"] == 3, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+    c, out = _epi8_run("col_major_c", 0, bias=True, row_bias=True, act="relu", alpha=1.5)
+    assert c.plan["fast_epilogue"] == 3, c.plan
+    check_close(c, c.result(out), c.oracle_full())
+
+
 def test_copied_operand_calls_back_to_back():
     # B with 601-element rows is copied into the workspace before each GEMM,
     # which is launched as the copy's programmatic dependent.  Three calls on

@@ -148,10 +148,20 @@ def test_batched_beta_rows_read_c_by_tma_loads():
         assert p["fast_epilogue"] == 2 and p["cta_pair"] == 2 and p["block_k"] == 64
 
 
-def test_ragged_row_copies_b_and_stores_with_st_global():
+def test_ragged_row_copies_b_and_stores_with_st_global(options):
     p = plan(4097, 3001, 1000, cdt=2, ws=UNLIMITED)
     assert p["pack_b"] == 1 and p["pack_a"] == 0 and p["launches"] == 2
-    assert p["fast_epilogue"] == 0 and p["workspace_bytes"] > 0
+    # plain stores (3001-float rows) on eight epilogue warps: 64 KB of staging,
+    # one pipeline stage fewer
+    assert p["fast_epilogue"] == 3 and p["workspace_bytes"] > 0
+    assert p["cta_pair"] == 2 and p["block_n"] == 256 and p["stages"] == 5
+    options(EPILOGUE_WARPS=4)
+    q = plan(4097, 3001, 1000, cdt=2, ws=UNLIMITED)
+    assert q["fast_epilogue"] == 0 and q["stages"] == 6
+    options(EPILOGUE_WARPS=0)
+    # not for C that TMA can store, nor for stream-K pieces or split-K slices
+    assert plan(4096, 3008, 1000, cdt=2, ws=UNLIMITED)["fast_epilogue"] == 1
+    assert plan(4097, 3001, 1000, cdt=2, ws=UNLIMITED, split_k=2)["fast_epilogue"] != 3
     # B's rows of 3001 bf16 are not 16-byte aligned: TMA cannot read it in place
     st, _ = dg.gemm_plan_query(0, 1, 4097, 3001, 1000, BASE, 1000, 0, 0, BASE, 3001, 0, 0,
                                BASE, 3001, 0, 0, 2, 1.0, 0.0, None, 0, 0, 0)
@@ -223,6 +233,7 @@ INSTANTIATED = {
     0: {(16, 0), (32, 0), (64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
     1: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
     2: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2)},
+    3: {(256, 2)},
 }
 # (tile width, mode, epilogue form) compiled with two K blocks per load
 TWO_K_BLOCKS = {(128, 2, 1), (256, 2, 1), (16, 0, 0), (32, 0, 0), (64, 0, 0), (64, 0, 1),
@@ -257,7 +268,7 @@ OPTION_SETS = [
     {"CTA_PAIR": 3, "WIDE_TILE": 2}, {"SWAP_AB": 1}, {"SWAP_AB": 2}, {"STREAM_K": 1},
     {"STREAM_K": 2}, {"STREAM_K": 3}, {"FAST_EPILOGUE": 1}, {"SPLIT_REDUCE": 1},
     {"SPLIT_REDUCE": 2}, {"BLOCK_N": 16}, {"BLOCK_N": 64}, {"BLOCK_N": 128}, {"DOUBLE_K": 1},
-    {"MAX_CTAS": 37}, {"GROUP_M": 1},
+    {"MAX_CTAS": 37}, {"GROUP_M": 1}, {"CTA_PAIR": 3, "EPILOGUE_WARPS": 4},
 ]
 
 
@@ -318,6 +329,9 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
             assert p["block_k"] == 64, (p, ctx)
         if form == 2:
             assert kw["beta"] != 0.0 and kw["cdt"] in (0, 1), (p, ctx)
+        if form == 3:                # eight epilogue warps: whole tiles, plain stores
+            assert p["stream_k"] == 0 and p["split_k"] == 1 and p["block_k"] == 64, (p, ctx)
+            assert opts.get("EPILOGUE_WARPS", 0) == 0, (p, ctx)
         if p["stream_k"] == 3:       # the spread reduction runs on single CTAs only
             assert mode == 0 and p["workspace_bytes"] > 0, (p, ctx)
             assert p["launches"] == 1 + p["pack_a"] + p["pack_b"], (p, ctx)   # no reduction pass
