@@ -940,6 +940,18 @@ def test_exact_stream_k_split_pieces_two_k_blocks(name):
     assert np.array_equal(out.view(np.uint8), out1.view(np.uint8))
 
 
+# The operand copy (2-byte loads, 16-byte stores) at every base offset of 0-7
+# elements, rows of one 8-element group or less and of many, pitches that put
+# later rows at other offsets.
+@pytest.mark.parametrize("off", range(8))
+@pytest.mark.parametrize("shape", [(37, 70, 45), (130, 300, 1000), (64, 9, 7)])
+def test_exact_operand_copy_offsets(off, shape):
+    M, N, K = shape
+    c = run_exact(Case("bf16", M, N, K, la="row", lb="row", values="ints", pads=(1, 3, 0),
+                       offsets=(off, 7 - off, 0), seed=1601 + off))
+    assert c.plan["pack_a"] + c.plan["pack_b"] >= 1, c.plan
+
+
 # Operands copied for alignment before the GEMM (A, B, both, batched per
 # entry, a broadcast B), each GEMM launched as its copy's programmatic
 # dependent: exact against the oracle, and byte-identical to plain stream
