@@ -196,7 +196,7 @@ struct Plan {
     int bn = 0, stages = 0, splits = 1, group_m = 8, grid = 0, launches = 0, cm = 1, mode = 0;
     bool fast_epi = false;  // TMA-store-only epilogue form
     bool beta_epi = false;  // TMA-store epilogue that reads beta * C by TMA loads
-    bool epi8 = false;      // general epilogue on eight warps (form 3)
+    bool epi8 = false;      // epilogue on eight warps (forms 3 and 4)
     int ks = 1;             // 64-deep K blocks per stage and per operand load
     int sk = 0;  // stream-K: 0 off, 1 contiguous K ranges, 2 last wave split into equal pieces
     int inkernel_split = 0;  // automatic split-K done in one kernel by the split form
@@ -659,22 +659,29 @@ gemm_status_t make_plan(const Call& c, const DevState& d, Plan& pl) {
         pl.ks = 2;
         pl.stages = tc_stages_ks2(pl.bn, pl.mode, epi_form);
     }
-    // Form 3: a general (plain-store) epilogue of whole 256-wide pair tiles
-    // runs on eight warps, two per tensor-memory lane quarter, each writing
-    // half the columns.  For an output TMA cannot store (a row-major C whose
-    // base, rows or batch stride are not 16-byte aligned; a column-major one)
-    // the epilogue's chain of shared-memory transposes and plain stores is
-    // latency-bound, and short-K tiles wait for it through the two
-    // accumulators.  GEMM_OPT_EPILOGUE_WARPS = 4 keeps four warps.
+    // Forms 3 and 4: the epilogue of whole 256-wide pair tiles runs on eight
+    // warps, two per tensor-memory lane quarter, each writing half the
+    // columns.  Form 3 takes a general (plain-store) epilogue, for an output
+    // TMA cannot store (a row-major C whose base, rows or batch stride are not
+    // 16-byte aligned; a column-major one): its chain of shared-memory
+    // transposes and plain stores is latency-bound, and short-K tiles wait for
+    // it through the two accumulators.  Form 4 takes the epilogue that reads
+    // beta * C by TMA loads, for short-K tiles (at most 32 K blocks), with one
+    // output box per warp so that the pipeline keeps four stages.
+    // GEMM_OPT_EPILOGUE_WARPS = 4 keeps four warps.
     {
         const int64_t es = dt_bytes(c.cdt);
         const bool c_tma_able = pl.c_row_major_c && aligned(c.C, 16) && (c.ldc * es) % 16 == 0 &&
                                 (c.batch == 1 || (c.sc * es) % 16 == 0);
-        if (pl.kernel == 1 && epi_form == 0 && pl.ks == 1 && !c_tma_able && pl.splits == 1 &&
-            pl.sk == 0 && !pl.atomic && !pl.spread && pl.inkernel_split == 0 &&
-            tc_has_general8(pl.bn, pl.mode) && g_opt_epilogue_warps.load() == 0) {
+        const bool whole = pl.kernel == 1 && pl.ks == 1 && pl.splits == 1 && pl.sk == 0 &&
+                           !pl.atomic && !pl.spread && pl.inkernel_split == 0 &&
+                           g_opt_epilogue_warps.load() == 0;
+        const int form = (epi_form == 0 && !c_tma_able) ? 3
+                         : (epi_form == 2 && pl.kblocks <= 32) ? 4
+                                                                : 0;
+        if (whole && form != 0 && tc_has_epi8(pl.bn, pl.mode, form)) {
             pl.epi8 = true;
-            pl.stages = tc_stages_general8(pl.bn, pl.mode);
+            pl.stages = tc_stages_epi8(pl.bn, pl.mode, form);
         }
     }
     // the contiguous form's iterations are steps of ks K blocks
@@ -940,8 +947,9 @@ gemm_status_t run(const Call& c) {
         p.c_tma_3d = c3 ? 1 : 0;
         epi_form = ok && pl.beta_epi ? 2 : (ok && pl.fast_epi ? 1 : 0);
         if (pl.epi8) {
-            if (ok) return GEMM_ERR_UNSUPPORTED;  // the plan took C as not TMA-storable
-            epi_form = 3;
+            // the plan took C as TMA-storable exactly for form 4
+            if (ok != pl.beta_epi) return GEMM_ERR_UNSUPPORTED;
+            epi_form = pl.beta_epi ? 4 : 3;
         }
     } else if (pl.atomic) {
         // column-major computed C, one matrix: boxes of 32 contiguous rows by
@@ -1212,7 +1220,7 @@ gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch, int64_t M, i
     plan->launches = pl.launches;
     plan->workspace_bytes = static_cast<int64_t>(pl.ws_need);
     plan->cta_pair = pl.mode;
-    plan->fast_epilogue = pl.epi8 ? 3 : (pl.beta_epi ? 2 : (pl.fast_epi ? 1 : 0));
+    plan->fast_epilogue = pl.epi8 ? (pl.beta_epi ? 4 : 3) : (pl.beta_epi ? 2 : (pl.fast_epi ? 1 : 0));
     plan->stream_k = pl.atomic ? 4 : (pl.spread ? 3 : pl.sk);
     return st;
 }

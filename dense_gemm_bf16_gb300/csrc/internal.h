@@ -113,10 +113,10 @@ struct TcParams {
 // beta == 0 or split-K partials, with tmap_c boxes of 128-byte rows
 // (tc_has_fast tells the tile widths that have it); 2 the same with beta * C
 // read by TMA loads through tmap_c, for a 16-bit C (tc_has_beta_form tells the
-// tile widths and modes, tc_stages_beta its pipeline depth); 3 the general
-// form on eight epilogue warps, two per tensor-memory lane quarter, each
-// writing half of the tile's columns, for whole tiles with plain stores only
-// (tc_has_general8 / tc_stages_general8).  ks: 64-deep K
+// tile widths and modes, tc_stages_beta its pipeline depth); 3 and 4 forms 0
+// and 2 on eight epilogue warps, two per tensor-memory lane quarter, each
+// writing half of the tile's columns, for whole tiles only (tc_has_epi8 /
+// tc_stages_epi8).  ks: 64-deep K
 // blocks per stage and per TMA load of each operand, 1 or 2 (tc_has_ks2
 // tells where 2 exists; a K-major operand's map is then the three-dimensional
 // view 64 K x rows x K blocks, an MN-major one's takes boxes of 128 K rows).
@@ -131,8 +131,8 @@ cudaError_t tc_launch(int block_n, int mode, int epi, int ks, const TcParams& p,
 bool tc_has_ks2(int block_n, int mode, int epi);
 int tc_stages_ks2(int block_n, int mode, int epi);
 int tc_max_pairs(int block_n, int mode);  // two-CTA clusters resident at once on this device
-bool tc_has_general8(int block_n, int mode);
-int tc_stages_general8(int block_n, int mode);
+bool tc_has_epi8(int block_n, int mode, int epi);
+int tc_stages_epi8(int block_n, int mode, int epi);
 
 struct SgemmParams {
     const float* A; int64_t lda; int64_t stride_a; int32_t a_row;

@@ -1,6 +1,6 @@
 // Host dispatch of the tensor-core GEMM kernel over tile width, CTA mode and
 // epilogue form; the instantiations live in tc_gemm_general.cu,
-// tc_gemm_general8.cu, tc_gemm_fast.cu, tc_gemm_beta.cu and tc_gemm_ks2*.cu.
+// tc_gemm_epi8.cu, tc_gemm_fast.cu, tc_gemm_beta.cu and tc_gemm_ks2*.cu.
 #include "tc_kernel.cuh"
 
 namespace dg {
@@ -15,8 +15,9 @@ cudaError_t tc_prepare_ks2(int bn);
 cudaError_t tc_launch_ks2(int bn, int mode, int epi, const TcParams& p, int grid,
                           cudaStream_t stream);
 cudaError_t tc_launch_beta(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
-cudaError_t tc_prepare_general8(int bn);
-cudaError_t tc_launch_general8(int bn, int mode, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc_prepare_epi8(int bn);
+cudaError_t tc_launch_epi8(int bn, int mode, int epi, const TcParams& p, int grid,
+                           cudaStream_t stream);
 
 int tc_stages_for(int bn, int mode) {
     if (mode == 2) {
@@ -40,7 +41,7 @@ cudaError_t tc_prepare(int bn) {
     if (e == cudaSuccess) e = tc_prepare_fast(bn);
     if (e == cudaSuccess) e = tc_prepare_beta(bn);
     if (e == cudaSuccess) e = tc_prepare_ks2(bn);
-    if (e == cudaSuccess) e = tc_prepare_general8(bn);
+    if (e == cudaSuccess) e = tc_prepare_epi8(bn);
     return e;
 }
 
@@ -62,7 +63,7 @@ cudaError_t tc_launch(int bn, int mode, int epi, int ks, const TcParams& p, int 
     }
     if (epi == 1 && tc_has_fast(bn)) return tc_launch_fast(bn, mode, p, grid, stream);
     if (epi == 2 && tc_has_beta_form(bn, mode)) return tc_launch_beta(bn, mode, p, grid, stream);
-    if (epi == 3) return tc_launch_general8(bn, mode, p, grid, stream);
+    if (epi == 3 || epi == 4) return tc_launch_epi8(bn, mode, epi, p, grid, stream);
     return tc_launch_general(bn, mode, p, grid, stream);
 }
 

@@ -51,13 +51,13 @@ constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
 // bytes, 128-byte swizzled) for the TMA-store epilogue, or one staging tile
 // of 32 rows x 32 fp32 columns (rows padded to 33 words so that row-wise
 // writes and column-wise reads each touch 32 distinct banks) for the
-// st.global fallback.  The epilogue form that reads beta * C (EPI 2) adds a
-// ring of two more boxes per warp that TMA loads fill with C.
+// st.global fallback.  The epilogue forms that read beta * C (kind 2: EPI 2
+// and 4) add a ring of two more boxes per warp that TMA loads fill with C;
+// form 4 keeps one output box per warp.
 constexpr int STAGE_LD = 33;
 constexpr uint32_t EPI_WARP_BYTES = 8192;
 constexpr uint32_t EPI_BOX_BYTES = 4096;
-constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;  // four epilogue warps
-constexpr uint32_t C_RING_BYTES = 4 * 2 * EPI_BOX_BYTES;
+constexpr uint32_t C_RING_WARP_BYTES = 2 * EPI_BOX_BYTES;  // two C boxes per epilogue warp
 static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
 
 // MODE 0: one CTA per 128 x BN tile.
@@ -88,22 +88,27 @@ struct Cfg {
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t BAR_BYTES = 512;
     // epilogue warps: four (one per tensor-memory lane quarter), or eight in
-    // form 3 (two per quarter, each taking half of the tile's columns)
-    static constexpr int EPI_WARPS = EPI == 3 ? 8 : 4;
+    // forms 3 and 4 (two per quarter, each taking half of the tile's columns),
+    // which are forms 0 and 2 (KIND) on eight warps; form 4 keeps one output
+    // box per warp so that the pipeline keeps four stages
+    static constexpr int KIND = EPI == 3 ? 0 : (EPI == 4 ? 2 : EPI);
+    static constexpr int EPI_WARPS = EPI >= 3 ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr uint32_t EPI_SMEM = EPI_WARPS * EPI_WARP_BYTES + (EPI == 2 ? C_RING_BYTES : 0);
+    static constexpr uint32_t EPI_WARP = EPI == 4 ? EPI_BOX_BYTES : EPI_WARP_BYTES;
+    static constexpr uint32_t EPI_SMEM =
+        EPI_WARPS * (EPI_WARP + (KIND == 2 ? C_RING_WARP_BYTES : 0));
     static constexpr int STAGES_FIT = (kMaxDynSmem - 1024 - BAR_BYTES - EPI_SMEM) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 12 ? 12 : STAGES_FIT;
     static constexpr uint32_t TMEM_COLS = ACC_BUFS * BN < 32 ? 32 : ACC_BUFS * BN;
     static constexpr int CHUNK = BN < 32 ? BN : 32;
     static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + BAR_BYTES + EPI_SMEM;
     static_assert(STAGES >= 2, "pipeline needs two stages");
-    static_assert((2 * STAGES + 14) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+    static_assert((2 * STAGES + 6 + 2 * EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
     static_assert(B_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
     static_assert(EPI_BOX_BYTES % 1024 == 0 && EPI_WARP_BYTES % 1024 == 0,
                   "swizzled output boxes must be 1024-byte aligned");
     static_assert(MODE != 2 || BN >= 128, "pair MMA splits B into 64-column atoms");
-    static_assert(EPI != 3 || (BN % 64 == 0 && KS == 1), "form 3: 32-column chunks per half tile");
+    static_assert(EPI < 3 || (BN % 128 == 0 && KS == 1), "forms 3, 4: whole 64-column steps per half tile");
     static_assert(BN <= 256 || MODE == 2, "N > 256 only as two pair MMAs");
 };
 
@@ -1101,11 +1106,17 @@ __device__ __forceinline__ void tile_reduce_cols(const TcParams& p, const Unit& 
 // r at j ^ (r % 8); the boxes are 1024-byte aligned).  With BETA (epilogue
 // form 2, 16-bit C) each step also adds beta * C from the warp's C ring, whose
 // boxes have the same swizzle.  Returns false when a C box never arrived.
-template <int BN, int ES, bool BETA = false>
+//
+// [c_lo, c_hi): the 64-column steps of the tile this warp writes (all of them,
+// or one half when two warps share a lane quarter).  SINGLE (16-bit C): one
+// output box per warp instead of two alternating ones.
+template <int BN, int ES, bool BETA = false, bool SINGLE = false>
 __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, int q, int lane,
                                               uint32_t tmem_row, uint8_t* wbuf, uint32_t& nbox,
                                               uint64_t pol, CRing* cr = nullptr,
-                                              volatile int* abort_flag = nullptr) {
+                                              volatile int* abort_flag = nullptr, int c_lo = 0,
+                                              int c_hi = BN / 64) {
+    static_assert(!SINGLE || ES == 2, "one box per step: 16-bit C");
     static_assert(BN % 64 == 0, "64-column steps");
     static_assert(!BETA || ES == 2, "beta * C by TMA loads for 16-bit outputs");
     constexpr int NB = ES == 4 ? 2 : 1;  // boxes per step
@@ -1122,8 +1133,9 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
     // atomic split-K: add alpha * acc into C (initialised to beta * C + bias)
     const bool reduce = !BETA && ES == 4 && p.sk_atomic != 0;
     const int nsteps = fast_steps<BN>(p, w);
+    const int c_end = nsteps < c_hi ? nsteps : c_hi;
 #pragma unroll 1
-    for (int c = 0; c < BN / 64; ++c) {
+    for (int c = c_lo; c < c_hi; ++c) {
         const int col0 = w.pid_n * BN + c * 64;
         if (col0 >= p.N) break;
         const bool full = col0 + 64 <= p.N;
@@ -1173,7 +1185,7 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
                     }
                     ++cr->used;
                     __syncwarp();  // every lane has read the box before it is refilled
-                    if (c + 2 < nsteps) c_ring_issue<BN>(p, w, q, lane, *cr, c + 2);
+                    if (c + 2 < c_end) c_ring_issue<BN>(p, w, q, lane, *cr, c + 2);
                 }
             }
             if (e.bias) {
@@ -1197,7 +1209,7 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
         // the box(es) written before must have been read by their TMA stores:
         // 16-bit C alternates two boxes, fp32 fills both every step
         if (lane == 0) {
-            if constexpr (NB == 2)
+            if constexpr (NB == 2 || SINGLE)
                 bulk_wait_group_read<0>();
             else
                 bulk_wait_group_read<1>();
@@ -1205,7 +1217,7 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < NB; ++k) {
-            uint8_t* box = wbuf + (NB == 2 ? k : (nbox & 1u)) * EPI_BOX_BYTES;
+            uint8_t* box = wbuf + (NB == 2 ? k : (SINGLE ? 0u : (nbox & 1u))) * EPI_BOX_BYTES;
             uint8_t* line = box + lane * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1231,7 +1243,8 @@ __device__ __forceinline__ bool tile_out_fast(const TcParams& p, const Unit& w, 
             for (int k = 0; k < NB; ++k) {
                 const int bc = col0 + k * BOXC;
                 if (bc >= p.N) break;
-                const uint32_t box = smem_u32(wbuf + (NB == 2 ? k : (nbox & 1u)) * EPI_BOX_BYTES);
+                const uint32_t box =
+                    smem_u32(wbuf + (NB == 2 ? k : (SINGLE ? 0u : (nbox & 1u))) * EPI_BOX_BYTES);
                 if (!out_box_ok(p, bc, row0, zc)) continue;
                 if (reduce) {
                     if (p.c_tma_3d)
@@ -1283,12 +1296,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sA0 = smem_u32(smem);
     const uint32_t sB0 = sA0 + C::STAGES * C::A_BYTES;
-    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][C ring (EPI 2)][barriers]
+    // layout: [A stages][B stages][epilogue boxes (1024-aligned)][C ring (kind 2)][barriers]
     uint8_t* epi_smem = smem + C::STAGES * C::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + C::EPI_SMEM);
     const uint32_t bar0 = smem_u32(bars);
     // barrier slots: full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain,
-    // gather (the spread reduction's copies), C boxes [4 epilogue warps][2]
+    // gather (the spread reduction's copies), C boxes [epilogue warps][2]
     const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8u * C::STAGES;
     const uint32_t tfull0 = bar0 + 16u * C::STAGES;
@@ -1296,7 +1309,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
     const uint32_t drain_bar = tempty0 + 16u;
     const uint32_t gather_bar = drain_bar + 8u;
     const uint32_t cbar0 = gather_bar + 8u;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 14);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 6 + 2 * C::EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -1305,7 +1318,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
     // rows (128 bytes each, 128-byte swizzled): one column takes 8 KB * KS.
     constexpr uint32_t kAtomCol = 8192u * KS;
 
-    if constexpr (EPI == 2 || (EPI == 0 && BN > 64)) {
+    if constexpr (C::KIND == 2 || (C::KIND == 0 && BN > 64)) {
         // the atomic split-K runs with the TMA-store epilogue, or with the
         // general one for a column-major C and tiles up to 64 wide (the plan
         // never asks otherwise); report instead of skipping work
@@ -1314,11 +1327,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
             return;
         }
     }
-    if constexpr (EPI == 3) {
-        // form 3 takes whole tiles with plain stores only (the plan never asks
-        // otherwise); report instead of skipping work
+    if constexpr (EPI >= 3) {
+        // forms 3 and 4 take whole tiles only, form 3 with plain stores and form
+        // 4 with TMA stores (the plan never asks otherwise); report instead of
+        // skipping work
         if (p.sk_atomic || p.sk_iters > 0 || p.sk_split > 0 || p.sk_spread || p.partials ||
-            p.c_tma) {
+            (EPI == 3 ? p.c_tma != 0 : p.c_tma == 0)) {
             if (threadIdx.x == 0 && p.status) DG_SET_TIMEOUT(p.status);
             return;
         }
@@ -1360,7 +1374,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         }
         mbar_init(drain_bar, 1);
         mbar_init(gather_bar, 1);
-        for (int b = 0; b < 8; ++b) mbar_init(cbar0 + 8u * b, 1);
+        for (int b = 0; b < 2 * C::EPI_WARPS; ++b) mbar_init(cbar0 + 8u * b, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tmap_a);
@@ -1592,9 +1606,12 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         // ------------------------------------------------ epilogue (warps 2..5, or 2..9)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_field = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* wbuf = epi_smem + (warp - 2) * EPI_WARP_BYTES;
-        // form 3: the column half of each tile this warp writes
+        uint8_t* wbuf = epi_smem + (warp - 2) * C::EPI_WARP;
+        // forms 3, 4: the column half of each tile this warp writes; its
+        // 64-column steps [step_lo, step_hi)
         const int col_half = (warp - 2) >> 2;
+        const int step_lo = C::EPI_WARPS == 8 ? col_half * (BN / 128) : 0;
+        const int step_hi = C::EPI_WARPS == 8 ? step_lo + BN / 128 : BN / 64;
         float* stage = reinterpret_cast<float*>(wbuf);
         uint32_t nbox = 0;
         // outputs leave L2 first; split-K partials stay for the reduction that follows
@@ -1602,7 +1619,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         int abuf = 0;
         uint32_t aphase = 0;
         // epilogue form 2: this warp's ring of C boxes and their barriers
-        CRing cring{epi_smem + C::EPI_WARPS * EPI_WARP_BYTES + (warp - 2) * 2 * EPI_BOX_BYTES,
+        CRing cring{epi_smem + C::EPI_WARPS * C::EPI_WARP + (warp - 2) * C_RING_WARP_BYTES,
                     cbar0 + 16u * static_cast<uint32_t>(warp - 2), 0u, 0u};
         WorkIter wi = work_begin(p, cta0, ncta);
         Unit w;
@@ -1618,15 +1635,17 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
                 atomic_init_c(p, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), q, lane);
         }
         while (work_next<CM, KS>(p, wi, ncta, rank, w)) {
-            if constexpr (EPI == 2) {
+            if constexpr (C::KIND == 2) {
                 // the first two C boxes of a tile this warp will write, requested
                 // before its accumulator is waited for
                 if (p.epi.beta != 0.0f && (w.kind == UNIT_FULL || w.kind == UNIT_HEAD)) {
                     const int n = fast_steps<BN>(p, w);
-                    for (int c = 0; c < 2 && c < n; ++c) c_ring_issue<BN>(p, w, q, lane, cring, c);
+                    const int end = n < step_hi ? n : step_hi;
+                    for (int c = step_lo; c < step_lo + 2 && c < end; ++c)
+                        c_ring_issue<BN>(p, w, q, lane, cring, c);
                 }
             }
-            if constexpr (EPI == 0 || EPI == 2 || EPI == 3) {
+            if constexpr (C::KIND == 0 || C::KIND == 2) {
                 // C tile of the next item into L2 (and of this one, the first time)
                 if (first)
                     prefetch_c_tile<BN>(p, w, static_cast<int64_t>(w.pid_m) * BM + q * 32 + lane);
@@ -1734,10 +1753,11 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
                         tile_out_fast<BN, 4>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
                     else
                         tile_out_fast<BN, 2>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol);
-                } else if constexpr (EPI == 2) {
+                } else if constexpr (C::KIND == 2) {
                     // the plan takes this form for a 16-bit C only
-                    if (!tile_out_fast<BN, 2, true>(p, w, q, lane, tmem_row, wbuf, nbox, store_pol,
-                                                    &cring, abort_flag))
+                    if (!tile_out_fast<BN, 2, true, EPI == 4>(p, w, q, lane, tmem_row, wbuf, nbox,
+                                                              store_pol, &cring, abort_flag,
+                                                              step_lo, step_hi))
                         break;
                 } else if (p.c_tma) {
                     if constexpr (BN >= 32) {
@@ -1780,7 +1800,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         // piece is found again from the cluster index, so nothing stays live
         // across the loop).  The plan runs the spread form with single-CTA
         // tiles only.
-        if constexpr (MODE == 0 && EPI != 3) {
+        if constexpr (MODE == 0 && EPI < 3) {
             if (p.sk_spread && !*abort_flag) {
                 WorkIter sw = work_begin(p, cta0, ncta);
                 sw.rr_left = 0;
@@ -1794,7 +1814,7 @@ __global__ void __launch_bounds__(Cfg<BN, MODE, EPI, KS>::THREADS, 1)
         }
         // the TMA stores must finish, and no C box may still be loading, before
         // the CTA exits
-        if constexpr (EPI == 2) c_ring_drain(cring, lane, p.timeout_ns);
+        if constexpr (C::KIND == 2) c_ring_drain(cring, lane, p.timeout_ns);
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
     }

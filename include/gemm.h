@@ -312,8 +312,8 @@ typedef struct {
                                 into C (GEMM_OPT_SPLIT_REDUCE = 4)                */
     int32_t fast_epilogue;   /* 0: the general epilogue (four warps); 1: the TMA-store-only
                                 epilogue; 2: the TMA-store epilogue that reads beta * C by
-                                TMA loads (GEMM_OPT_FAST_EPILOGUE); 3: the general
-                                epilogue on eight warps (GEMM_OPT_EPILOGUE_WARPS)      */
+                                TMA loads (GEMM_OPT_FAST_EPILOGUE); 3 and 4: 0 and 2 on
+                                eight warps (GEMM_OPT_EPILOGUE_WARPS)                  */
 } gemm_plan_t;
 
 gemm_status_t gemm_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
@@ -430,11 +430,13 @@ gemm_status_t gemm_strided_plan_query(gemm_dtype_t ab_dtype, int64_t batch,
  *                         CTAs set up while the copy runs and wait for the copy's
  *                         completion before their first operand load; 1: the GEMM
  *                         starts after the copy in plain stream order.
- *   GEMM_OPT_EPILOGUE_WARPS 0 (default): whole 256-wide CTA-pair tiles whose output the
- *                         TMA unit cannot store (plain stores: rows, base or batch
- *                         stride not 16-byte aligned, or a column-major C) run their
+ *   GEMM_OPT_EPILOGUE_WARPS 0 (default): whole 256-wide CTA-pair tiles run their
  *                         epilogue on eight warps, each writing half of a lane
- *                         quarter's columns (plan fast_epilogue 3); 4: four warps.
+ *                         quarter's columns, when their output takes plain stores
+ *                         (rows, base or batch stride not 16-byte aligned, or a
+ *                         column-major C; plan fast_epilogue 3) or when beta * C
+ *                         is read by TMA loads and K is at most 32 blocks of 64
+ *                         (plan fast_epilogue 4); 4: four warps always.
  *   GEMM_OPT_TEST_SIM_SMS test only: n > 0 makes gemm_plan_query and
  *                         gemm_workspace_size plan for a simulated sm_103 device of n
  *                         SMs whose CTA pairs of every tile width fit n / 2 at once,

@@ -67,6 +67,9 @@ CLEAN = {
                                   {"CTA_PAIR": 3, "BLOCK_N": 256}, True),
     "eight_epilogue_warps_col_major": (dict(M=600, N=520, K=256, lc="col"),
                                        {"CTA_PAIR": 3, "BLOCK_N": 256}, True),
+    "eight_epilogue_warps_beta_tma": (dict(M=520, N=700, K=300, c_dtype="bf16", beta=1.0,
+                                           values="uniform", split_k=1),
+                                      {"CTA_PAIR": 3, "BLOCK_N": 256}, False),
     "stream_k_split_pairs": (dict(M=700, N=600, K=1088, lb="col"),
                              {"STREAM_K": 3, "CTA_PAIR": 3, "MAX_CTAS": 8, "BLOCK_N": 256}, True),
     "stream_k_contiguous": (dict(M=700, N=600, K=1000),

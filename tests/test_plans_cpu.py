@@ -145,7 +145,9 @@ def test_batched_beta_rows_read_c_by_tma_loads():
     s = 1024
     for sb in (s * s, 0):
         p = plan(s, s, s, batch=64, alpha=0.5, beta=1.0, sa=s * s, sb=sb, sc=s * s)
-        assert p["fast_epilogue"] == 2 and p["cta_pair"] == 2 and p["block_k"] == 64
+        # the TMA-store epilogue reading beta * C, on eight warps (16 K blocks)
+        assert p["fast_epilogue"] == 4 and p["cta_pair"] == 2 and p["block_k"] == 64
+        assert p["stages"] == 4
 
 
 def test_ragged_row_copies_b_and_stores_with_st_global(options):
@@ -234,6 +236,7 @@ INSTANTIATED = {
     1: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2), (512, 2)},
     2: {(64, 0), (128, 0), (256, 0), (128, 2), (256, 2)},
     3: {(256, 2)},
+    4: {(256, 2)},
 }
 # (tile width, mode, epilogue form) compiled with two K blocks per load
 TWO_K_BLOCKS = {(128, 2, 1), (256, 2, 1), (16, 0, 0), (32, 0, 0), (64, 0, 0), (64, 0, 1),
@@ -327,11 +330,13 @@ def test_every_plan_names_a_compiled_kernel_and_keeps_its_invariants(options, op
             assert mode == 2 or K > 7 * 64, (p, ctx)    # single CTAs: 8 K blocks at least
         else:
             assert p["block_k"] == 64, (p, ctx)
-        if form == 2:
+        if form in (2, 4):
             assert kw["beta"] != 0.0 and kw["cdt"] in (0, 1), (p, ctx)
-        if form == 3:                # eight epilogue warps: whole tiles, plain stores
+        if form in (3, 4):           # eight epilogue warps: whole tiles
             assert p["stream_k"] == 0 and p["split_k"] == 1 and p["block_k"] == 64, (p, ctx)
             assert opts.get("EPILOGUE_WARPS", 0) == 0, (p, ctx)
+        if form == 4:
+            assert K <= 32 * 64, (p, ctx)
         if p["stream_k"] == 3:       # the spread reduction runs on single CTAs only
             assert mode == 0 and p["workspace_bytes"] > 0, (p, ctx)
             assert p["launches"] == 1 + p["pack_a"] + p["pack_b"], (p, ctx)   # no reduction pass
