@@ -16,7 +16,10 @@ enum : int { ACT_NONE = 0, ACT_GELU_TANH = 1, ACT_RELU = 2, ACT_GELU_ERF = 3 };
 // BLOCK_K = 64 slices (64 bf16 = one 128-byte swizzle row).
 constexpr int TC_BLOCK_M = 128;
 constexpr int TC_BLOCK_K = 64;
-constexpr int TC_THREADS = 192;       // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+// threads of the tensor-core kernel's four-warp epilogue forms (0-2): warp 0
+// TMA producer, warp 1 MMA issuer, warps 2-5 epilogue (forms 3 and 4 have
+// eight epilogue warps, 320 threads: Cfg::THREADS)
+constexpr int TC_THREADS = 192;
 constexpr int TC_EPI_THREADS = 128;
 
 // Epilogue description shared by the tensor-core kernel and the split-K reduce.

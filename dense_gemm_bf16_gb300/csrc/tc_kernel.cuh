@@ -13,9 +13,11 @@
 //                      4 KS per stage, into one of two TMEM accumulators;
 //                      tcgen05.commit frees the stage / publishes the tile.
 //   warps 2-5          epilogue: tcgen05.ld of the accumulator (one TMEM lane =
-//                      one output row per thread), alpha/beta/bias/GELU in fp32,
-//                      one rounding to the output type, masked global stores;
-//                      or, for split-K, the raw fp32 partial tile.
+//   (2-9 in forms      one output row per thread), alpha/beta/bias/GELU in fp32,
+//   3 and 4)           one rounding to the output type, masked global stores;
+//                      or, for split-K, the raw fp32 partial tile.  Forms 3
+//                      and 4 put two warps on each TMEM lane quarter, each
+//                      writing half of the tile's columns.
 //
 // The two TMEM accumulators let the epilogue of tile i overlap the main loop
 // of tile i+1.  Work units (batch, K slice, tile) are dealt to CTAs round
@@ -27,11 +29,12 @@
 // read with loads one chunk ahead, TMA store or an st.global fallback for a C
 // that TMA cannot address); 1 only the TMA store with beta == 0 or a split-K
 // partial, in 64-column steps, and so needs far fewer registers; 2 the same
-// TMA store with beta * C of a 16-bit C brought in by TMA loads.  KS is the
+// TMA store with beta * C of a 16-bit C brought in by TMA loads; 3 and 4 are
+// 0 and 2 on eight epilogue warps (whole 256-wide pair tiles).  KS is the
 // number of 64-deep K blocks per stage (2: one TMA load brings two K blocks of
 // a K-major operand).  The forms are instantiated in separate translation
-// units (tc_gemm_general.cu, tc_gemm_fast.cu, tc_gemm_beta.cu, tc_gemm_ks2.cu)
-// that compile in parallel.
+// units (tc_gemm_general.cu, tc_gemm_fast.cu, tc_gemm_beta.cu, tc_gemm_ks2*.cu,
+// tc_gemm_epi8.cu) that compile in parallel.
 #pragma once
 #include <stdint.h>
 
