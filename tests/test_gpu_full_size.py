@@ -202,6 +202,65 @@ def test_c4_boundary_and_skinny_full_size(name, M, N, K):
     check_f32(got[i, j], ref, math.sqrt(K) * amax * bmax)
 
 
+@pytest.mark.parametrize("name", ["flat_4096x4096x16", "flat_4096x4096x16_f32"])
+def test_flat_small_k_full_size(name):
+    """The flat product (K = 16), bf16 and fp32 output: every element against
+    the full oracle."""
+    import torch
+    fn, plan, keep = _row(name)
+    A, B, C = keep[0], keep[1], keep[2]
+    n, k = 4096, 16
+    # no stale value may pass as a result (bf16 bits 0xFFFF are a NaN)
+    C.fill_(float("nan") if C.dtype == torch.float32 else -1)
+    fn()
+    torch.cuda.synchronize()
+    a = A.cpu().numpy().view(np.uint16)
+    b = B.cpu().numpy().view(np.uint16)
+    f32 = name.endswith("f32")
+    p = oracle.Problem(ab_dtype="bf16", M=n, N=n, K=k, A=a.ravel(), lda=k, la="row",
+                       B=b.ravel(), ldb=n, lb="row", c_dtype="f32" if f32 else "bf16")
+    ref = oracle.gemm(p)[0]
+    if f32:
+        got = C.cpu().numpy().astype(np.float64)
+        amax = np.abs(bf16_to_f64(a)).max()
+        bmax = np.abs(bf16_to_f64(b)).max()
+        check_f32(got, ref, math.sqrt(k) * amax * bmax)
+    else:
+        check_16bit(bf16_to_f64(C.cpu().numpy().view(np.uint16)), ref)
+
+
+@pytest.mark.parametrize("name", ["streamk_2560x2560x16384", "streamk_off_2560x2560x16384"])
+def test_stream_k_row_full_size(name):
+    """2560 x 2560 x 16384, bf16 output, with stream-K cutting the partial
+    wave along K and with it switched off, as the bench rows run it."""
+    import torch
+
+    import bench
+    import dense_gemm_bf16_gb300 as dg
+    opts = bench.ROW_OPTIONS.get(name, {})
+    saved = {k: dg.gemm_get_option(dg.Option[k]) for k in opts}
+    try:
+        for k_, v in opts.items():
+            assert dg.gemm_set_option(dg.Option[k_], v) == 0
+        fn, plan, keep = _row(name)
+        assert (plan["stream_k"] == 0) == bool(opts), plan
+        A, B, C = keep[0], keep[1], keep[2]
+        C.fill_(-1)  # bf16 bits 0xFFFF: a NaN
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        for k_, v in saved.items():
+            dg.gemm_set_option(dg.Option[k_], v)
+    n, k = 2560, 16384
+    a = A.cpu().numpy().view(np.uint16)
+    b = B.cpu().numpy().view(np.uint16)
+    got = bf16_to_f64(C.cpu().numpy().view(np.uint16))
+    _, i, j = sample_positions(n, n, 1024, seed=9005)
+    p = oracle.Problem(ab_dtype="bf16", M=n, N=n, K=k, A=a.ravel(), lda=k, la="row",
+                       B=b.ravel(), ldb=n, lb="row", c_dtype="bf16")
+    check_16bit(got[i, j], oracle.gemm_sampled(p, None, i, j))
+
+
 @pytest.mark.parametrize("name", ["batched_64x1024", "batched_64x1024_bcast"])
 def test_c5_batched_full_size(name):
     """alpha 0.5, beta 1 on a bf16 N(0,1) C, per-batch or broadcast B."""
