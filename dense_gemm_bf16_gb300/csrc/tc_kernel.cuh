@@ -52,16 +52,19 @@ constexpr uint32_t kMaxDynSmem = 232448;  // 227 KB opt-in limit per CTA
 
 // Shared memory of each epilogue warp: two 4 KB output boxes (32 rows x 128
 // bytes, 128-byte swizzled) for the TMA-store epilogue, or one staging tile
-// of 32 rows x 32 fp32 columns (rows padded to 33 words so that row-wise
-// writes and column-wise reads each touch 32 distinct banks) for the
-// st.global fallback.  The epilogue forms that read beta * C (kind 2: EPI 2
+// of 32 rows x 32 fp32 columns for the st.global fallback.  Its rows are
+// padded to 36 words: a lane writes its row as 16-byte stores, and the eight
+// lanes of each 128-byte phase (words 36 t + c .. 36 t + c + 3, t = 0..7) then
+// cover 32 distinct banks; the column-wise reads (word 36 r + t for lane t)
+// do too.  The epilogue forms that read beta * C (kind 2: EPI 2
 // and 4) add a ring of two more boxes per warp that TMA loads fill with C;
 // form 4 keeps one output box per warp.
-constexpr int STAGE_LD = 33;
+constexpr int STAGE_LD = 36;
 constexpr uint32_t EPI_WARP_BYTES = 8192;
 constexpr uint32_t EPI_BOX_BYTES = 4096;
 constexpr uint32_t C_RING_WARP_BYTES = 2 * EPI_BOX_BYTES;  // two C boxes per epilogue warp
 static_assert(32 * STAGE_LD * 4 <= EPI_WARP_BYTES, "staging tile must fit");
+static_assert(STAGE_LD % 4 == 0, "16-byte row writes");
 
 // MODE 0: one CTA per 128 x BN tile.
 // MODE 2: two CTAs of a cluster compute one 256 x BN tile with cta_group::2
@@ -513,6 +516,18 @@ __device__ __forceinline__ bool partial_ok(const TcParams& p, const float* at) {
 #endif
 }
 
+// Lane t's CH accumulator columns into row t of the staging tile (16-byte
+// stores; the tile is 16-byte aligned and STAGE_LD a multiple of 4).
+template <int CH>
+__device__ __forceinline__ void stage_row(float* stage, int lane, const uint32_t (&r)[32]) {
+    static_assert(CH % 4 == 0, "whole 16-byte stores");
+    float4* dst = reinterpret_cast<float4*>(stage + lane * STAGE_LD);
+#pragma unroll
+    for (int c = 0; c < CH; c += 4)
+        dst[c / 4] = make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                 __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+}
+
 // Epilogue of one CH-column chunk of this warp's 32 rows.  On entry lane t
 // holds row row_base + t, columns col0 .. col0+CH-1 (fp32 accumulators).
 template <int CH>
@@ -535,8 +550,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w,
             }
             return;
         }
-#pragma unroll
-        for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
+        stage_row<CH>(stage, lane, r);
         __syncwarp();
         const int col = col0 + lane;
         if (lane < CH && col < p.N) {
@@ -561,8 +575,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcParams& p, const Unit& w,
     }
     // row-major output: transpose through shared memory so that each warp
     // store covers consecutive columns of one row.
-#pragma unroll
-    for (int c = 0; c < CH; ++c) stage[lane * STAGE_LD + c] = __uint_as_float(r[c]);
+    stage_row<CH>(stage, lane, r);
     __syncwarp();
     if (e.c_dtype == DT_BF16)
         rows_out<CH, __nv_bfloat16>(e, w, p.M, p.N, row_base, lane, col0, stage);
